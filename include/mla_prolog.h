@@ -1,0 +1,209 @@
+/*
+ * mla_prolog.h -- C ABI of the GB300 (sm_103a) MLA KV prolog library
+ * (libmla_prolog.so).
+ *
+ * The operation is the "KV prolog" of DeepSeek-V2 Multi-head Latent
+ * Attention.  Sources (web pages, cited by title and section):
+ *
+ *   [MIG] "DeepSeek-V2-Lite-Chat MLA KV Prolog 迁移指南：基于 PyPTO 融合算子与
+ *         aclgraph 的 NPU 推理优化实践"
+ *   [R1]  "DeepSeek-R1或Kimi-K2模型在NPU实现高性能推理"
+ *
+ * [MIG] §"背景：为什么要迁移 MLA KV Prolog" lists the seven steps this
+ * library fuses:
+ *   1. kv_a_proj  C = X * W_kva                        [T, hidden] x [hidden, 576]
+ *   2. split      compressed_kv = C[:, 0:512], k_pe_raw = C[:, 512:576]
+ *   3. RMSNorm    n = compressed_kv / sqrt(mean(compressed_kv^2) + eps) * gamma
+ *   4. kv_b_proj  KV = n * W_kvb                       [T, 512] x [512, H*256]
+ *   5. reshape + split: KV -> [T, H, 256]; k_nope = [..., 0:128], value = [..., 128:256]
+ *   6. RoPE on k_pe_raw at each token's position
+ *   7. assemble the head-major outputs k_nope [b,H,s,128], value [b,H,s,128],
+ *      k_pe [b,1,s,64]
+ * with T = b*s token rows, row t = bi*s + si ([MIG] §"源码级原理：KV Prolog 的
+ * 混合优化实现", steps 1 and 5).  Shapes: [MIG] §"精度验证：Golden 对比测试"
+ * (hidden 2048, W_kva [2048, 576], W_kvb [512, 4096], gamma [512], eps 1e-6,
+ * outputs [1,16,1,128], [1,16,1,128], [1,1,1,64]).
+ *
+ * Readings taken where the pages are silent (the library and its tests use
+ * the same ones):
+ *   - RoPE (step 6): [MIG] says only "x*cos + x_rot*sin".  The library uses
+ *     the DeepSeek-V2 convention: de-interleave x'[j] = x[2j], x'[32+j] =
+ *     x[2j+1] (j < 32), then out = x'*cos[p] + rotate_half(x')*sin[p] with
+ *     rotate_half(x') = [-x'[32:64], x'[0:32]].  The output keeps the
+ *     de-interleaved order.  cos/sin are caller tables [max_pos, 64] fp32,
+ *     read entry by entry (any rope scaling is the caller's business).
+ *   - Accumulation is fp32; steps 1-3 stay in fp32 on chip and n is rounded
+ *     once to the I/O dtype as the operand of step 4; outputs are rounded
+ *     to nearest even.
+ *   - W8A8 ([R1] §"权重转换" names the W8A8 weight modes; the fused "MLA
+ *     prolog" switch enable_mla_prolog is in [R1] §"推理执行"): int8 weights
+ *     with one fp32 scale per output channel, per-token dynamic symmetric
+ *     int8 activations, int32 accumulation, dequantisation acc*s_x*s_w.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every tensor.  Device pointers must be 16-byte
+ *     aligned (else MLA_ERR_MISALIGNED) and the tensors dense row-major in
+ *     the layouts given.  Weights use the pre-transposed [in, out] layout of
+ *     [MIG] §"源码级原理" step 1; nothing is pre-packed.
+ *   - A handle owns only its device workspace (allocated by create, freed
+ *     by destroy).  run never allocates and never synchronises: it enqueues
+ *     its kernels on `stream` and returns.  Launch failures come back as
+ *     MLA_ERR_CUDA (text in mla_last_cuda_error()).
+ *   - Faults the device detects (a position outside [0, max_pos), which is
+ *     clamped so that no out-of-bounds read happens; a device wait that ran
+ *     out of its time budget) are recorded in a status word in the
+ *     workspace; mla_kv_prolog_status() reports and clears it.
+ *   - A handle is not safe to use from two streams at once (one workspace).
+ */
+#ifndef MLA_PROLOG_H
+#define MLA_PROLOG_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_PROLOG_ABI_VERSION 1
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,     /* null handle/pointer, b or s < 0, bad config value      */
+  MLA_ERR_UNSUPPORTED = 2,     /* dimensions outside what the kernels implement          */
+  MLA_ERR_TOO_MANY_TOKENS = 3, /* b*s > config.max_tokens                                 */
+  MLA_ERR_MISALIGNED = 4,      /* a device pointer not 16-byte aligned                    */
+  MLA_ERR_CUDA = 5,            /* a CUDA runtime call failed; see mla_last_cuda_error()   */
+  MLA_ERR_DEVICE_TIMEOUT = 6,  /* a device-side wait ran past config.spin_budget_ns       */
+  MLA_ERR_BAD_POSITION = 7,    /* a position outside [0, max_pos) was seen (and clamped)  */
+  MLA_ERR_NO_MEMORY = 8,       /* workspace allocation failed in create                   */
+  MLA_ERR_WRONG_MODE = 9       /* run of one quant mode on a handle made for the other    */
+} mla_status;
+
+typedef enum mla_dtype { MLA_F16 = 0, MLA_BF16 = 1 } mla_dtype;
+typedef enum mla_quant { MLA_QUANT_NONE = 0, MLA_QUANT_W8A8 = 1 } mla_quant;
+
+/* Kernel-path selection.  AUTO picks by token count T (the T-bucketed
+ * selection that replaces the short/long dynamic selection of [MIG]
+ * §"源码级原理", last paragraph): the fused split-K decode kernel for small
+ * T, the tcgen05 tensor-core prefill kernel for large T.  DECODE / PREFILL
+ * force one path (for tests and benchmarks). */
+typedef enum mla_path { MLA_PATH_AUTO = 0, MLA_PATH_DECODE = 1, MLA_PATH_PREFILL = 2 } mla_path;
+
+typedef struct mla_prolog_config {
+  int hidden;       /* model width: 2048 (V2-Lite), 7168 (R1); multiple of 64          */
+  int kv_lora_rank; /* latent width; must be 512                                        */
+  int rope_dim;     /* rope width; must be 64                                           */
+  int num_heads;    /* H >= 1 (16 V2-Lite, 128 R1)                                      */
+  int nope_dim;     /* must be 128                                                      */
+  int v_dim;        /* must be 128                                                      */
+  int dtype;        /* mla_dtype of hidden, fp weights, gamma and all outputs           */
+  float eps;        /* RMSNorm epsilon (1e-6)                                           */
+  int max_tokens;   /* largest b*s any run on this handle will pass (sizes workspace)  */
+  int max_pos;      /* rows of the cos/sin tables                                       */
+  int quant;        /* mla_quant                                                        */
+  int q_lora_rank;  /* W8A8 only: q latent width (1536); multiple of 64                 */
+  unsigned long long spin_budget_ns; /* device wait limit; 0 selects 1 s               */
+} mla_prolog_config;
+
+typedef struct mla_prolog_s* mla_prolog_t;
+
+/* Validate `cfg`, allocate the workspace (split-K partials, normalised
+ * latent rows, barrier counters, status word) on the current device and
+ * return a handle in *out.  Errors: MLA_ERR_INVALID_ARG (null, non-positive
+ * sizes, eps < 0), MLA_ERR_UNSUPPORTED (kv_lora_rank != 512, rope_dim != 64,
+ * nope/v != 128, hidden % 64 != 0, W8A8 with dtype != BF16 or
+ * q_lora_rank % 64 != 0), MLA_ERR_NO_MEMORY, MLA_ERR_CUDA. */
+mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out);
+
+/* Enqueue one KV prolog (steps 1-7 above) of T = b*s token rows on `stream`.
+ *   hidden_states [b*s, hidden]        dtype      (row t = bi*s + si)
+ *   positions     [b*s]                int32      rope position of each row
+ *   W_kva         [hidden, 576]        dtype      pre-transposed kv_a_proj_with_mqa
+ *   gamma_kv      [512]                dtype      kv_a_layernorm weight
+ *   W_kvb         [512, H*256]         dtype      pre-transposed kv_b_proj
+ *   cos_table, sin_table [max_pos, 64] float32
+ *   k_nope        [b, H, s, 128]       dtype      output
+ *   value         [b, H, s, 128]       dtype      output
+ *   k_pe          [b, 1, s, 64]        dtype      output
+ * T = 0 is a no-op returning MLA_OK.  Errors: MLA_ERR_INVALID_ARG,
+ * MLA_ERR_TOO_MANY_TOKENS, MLA_ERR_MISALIGNED, MLA_ERR_WRONG_MODE (handle
+ * created for W8A8), MLA_ERR_CUDA.  Device-side faults: see
+ * mla_kv_prolog_status. */
+mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_states,
+                             const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                             const void* W_kvb, const float* cos_table, const float* sin_table,
+                             void* k_nope, void* value, void* k_pe, cudaStream_t stream);
+
+/* Enqueue the W8A8 full MLA prolog (Q side + KV side) of T = b*s rows on a
+ * handle created with quant = MLA_QUANT_W8A8 and dtype = MLA_BF16.
+ *   hidden_states [b*s, hidden] bf16; positions [b*s] int32
+ *   W_qa  [hidden, q_lora_rank] int8,  sW_qa  [q_lora_rank] f32,  gamma_q [q_lora_rank] bf16
+ *   W_qb  [q_lora_rank, H*192]  int8,  sW_qb  [H*192] f32
+ *   W_kva [hidden, 576]         int8,  sW_kva [576] f32,          gamma_kv [512] bf16
+ *   W_kvb [512, H*256]          int8,  sW_kvb [H*256] f32
+ *   cos_table, sin_table [max_pos, 64] f32
+ * Outputs (bf16): q_nope [b,H,s,128], q_pe [b,H,s,64], k_nope [b,H,s,128],
+ * value [b,H,s,128], k_pe [b,1,s,64].  Steps: quantise each hidden row
+ * (amax, inv = 127/amax, q = clamp(rint(x*inv), +-127), s_x = amax/127, all
+ * single fp32 operations); q_a_proj and kv_a_proj as int8 GEMMs with int32
+ * accumulators, dequantised acc*s_x*s_w; RMSNorm of the q latent (gamma_q)
+ * and of compressed_kv (gamma_kv); requantise both rows the same way;
+ * q_b_proj -> [H,192] split into q_nope (0:128) and q_pe (128:192), RoPE on
+ * q_pe; kv_b_proj -> k_nope / value; RoPE on k_pe.  Errors as for
+ * mla_kv_prolog_run. */
+mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_states,
+                               const int32_t* positions, const int8_t* W_qa, const float* sW_qa,
+                               const void* gamma_q, const int8_t* W_qb, const float* sW_qb,
+                               const int8_t* W_kva, const float* sW_kva, const void* gamma_kv,
+                               const int8_t* W_kvb, const float* sW_kvb,
+                               const float* cos_table, const float* sin_table, void* q_nope,
+                               void* q_pe, void* k_nope, void* value, void* k_pe,
+                               cudaStream_t stream);
+
+/* Synchronise `stream`, read the device status word of the handle, clear
+ * it (and reset the device barrier counters if a wait timed out) and
+ * return MLA_OK, MLA_ERR_BAD_POSITION or MLA_ERR_DEVICE_TIMEOUT (the first
+ * fault recorded since the last call). */
+mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream);
+
+/* Free the workspace and the handle.  The caller must make sure no run on
+ * the handle is still executing (synchronise its stream first). */
+mla_status mla_kv_prolog_destroy(mla_prolog_t h);
+
+/* Force a kernel path (mla_path) for later runs on this handle. */
+mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path);
+
+/* Number of kernels the last run on this handle enqueued, and the path
+ * (mla_path, never AUTO) it took. */
+int mla_kv_prolog_last_launches(mla_prolog_t h);
+int mla_kv_prolog_last_path(mla_prolog_t h);
+
+/* W8A8 building blocks, callable on their own (the full run uses the same
+ * kernels; the tests check them bit-exactly):
+ *   mla_w8a8_quant_rows: per-row symmetric int8 quantisation of a bf16
+ *     matrix x [rows, cols] -> q [rows, cols] int8, scale [rows] f32 (the
+ *     fp32 operation sequence described for mla_prolog_w8a8_run).
+ *   mla_w8a8_gemm_s32: acc [M, N] int32 = A [M, K] int8 x W [K, N] int8,
+ *     W in [in, out] layout; K % 32 == 0, N % 8 == 0, 16-byte aligned rows.
+ *   mla_prolog_w8a8_operands: copy the int8 operands and fp32 scales that
+ *     the last W8A8 run fed to q_b_proj (q1 [T, q_lora_rank], s1 [T]) and
+ *     kv_b_proj (c1 [T, 512], s2 [T]) into caller device buffers.          */
+mla_status mla_w8a8_quant_rows(const void* x_bf16, int rows, int cols, int8_t* q, float* scale,
+                               cudaStream_t stream);
+mla_status mla_w8a8_gemm_s32(const int8_t* A, const int8_t* W, int M, int K, int N,
+                             int32_t* acc, cudaStream_t stream);
+mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1, int8_t* c1,
+                                    float* s2, cudaStream_t stream);
+
+/* Text of a status code (static storage), the text of the last CUDA error
+ * seen by this library on the calling thread, and the ABI version. */
+const char* mla_status_string(mla_status s);
+const char* mla_last_cuda_error(void);
+int mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PROLOG_H */
