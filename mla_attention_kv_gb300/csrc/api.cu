@@ -1,0 +1,287 @@
+// api.cu -- the C ABI of include/mla_prolog.h: handle lifetime, argument
+// validation, workspace, T-bucketed path selection and kernel dispatch.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/mla_prolog.h"
+#include "internal.h"
+
+using namespace mla;
+
+struct mla_prolog_s {
+  mla_prolog_config cfg;
+  int device;
+  int num_sms;
+  int path_override;
+  int last_launches;
+  int last_path;
+  unsigned long long budget_ns;
+  // workspace
+  void* ws;
+  size_t ws_bytes;
+  unsigned* status;    // [1]
+  unsigned* counters;  // [2] grid barrier
+  float* partials;
+  void* nrm;
+  DecodePlan dplan;
+  bool decode_ok;
+  // W8A8 workspace (see w8a8.cu)
+  W8Workspace w8;
+};
+
+static thread_local char g_last_cuda_error[256] = "no error";
+
+static mla_status cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%d)", what,
+           cudaGetErrorString(e), (int)e);
+  return MLA_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_PROLOG_ABI_VERSION; }
+
+const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MLA_ERR_TOO_MANY_TOKENS: return "b*s exceeds max_tokens";
+    case MLA_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MLA_ERR_BAD_POSITION: return "position outside [0, max_pos)";
+    case MLA_ERR_NO_MEMORY: return "workspace allocation failed";
+    case MLA_ERR_WRONG_MODE: return "run does not match the handle's quant mode";
+  }
+  return "unknown status";
+}
+
+mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out) {
+  if (!cfg || !out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mla_prolog_config& c = *cfg;
+  if (c.hidden <= 0 || c.num_heads <= 0 || c.max_tokens <= 0 || c.max_pos <= 0 ||
+      !(c.eps >= 0.0f) || (c.dtype != MLA_F16 && c.dtype != MLA_BF16) ||
+      (c.quant != MLA_QUANT_NONE && c.quant != MLA_QUANT_W8A8))
+    return MLA_ERR_INVALID_ARG;
+  if (c.kv_lora_rank != kRank || c.rope_dim != kRope || c.nope_dim != kNope || c.v_dim != kV ||
+      c.hidden % 64 != 0)
+    return MLA_ERR_UNSUPPORTED;
+  if (c.quant == MLA_QUANT_W8A8 &&
+      (c.dtype != MLA_BF16 || c.q_lora_rank <= 0 || c.q_lora_rank % 64 != 0))
+    return MLA_ERR_UNSUPPORTED;
+
+  mla_prolog_s* h = new (std::nothrow) mla_prolog_s();
+  if (!h) return MLA_ERR_NO_MEMORY;
+  memset(h, 0, sizeof(*h));
+  h->cfg = c;
+  h->budget_ns = c.spin_budget_ns ? c.spin_budget_ns : 1000000000ull;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "device query");
+  }
+  h->decode_ok = decode_plan(c.hidden, c.num_heads, h->num_sms, &h->dplan);
+  if (c.quant == MLA_QUANT_NONE && !h->decode_ok) {
+    delete h;
+    return MLA_ERR_UNSUPPORTED;
+  }
+  // workspace: [status][counters x2][pad] | partials | nrm | w8a8
+  size_t off = 256;
+  const size_t part_off = off;
+  off += h->decode_ok ? h->dplan.partial_floats * sizeof(float) : 0;
+  off = (off + 255) & ~(size_t)255;
+  const size_t nrm_off = off;
+  off += (size_t)kDecodeMaxTokens * kRank * 2;
+  off = (off + 255) & ~(size_t)255;
+  size_t w8_off = off;
+  if (c.quant == MLA_QUANT_W8A8) off += w8_workspace_bytes(c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens);
+  h->ws_bytes = off;
+  e = cudaMalloc(&h->ws, h->ws_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    cuda_fail(e, "cudaMalloc workspace");
+    return MLA_ERR_NO_MEMORY;
+  }
+  e = cudaMemset(h->ws, 0, 256);
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return cuda_fail(e, "cudaMemset workspace");
+  }
+  unsigned char* base = static_cast<unsigned char*>(h->ws);
+  h->status = reinterpret_cast<unsigned*>(base);
+  h->counters = reinterpret_cast<unsigned*>(base + 64);
+  h->partials = reinterpret_cast<float*>(base + part_off);
+  h->nrm = base + nrm_off;
+  if (c.quant == MLA_QUANT_W8A8) w8_workspace_carve(base + w8_off, c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens, &h->w8);
+  *out = h;
+  return MLA_OK;
+}
+
+mla_status mla_kv_prolog_destroy(mla_prolog_t h) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  cudaError_t e = cudaFree(h->ws);
+  delete h;
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "cudaFree workspace");
+}
+
+mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path) {
+  if (!h || path < MLA_PATH_AUTO || path > MLA_PATH_PREFILL) return MLA_ERR_INVALID_ARG;
+  h->path_override = path;
+  return MLA_OK;
+}
+
+int mla_kv_prolog_last_launches(mla_prolog_t h) { return h ? h->last_launches : -1; }
+int mla_kv_prolog_last_path(mla_prolog_t h) { return h ? h->last_path : -1; }
+
+mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned st = 0;
+  e = cudaMemcpy(&st, h->status, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (st) {
+    // clear the status word and, after a timeout, the barrier counters
+    e = cudaMemset(h->ws, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  }
+  if (st & kStatusBadPosition) return MLA_ERR_BAD_POSITION;
+  if (st & kStatusTimeout) return MLA_ERR_DEVICE_TIMEOUT;
+  return MLA_OK;
+}
+
+mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_states,
+                             const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                             const void* W_kvb, const float* cos_table, const float* sin_table,
+                             void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
+  if (!h || b < 0 || s < 0) return MLA_ERR_INVALID_ARG;
+  if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
+  const long long T = (long long)b * s;
+  h->last_launches = 0;
+  if (T == 0) return MLA_OK;
+  if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
+  const void* ptrs[] = {hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
+                        k_nope, value, k_pe};
+  for (const void* q : ptrs)
+    if (!q) return MLA_ERR_INVALID_ARG;
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MLA_ERR_MISALIGNED;
+
+  const bool bf16 = h->cfg.dtype == MLA_BF16;
+  int path = h->path_override;
+  if (path == MLA_PATH_AUTO) path = prefill_preferred(h->cfg.hidden, h->cfg.num_heads, (int)T, h->num_sms) ? MLA_PATH_PREFILL : MLA_PATH_DECODE;
+  h->last_path = path;
+
+  if (path == MLA_PATH_PREFILL) {
+    PrefillParams pp = {};
+    pp.hidden = hidden_states; pp.positions = positions; pp.W_kva = W_kva; pp.gamma = gamma_kv;
+    pp.W_kvb = W_kvb; pp.cos_t = cos_table; pp.sin_t = sin_table; pp.k_nope = k_nope;
+    pp.value = value; pp.k_pe = k_pe; pp.status = h->status;
+    pp.hidden_dim = h->cfg.hidden; pp.heads = h->cfg.num_heads; pp.s = s; pp.T = (int)T;
+    pp.max_pos = h->cfg.max_pos; pp.eps = h->cfg.eps; pp.budget_ns = h->budget_ns;
+    int launches = 0;
+    cudaError_t e = prefill_launch(bf16, pp, h->num_sms, stream, &launches);
+    h->last_launches = launches;
+    if (e == cudaErrorNotSupported) return MLA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return MLA_OK;
+  }
+
+  DecodeParams p = {};
+  p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
+  p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
+  p.k_pe = k_pe; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
+  p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
+  p.max_pos = h->cfg.max_pos; p.KB = h->dplan.KB; p.KC = h->dplan.KC; p.eps = h->cfg.eps;
+  p.budget_ns = h->budget_ns;
+  for (long long t0 = 0; t0 < T; t0 += kDecodeMaxTokens) {
+    p.t0 = (int)t0;
+    p.TT = (int)((T - t0) < kDecodeMaxTokens ? (T - t0) : kDecodeMaxTokens);
+    cudaError_t e = decode_launch(bf16, h->dplan, p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    h->last_launches += 1;
+  }
+  return MLA_OK;
+}
+
+mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_states,
+                               const int32_t* positions, const int8_t* W_qa, const float* sW_qa,
+                               const void* gamma_q, const int8_t* W_qb, const float* sW_qb,
+                               const int8_t* W_kva, const float* sW_kva, const void* gamma_kv,
+                               const int8_t* W_kvb, const float* sW_kvb,
+                               const float* cos_table, const float* sin_table, void* q_nope,
+                               void* q_pe, void* k_nope, void* value, void* k_pe,
+                               cudaStream_t stream) {
+  if (!h || b < 0 || s < 0) return MLA_ERR_INVALID_ARG;
+  if (h->cfg.quant != MLA_QUANT_W8A8) return MLA_ERR_WRONG_MODE;
+  const long long T = (long long)b * s;
+  h->last_launches = 0;
+  if (T == 0) return MLA_OK;
+  if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
+  const void* ptrs[] = {hidden_states, positions, W_qa, sW_qa, gamma_q, W_qb, sW_qb, W_kva,
+                        sW_kva, gamma_kv, W_kvb, sW_kvb, cos_table, sin_table, q_nope, q_pe,
+                        k_nope, value, k_pe};
+  for (const void* q : ptrs)
+    if (!q) return MLA_ERR_INVALID_ARG;
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MLA_ERR_MISALIGNED;
+  W8Params p = {};
+  p.hidden = hidden_states; p.positions = positions; p.W_qa = W_qa; p.sW_qa = sW_qa;
+  p.gamma_q = gamma_q; p.W_qb = W_qb; p.sW_qb = sW_qb; p.W_kva = W_kva; p.sW_kva = sW_kva;
+  p.gamma_kv = gamma_kv; p.W_kvb = W_kvb; p.sW_kvb = sW_kvb; p.cos_t = cos_table;
+  p.sin_t = sin_table; p.q_nope = q_nope; p.q_pe = q_pe; p.k_nope = k_nope; p.value = value;
+  p.k_pe = k_pe; p.status = h->status; p.hidden_dim = h->cfg.hidden;
+  p.q_rank = h->cfg.q_lora_rank; p.heads = h->cfg.num_heads; p.s = s; p.T = (int)T;
+  p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
+  int launches = 0;
+  cudaError_t e = w8a8_launch(p, h->w8, h->num_sms, stream, &launches);
+  h->last_launches = launches;
+  h->last_path = MLA_PATH_AUTO;
+  if (e != cudaSuccess) return cuda_fail(e, "w8a8 launch");
+  return MLA_OK;
+}
+
+mla_status mla_w8a8_quant_rows(const void* x_bf16, int rows, int cols, int8_t* q, float* scale,
+                               cudaStream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 8 != 0) return rows < 0 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+  if (rows == 0) return MLA_OK;
+  if (!x_bf16 || !q || !scale) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scale)) return MLA_ERR_MISALIGNED;
+  cudaError_t e = w8a8_quant_rows_launch(x_bf16, rows, cols, q, scale, stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "quant launch");
+}
+
+mla_status mla_w8a8_gemm_s32(const int8_t* A, const int8_t* W, int M, int K, int N,
+                             int32_t* acc, cudaStream_t stream) {
+  if (M < 0 || K <= 0 || N <= 0) return MLA_ERR_INVALID_ARG;
+  if (K % 32 != 0 || N % 8 != 0) return MLA_ERR_UNSUPPORTED;
+  if (M == 0) return MLA_OK;
+  if (!A || !W || !acc) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(acc)) return MLA_ERR_MISALIGNED;
+  cudaError_t e = w8a8_gemm_s32_launch(A, W, M, K, N, acc, stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "gemm launch");
+}
+
+mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1, int8_t* c1,
+                                    float* s2, cudaStream_t stream) {
+  if (!h || T < 0 || !q1 || !s1 || !c1 || !s2) return MLA_ERR_INVALID_ARG;
+  if (h->cfg.quant != MLA_QUANT_W8A8) return MLA_ERR_WRONG_MODE;
+  if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
+  cudaError_t e = w8a8_copy_operands(h->w8, T, h->cfg.q_lora_rank, q1, s1, c1, s2, stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "copy operands");
+}
+
+}  // extern "C"

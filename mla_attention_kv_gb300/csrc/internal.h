@@ -1,0 +1,136 @@
+// internal.h -- launch interfaces between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Device status bits (kept in the handle's workspace).
+enum : unsigned { kStatusBadPosition = 1u, kStatusTimeout = 2u };
+
+// Fixed dimensions of the DeepSeek MLA KV prolog this library implements.
+constexpr int kRank = 512;         // kv_lora_rank
+constexpr int kRope = 64;          // qk_rope_head_dim
+constexpr int kNa = kRank + kRope; // kv_a_proj output width (576)
+constexpr int kNope = 128;         // qk_nope_head_dim
+constexpr int kV = 128;            // v_head_dim
+constexpr int kHeadCols = kNope + kV;  // kv_b_proj columns per head (256)
+
+// ---------------------------------------------------------------- decode path
+// Token rows per decode launch (larger T is processed in chunks).
+constexpr int kDecodeMaxTokens = 64;
+
+struct DecodeParams {
+  const void* hidden;       // [T, hidden]
+  const int32_t* positions; // [T]
+  const void* W_kva;        // [hidden, 576]
+  const void* gamma;        // [512]
+  const void* W_kvb;        // [512, H*256]
+  const float* cos_t;       // [max_pos, 64]
+  const float* sin_t;
+  void* k_nope;             // [b, H, s, 128]
+  void* value;              // [b, H, s, 128]
+  void* k_pe;               // [b, 1, s, 64]
+  float* partials;          // workspace [KC][kDecodeMaxTokens][576] fp32
+  void* nrm;                // workspace [kDecodeMaxTokens][512] dtype
+  unsigned* counters;       // workspace: grid barrier {arrivals, generation}
+  unsigned* status;         // workspace: device status word
+  int hidden_dim, heads, s, t0, TT, max_pos;
+  int KB, KC;               // split-K: rows per chunk (multiple of 64), chunk count
+  float eps;
+  unsigned long long budget_ns;
+};
+
+struct DecodePlan {
+  int grid;        // CTAs (cooperative, one per SM)
+  int KB, KC;      // split-K of kv_a
+  size_t smem;     // dynamic shared memory bytes
+  size_t partial_floats;  // workspace floats needed for partials
+};
+
+// Plan for a given model shape on the current device; returns false if the
+// shape cannot be handled (shared memory or register budget).
+bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan);
+cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p,
+                          cudaStream_t stream);
+
+}  // namespace mla
+
+namespace mla {
+
+// ---------------------------------------------------------------- prefill path
+struct PrefillParams {
+  const void* hidden;
+  const int32_t* positions;
+  const void* W_kva;
+  const void* gamma;
+  const void* W_kvb;
+  const float* cos_t;
+  const float* sin_t;
+  void* k_nope;
+  void* value;
+  void* k_pe;
+  unsigned* status;
+  int hidden_dim, heads, s, T, max_pos;
+  float eps;
+  unsigned long long budget_ns;
+};
+
+// True when the tensor-core prefill kernel is the faster path for T rows.
+bool prefill_preferred(int hidden, int heads, int T, int num_sms);
+// Enqueue the prefill kernel(s); *launches receives the kernel count.
+// Returns cudaErrorNotSupported for shapes the kernel does not handle.
+cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaStream_t stream,
+                           int* launches);
+
+// ---------------------------------------------------------------- W8A8 path
+struct W8Workspace {
+  int8_t* xq;     // [max_tokens, hidden]
+  float* sx;      // [max_tokens]
+  int32_t* acc1;  // [max_tokens, q_rank + 576]
+  int8_t* q1;     // [max_tokens, q_rank]
+  float* s1;      // [max_tokens]
+  int8_t* c1;     // [max_tokens, 512]
+  float* s2;      // [max_tokens]
+  int32_t* acc2;  // [max_tokens, max(H*192, H*256)]
+};
+
+struct W8Params {
+  const void* hidden;
+  const int32_t* positions;
+  const int8_t* W_qa;
+  const float* sW_qa;
+  const void* gamma_q;
+  const int8_t* W_qb;
+  const float* sW_qb;
+  const int8_t* W_kva;
+  const float* sW_kva;
+  const void* gamma_kv;
+  const int8_t* W_kvb;
+  const float* sW_kvb;
+  const float* cos_t;
+  const float* sin_t;
+  void* q_nope;
+  void* q_pe;
+  void* k_nope;
+  void* value;
+  void* k_pe;
+  unsigned* status;
+  int hidden_dim, q_rank, heads, s, T, max_pos;
+  float eps;
+};
+
+size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens);
+void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,
+                        W8Workspace* w);
+cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, int num_sms,
+                        cudaStream_t stream, int* launches);
+cudaError_t w8a8_quant_rows_launch(const void* x_bf16, int rows, int cols, int8_t* q,
+                                   float* scale, cudaStream_t stream);
+cudaError_t w8a8_gemm_s32_launch(const int8_t* A, const int8_t* W, int M, int K, int N,
+                                 int32_t* acc, cudaStream_t stream);
+cudaError_t w8a8_copy_operands(const W8Workspace& w, int T, int q_rank, int8_t* q1, float* s1,
+                               int8_t* c1, float* s2, cudaStream_t stream);
+
+}  // namespace mla

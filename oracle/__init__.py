@@ -97,6 +97,8 @@ def lib():
             L.oracle_w8a8_token_operands.restype = ctypes.c_int
             L.oracle_w8a8_token_operands.argtypes = [ctypes.POINTER(_W8Dims), ctypes.c_int64,
                                                      P, P, P, P, P, P, P, P, P, P, P, P, P, P]
+            L.oracle_round_array.restype = None
+            L.oracle_round_array.argtypes = [P, ctypes.c_int64, ctypes.c_int, P]
             L.oracle_openmp_max_threads.restype = ctypes.c_int
             L.oracle_openmp_max_threads.argtypes = []
             _lib = L
@@ -155,10 +157,9 @@ def round_to(x: np.ndarray, dtype: int) -> np.ndarray:
     """Round float64 values to fp16 (0) / bf16 (1), nearest-even, and return
     them as float64 (the value of the rounded 16-bit number)."""
     x = np.ascontiguousarray(x, dtype=np.float64)
-    enc = lib().oracle_double_to_f16 if dtype == 0 else lib().oracle_double_to_bf16
-    flat = x.reshape(-1)
-    bits = np.fromiter((enc(float(v)) for v in flat), dtype=np.uint16, count=flat.size)
-    return promote16(bits, dtype).reshape(x.shape)
+    out = np.empty_like(x)
+    lib().oracle_round_array(_ptr(x), x.size, dtype, _ptr(out))
+    return out
 
 
 # ---------------------------------------------------------------- steps

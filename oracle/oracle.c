@@ -479,3 +479,18 @@ int oracle_openmp_max_threads(void) {
   return 1;
 #endif
 }
+
+/* Round n doubles to fp16 (dtype 0) or bf16 (dtype 1), nearest-even, and
+ * return the rounded values as doubles (used to compare against outputs
+ * stored in those formats).                                                */
+void oracle_round_array(const double* x, int64_t n, int dtype, double* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (isnan(x[i])) {
+      out[i] = x[i];
+    } else if (dtype == 0) {
+      out[i] = oracle_f16_to_double(oracle_double_to_f16(x[i]));
+    } else {
+      out[i] = oracle_bf16_to_double(oracle_double_to_bf16(x[i]));
+    }
+  }
+}

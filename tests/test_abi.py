@@ -1,0 +1,85 @@
+"""C-ABI library: builds, loads, exports every declared symbol, and rejects
+bad arguments on the host (no GPU needed for any of these)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_attention_kv_gb300 import binding as B
+from mla_attention_kv_gb300 import build as BLD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    BLD.build()
+    return B.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla_prolog.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_surface():
+    assert set(declared_functions()) == set(B.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_abi_version_and_strings(L):
+    assert L.mla_abi_version() == 1
+    for code in range(10):
+        assert L.mla_status_string(code).decode() not in ("", "unknown status")
+    assert L.mla_status_string(99).decode() == "unknown status"
+
+
+def _cfg(**over):
+    c = dict(hidden=2048, kv_lora_rank=512, rope_dim=64, num_heads=16, nope_dim=128, v_dim=128,
+             dtype=B.MLA_F16, eps=1e-6, max_tokens=16, max_pos=4096, quant=0, q_lora_rank=0,
+             spin_budget_ns=0)
+    c.update(over)
+    return B.Config(**c)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(hidden=0), 1), (dict(num_heads=0), 1), (dict(max_tokens=0), 1), (dict(max_pos=0), 1),
+    (dict(eps=-1.0), 1), (dict(dtype=5), 1), (dict(quant=3), 1),
+    (dict(kv_lora_rank=256), 2), (dict(rope_dim=32), 2), (dict(nope_dim=64), 2),
+    (dict(v_dim=64), 2), (dict(hidden=2000), 2),
+    (dict(quant=1, dtype=B.MLA_F16, q_lora_rank=1536), 2),
+    (dict(quant=1, dtype=B.MLA_BF16, q_lora_rank=100), 2),
+])
+def test_create_rejects_bad_config(L, over, code):
+    h = ctypes.c_void_p()
+    assert L.mla_kv_prolog_create(ctypes.byref(_cfg(**over)), ctypes.byref(h)) == code
+    assert not h.value
+
+
+def test_null_arguments(L):
+    h = ctypes.c_void_p()
+    assert L.mla_kv_prolog_create(None, ctypes.byref(h)) == 1
+    assert L.mla_kv_prolog_run(None, 1, 1, *([None] * 10), None) == 1
+    assert L.mla_prolog_w8a8_run(None, 1, 1, *([None] * 19), None) == 1
+    assert L.mla_kv_prolog_status(None, None) == 1
+    assert L.mla_kv_prolog_destroy(None) == 1
+    assert L.mla_kv_prolog_set_path(None, 0) == 1
+    assert L.mla_kv_prolog_last_launches(None) == -1
+    assert L.mla_prolog_w8a8_operands(None, 1, None, None, None, None, None) == 1
+
+
+def test_building_block_shape_checks(L):
+    # K must be a multiple of 32 and N of 8 for the int8 GEMM; zero rows is a no-op
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 48, 8, None, None) == 2
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 12, None, None) == 2
+    assert L.mla_w8a8_gemm_s32(None, None, 0, 64, 8, None, None) == 0
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 8, None, None) == 1
+    assert L.mla_w8a8_quant_rows(None, 4, 12, None, None, None) == 2
+    assert L.mla_w8a8_quant_rows(None, 0, 16, None, None, None) == 0
+    assert L.mla_w8a8_quant_rows(None, -1, 16, None, None, None) == 1

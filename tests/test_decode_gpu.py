@@ -1,0 +1,144 @@
+"""GPU parity of the fused decode kernel against the fp64 oracle (through the
+C ABI).  Covers the tiny V2-Lite case (b=1, s=2, positions {7, 8}), the
+single-token shape of the pages' golden case (b=1, s=1), every point of the
+V2-Lite decode sweep (s in {1, 2} x b in {1 .. 128}), the R1-shaped decode
+(b=64, s=1, bf16), ragged token counts around the 16-row m-tiles and the
+64-row launch chunks, small head counts, determinism, the position check
+and the bounded device wait."""
+import numpy as np
+import pytest
+import torch
+
+from mla_attention_kv_gb300 import binding as B
+from mla_attention_kv_gb300 import build as BLD
+from mla_attention_kv_gb300 import inputs as I
+
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    BLD.build()
+    B.load()
+
+
+def run_case(cfg, b, s, seed, positions="decode", path=B.PATH_DECODE, max_tokens=None,
+             rows=None, oracle_mod=None, nan_fill=True):
+    inp = I.kv_inputs(cfg, b, s, seed, positions)
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, max_tokens or max(1, b * s))
+    m.set_path(path)
+    out = m.alloc_outputs(b, s)
+    if nan_fill:
+        for t in out.values():
+            t.fill_(float("nan"))
+    m.run(b, s, d, out)
+    torch.cuda.synchronize()
+    st = m.status()
+    res = dict(inp=inp, out=out, status=st, launches=m.last_launches, path=m.last_path)
+    if oracle_mod is not None:
+        ref = oracle_mod.kv_prolog(inp, rows=rows)
+        res["err"] = {}
+        for name, r in zip(("k_nope", "value", "k_pe"), ref):
+            res["err"][name] = compare(name, out[name], r, oracle_mod)
+    m.close()
+    return res
+
+
+def test_tiny_config_v2lite(oracle_mod):
+    r = run_case(I.V2_LITE, 1, 2, I.seed_for(0), positions=[7, 8], oracle_mod=oracle_mod)
+    assert r["status"] == 0 and r["launches"] == 1
+
+
+def test_single_token_golden_shape(oracle_mod):
+    # shapes of the pages' golden case: hidden [1,1,2048] -> [1,16,1,128] x2, [1,1,1,64]
+    r = run_case(I.V2_LITE, 1, 1, 7, oracle_mod=oracle_mod)
+    assert tuple(r["out"]["k_nope"].shape) == (1, 16, 1, 128)
+    assert tuple(r["out"]["k_pe"].shape) == (1, 1, 1, 64)
+
+
+@pytest.mark.parametrize("s", [1, 2])
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_decode_sweep_v2lite(oracle_mod, b, s):
+    point = [1, 2, 4, 8, 16, 32, 64, 128].index(b) + 8 * (s - 1)
+    r = run_case(I.V2_LITE, b, s, I.seed_for(1, point), oracle_mod=oracle_mod)
+    assert r["status"] == 0
+
+
+def test_r1_decode(oracle_mod):
+    r = run_case(I.R1, 64, 1, I.seed_for(3), oracle_mod=oracle_mod)
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("T", [3, 15, 17, 63, 64, 65, 129, 200])
+def test_ragged_token_counts(oracle_mod, T):
+    r = run_case(I.V2_LITE, T, 1, 500 + T, oracle_mod=oracle_mod)
+    assert r["launches"] == (T + 63) // 64
+
+
+@pytest.mark.parametrize("H,hidden,dtype", [(1, 64, "fp16"), (3, 192, "bf16"), (5, 640, "fp16"),
+                                            (16, 2048, "bf16")])
+def test_small_shapes(oracle_mod, H, hidden, dtype):
+    cfg = I.small_config(I.V2_LITE, hidden=hidden, num_heads=H, dtype=dtype)
+    run_case(cfg, 3, 2, 900 + H, oracle_mod=oracle_mod)
+
+
+def test_deterministic():
+    a = run_case(I.V2_LITE, 8, 2, 42)
+    b = run_case(I.V2_LITE, 8, 2, 42)
+    for k in ("k_nope", "value", "k_pe"):
+        assert torch.equal(a["out"][k].view(torch.int16), b["out"][k].view(torch.int16))
+
+
+def test_bad_position_is_flagged_and_clamped(oracle_mod):
+    cfg = I.V2_LITE
+    pos = [5, 4096, -3, 100]  # rows 1 and 2 are out of range
+    r = run_case(cfg, 4, 1, 77, positions=pos)
+    assert r["status"] == 7
+    # rows with valid positions are still exact; k_nope/value never depend on position
+    ref = oracle_mod.kv_prolog(dict(r["inp"], positions=torch.tensor([5, 0, 0, 100], dtype=torch.int32)),
+                               rows=[0, 3])
+    compare("k_pe", r["out"]["k_pe"][[0, 3]], ref[2][[0, 3]], oracle_mod)
+    ref_all = oracle_mod.kv_prolog(dict(r["inp"], positions=torch.tensor([5, 0, 0, 100], dtype=torch.int32)))
+    compare("k_nope", r["out"]["k_nope"], ref_all[0], oracle_mod)
+
+
+def test_device_wait_budget_expires_cleanly():
+    """A 1 ns wait budget makes the grid barrier give up: the kernel must
+    return (no hang), report MLA_ERR_DEVICE_TIMEOUT, and the next run on a
+    normal handle must be correct again."""
+    cfg = I.V2_LITE
+    inp = I.kv_inputs(cfg, 2, 1, 3)
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, 2, spin_budget_ns=1)
+    m.set_path(B.PATH_DECODE)
+    out = m.alloc_outputs(2, 1)
+    m.run(2, 1, d, out)
+    torch.cuda.synchronize()
+    assert m.status() == 6
+    assert m.status() == 0  # cleared
+    m.close()
+    run_case(cfg, 2, 1, 3)
+
+
+def test_host_errors_on_device_buffers():
+    cfg = I.V2_LITE
+    inp = I.kv_inputs(cfg, 1, 2, 1)
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, 2)
+    out = m.alloc_outputs(1, 2)
+    with pytest.raises(B.MLAError) as e:
+        m.run(2, 2, d, out)  # 4 tokens > max_tokens 2
+    assert e.value.code == 3
+    raw = torch.empty(d["hidden"].numel() + 8, dtype=torch.float16, device="cuda")
+    mis = raw[1:1 + d["hidden"].numel()].view_as(d["hidden"])
+    with pytest.raises(B.MLAError) as e:
+        m.run(1, 2, dict(d, hidden=mis), out)
+    assert e.value.code == 4
+    m.run(0, 2, d, out)  # T = 0 is a no-op
+    assert m.last_launches == 0
+    m.close()
