@@ -185,7 +185,8 @@ int mla_kv_prolog_last_path(mla_prolog_t h);
  *     matrix x [rows, cols] -> q [rows, cols] int8, scale [rows] f32 (the
  *     fp32 operation sequence described for mla_prolog_w8a8_run).
  *   mla_w8a8_gemm_s32: acc [M, N] int32 = A [M, K] int8 x W [K, N] int8,
- *     W in [in, out] layout; K % 32 == 0, N % 8 == 0, 16-byte aligned rows.
+ *     W in [in, out] layout; K % 32 == 0, N % 64 == 0 (else
+ *     MLA_ERR_UNSUPPORTED); exact for any K (int32 accumulators).
  *   mla_prolog_w8a8_operands: copy the int8 operands and fp32 scales that
  *     the last W8A8 run fed to q_b_proj (q1 [T, q_lora_rank], s1 [T]) and
  *     kv_b_proj (c1 [T, 512], s2 [T]) into caller device buffers.          */

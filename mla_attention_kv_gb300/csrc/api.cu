@@ -9,6 +9,7 @@
 
 #include "../../include/mla_prolog.h"
 #include "internal.h"
+#include "tma.h"
 
 using namespace mla;
 
@@ -31,7 +32,28 @@ struct mla_prolog_s {
   bool decode_ok;
   // W8A8 workspace (see w8a8.cu)
   W8Workspace w8;
+  // tensor maps of recently seen W_kvb pointers (decode kernel)
+  static constexpr int kMapCache = 64;
+  const void* map_ptr[kMapCache];
+  CUtensorMap map[kMapCache];
+  int map_next;
 };
+
+// Tensor map of W_kvb [512, H*256] for the decode kernel, cached per pointer.
+static const CUtensorMap* wkvb_map(mla_prolog_s* h, const void* W_kvb) {
+  for (int i = 0; i < mla_prolog_s::kMapCache; ++i)
+    if (h->map_ptr[i] == W_kvb) return &h->map[i];
+  const int slot = h->map_next;
+  const uint64_t NB = (uint64_t)h->cfg.num_heads * kHeadCols;
+  const CUtensorMapDataType dt = h->cfg.dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_tmap_2d(&h->map[slot], dt, W_kvb, NB, kRank, NB * 2, (uint32_t)h->dplan.ngbox * 8,
+                      kWkvbBoxRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return nullptr;
+  h->map_ptr[slot] = W_kvb;
+  h->map_next = (slot + 1) % mla_prolog_s::kMapCache;
+  return &h->map[slot];
+}
 
 static thread_local char g_last_cuda_error[256] = "no error";
 
@@ -200,12 +222,18 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
     return MLA_OK;
   }
 
+  const CUtensorMap* tm = wkvb_map(h, W_kvb);
+  if (!tm) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed for W_kvb");
+    return MLA_ERR_CUDA;
+  }
   DecodeParams p = {};
+  p.tmap_wkvb = *tm;
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
   p.k_pe = k_pe; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
-  p.max_pos = h->cfg.max_pos; p.KB = h->dplan.KB; p.KC = h->dplan.KC; p.eps = h->cfg.eps;
+  p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
   for (long long t0 = 0; t0 < T; t0 += kDecodeMaxTokens) {
     p.t0 = (int)t0;
@@ -267,7 +295,7 @@ mla_status mla_w8a8_quant_rows(const void* x_bf16, int rows, int cols, int8_t* q
 mla_status mla_w8a8_gemm_s32(const int8_t* A, const int8_t* W, int M, int K, int N,
                              int32_t* acc, cudaStream_t stream) {
   if (M < 0 || K <= 0 || N <= 0) return MLA_ERR_INVALID_ARG;
-  if (K % 32 != 0 || N % 8 != 0) return MLA_ERR_UNSUPPORTED;
+  if (K % 32 != 0 || N % 64 != 0) return MLA_ERR_UNSUPPORTED;
   if (M == 0) return MLA_OK;
   if (!A || !W || !acc) return MLA_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(W) || !aligned16(acc)) return MLA_ERR_MISALIGNED;

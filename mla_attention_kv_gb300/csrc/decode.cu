@@ -3,365 +3,590 @@
 // One cooperative launch (one CTA per SM) performs all seven prolog steps
 // of "DeepSeek-V2-Lite-Chat MLA KV Prolog 迁移指南" §背景 for up to
 // kDecodeMaxTokens token rows.  At these sizes the work is bound by the
-// weight stream (W_kva + W_kvb, 6.5 MB for V2-Lite, 41.8 MB for R1), so the
-// kernel is organised around reading every weight byte exactly once, with
-// 16-byte coalesced copies, from as many SMs as possible:
+// weight stream (W_kva + W_kvb: 6.5 MB for V2-Lite, 41.8 MB for R1), so the
+// kernel is built to put every weight byte in flight at kernel start, read
+// it exactly once with 16-byte coalesced copies, and keep the number of
+// dependent global round trips after the last weight byte arrives small:
 //
-//   phase A  kv_a_proj split-K: the [hidden, 576] weight is cut into
-//            (KB rows x 64 columns) tiles, one or more per CTA; each CTA
-//            multiplies its tile by the matching hidden columns on the
-//            tensor cores (mma.sync m16n8k16, tokens as M) and writes fp32
-//            partial sums [KC, T, 576] to the workspace.  At kernel start
-//            every CTA also issues an L2 prefetch of its W_kvb slice, so
-//            the whole weight set is in flight at once.
-//   barrier  grid-wide, bounded wait (the RMSNorm needs the full row).
-//   phase R  one CTA per token row: fixed-order sum of the KC partials
-//            (deterministic), split (step 2), RMSNorm in fp32 (step 3),
-//            the normalised row rounded once to the I/O dtype into the
-//            workspace, RoPE of k_pe (step 6) stored straight to k_pe.
-//   barrier
-//   phase B  kv_b_proj split-N: each CTA owns a contiguous range of 8-column
-//            groups of W_kvb, streams it through shared memory (3-stage
-//            cp.async pipeline) and multiplies by the normalised rows; the
-//            epilogue does the reshape/split (step 5) and the head-major
-//            stores (step 7) directly from the accumulators.
+//   start    each CTA issues (a) TMA box copies of its W_kvb column slice
+//            into shared memory (rows [0, kpre); when the slice is larger
+//            than the shared-memory budget, rows past kpre are prefetched
+//            into L2 now and copied in, in chunks, once phase A is done),
+//            (b) cp.async copies of its kv_a tile and of the hidden columns
+//            that tile needs, (c) gamma and the cos/sin row of the token row
+//            it owns.
+//   phase A  kv_a_proj split-K: tile = (KB rows x 32 columns) of W_kva;
+//            tokens are the M side of mma.sync m16n8k16 (fp32 accumulate);
+//            the CTA writes fp32 partial sums [KC, T, 576] to the workspace.
+//   barrier  grid-wide, bounded wait (RMSNorm needs the whole 576 row).
+//   phase R  fixed-order sum of the KC partials (deterministic), split
+//            (step 2), RMSNorm in fp32 (step 3) and RoPE of k_pe (step 6).
+//            Small T: every CTA reduces every row itself into shared memory
+//            (no second barrier); otherwise one CTA per row writes the
+//            normalised row (rounded once to the I/O dtype) to the
+//            workspace and a second barrier publishes it.
+//   phase B  kv_b_proj split-N over the resident W_kvb slice; the epilogue
+//            does the reshape/split (step 5) and the head-major stores
+//            (step 7) straight from the accumulators.
 #include "common.cuh"
 #include "internal.h"
+#include "tma.h"
 
 namespace mla {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSubK = 64;          // K rows per pipeline stage
-constexpr int kStagesA = 6;
-constexpr int kStagesB = 3;
-constexpr int kPitchA = 144;       // bytes per smem row of a 64-element tile (odd multiple of 16)
-constexpr int kPitchN = 1040;      // bytes per smem row of a 512-element latent row
+constexpr int kSubK = 64;          // K rows per phase-A pipeline stage
+constexpr int kNbA = 32;           // kv_a columns per split-K tile
+constexpr int kNblkA = kNa / kNbA; // 18 column blocks
+constexpr int kPitchWA = 80;       // smem row pitch of a 32-column tile (odd multiple of 16)
+constexpr int kPitchX = 144;       // smem row pitch of a 64-column hidden tile
+constexpr int kPitchN = 1040;      // smem row pitch of a 512-column latent row
 constexpr int kMaxMT = kDecodeMaxTokens / 16;
-constexpr int kMaxPairs = 16;      // phase-B (m-tile, column group) pairs per warp
-
-__host__ __device__ constexpr int odd16_pitch(int bytes) {
-  int p = (bytes + 15) / 16 * 16;
-  if (((p / 16) & 1) == 0) p += 16;
-  return p;
-}
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kRedBytes = 8192;    // cross-warp reduction scratch
+constexpr int kMiscBytes = 2048;   // gamma + cos/sin row
 
 __device__ __forceinline__ int col_group_begin(int cta, int ngroups, int grid) {
   return (int)(((long long)cta * ngroups) / grid);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p) {
+// Arrive on counter c and wait until all G CTAs arrived (bounded).
+__device__ __forceinline__ bool bar_arrive_wait(unsigned* c, unsigned G,
+                                                unsigned long long budget_ns, unsigned* status) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+    if (ld_acquire_gpu(c) < G) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(c) < G) {
+        if (globaltimer_ns() - t0 > budget_ns) {
+          atomicOr(status, kStatusTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// Bounded wait on an mbarrier phase, with one CTA-wide answer: thread 0
+// waits with the time budget, then (on success) every thread observes the
+// completed phase itself so the async-proxy writes are visible to it.
+__device__ __forceinline__ bool mbar_wait_cta(uint32_t bar, uint32_t parity,
+                                              unsigned long long budget_ns, int* flag) {
+  if (threadIdx.x == 0) *flag = mbar_wait_bounded(bar, parity, budget_ns) ? 1 : 0;
+  __syncthreads();
+  const bool ok = *reinterpret_cast<volatile int*>(flag) != 0;
+  if (ok) {
+    while (!mbar_try_wait(bar, parity)) {
+    }
+  }
+  return ok;
+}
+
+// Last CTA out resets the barrier counters for the next launch.
+__device__ __forceinline__ void bar_exit(unsigned* counters, unsigned G) {
+  if (threadIdx.x == 0) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counters + 2) : "memory");
+    if (old == G - 1) {
+      counters[0] = 0;
+      counters[1] = 0;
+      __threadfence();
+      counters[2] = 0;
+    }
+  }
+}
+
+template <typename T, int MAXP>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int TT = p.TT;
   const int MT = (TT + 15) >> 4;
+  const int rows_x = MT * 16;
   const int H = p.heads;
   const int NB = H * kHeadCols;      // kv_b columns
   const int NG = NB / 8;             // 8-column groups
   const int g0 = col_group_begin(cta, NG, G), g1 = col_group_begin(cta + 1, NG, G);
   const int ng = g1 - g0;
   const int col0 = g0 * 8;
+  const int pitchB = p.ngbox * 16;   // odd multiple of 16: conflict-free ldmatrix
   const T* __restrict__ hid = static_cast<const T*>(p.hidden) + (size_t)p.t0 * p.hidden_dim;
   const T* __restrict__ Wa = static_cast<const T*>(p.W_kva);
-  const T* __restrict__ Wb = static_cast<const T*>(p.W_kvb);
+  unsigned char* sWB = smem + p.off_wb;
+  unsigned char* sA = smem + p.off_a;
+  float* sRed = reinterpret_cast<float*>(smem + p.off_red);
+  T* sGam = reinterpret_cast<T*>(smem + p.off_misc);
+  float* sCos = reinterpret_cast<float*>(smem + p.off_misc + 1024);
+  float* sSin = sCos + kRope;
+  const bool owner = cta < TT;           // this CTA ropes / normalises token row `cta`
+  int pos = 0;
+  if (owner && tid == 0) pos = p.positions[p.t0 + cta];
+  const unsigned st0 = *reinterpret_cast<volatile unsigned*>(p.status);
 
-  // ---- warm L2 with this CTA's W_kvb slice (rows of ng*16 bytes)
-  if (ng > 0) {
-    for (int r = tid; r < kRank; r += kThreads)
-      prefetch_l2_bulk(Wb + (size_t)r * NB + col0, (uint32_t)ng * 16u);
+  // ---- start: mbarriers, resident W_kvb rows (TMA), L2 prefetch of the rest
+  const uint32_t bar_res = smem_u32(smem + p.off_misc + 1536);
+  const uint32_t bar_s0 = bar_res + 8;  // streamed chunk buffers 0 / 1
+  int* sFlag = reinterpret_cast<int*>(smem + p.off_misc + 1600);
+  if (tid == 0) {
+    tma_prefetch_desc(&p.tmap_wkvb);
+    mbar_init(bar_res, 1);
+    mbar_init(bar_s0, 1);
+    mbar_init(bar_s0 + 8, 1);
+    fence_mbar_init();
   }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchB : 0));
+    if (ng > 0) {
+      for (int r = 0; r < p.kpre; r += kWkvbBoxRows)
+        tma_load_2d(smem_u32(sWB + r * pitchB), &p.tmap_wkvb, col0, r, bar_res);
+      for (int r = p.kpre; r < kRank; r += kWkvbBoxRows)
+        tma_prefetch_2d(&p.tmap_wkvb, col0, r);
+    }
+  }
+  if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
 
   // ================================================================ phase A
   {
-    const int units = p.KC * (kNa / 64);
-    const int subs_per_unit = p.KB / kSubK;
+    const int units = p.KC * kNblkA;
+    const int subs = p.KB / kSubK;
     const int my_units = (units > cta) ? (units - cta + G - 1) / G : 0;
-    const int nsub = my_units * subs_per_unit;
-    const int stage_bytes = 2 * 64 * kPitchA;
-    const int rows_x = MT * 16;
+    const int nsub = my_units * subs;
+    const int stage_bytes = kSubK * kPitchWA + rows_x * kPitchX;
+    const int nst = p.nstA;
 
     auto load_sub = [&](int i) {
-      const int u = cta + (i / subs_per_unit) * G;
-      const int kc = u / (kNa / 64), nc = u % (kNa / 64);
-      const int k0 = kc * p.KB + (i % subs_per_unit) * kSubK;
-      unsigned char* st = smem + (i % kStagesA) * stage_bytes;
-      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + 64 * kPitchA);
-      // W tile: 64 rows x 64 cols = 64 x 8 chunks of 16 B
-      for (int c = tid; c < 64 * 8; c += kThreads) {
-        const int r = c >> 3, ch = c & 7;
-        cp_async16(w_s + r * kPitchA + ch * 16, Wa + (size_t)(k0 + r) * kNa + nc * 64 + ch * 8);
+      const int u = cta + (i / subs) * G;
+      const int kc = u / kNblkA, nb = u - kc * kNblkA;
+      const int k0 = kc * p.KB + (i % subs) * kSubK;
+      unsigned char* st = sA + (i % nst) * stage_bytes;
+      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + kSubK * kPitchWA);
+      if (tid < kSubK * 4) {
+        const int r = tid >> 2, ch = tid & 3;
+        cp_async16(w_s + r * kPitchWA + ch * 16, Wa + (size_t)(k0 + r) * kNa + nb * kNbA + ch * 8);
       }
-      // hidden columns k0..k0+63 of the token rows (zero rows past TT)
       for (int c = tid; c < rows_x * 8; c += kThreads) {
         const int r = c >> 3, ch = c & 7;
         const int rr = r < TT ? r : 0;
-        cp_async16(x_s + r * kPitchA + ch * 16, hid + (size_t)rr * p.hidden_dim + k0 + ch * 8,
+        cp_async16(x_s + r * kPitchX + ch * 16, hid + (size_t)rr * p.hidden_dim + k0 + ch * 8,
                    r < TT ? 16 : 0);
       }
     };
 
+    const int nb8 = warp & 3, khalf = warp >> 2;
     float acc[kMaxMT][4];
 #pragma unroll
     for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
 
 #pragma unroll 1
-    for (int s = 0; s < kStagesA - 1; ++s) {
+    for (int s = 0; s < nst - 1; ++s) {
       if (s < nsub) load_sub(s);
       cp_async_commit();
     }
+    // cos/sin row of the owned token (position arrived by now or soon)
+    if (owner) {
+      if (tid == 0) reinterpret_cast<volatile int*>(sRed)[0] = pos;
+      __syncthreads();
+      int pp = reinterpret_cast<volatile int*>(sRed)[0];
+      if (pp < 0 || pp >= p.max_pos) {
+        if (tid == 0) atomicOr(p.status, kStatusBadPosition);
+        pp = pp < 0 ? 0 : p.max_pos - 1;
+      }
+      if (tid < 16) cp_async16(smem_u32(sCos) + tid * 16, p.cos_t + (size_t)pp * kRope + tid * 4);
+      else if (tid < 32) cp_async16(smem_u32(sSin) + (tid - 16) * 16, p.sin_t + (size_t)pp * kRope + (tid - 16) * 4);
+    }
 #pragma unroll 1
     for (int i = 0; i < nsub; ++i) {
-      cp_async_wait<kStagesA - 2>();
+      cp_async_wait_dyn(nst - 2);
       __syncthreads();
-      if (i + kStagesA - 1 < nsub) load_sub(i + kStagesA - 1);
+      if (i + nst - 1 < nsub) load_sub(i + nst - 1);
       cp_async_commit();
-      const unsigned char* st = smem + (i % kStagesA) * stage_bytes;
-      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + 64 * kPitchA);
+      const unsigned char* st = sA + (i % nst) * stage_bytes;
+      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + kSubK * kPitchWA);
 #pragma unroll
-      for (int kk = 0; kk < kSubK / 16; ++kk) {
+      for (int j = 0; j < 2; ++j) {
+        const int kk = khalf + 2 * j;
         uint32_t b0, b1;
-        ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * kPitchA + warp * 16, b0, b1);
+        ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * kPitchWA + nb8 * 16, b0, b1);
 #pragma unroll
         for (int m = 0; m < kMaxMT; ++m) {
           if (m < MT) {
             uint32_t a[4];
-            ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchA + (kk * 16 + (lane >> 4) * 8) * 2, a[0],
+            ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchX + (kk * 16 + (lane >> 4) * 8) * 2, a[0],
                     a[1], a[2], a[3]);
             mma16816<E::kBf16>(acc[m], a, b0, b1);
           }
         }
       }
-      if ((i % subs_per_unit) == subs_per_unit - 1) {
-        const int u = cta + (i / subs_per_unit) * G;
-        const int kc = u / (kNa / 64), nc = u % (kNa / 64);
-        float* P = p.partials + (size_t)kc * kDecodeMaxTokens * kNa;
-        const int col = nc * 64 + warp * 8 + 2 * (lane & 3);
+      if ((i % subs) == subs - 1) {
+        // unit done: fold the two k-halves, write the fp32 partial tile
+        const int u = cta + (i / subs) * G;
+        const int kc = u / kNblkA, nb = u - kc * kNblkA;
+        if (khalf == 1) {
 #pragma unroll
-        for (int m = 0; m < kMaxMT; ++m) {
-          const int r0 = m * 16 + (lane >> 2);
-          if (m < MT) {
-            if (r0 < TT) *reinterpret_cast<float2*>(P + (size_t)r0 * kNa + col) = make_float2(acc[m][0], acc[m][1]);
-            if (r0 + 8 < TT) *reinterpret_cast<float2*>(P + (size_t)(r0 + 8) * kNa + col) = make_float2(acc[m][2], acc[m][3]);
-          }
-          acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+          for (int m = 0; m < kMaxMT; ++m)
+            if (m < MT)
+              *reinterpret_cast<float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4) =
+                  make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
         }
-      }
-    }
-    cp_async_wait<0>();
-  }
-
-  if (!grid_barrier(p.counters, G, p.budget_ns, p.status)) return;
-
-  // ================================================================ phase R
-  {
-    __shared__ float red[kWarps];
-    T* nrm = static_cast<T*>(p.nrm);
-    const T* gam = static_cast<const T*>(p.gamma);
-#pragma unroll 1
-    for (int t = cta; t < TT; t += G) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tid < kNa / 4) {
-        const float* P = p.partials + (size_t)t * kNa + tid * 4;
-#pragma unroll 4
-        for (int kc = 0; kc < p.KC; ++kc) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(P + (size_t)kc * kDecodeMaxTokens * kNa));
-          v.x += x.x; v.y += x.y; v.z += x.z; v.w += x.w;
-        }
-      }
-      // step 3: mean of squares over the 512 latent entries (threads 0..127)
-      float ss = (tid < kRank / 4) ? (v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) : 0.f;
+        __syncthreads();
+        if (khalf == 0) {
+          float* P = p.partials + (size_t)kc * kDecodeMaxTokens * kNa;
+          const int col = nb * kNbA + nb8 * 8 + 2 * (lane & 3);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) red[warp] = ss;
-      __syncthreads();
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) tot += red[w];
-      __syncthreads();
-      if (tid < kRank / 4) {
-        const float inv = 1.0f / sqrtf(tot / (float)kRank + p.eps);
-        const int c = tid * 4;
-        const float n0 = v.x * inv * E::to_f(gam[c + 0]);
-        const float n1 = v.y * inv * E::to_f(gam[c + 1]);
-        const float n2 = v.z * inv * E::to_f(gam[c + 2]);
-        const float n3 = v.w * inv * E::to_f(gam[c + 3]);
-        uint2 pk = make_uint2(E::pack(n0, n1), E::pack(n2, n3));
-        *reinterpret_cast<uint2*>(nrm + (size_t)t * kRank + c) = pk;
-      } else if (tid < kNa / 4) {
-        // step 6: RoPE; this thread holds raw k_pe columns 4i..4i+3, i.e.
-        // rotation pairs j = 2i and 2i+1 -> outputs j, j+32 (de-interleaved)
-        const int i = tid - kRank / 4;
-        const int tg = p.t0 + t;
-        int pos = p.positions[tg];
-        if (pos < 0 || pos >= p.max_pos) {
-          atomicOr(p.status, kStatusBadPosition);
-          pos = pos < 0 ? 0 : p.max_pos - 1;
-        }
-        const float* cr = p.cos_t + (size_t)pos * kRope;
-        const float* sr = p.sin_t + (size_t)pos * kRope;
-        const int j0 = 2 * i, j1 = 2 * i + 1;
-        const float o0 = v.x * cr[j0] - v.y * sr[j0];
-        const float o1 = v.z * cr[j1] - v.w * sr[j1];
-        const float o2 = v.y * cr[j0 + 32] + v.x * sr[j0 + 32];
-        const float o3 = v.w * cr[j1 + 32] + v.z * sr[j1 + 32];
-        T* kp = static_cast<T*>(p.k_pe) + (size_t)tg * kRope;
-        *reinterpret_cast<uint32_t*>(kp + j0) = E::pack(o0, o1);
-        *reinterpret_cast<uint32_t*>(kp + j0 + 32) = E::pack(o2, o3);
-      }
-    }
-  }
-
-  if (!grid_barrier(p.counters, G, p.budget_ns, p.status)) return;
-
-  // ================================================================ phase B
-  if (ng > 0) {
-    const int pitchB = odd16_pitch(ng * 16);
-    unsigned char* nrm_s = smem;
-    unsigned char* wst = smem + kDecodeMaxTokens * kPitchN;
-    float* redbuf = reinterpret_cast<float*>(wst + kStagesB * kSubK * odd16_pitch(((NG + G - 1) / G) * 16));
-    const uint32_t nrm_u = smem_u32(nrm_s);
-    const T* nrm = static_cast<const T*>(p.nrm);
-    const int rows_x = MT * 16;
-    // normalised latent rows (zero rows past TT)
-    for (int c = tid; c < rows_x * 64; c += kThreads) {
-      const int r = c >> 6, ch = c & 63;
-      const int rr = r < TT ? r : 0;
-      cp_async16(nrm_u + r * kPitchN + ch * 16, nrm + (size_t)rr * kRank + ch * 8, r < TT ? 16 : 0);
-    }
-    auto load_w = [&](int kb) {
-      const uint32_t dst = smem_u32(wst + (kb % kStagesB) * kSubK * pitchB);
-      const int nch = ng;  // 16-byte chunks per row
-      for (int c = tid; c < kSubK * nch; c += kThreads) {
-        const int r = c / nch, ch = c - r * nch;
-        cp_async16(dst + r * pitchB + ch * 16, Wb + (size_t)(kb * kSubK + r) * NB + col0 + ch * 8);
-      }
-    };
-    // work split: pairs (m-tile, column group); with few pairs the k16 steps
-    // of each stage are also split across warps and reduced at the end
-    const int npairs = MT * ng;
-    int ksplit = 1;
-    while (ksplit < 4 && npairs * ksplit * 2 <= kWarps) ksplit *= 2;
-    const int wpg = kWarps / ksplit;   // warps per k-slice
-    const int kslice = warp / wpg, pbase = warp % wpg;
-    float acc[kMaxPairs][4];
-#pragma unroll
-    for (int q = 0; q < kMaxPairs; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-
-    load_w(0);
-    cp_async_commit();
-    load_w(1);
-    cp_async_commit();
-    constexpr int kSteps = kRank / kSubK;
-#pragma unroll 1
-    for (int kb = 0; kb < kSteps; ++kb) {
-      cp_async_wait<1>();
-      __syncthreads();
-      if (kb + 2 < kSteps) load_w(kb + 2);
-      cp_async_commit();
-      const uint32_t w_s = smem_u32(wst + (kb % kStagesB) * kSubK * pitchB);
-#pragma unroll
-      for (int kk = 0; kk < kSubK / 16; ++kk) {
-        if ((kk % ksplit) != kslice) continue;
-#pragma unroll
-        for (int q = 0; q < kMaxPairs; ++q) {
-          const int pr = pbase + q * wpg;
-          if (pr < npairs) {
-            const int m = pr % MT, gi = pr / MT;
-            uint32_t b0, b1, a[4];
-            ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * pitchB + gi * 16, b0, b1);
-            ldsm_x4(nrm_u + (m * 16 + (lane & 15)) * kPitchN + (kb * kSubK + kk * 16 + (lane >> 4) * 8) * 2,
-                    a[0], a[1], a[2], a[3]);
-            mma16816<E::kBf16>(acc[q], a, b0, b1);
-          }
-        }
-      }
-    }
-    cp_async_wait<0>();
-    if (ksplit > 1) {
-      // each warp holds at most one pair when ksplit > 1
-      if (kslice > 0 && pbase < npairs) {
-        float* dst = redbuf + ((kslice * wpg + pbase) * 32 + lane) * 4;
-        dst[0] = acc[0][0]; dst[1] = acc[0][1]; dst[2] = acc[0][2]; dst[3] = acc[0][3];
-      }
-      __syncthreads();
-      if (kslice == 0 && pbase < npairs) {
-        for (int ks = 1; ks < ksplit; ++ks) {
-          const float* src = redbuf + ((ks * wpg + pbase) * 32 + lane) * 4;
-          acc[0][0] += src[0]; acc[0][1] += src[1]; acc[0][2] += src[2]; acc[0][3] += src[3];
-        }
-      }
-    }
-    if (kslice == 0) {
-      T* kn = static_cast<T*>(p.k_nope);
-      T* vv = static_cast<T*>(p.value);
-#pragma unroll
-      for (int q = 0; q < kMaxPairs; ++q) {
-        const int pr = pbase + q * wpg;
-        if (pr < npairs) {
-          const int m = pr % MT, gi = pr / MT;
-          const int j = col0 + gi * 8 + 2 * (lane & 3);
-          const int hh = j / kHeadCols, e = j % kHeadCols;
-          T* base = (e < kNope) ? kn : vv;
-          const int ee = (e < kNope) ? e : e - kNope;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int r = m * 16 + (lane >> 2) + half * 8;
-            if (r < TT) {
-              const int tg = p.t0 + r;
-              const int bi = tg / p.s, si = tg - bi * p.s;
-              T* dst = base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee;
-              *reinterpret_cast<uint32_t*>(dst) = E::pack(acc[q][2 * half], acc[q][2 * half + 1]);
+          for (int m = 0; m < kMaxMT; ++m) {
+            if (m < MT) {
+              const float4 o = *reinterpret_cast<const float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4);
+              const int r0 = m * 16 + (lane >> 2);
+              if (r0 < TT) *reinterpret_cast<float2*>(P + (size_t)r0 * kNa + col) = make_float2(acc[m][0] + o.x, acc[m][1] + o.y);
+              if (r0 + 8 < TT) *reinterpret_cast<float2*>(P + (size_t)(r0 + 8) * kNa + col) = make_float2(acc[m][2] + o.z, acc[m][3] + o.w);
             }
           }
         }
+#pragma unroll
+        for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+      }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+  }
+
+  // ---- streamed W_kvb rows [kpre, 512): TMA into two chunk buffers in the
+  // freed phase-A region, behind the latent rows (they land during the barrier)
+  const int nrm_bytes = rows_x * kPitchN;
+  unsigned char* sN = sA;
+  unsigned char* sWS = sA + nrm_bytes;
+  const int nstream = kRank - p.kpre;
+  const int nchunks = (ng > 0 && nstream > 0) ? (nstream + p.kchunk - 1) / p.kchunk : 0;
+  auto issue_chunk = [&](int c) {  // thread 0 only
+    const int r0 = p.kpre + c * p.kchunk;
+    const int nr = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
+    const uint32_t bar = bar_s0 + 8 * (c & 1);
+    const uint32_t dst = smem_u32(sWS + (c & 1) * p.kchunk * pitchB);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nr * pitchB));
+    for (int r = 0; r < nr; r += kWkvbBoxRows)
+      tma_load_2d(dst + r * pitchB, &p.tmap_wkvb, col0, r0 + r, bar);
+  };
+  if (tid == 0) {
+    if (nchunks > 0) issue_chunk(0);
+    if (nchunks > 1) issue_chunk(1);
+  }
+  int issued = nchunks < 2 ? nchunks : 2;
+  // on an early exit, wait (bounded) for this CTA's copies still in flight
+  auto drain = [&]() {
+    cp_async_wait<0>();
+    if (tid == 0) {
+      mbar_wait_bounded(bar_res, 0, p.budget_ns);
+      for (int c = 0; c < issued && c < 2; ++c) mbar_wait_bounded(bar_s0 + 8 * c, 0, p.budget_ns);
+    }
+    __syncthreads();
+  };
+
+  if (st0 & kStatusTimeout) {  // poisoned by an earlier timeout: do nothing
+    drain();
+    return;
+  }
+  if (!bar_arrive_wait(p.counters + 0, G, p.budget_ns, p.status)) {
+    drain();
+    return;
+  }
+
+  // ================================================================ phase R
+  const float rms_scale = 1.0f / (float)kRank;
+  if (p.single_barrier) {
+    // every CTA reduces every row into its own shared memory
+    for (int t = 0; t < TT; ++t) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool rope_row = (t == cta);
+      const int ncol = rope_row ? kNa / 4 : kRank / 4;
+      if (tid < ncol) {
+        const float* P = p.partials + (size_t)t * kNa + tid * 4;
+        float4 x[16];
+#pragma unroll
+        for (int kc = 0; kc < 16; ++kc)
+          if (kc < p.KC) x[kc] = __ldcg(reinterpret_cast<const float4*>(P + (size_t)kc * kDecodeMaxTokens * kNa));
+#pragma unroll
+        for (int kc = 0; kc < 16; ++kc)
+          if (kc < p.KC) { v.x += x[kc].x; v.y += x[kc].y; v.z += x[kc].z; v.w += x[kc].w; }
+      }
+      float ss = (tid < kRank / 4) ? (v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) sRed[64 + warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += sRed[64 + w];
+      __syncthreads();
+      if (tid < kRank / 4) {
+        const float inv = 1.0f / sqrtf(tot * rms_scale + p.eps);
+        const int c = tid * 4;
+        uint2 pk = make_uint2(E::pack(v.x * inv * E::to_f(sGam[c]), v.y * inv * E::to_f(sGam[c + 1])),
+                              E::pack(v.z * inv * E::to_f(sGam[c + 2]), v.w * inv * E::to_f(sGam[c + 3])));
+        *reinterpret_cast<uint2*>(sN + t * kPitchN + c * 2) = pk;
+      } else if (rope_row && tid < kNa / 4) {
+        const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
+        T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
+        *reinterpret_cast<uint32_t*>(kp + j0) =
+            E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
+        *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
+            E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+      }
+    }
+    // zero the padding rows of the last m-tile
+    for (int c = tid; c < (rows_x - TT) * 64; c += kThreads) {
+      const int r = TT + (c >> 6), ch = c & 63;
+      *reinterpret_cast<uint4*>(sN + r * kPitchN + ch * 16) = make_uint4(0, 0, 0, 0);
+    }
+  } else {
+    if (owner) {
+      const int t = cta;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tid < kNa / 4) {
+        const float* P = p.partials + (size_t)t * kNa + tid * 4;
+        float4 x[16];
+#pragma unroll
+        for (int kc = 0; kc < 16; ++kc)
+          if (kc < p.KC) x[kc] = __ldcg(reinterpret_cast<const float4*>(P + (size_t)kc * kDecodeMaxTokens * kNa));
+#pragma unroll
+        for (int kc = 0; kc < 16; ++kc)
+          if (kc < p.KC) { v.x += x[kc].x; v.y += x[kc].y; v.z += x[kc].z; v.w += x[kc].w; }
+      }
+      float ss = (tid < kRank / 4) ? (v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) sRed[64 + warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += sRed[64 + w];
+      if (tid < kRank / 4) {
+        const float inv = 1.0f / sqrtf(tot * rms_scale + p.eps);
+        const int c = tid * 4;
+        uint2 pk = make_uint2(E::pack(v.x * inv * E::to_f(sGam[c]), v.y * inv * E::to_f(sGam[c + 1])),
+                              E::pack(v.z * inv * E::to_f(sGam[c + 2]), v.w * inv * E::to_f(sGam[c + 3])));
+        *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * kRank + c) = pk;
+      } else if (tid < kNa / 4) {
+        const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
+        T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
+        *reinterpret_cast<uint32_t*>(kp + j0) =
+            E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
+        *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
+            E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+      }
+    }
+    if (!bar_arrive_wait(p.counters + 1, G, p.budget_ns, p.status)) {
+      drain();
+      return;
+    }
+    // latent rows (zero rows past TT) -> shared memory
+    const T* nrm = static_cast<const T*>(p.nrm);
+    const uint32_t nu = smem_u32(sN);
+    for (int c = tid; c < rows_x * 64; c += kThreads) {
+      const int r = c >> 6, ch = c & 63;
+      const int rr = r < TT ? r : 0;
+      cp_async16(nu + r * kPitchN + ch * 16, nrm + (size_t)rr * kRank + ch * 8, r < TT ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+  bar_exit(p.counters, G);
+
+  // ================================================================ phase B
+  if (ng == 0) return;
+  const int npairs = MT * ng;
+  int ksplit = 1;
+  while (ksplit < 4 && npairs * ksplit * 2 <= kWarps) ksplit *= 2;
+  const int wpg = kWarps / ksplit;   // warps per k-slice
+  const int kslice = warp / wpg, pbase = warp % wpg;
+  float acc[MAXP][4];
+#pragma unroll
+  for (int q = 0; q < MAXP; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+  const uint32_t nrm_u = smem_u32(sN);
+
+  // K rows are consumed in chunks: the resident rows, then streamed chunks
+  cp_async_wait<0>();
+  __syncthreads();
+  if (!mbar_wait_cta(bar_res, 0, p.budget_ns, sFlag)) {
+    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+    drain();
+    return;
+  }
+  int kbase = 0, krows = p.kpre;
+  uint32_t wchunk = smem_u32(sWB);
+#pragma unroll 1
+  for (int c = -1; c < nchunks; ++c) {
+    if (c >= 0) {
+      const int r0 = p.kpre + c * p.kchunk;
+      krows = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
+      wchunk = smem_u32(sWS + (c & 1) * p.kchunk * pitchB);
+      if (!mbar_wait_cta(bar_s0 + 8 * (c & 1), (c >> 1) & 1, p.budget_ns, sFlag)) {
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        drain();
+        return;
+      }
+    }
+    const int steps = krows / 16;
+#pragma unroll 1
+    for (int st = kslice; st < steps; st += ksplit) {
+      const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchB;
+      const uint32_t arow = nrm_u + (lane & 15) * kPitchN + ((kbase + st * 16) + (lane >> 4) * 8) * 2;
+#pragma unroll
+      for (int q = 0; q < MAXP; ++q) {
+        const int pr = pbase + q * wpg;
+        if (pr < npairs) {
+          const int m = pr % MT, gi = pr / MT;
+          uint32_t b0, b1, a[4];
+          ldsm_x2_trans(wrow + gi * 16, b0, b1);
+          ldsm_x4(arow + m * 16 * kPitchN, a[0], a[1], a[2], a[3]);
+          mma16816<E::kBf16>(acc[q], a, b0, b1);
+        }
+      }
+    }
+    kbase += krows;
+    if (c >= 0 && c + 2 < nchunks) {
+      __syncthreads();  // every warp is done with buffer c & 1
+      if (tid == 0) issue_chunk(c + 2);
+      issued = c + 3;
+    }
+  }
+
+  if (ksplit > 1) {
+    // each warp holds at most one pair when ksplit > 1
+    __syncthreads();
+    if (kslice > 0 && pbase < npairs)
+      *reinterpret_cast<float4*>(sRed + ((kslice * wpg + pbase) * 32 + lane) * 4) =
+          make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+    __syncthreads();
+    if (kslice == 0 && pbase < npairs) {
+      for (int ks = 1; ks < ksplit; ++ks) {
+        const float4 o = *reinterpret_cast<const float4*>(sRed + ((ks * wpg + pbase) * 32 + lane) * 4);
+        acc[0][0] += o.x; acc[0][1] += o.y; acc[0][2] += o.z; acc[0][3] += o.w;
       }
     }
   }
+  if (kslice != 0) return;
+  T* kn = static_cast<T*>(p.k_nope);
+  T* vv = static_cast<T*>(p.value);
+#pragma unroll
+  for (int q = 0; q < MAXP; ++q) {
+    const int pr = pbase + q * wpg;
+    if (pr < npairs) {
+      const int m = pr % MT, gi = pr / MT;
+      const int j = col0 + gi * 8 + 2 * (lane & 3);
+      const int hh = j / kHeadCols, e = j % kHeadCols;
+      T* base = (e < kNope) ? kn : vv;
+      const int ee = (e < kNope) ? e : e - kNope;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int r = m * 16 + (lane >> 2) + half * 8;
+        if (r < TT) {
+          const int tg = p.t0 + r;
+          const int bi = tg / p.s, si = tg - bi * p.s;
+          T* dst = base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee;
+          *reinterpret_cast<uint32_t*>(dst) = E::pack(acc[q][2 * half], acc[q][2 * half + 1]);
+        }
+      }
+    }
+  }
+}
+
+template <typename T>
+const void* kernel_for(int maxp) {
+  if (maxp <= 2) return (const void*)decode_kernel<T, 2>;
+  if (maxp <= 4) return (const void*)decode_kernel<T, 4>;
+  return (const void*)decode_kernel<T, 16>;
 }
 
 }  // namespace
 
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
-  if (hidden % 64 != 0 || heads < 1 || num_sms < 1) return false;
+  if (hidden % 64 != 0 || heads < 1 || num_sms < kDecodeMaxTokens) return false;
   const int G = num_sms;
-  // split-K chunk: the smallest multiple of 64 dividing hidden that gives at
-  // most one (chunk x 64-column) unit per CTA; fewer chunks means fewer
-  // partial rows to reduce after the barrier
-  int KB = hidden;
+  // split-K of kv_a: the smallest KB (multiple of 64 dividing hidden) with
+  // at most one (KB x 32-column) tile per CTA
+  int KB = 0;
   for (int kb = 64; kb <= hidden; kb += 64) {
-    if (hidden % kb == 0 && (hidden / kb) * (kNa / 64) <= G) {
+    if (hidden % kb == 0 && (hidden / kb) * kNblkA <= G) {
       KB = kb;
       break;
     }
   }
+  if (KB == 0 || hidden / KB > 16) return false;
   const int KC = hidden / KB;
   const int NG = heads * kHeadCols / 8;
   const int ngmax = (NG + G - 1) / G;
-  // phase-B pairs per warp must fit the register tile
-  if ((kMaxMT * ngmax + kWarps - 1) / kWarps > kMaxPairs) return false;
-  const size_t smemA = (size_t)kStagesA * 2 * 64 * kPitchA;
-  const size_t smemB = (size_t)kDecodeMaxTokens * kPitchN +
-                       (size_t)kStagesB * kSubK * odd16_pitch(ngmax * 16) +
-                       (size_t)kWarps * 32 * 4 * sizeof(float);
-  const size_t smem = smemA > smemB ? smemA : smemB;
-  if (smem > 227 * 1024) return false;
+  const int ngbox = ngmax | 1;            // odd 16-byte chunks per row: conflict-free ldmatrix
+  if (ngbox * 8 > 256) return false;      // TMA box inner extent
+  const int maxp = (kMaxMT * ngmax + kWarps - 1) / kWarps;
+  if (maxp > 16) return false;
+  const int pitchB = ngbox * 16;
+  const int subs = KB / kSubK;
+  const int stageA = kSubK * kPitchWA + kDecodeMaxTokens * kPitchX;
+  const int nstA = subs < 4 ? (subs < 2 ? 2 : subs) : 4;
+  const int nrm_bytes = kDecodeMaxTokens * kPitchN;
+  const int fixed = kRedBytes + kMiscBytes + 256;
+  // Region A holds the phase-A ring, later the latent rows plus (when the
+  // W_kvb slice does not fit) two stream buffers; the rest of the budget
+  // keeps W_kvb rows resident from kernel start.
+  int regionA = nstA * stageA;
+  if (regionA < nrm_bytes) regionA = nrm_bytes;
+  int kpre = (kSmemBudget - fixed - regionA) / pitchB;
+  int kchunk = kWkvbBoxRows;
+  if (kpre >= kRank) {
+    kpre = kRank;
+  } else {
+    if (regionA < nrm_bytes + 2 * kWkvbBoxRows * pitchB) regionA = nrm_bytes + 2 * kWkvbBoxRows * pitchB;
+    kpre = (kSmemBudget - fixed - regionA) / pitchB / kWkvbBoxRows * kWkvbBoxRows;
+    kchunk = (regionA - nrm_bytes) / (2 * pitchB) / kWkvbBoxRows * kWkvbBoxRows;
+    if (kpre < 0 || kchunk < kWkvbBoxRows) return false;
+  }
   plan->grid = G;
   plan->KB = KB;
   plan->KC = KC;
-  plan->smem = smem;
+  plan->kpre = kpre;
+  plan->kchunk = kchunk;
+  plan->nstA = nstA;
+  plan->ngbox = ngbox;
+  plan->maxp = maxp;
+  plan->off_wb = 0;
+  plan->off_a = (kpre * pitchB + 127) / 128 * 128;
+  plan->off_red = plan->off_a + (regionA + 127) / 128 * 128;
+  plan->off_misc = plan->off_red + kRedBytes;
+  plan->smem = (size_t)plan->off_misc + kMiscBytes;
+  if (plan->smem > (size_t)kSmemBudget) return false;
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
   return true;
 }
 
-cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p,
+cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p0,
                           cudaStream_t stream) {
-  const void* fn = bf16 ? (const void*)decode_kernel<__nv_bfloat16> : (const void*)decode_kernel<__half>;
+  const void* fn = bf16 ? kernel_for<__nv_bfloat16>(plan.maxp) : kernel_for<__half>(plan.maxp);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
+  DecodeParams p = p0;
+  p.KB = plan.KB;
+  p.KC = plan.KC;
+  p.kpre = plan.kpre;
+  p.kchunk = plan.kchunk;
+  p.nstA = plan.nstA;
+  p.ngbox = plan.ngbox;
+  p.off_wb = plan.off_wb;
+  p.off_a = plan.off_a;
+  p.off_red = plan.off_red;
+  p.off_misc = plan.off_misc;
+  // one barrier when every CTA can afford to reduce all rows itself
+  p.single_barrier = (p.TT * plan.KC <= kSingleBarrierRowsTimesChunks) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(kThreads);
@@ -372,8 +597,7 @@ cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams&
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  DecodeParams pp = p;
-  void* args[] = {&pp};
+  void* args[] = {&p};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

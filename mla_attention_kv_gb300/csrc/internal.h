@@ -1,6 +1,7 @@
 // internal.h -- launch interfaces between the C-ABI layer (api.cu) and the
 // kernel translation units.  Not installed; not part of the ABI.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,7 @@ constexpr int kHeadCols = kNope + kV;  // kv_b_proj columns per head (256)
 constexpr int kDecodeMaxTokens = 64;
 
 struct DecodeParams {
+  CUtensorMap tmap_wkvb;    // W_kvb [512, H*256], box = (ngbox*8 columns, 32 rows)
   const void* hidden;       // [T, hidden]
   const int32_t* positions; // [T]
   const void* W_kva;        // [hidden, 576]
@@ -37,14 +39,25 @@ struct DecodeParams {
   unsigned* counters;       // workspace: grid barrier {arrivals, generation}
   unsigned* status;         // workspace: device status word
   int hidden_dim, heads, s, t0, TT, max_pos;
-  int KB, KC;               // split-K: rows per chunk (multiple of 64), chunk count
   float eps;
   unsigned long long budget_ns;
+  // filled from the plan by decode_launch
+  int KB, KC;               // kv_a split-K: rows per chunk (multiple of 64), chunk count
+  int kpre, kchunk, nstA;   // W_kvb rows resident / per streamed chunk; phase-A stages
+  int ngbox;                // 8-column groups per W_kvb box (odd; >= groups per CTA)
+  int off_wb, off_a, off_red, off_misc;  // smem layout (bytes)
+  int single_barrier;       // 1: every CTA reduces every row (one grid barrier)
 };
+
+// Rows x split-K chunks up to which every CTA reduces all partial rows itself
+// (one grid barrier) instead of one CTA per row plus a second barrier.
+constexpr int kSingleBarrierRowsTimesChunks = 32;
 
 struct DecodePlan {
   int grid;        // CTAs (cooperative, one per SM)
   int KB, KC;      // split-K of kv_a
+  int kpre, kchunk, nstA, ngbox, maxp;
+  int off_wb, off_a, off_red, off_misc;
   size_t smem;     // dynamic shared memory bytes
   size_t partial_floats;  // workspace floats needed for partials
 };
@@ -52,6 +65,8 @@ struct DecodePlan {
 // Plan for a given model shape on the current device; returns false if the
 // shape cannot be handled (shared memory or register budget).
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan);
+// Rows of W_kvb per TMA box of the decode kernel.
+constexpr int kWkvbBoxRows = 32;
 cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p,
                           cudaStream_t stream);
 
@@ -77,6 +92,8 @@ struct PrefillParams {
   unsigned long long budget_ns;
 };
 
+// Token count from which AUTO selects the tensor-core prefill kernel.
+constexpr int kPrefillMinTokens = 1024;
 // True when the tensor-core prefill kernel is the faster path for T rows.
 bool prefill_preferred(int hidden, int heads, int T, int num_sms);
 // Enqueue the prefill kernel(s); *launches receives the kernel count.

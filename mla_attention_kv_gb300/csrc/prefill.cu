@@ -1,14 +1,436 @@
-// prefill.cu -- tensor-core (tcgen05) MLA KV prolog for large token counts.
+// prefill.cu -- tensor-core (tcgen05 / TMEM / TMA) MLA KV prolog for large
+// token counts.
+//
+// One CTA per 128-row token tile (persistent over tiles when there are
+// more tiles than SMs).  The two contractions of "DeepSeek-V2-Lite-Chat MLA
+// KV Prolog 迁移指南" §背景 (steps 1 and 4) run as tcgen05.mma with fp32
+// accumulators in tensor memory; RMSNorm (step 3) sits between them in the
+// epilogue warps, and split / RoPE / reshape / head-major assemble (steps
+// 2, 5, 6, 7) are the epilogues, so nothing but the inputs and the three
+// outputs touches global memory.
+//
+// Warp roles (192 threads):
+//   warp 0   TMA producer: hidden tile [128 x 64] and W_kva / W_kvb boxes
+//            [64 x 64], 128-byte swizzled, into a 2-stage (kv_a) and a
+//            3-stage (kv_b) shared-memory ring.
+//   warp 1   allocates 512 TMEM columns; one thread issues every MMA.
+//   warps 2-5 epilogue; warp w owns TMEM lanes 32*(w%4) .. +31, i.e. token
+//            rows of the tile, one row per thread.
+// Per tile:
+//   (a) k_pe pass: C[:, 512:576] = X * W_kva[:, 512:576] (N = 64), drained
+//       by the epilogue: RoPE (de-interleave + rotate_half) -> k_pe.
+//   (b) compressed_kv pass: C[:, 0:512] as two N = 256 MMAs per K step,
+//       filling all 512 TMEM columns; the epilogue reads each row twice
+//       (sum of squares, then normalise * gamma) and writes the normalised
+//       tile, rounded once to the I/O dtype, into shared memory in the
+//       K-major 128-byte-swizzled layout of the next MMA's A operand.
+//   (c) kv_b: one N = 256 MMA tile per head (128 k_nope + 128 value
+//       columns), K = 512 from the shared-memory tile, accumulators
+//       double-buffered in TMEM so head j+1 runs while the epilogue stores
+//       head j as k_nope[b, j, s, :] / value[b, j, s, :].
+// The fp32 accumulator width is 512 TMEM columns, which is why the 576
+// kv_a columns take two passes (the second reads the hidden tile from L2).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
+#include "tma.h"
 
 namespace mla {
+namespace {
 
-bool prefill_preferred(int, int, int, int) { return false; }
+constexpr int kPfThreads = 192;
+constexpr int kBM = 128;                    // token rows per tile
+constexpr int kBK = 64;                     // K elements per TMA box / stage
+constexpr uint32_t kA2Bytes = 8 * 16384;    // normalised tile: 8 K-chunks x [128 x 64]
+constexpr uint32_t kS1Bytes = 81920;        // kv_a stage: X 16 KB + W 64 KB
+constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 tile
+constexpr uint32_t kS2Bytes = 32768;        // kv_b stage: [64 K x 256 N]
+constexpr int kS2Stages = 3;
+constexpr uint32_t kBarBase = kS2Base + kS2Stages * kS2Bytes;  // 229376
+constexpr uint32_t kSmemBytes = kBarBase + 256 + 1024;         // + alignment slack
 
-cudaError_t prefill_launch(bool, const PrefillParams&, int, cudaStream_t, int* launches) {
+struct PfShared {
+  uint64_t full1[2], empty1[2];
+  uint64_t full2[kS2Stages], empty2[kS2Stages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t a2_ready, a2_free, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PfShared) <= 256, "barrier block");
+
+struct PfArgs {
+  CUtensorMap tm_x;    // hidden [T, hidden], box {64, 128}, SW128
+  CUtensorMap tm_wa;   // W_kva [hidden, 576], box {64, 64}, SW128
+  CUtensorMap tm_wb;   // W_kvb [512, H*256], box {64, 64}, SW128
+  PrefillParams p;
+};
+
+// Bounded mbarrier wait shared by all roles; gives up on the time budget
+// or when another role has already given up.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                        unsigned long long budget, unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (((++n) & 63) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > budget) {
+        *abort = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PfArgs args) {
+  using E = Elem<T>;
+  const PrefillParams& p = args.p;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned base (128-byte swizzle atoms)
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  PfShared* sh = reinterpret_cast<PfShared*>(smem + kBarBase);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = p.hidden_dim, H = p.heads, ntok = p.T;
+  const int nk = h / kBK;
+  const int ntiles = (ntok + kBM - 1) / kBM;
+  volatile int* abort = &sh->abort;
+  const unsigned long long budget = p.budget_ns;
+
+  auto bar = [&](uint64_t* b) { return smem_u32(b); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(&sh->full1[i]), 1);
+      mbar_init(bar(&sh->empty1[i]), 1);
+      mbar_init(bar(&sh->tfull[i]), 1);
+      mbar_init(bar(&sh->tempty[i]), 128);
+    }
+    for (int i = 0; i < kS2Stages; ++i) {
+      mbar_init(bar(&sh->full2[i]), 1);
+      mbar_init(bar(&sh->empty2[i]), 1);
+    }
+    mbar_init(bar(&sh->a2_ready), 128);
+    mbar_init(bar(&sh->a2_free), 1);
+    mbar_init(bar(&sh->mma_done), 1);
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(smem_u32(&sh->tmem_base), 512);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&args.tm_x);
+    tma_prefetch_desc(&args.tm_wa);
+    tma_prefetch_desc(&args.tm_wb);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ============================================================ TMA producer
+    if (lane == 0) {
+      uint32_t u1 = 0, u2 = 0;  // uses of pipeline 1 / 2
+      int tiles_done = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
+        const int m0 = tile * kBM;
+        if (tiles_done > 0 && !pf_wait(bar(&sh->a2_free), (tiles_done - 1) & 1, abort, budget, p.status)) { ok = false; break; }
+        // (a) k_pe pass then (b) compressed_kv pass over the hidden dimension
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int kc = 0; kc < nk; ++kc, ++u1) {
+            const int s = u1 & 1;
+            if (!pf_wait(bar(&sh->empty1[s]), ((u1 >> 1) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
+            const uint32_t st = sbase + s * kS1Bytes;
+            const uint32_t fb = bar(&sh->full1[s]);
+            mbar_arrive_expect_tx(fb, pass == 0 ? 16384 + 8192 : 16384 + 65536);
+            tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
+            if (pass == 0) {
+              tma_load_2d(st + 16384, &args.tm_wa, kRank, kc * kBK, fb);
+            } else {
+              for (int j = 0; j < 8; ++j) tma_load_2d(st + 16384 + j * 8192, &args.tm_wa, j * 64, kc * kBK, fb);
+            }
+          }
+        }
+        if (!ok) break;
+        // kv_a stages overlap the kv_b ring: wait until both were released
+        for (int s = 0; s < 2 && ok; ++s) {
+          const uint32_t last = (u1 - 1 - s);  // uses u1-1 and u1-2 cover both stages
+          if (!pf_wait(bar(&sh->empty1[last & 1]), (last >> 1) & 1, abort, budget, p.status)) ok = false;
+        }
+        // (c) kv_b: per head, 8 K-chunks of [64 x 256]
+        for (int j = 0; j < H && ok; ++j) {
+          for (int kc = 0; kc < kRank / kBK; ++kc, ++u2) {
+            const int s = u2 % kS2Stages;
+            if (!pf_wait(bar(&sh->empty2[s]), ((u2 / kS2Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
+            const uint32_t st = sbase + kS2Base + s * kS2Bytes;
+            const uint32_t fb = bar(&sh->full2[s]);
+            mbar_arrive_expect_tx(fb, kS2Bytes);
+            for (int q = 0; q < 4; ++q) tma_load_2d(st + q * 8192, &args.tm_wb, j * kHeadCols + q * 64, kc * kBK, fb);
+          }
+        }
+      }
+      // drain: every issued load has landed before the CTA may exit
+      for (uint32_t u = (u1 > 2 ? u1 - 2 : 0); u < u1; ++u)
+        pf_wait(bar(&sh->full1[u & 1]), (u >> 1) & 1, abort, budget, p.status);
+      for (uint32_t u = (u2 > kS2Stages ? u2 - kS2Stages : 0); u < u2; ++u)
+        pf_wait(bar(&sh->full2[u % kS2Stages]), (u / kS2Stages) & 1, abort, budget, p.status);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const bool bf = E::kBf16;
+      const uint32_t id64 = tc::idesc_f16(bf, 128, 64, false, true);
+      const uint32_t id256 = tc::idesc_f16(bf, 128, 256, false, true);
+      uint32_t u1 = 0, u2 = 0;
+      uint32_t wcount[2] = {0, 0}, dcount[2] = {0, 0};
+      int tiles_done = 0;
+      bool ok = true;
+      auto drain_buf = [&](int b) -> bool {
+        while (dcount[b] < wcount[b]) {
+          if (!pf_wait(bar(&sh->tempty[b]), dcount[b] & 1, abort, budget, p.status)) return false;
+          ++dcount[b];
+        }
+        return true;
+      };
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
+        // (a) k_pe into TMEM columns [0, 64)
+        if (!drain_buf(0)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int kc = 0; kc < nk; ++kc, ++u1) {
+          const int s = u1 & 1;
+          if (!pf_wait(bar(&sh->full1[s]), (u1 >> 1) & 1, abort, budget, p.status)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t st = sbase + s * kS1Bytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = tc::sdesc_sw128(st + k * 32, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(st + 16384 + k * 2048, 8192, 1024);
+            tc::mma_f16(tmem, ad, bd, id64, kc > 0 || k > 0);
+          }
+          tc::commit(bar(&sh->empty1[s]));
+        }
+        if (!ok) break;
+        tc::commit(bar(&sh->tfull[0]));
+        ++wcount[0];
+        // (b) compressed_kv into TMEM columns [0, 512)
+        if (!drain_buf(0) || !drain_buf(1)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int kc = 0; kc < nk; ++kc, ++u1) {
+          const int s = u1 & 1;
+          if (!pf_wait(bar(&sh->full1[s]), (u1 >> 1) & 1, abort, budget, p.status)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t st = sbase + s * kS1Bytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = tc::sdesc_sw128(st + k * 32, 16, 1024);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint64_t bd = tc::sdesc_sw128(st + 16384 + half * 32768 + k * 2048, 8192, 1024);
+              tc::mma_f16(tmem + half * 256, ad, bd, id256, kc > 0 || k > 0);
+            }
+          }
+          tc::commit(bar(&sh->empty1[s]));
+        }
+        if (!ok) break;
+        tc::commit(bar(&sh->tfull[0]));  // the epilogue drains both halves, then signals a2_ready
+        // (c) kv_b, one head per N = 256 tile
+        if (!pf_wait(bar(&sh->a2_ready), tiles_done & 1, abort, budget, p.status)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int j = 0; j < H && ok; ++j) {
+          const int b = j & 1;
+          if (j >= 2 && !drain_buf(b)) { ok = false; break; }
+          tc::fence_after_sync();
+          for (int kc = 0; kc < kRank / kBK; ++kc, ++u2) {
+            const int s = u2 % kS2Stages;
+            if (!pf_wait(bar(&sh->full2[s]), (u2 / kS2Stages) & 1, abort, budget, p.status)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint32_t st = sbase + kS2Base + s * kS2Bytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = tc::sdesc_sw128(sbase + kc * 16384 + k * 32, 16, 1024);
+              const uint64_t bd = tc::sdesc_sw128(st + k * 2048, 8192, 1024);
+              tc::mma_f16(tmem + b * 256, ad, bd, id256, kc > 0 || k > 0);
+            }
+            tc::commit(bar(&sh->empty2[s]));
+          }
+          if (!ok) break;
+          tc::commit(bar(&sh->tfull[b]));
+          ++wcount[b];
+        }
+        if (!ok) break;
+        tc::commit(bar(&sh->a2_free));
+      }
+      // every MMA issued so far has completed before TMEM is released
+      tc::commit(bar(&sh->mma_done));
+      pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
+    }
+  } else {
+    // ============================================================ epilogue
+    const int q = warp & 3;                // TMEM lane quadrant
+    const int r = q * 32 + lane;           // row within the tile
+    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+    const T* gam = static_cast<const T*>(p.gamma);
+    uint32_t uf[2] = {0, 0};
+    int tiles_done = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
+      const int t = tile * kBM + r;
+      const bool live = t < ntok;
+      const int bi = live ? t / p.s : 0, si = live ? t - bi * p.s : 0;
+      // (a) k_pe: RoPE on the 64 raw columns
+      if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
+      ++uf[0];
+      tc::fence_after_sync();
+      {
+        uint32_t x[64];
+        tc::ld32(lane_addr + 0, x);
+        tc::ld32(lane_addr + 32, x + 32);
+        tc::wait_ld();
+        if (live) {
+          int pos = p.positions[t];
+          if (pos < 0 || pos >= p.max_pos) {
+            atomicOr(p.status, kStatusBadPosition);
+            pos = pos < 0 ? 0 : p.max_pos - 1;
+          }
+          const float* cr = p.cos_t + (size_t)pos * kRope;
+          const float* sr = p.sin_t + (size_t)pos * kRope;
+          uint32_t o[32];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float a0 = __uint_as_float(x[2 * j]), b0 = __uint_as_float(x[2 * j + 1]);
+            const float a1 = __uint_as_float(x[2 * j + 2]), b1 = __uint_as_float(x[2 * j + 3]);
+            o[j / 2] = E::pack(a0 * cr[j] - b0 * sr[j], a1 * cr[j + 1] - b1 * sr[j + 1]);
+            o[16 + j / 2] = E::pack(b0 * cr[j + 32] + a0 * sr[j + 32], b1 * cr[j + 33] + a1 * sr[j + 33]);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_pe) + (size_t)t * kRope);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(bar(&sh->tempty[0]));
+      // (b) RMSNorm of compressed_kv -> normalised A tile in shared memory
+      if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
+      ++uf[0];
+      tc::fence_after_sync();
+      {
+        float ss = 0.f;
+        for (int c = 0; c < kRank / 32; ++c) {
+          uint32_t x[32];
+          tc::ld32(lane_addr + c * 32, x);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float v = __uint_as_float(x[j]);
+            ss += v * v;
+          }
+        }
+        const float inv = 1.0f / sqrtf(ss / (float)kRank + p.eps);
+        unsigned char* a2row = smem + r * 128;
+        for (int c = 0; c < kRank / 32; ++c) {
+          uint32_t x[32];
+          tc::ld32(lane_addr + c * 32, x);
+          tc::wait_ld();
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int col = c * 32 + j;
+            o[j / 2] = E::pack(__uint_as_float(x[j]) * inv * E::to_f(gam[col]),
+                               __uint_as_float(x[j + 1]) * inv * E::to_f(gam[col + 1]));
+          }
+          // K-chunk c/2 (64 columns), 16-byte chunks (c%2)*4 .. +3 of this row
+          unsigned char* chunk = a2row + (c >> 1) * 16384;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int lc = (c & 1) * 4 + v;
+            *reinterpret_cast<uint4*>(chunk + ((lc ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(bar(&sh->a2_ready));
+      // (c) per head: split into k_nope / value, head-major stores
+      T* kn = static_cast<T*>(p.k_nope);
+      T* vv = static_cast<T*>(p.value);
+      for (int j = 0; j < H; ++j) {
+        const int b = j & 1;
+        if (!pf_wait(bar(&sh->tfull[b]), uf[b] & 1, abort, budget, p.status)) { ok = false; break; }
+        ++uf[b];
+        tc::fence_after_sync();
+        const size_t orow = (((size_t)bi * H + j) * p.s + si) * kNope;
+#pragma unroll 1
+        for (int c = 0; c < kHeadCols / 32; ++c) {
+          uint32_t x[32];
+          tc::ld32(lane_addr + b * 256 + c * 32, x);
+          tc::wait_ld();
+          if (live) {
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = E::pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+            T* dst = (c < 4 ? kn : vv) + orow + (c & 3) * 32;
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
+        }
+        tc::fence_before_sync();
+        mbar_arrive(bar(&sh->tempty[b]));
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool prefill_preferred(int hidden, int heads, int T, int num_sms) {
+  (void)hidden;
+  (void)heads;
+  (void)num_sms;
+  return T >= kPrefillMinTokens;
+}
+
+cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaStream_t stream,
+                           int* launches) {
   *launches = 0;
-  return cudaErrorNotSupported;
+  if (p.hidden_dim % kBK != 0 || p.T <= 0) return cudaErrorNotSupported;
+  PfArgs a;
+  a.p = p;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t h = (uint64_t)p.hidden_dim, NB = (uint64_t)p.heads * kHeadCols;
+  if (!encode_tmap_2d(&a.tm_x, dt, p.hidden, h, (uint64_t)p.T, h * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&a.tm_wa, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&a.tm_wb, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const void* fn = bf16 ? (const void*)prefill_kernel<__nv_bfloat16> : (const void*)prefill_kernel<__half>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int ntiles = (p.T + kBM - 1) / kBM;
+  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  void* kargs[] = {&a};
+  e = cudaLaunchKernelExC(&cfg, fn, kargs);
+  if (e == cudaSuccess) *launches = 1;
+  return e;
 }
 
 }  // namespace mla

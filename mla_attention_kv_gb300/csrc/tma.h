@@ -1,0 +1,40 @@
+// tma.h -- Tensor Memory Accelerator helpers: host-side encoding of 2-D
+// tiled tensor maps (through the runtime's driver entry point, so the
+// library does not link libcuda directly) and the device-side tiled copy.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Encode a 2-D row-major tensor map: `inner` elements per row (contiguous),
+// `outer` rows, `row_stride` bytes between rows (multiple of 16), box of
+// box_inner x box_outer elements.  Returns false if the driver rejects it.
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_stride, uint32_t box_inner,
+                    uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+#ifdef __CUDACC__
+// Tiled 2-D load of one box into shared memory; completion is counted in
+// bytes on `bar`.  c_inner * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c_inner,
+                                            int c_outer, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar)
+      : "memory");
+}
+// L2 prefetch of one box (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c_inner, int c_outer) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
+               "r"(c_inner), "r"(c_outer)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+#endif
+
+}  // namespace mla

@@ -76,10 +76,10 @@ def test_null_arguments(L):
 
 def test_building_block_shape_checks(L):
     # K must be a multiple of 32 and N of 8 for the int8 GEMM; zero rows is a no-op
-    assert L.mla_w8a8_gemm_s32(None, None, 4, 48, 8, None, None) == 2
-    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 12, None, None) == 2
-    assert L.mla_w8a8_gemm_s32(None, None, 0, 64, 8, None, None) == 0
-    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 8, None, None) == 1
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 48, 64, None, None) == 2
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 96, None, None) == 2
+    assert L.mla_w8a8_gemm_s32(None, None, 0, 64, 64, None, None) == 0
+    assert L.mla_w8a8_gemm_s32(None, None, 4, 64, 64, None, None) == 1
     assert L.mla_w8a8_quant_rows(None, 4, 12, None, None, None) == 2
     assert L.mla_w8a8_quant_rows(None, 0, 16, None, None, None) == 0
     assert L.mla_w8a8_quant_rows(None, -1, 16, None, None, None) == 1

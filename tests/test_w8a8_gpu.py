@@ -1,0 +1,132 @@
+"""GPU checks of the W8A8 full MLA prolog (through the C ABI).
+
+Bit-exact: the per-row int8 quantisation of bf16 rows and the int8 GEMM
+accumulators (against the oracle's brute-force integer GEMM), including the
+split-K path; the q_b / kv_b accumulators computed from the GPU's own int8
+operands.  Within tolerance: the five bf16 outputs against the fp64 oracle
+(tiny shapes, R1 shapes at T = 1, 64 and sampled rows of T = 8192)."""
+import numpy as np
+import pytest
+import torch
+
+from mla_attention_kv_gb300 import binding as B
+from mla_attention_kv_gb300 import build as BLD
+from mla_attention_kv_gb300 import inputs as I
+
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+NAMES = ("q_nope", "q_pe", "k_nope", "value", "k_pe")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    BLD.build()
+    B.load()
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 64), (7, 7168), (33, 1536), (3, 512)])
+def test_quant_rows_bit_exact(oracle_mod, rows, cols):
+    g = torch.Generator().manual_seed(rows * 1000 + cols)
+    x = (torch.randn(rows, cols, generator=g) * 3).to(torch.bfloat16)
+    x[0, :8] = torch.tensor([1.0, -2.0, 0.5, 0.0, 0.25, -0.125, 2.0, 1.5]).to(torch.bfloat16)
+    if rows > 2:
+        x[2] = 0  # amax == 0 row
+    q = torch.empty(rows, cols, dtype=torch.int8, device="cuda")
+    s = torch.empty(rows, dtype=torch.float32, device="cuda")
+    B.mla_w8a8_quant_rows(x.cuda(), q, s)
+    torch.cuda.synchronize()
+    for r in range(rows):
+        qo, so = oracle_mod.quant_row_f32(x[r].float().numpy())
+        assert np.array_equal(q[r].cpu().numpy(), qo), r
+        assert s[r].item() == so, r
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 7168, 1536), (1, 7168, 576), (64, 1536, 2048), (5, 512, 64),
+                                   (130, 256, 192), (8192, 64, 64)])
+def test_gemm_s32_bit_exact(oracle_mod, M, K, N):
+    g = torch.Generator().manual_seed(M + K + N)
+    A = torch.randint(-127, 128, (M, K), generator=g, dtype=torch.int8)
+    W = torch.randint(-127, 128, (K, N), generator=g, dtype=torch.int8)
+    acc = torch.empty(M, N, dtype=torch.int32, device="cuda")
+    B.mla_w8a8_gemm_s32(A.cuda(), W.cuda(), acc)
+    torch.cuda.synchronize()
+    rows = np.unique(np.linspace(0, M - 1, min(M, 40)).astype(int))
+    ref = oracle_mod.int_gemm(A.numpy()[rows], W.numpy())
+    assert np.array_equal(acc.cpu().numpy()[rows].astype(np.int64), ref)
+
+
+def run_w8(cfg, b, s, seed, positions="decode", rows=None, oracle_mod=None, keep=False):
+    inp = I.w8a8_inputs(cfg, b, s, seed, positions)
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, b * s)
+    out = m.alloc_outputs(b, s)
+    for t in out.values():
+        t.fill_(float("nan"))
+    m.run(b, s, d, out)
+    torch.cuda.synchronize()
+    st = m.status()
+    res = dict(inp=inp, d=d, out=out, status=st, launches=m.last_launches, m=m)
+    if oracle_mod is not None:
+        ref = oracle_mod.w8a8_prolog(inp, rows=rows)
+        res["err"] = {n: compare(n, out[n], r, oracle_mod) for n, r in zip(NAMES, ref)}
+    if not keep:
+        m.close()
+    return res
+
+
+def test_w8a8_tiny(oracle_mod):
+    cfg = I.small_config(I.R1_W8A8, hidden=256, q_lora_rank=192, num_heads=2, max_pos=64)
+    r = run_w8(cfg, 1, 3, 21, oracle_mod=oracle_mod)
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("b,s", [(1, 1), (64, 1)])
+def test_w8a8_r1_decode(oracle_mod, b, s):
+    r = run_w8(I.R1_W8A8, b, s, I.seed_for(4) + b, oracle_mod=oracle_mod)
+    assert r["status"] == 0
+
+
+def test_w8a8_r1_prefill_sampled(oracle_mod):
+    b, s = 1, 8192
+    rows = I.sampled_rows(b, s, 24, seed=2004)
+    r = run_w8(I.R1_W8A8, b, s, I.seed_for(4), positions="prefill", rows=rows, oracle_mod=oracle_mod)
+    assert r["status"] == 0
+
+
+def test_w8a8_operands_and_accumulators(oracle_mod):
+    """The int8 operands the GPU fed to q_b / kv_b agree with the oracle's
+    requantisation (>= 99.9 % equal, never off by more than 1), and the
+    int32 accumulators the GPU GEMM forms from them are bit-exact."""
+    cfg = I.R1_W8A8
+    b, s = 16, 1
+    r = run_w8(cfg, b, s, 4242, keep=True)
+    m, T = r["m"], b * s
+    rq = cfg["q_lora_rank"]
+    q1 = torch.empty(T, rq, dtype=torch.int8, device="cuda")
+    s1 = torch.empty(T, dtype=torch.float32, device="cuda")
+    c1 = torch.empty(T, 512, dtype=torch.int8, device="cuda")
+    s2 = torch.empty(T, dtype=torch.float32, device="cuda")
+    B.mla_prolog_w8a8_operands(m.h, T, q1, s1, c1, s2)
+    torch.cuda.synchronize()
+    m.close()
+    gq, gc = q1.cpu().numpy(), c1.cpu().numpy()
+    eq = tot = 0
+    for t in range(T):
+        oq, os1, oc, os2 = oracle_mod.w8a8_operands(r["inp"], t)
+        for g_, o_ in ((gq[t], oq), (gc[t], oc)):
+            d = np.abs(g_.astype(np.int32) - o_.astype(np.int32))
+            assert d.max() <= 1
+            eq += int((d == 0).sum())
+            tot += d.size
+        assert abs(s1[t].item() - os1) <= 1e-6 * os1 and abs(s2[t].item() - os2) <= 1e-6 * os2
+    assert eq / tot >= 0.999, eq / tot
+    # accumulators of the GPU's own operands: bit-exact against brute force
+    for A, W in ((q1, r["d"]["W_qb"]), (c1, r["d"]["W_kvb"])):
+        acc = torch.empty(T, W.shape[1], dtype=torch.int32, device="cuda")
+        B.mla_w8a8_gemm_s32(A, W, acc)
+        torch.cuda.synchronize()
+        ref = oracle_mod.int_gemm(A.cpu().numpy()[:4], W.cpu().numpy())
+        assert np.array_equal(acc.cpu().numpy()[:4].astype(np.int64), ref)
