@@ -197,6 +197,36 @@ mla_status mla_w8a8_gemm_s32(const int8_t* A, const int8_t* W, int M, int K, int
 mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1, int8_t* c1,
                                     float* s2, cudaStream_t stream);
 
+/* No counterpart in the pages: an extra entry point of this library for
+ * callers that cannot allocate device memory -- a serving engine or plugin
+ * host that owns all device memory in an arena planned up front, or a
+ * latency-critical caller that cannot risk a blocking or failing
+ * cudaMalloc mid-run.  It runs the fused decode kernel of
+ * mla_kv_prolog_run (T = b*s rows, any T, in chunks of 64 rows) with the
+ * same arguments, but needs no handle: its scratch (split-K partials,
+ * latent rows, barrier counters, status word) is one fixed __device__
+ * array inside the library, about 2.3 MB, held by every device that loads
+ * the library until the process exits.  It calls no cudaMalloc, cudaFree
+ * or allocating library routine.
+ *   cfg            model dimensions as for create; quant must be NONE
+ *                  (else MLA_ERR_WRONG_MODE); max_tokens is ignored
+ *   device_status  optional device pointer (may be NULL): receives the
+ *                  status word of this call (bit 0 bad position, bit 1
+ *                  device wait timed out), copied on `stream`
+ * Shapes whose split-K scratch would exceed the array are rejected with
+ * MLA_ERR_UNSUPPORTED and a message in mla_last_cuda_error().
+ * All calls on a device share the array: each call clears the counters
+ * and status word first, and calls that overlap on the same GPU race on
+ * it (serialise them on one stream).  The first call on each device looks
+ * up the array's address with cudaGetSymbolAddress while that device is
+ * current; make that first call before any stream capture begins. */
+mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, int b, int s,
+                                     const void* hidden_states, const int32_t* positions,
+                                     const void* W_kva, const void* gamma_kv, const void* W_kvb,
+                                     const float* cos_table, const float* sin_table,
+                                     void* k_nope, void* value, void* k_pe,
+                                     unsigned int* device_status, cudaStream_t stream);
+
 /* Text of a status code (static storage), the text of the last CUDA error
  * seen by this library on the calling thread, and the ABI version. */
 const char* mla_status_string(mla_status s);

@@ -27,7 +27,7 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
             "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
-            "mla_last_cuda_error", "mla_abi_version"]
+            "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc"]
 
 
 class MLAError(RuntimeError):
@@ -74,10 +74,12 @@ def load(path: str | None = None):
     L.mla_w8a8_quant_rows.argtypes = [P, I, I, P, P, P]
     L.mla_w8a8_gemm_s32.argtypes = [P, P, I, I, I, P, P]
     L.mla_prolog_w8a8_operands.argtypes = [H, I, P, P, P, P, P]
+    L.mla_kv_prolog_run_noalloc.argtypes = [ctypes.POINTER(Config), I, I] + [P] * 11 + [P]
     for fn in ("mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
                "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
                "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
-               "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_abi_version"):
+               "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_abi_version",
+               "mla_kv_prolog_run_noalloc"):
         getattr(L, fn).restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
     L.mla_status_string.restype = ctypes.c_char_p
@@ -114,12 +116,16 @@ def _tdt(cfg: dict) -> torch.dtype:
 
 
 # ------------------------------------------------------------------ C-named calls
+def _config(cfg: dict, max_tokens: int, spin_budget_ns: int = 0) -> Config:
+    return Config(cfg["hidden"], cfg["kv_lora_rank"], cfg["rope_dim"], cfg["num_heads"],
+                  cfg["nope_dim"], cfg["v_dim"], MLA_F16 if cfg["dtype"] == "fp16" else MLA_BF16,
+                  cfg["eps"], max_tokens, cfg["max_pos"],
+                  QUANT_W8A8 if cfg.get("quant") == "w8a8" else QUANT_NONE,
+                  cfg.get("q_lora_rank", 0), spin_budget_ns)
+
+
 def mla_kv_prolog_create(cfg: dict, max_tokens: int, spin_budget_ns: int = 0) -> ctypes.c_void_p:
-    c = Config(cfg["hidden"], cfg["kv_lora_rank"], cfg["rope_dim"], cfg["num_heads"],
-               cfg["nope_dim"], cfg["v_dim"], MLA_F16 if cfg["dtype"] == "fp16" else MLA_BF16,
-               cfg["eps"], max_tokens, cfg["max_pos"],
-               QUANT_W8A8 if cfg.get("quant") == "w8a8" else QUANT_NONE,
-               cfg.get("q_lora_rank", 0), spin_budget_ns)
+    c = _config(cfg, max_tokens, spin_budget_ns)
     h = ctypes.c_void_p()
     _check(load().mla_kv_prolog_create(ctypes.byref(c), ctypes.byref(h)), "mla_kv_prolog_create")
     return h
@@ -160,6 +166,21 @@ def mla_prolog_w8a8_run(h, b, s, hidden, positions, W_qa, sW_qa, gamma_q, W_qb, 
             _dev(sin, f32, "sin"), _dev(q_nope, bf, "q_nope"), _dev(q_pe, bf, "q_pe"),
             _dev(k_nope, bf, "k_nope"), _dev(value, bf, "value"), _dev(k_pe, bf, "k_pe")]
     _check(load().mla_prolog_w8a8_run(h, b, s, *args, _stream(stream)), "mla_prolog_w8a8_run")
+
+
+def mla_kv_prolog_run_noalloc(cfg, b, s, hidden, positions, W_kva, gamma_kv, W_kvb, cos, sin,
+                              k_nope, value, k_pe, device_status=None, stream=None):
+    """The allocation-free entry point: same computation as mla_kv_prolog_run,
+    no handle, scratch in the library's fixed device array."""
+    dt = _tdt(cfg)
+    c = _config(cfg, max(1, b * s))
+    args = [_dev(hidden, dt, "hidden_states"), _dev(positions, torch.int32, "positions"),
+            _dev(W_kva, dt, "W_kva"), _dev(gamma_kv, dt, "gamma_kv"), _dev(W_kvb, dt, "W_kvb"),
+            _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
+            _dev(k_nope, dt, "k_nope"), _dev(value, dt, "value"), _dev(k_pe, dt, "k_pe"),
+            None if device_status is None else _dev(device_status, torch.int32, "device_status")]
+    _check(load().mla_kv_prolog_run_noalloc(ctypes.byref(c), b, s, *args, _stream(stream)),
+           "mla_kv_prolog_run_noalloc")
 
 
 def mla_w8a8_quant_rows(x, q, scale, stream=None):

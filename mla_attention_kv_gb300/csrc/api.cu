@@ -63,6 +63,10 @@ static mla_status cuda_fail(cudaError_t e, const char* what) {
   return MLA_ERR_CUDA;
 }
 
+void mla::set_error_text(const char* what) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s", what);
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 extern "C" {

@@ -7,6 +7,9 @@
 
 namespace mla {
 
+// Record the text that mla_last_cuda_error() returns on this thread.
+void set_error_text(const char* what);
+
 // Device status bits (kept in the handle's workspace).
 enum : unsigned { kStatusBadPosition = 1u, kStatusTimeout = 2u };
 
