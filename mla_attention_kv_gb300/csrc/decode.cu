@@ -45,7 +45,7 @@ constexpr int kPitchX = 144;       // smem row pitch of a 64-column hidden tile
 constexpr int kPitchN = 1040;      // smem row pitch of a 512-column latent row
 constexpr int kMaxMT = kDecodeMaxTokens / 16;
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kRedBytes = 8192;    // cross-warp reduction scratch
+constexpr int kRedBytes = 16384;   // cross-warp reduction scratch (<= 32 chains x 512 B)
 constexpr int kMiscBytes = 2048;   // gamma + cos/sin row
 
 __device__ __forceinline__ int col_group_begin(int cta, int ngroups, int grid) {
@@ -91,17 +91,23 @@ __device__ __forceinline__ bool mbar_wait_cta(uint32_t bar, uint32_t parity,
   return ok;
 }
 
-// Last CTA out resets the barrier counters for the next launch.
-__device__ __forceinline__ void bar_exit(unsigned* counters, unsigned G) {
-  if (threadIdx.x == 0) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counters + 2) : "memory");
-    if (old == G - 1) {
-      counters[0] = 0;
-      counters[1] = 0;
-      __threadfence();
-      counters[2] = 0;
-    }
+// Exit counter: every CTA adds one once it has passed its last grid
+// barrier; the CTA that brings the count to G knows that every CTA has left
+// every barrier, and resets the counters for the next launch.  The add is
+// issued early and its result is only looked at when the CTA finishes, so
+// the round trip stays off the critical path.
+__device__ __forceinline__ unsigned bar_exit_arrive(unsigned* counters) {
+  unsigned old = 0;
+  if (threadIdx.x == 0)
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counters + 2));
+  return old;
+}
+__device__ __forceinline__ void bar_exit_finish(unsigned* counters, unsigned old, unsigned G) {
+  if (threadIdx.x == 0 && old == G - 1) {
+    counters[0] = 0;
+    counters[1] = 0;
+    __threadfence();
+    counters[2] = 0;
   }
 }
 
@@ -146,7 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
+  // The W_kvb slice is only needed after the grid barrier: its TMA copies
+  // are issued once this CTA's first kv_a stage has landed, so the kv_a
+  // loads (on the critical path) are not queued behind them in DRAM.
+  auto issue_wkvb = [&]() {
     mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchB : 0));
     if (ng > 0) {
       for (int r = 0; r < p.kpre; r += kWkvbBoxRows)
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       for (int r = p.kpre; r < kRank; r += kWkvbBoxRows)
         tma_prefetch_2d(&p.tmap_wkvb, col0, r);
     }
-  }
+  };
   if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
 
   // ================================================================ phase A
@@ -165,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int nsub = my_units * subs;
     const int stage_bytes = kSubK * kPitchWA + rows_x * kPitchX;
     const int nst = p.nstA;
+    if (nsub == 0 && tid == 0) issue_wkvb();
 
     auto load_sub = [&](int i) {
       const int u = cta + (i / subs) * G;
@@ -210,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     for (int i = 0; i < nsub; ++i) {
       cp_async_wait_dyn(nst - 2);
       __syncthreads();
+      if (i == 0 && tid == 0) issue_wkvb();
       if (i + nst - 1 < nsub) load_sub(i + nst - 1);
       cp_async_commit();
       const unsigned char* st = sA + (i % nst) * stage_bytes;
@@ -400,19 +411,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     cp_async_commit();
   }
-  bar_exit(p.counters, G);
+  const unsigned exit_old = bar_exit_arrive(p.counters);
 
   // ================================================================ phase B
-  if (ng == 0) return;
+  if (ng == 0) {
+    bar_exit_finish(p.counters, exit_old, G);
+    return;
+  }
+  // Work: npairs (m-tile, 8-column group) output tiles x 32 k16 steps.  Each
+  // pair's steps are split into kslices interleaved slices so that every
+  // warp carries up to MAXP independent accumulator chains (mma.sync is
+  // latency-bound on one chain); slices are summed through shared memory.
   const int npairs = MT * ng;
-  int ksplit = 1;
-  while (ksplit < 4 && npairs * ksplit * 2 <= kWarps) ksplit *= 2;
-  const int wpg = kWarps / ksplit;   // warps per k-slice
-  const int kslice = warp / wpg, pbase = warp % wpg;
+  int kslices = 1;
+  while (kslices < 8 && npairs * kslices * 2 <= kWarps * (MAXP < 4 ? MAXP : 4)) kslices *= 2;
+  const int nchains = npairs * kslices;
   float acc[MAXP][4];
 #pragma unroll
   for (int q = 0; q < MAXP; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
   const uint32_t nrm_u = smem_u32(sN);
+  // per chain: A-row and B-column offsets and its k-slice
+  uint32_t aoff[MAXP], boff[MAXP];
+  int kslc[MAXP];
+#pragma unroll
+  for (int q = 0; q < MAXP; ++q) {
+    const int ch = warp + q * kWarps;
+    const int pr = ch / kslices;
+    kslc[q] = ch < nchains ? ch - pr * kslices : -1;
+    const int m = pr % MT, gi = pr / MT;
+    aoff[q] = (uint32_t)(m * 16 * kPitchN);
+    boff[q] = (uint32_t)(gi * 16);
+  }
 
   // K rows are consumed in chunks: the resident rows, then streamed chunks
   cp_async_wait<0>();
@@ -420,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   if (!mbar_wait_cta(bar_res, 0, p.budget_ns, sFlag)) {
     if (tid == 0) atomicOr(p.status, kStatusTimeout);
     drain();
+    bar_exit_finish(p.counters, exit_old, G);
     return;
   }
   int kbase = 0, krows = p.kpre;
@@ -433,22 +463,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (!mbar_wait_cta(bar_s0 + 8 * (c & 1), (c >> 1) & 1, p.budget_ns, sFlag)) {
         if (tid == 0) atomicOr(p.status, kStatusTimeout);
         drain();
+        bar_exit_finish(p.counters, exit_old, G);
         return;
       }
     }
     const int steps = krows / 16;
+    const int gs0 = kbase / 16;
+    // kslices divides the warp count, so all chains of a warp share one slice
+    const int myslice = warp % kslices;
+    const int st0 = ((myslice - gs0 % kslices) + kslices) % kslices;
 #pragma unroll 1
-    for (int st = kslice; st < steps; st += ksplit) {
+    for (int st = st0; st < steps; st += kslices) {
       const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchB;
       const uint32_t arow = nrm_u + (lane & 15) * kPitchN + ((kbase + st * 16) + (lane >> 4) * 8) * 2;
 #pragma unroll
       for (int q = 0; q < MAXP; ++q) {
-        const int pr = pbase + q * wpg;
-        if (pr < npairs) {
-          const int m = pr % MT, gi = pr / MT;
+        if (kslc[q] >= 0) {
           uint32_t b0, b1, a[4];
-          ldsm_x2_trans(wrow + gi * 16, b0, b1);
-          ldsm_x4(arow + m * 16 * kPitchN, a[0], a[1], a[2], a[3]);
+          ldsm_x2_trans(wrow + boff[q], b0, b1);
+          ldsm_x4(arow + aoff[q], a[0], a[1], a[2], a[3]);
           mma16816<E::kBf16>(acc[q], a, b0, b1);
         }
       }
@@ -460,50 +493,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       issued = c + 3;
     }
   }
+  bar_exit_finish(p.counters, exit_old, G);
 
-  if (ksplit > 1) {
-    // each warp holds at most one pair when ksplit > 1
-    __syncthreads();
-    if (kslice > 0 && pbase < npairs)
-      *reinterpret_cast<float4*>(sRed + ((kslice * wpg + pbase) * 32 + lane) * 4) =
-          make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-    __syncthreads();
-    if (kslice == 0 && pbase < npairs) {
-      for (int ks = 1; ks < ksplit; ++ks) {
-        const float4 o = *reinterpret_cast<const float4*>(sRed + ((ks * wpg + pbase) * 32 + lane) * 4);
-        acc[0][0] += o.x; acc[0][1] += o.y; acc[0][2] += o.z; acc[0][3] += o.w;
-      }
-    }
-  }
-  if (kslice != 0) return;
+  // ---- epilogue: sum the k-slices of each pair, split + head-major stores
   T* kn = static_cast<T*>(p.k_nope);
   T* vv = static_cast<T*>(p.value);
+  auto store_pair = [&](int pr, const float* v) {
+    const int m = pr % MT, gi = pr / MT;
+    const int j = col0 + gi * 8 + 2 * (lane & 3);
+    const int hh = j / kHeadCols, e = j % kHeadCols;
+    T* base = (e < kNope) ? kn : vv;
+    const int ee = (e < kNope) ? e : e - kNope;
 #pragma unroll
-  for (int q = 0; q < MAXP; ++q) {
-    const int pr = pbase + q * wpg;
-    if (pr < npairs) {
-      const int m = pr % MT, gi = pr / MT;
-      const int j = col0 + gi * 8 + 2 * (lane & 3);
-      const int hh = j / kHeadCols, e = j % kHeadCols;
-      T* base = (e < kNope) ? kn : vv;
-      const int ee = (e < kNope) ? e : e - kNope;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int r = m * 16 + (lane >> 2) + half * 8;
-        if (r < TT) {
-          const int tg = p.t0 + r;
-          const int bi = tg / p.s, si = tg - bi * p.s;
-          T* dst = base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee;
-          *reinterpret_cast<uint32_t*>(dst) = E::pack(acc[q][2 * half], acc[q][2 * half + 1]);
-        }
+    for (int half = 0; half < 2; ++half) {
+      const int r = m * 16 + (lane >> 2) + half * 8;
+      if (r < TT) {
+        const int tg = p.t0 + r;
+        const int bi = tg / p.s, si = tg - bi * p.s;
+        T* dst = base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee;
+        *reinterpret_cast<uint32_t*>(dst) = E::pack(v[2 * half], v[2 * half + 1]);
       }
+    }
+  };
+  if (kslices == 1) {
+#pragma unroll
+    for (int q = 0; q < MAXP; ++q)
+      if (kslc[q] >= 0) store_pair(warp + q * kWarps, acc[q]);
+  } else {
+    // chains -> shared memory, then one warp per pair sums its slices
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < MAXP; ++q) {
+      const int ch = warp + q * kWarps;
+      if (ch < nchains)
+        *reinterpret_cast<float4*>(sRed + (ch * 32 + lane) * 4) = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+    }
+    __syncthreads();
+    for (int pr = warp; pr < npairs; pr += kWarps) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks = 0; ks < kslices; ++ks) {
+        const float4 o = *reinterpret_cast<const float4*>(sRed + ((pr * kslices + ks) * 32 + lane) * 4);
+        v[0] += o.x; v[1] += o.y; v[2] += o.z; v[3] += o.w;
+      }
+      store_pair(pr, v);
     }
   }
 }
 
 template <typename T>
 const void* kernel_for(int maxp) {
-  if (maxp <= 2) return (const void*)decode_kernel<T, 2>;
   if (maxp <= 4) return (const void*)decode_kernel<T, 4>;
   return (const void*)decode_kernel<T, 16>;
 }

@@ -47,7 +47,8 @@ constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 til
 constexpr uint32_t kS2Bytes = 32768;        // kv_b stage: [64 K x 256 N]
 constexpr int kS2Stages = 3;
 constexpr uint32_t kBarBase = kS2Base + kS2Stages * kS2Bytes;  // 229376
-constexpr uint32_t kSmemBytes = kBarBase + 256 + 1024;         // + alignment slack
+constexpr uint32_t kGamBase = kBarBase + 256;                  // gamma [512], I/O dtype
+constexpr uint32_t kSmemBytes = kGamBase + 1024 + 1024;        // + alignment slack
 
 struct PfShared {
   uint64_t full1[2], empty1[2];
@@ -276,7 +277,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int q = warp & 3;                // TMEM lane quadrant
     const int r = q * 32 + lane;           // row within the tile
     const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-    const T* gam = static_cast<const T*>(p.gamma);
+    // gamma -> shared memory once (read by every row of every tile)
+    const T* gam = reinterpret_cast<const T*>(smem + kGamBase);
+    {
+      const int e = threadIdx.x - 64;  // 0..127
+      reinterpret_cast<uint2*>(smem + kGamBase)[e] = reinterpret_cast<const uint2*>(p.gamma)[e];
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
     uint32_t uf[2] = {0, 0};
     int tiles_done = 0;
     bool ok = true;
@@ -299,8 +306,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             atomicOr(p.status, kStatusBadPosition);
             pos = pos < 0 ? 0 : p.max_pos - 1;
           }
-          const float* cr = p.cos_t + (size_t)pos * kRope;
-          const float* sr = p.sin_t + (size_t)pos * kRope;
+          float cr[kRope], sr[kRope];
+          {
+            const float4* c4 = reinterpret_cast<const float4*>(p.cos_t + (size_t)pos * kRope);
+            const float4* s4 = reinterpret_cast<const float4*>(p.sin_t + (size_t)pos * kRope);
+#pragma unroll
+            for (int v = 0; v < kRope / 4; ++v) {
+              const float4 a = __ldg(c4 + v), b = __ldg(s4 + v);
+              cr[4 * v] = a.x; cr[4 * v + 1] = a.y; cr[4 * v + 2] = a.z; cr[4 * v + 3] = a.w;
+              sr[4 * v] = b.x; sr[4 * v + 1] = b.y; sr[4 * v + 2] = b.z; sr[4 * v + 3] = b.w;
+            }
+          }
           uint32_t o[32];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
