@@ -40,6 +40,10 @@ sys.path.insert(0, ROOT)
 
 from mla_attention_kv_gb300 import inputs as I  # noqa: E402
 
+# mma.sync m16n8k32 s8 throughput measured on this machine's GB300 (the
+# tcgen05 int8 kind does not exist on sm_103a); see profiles/mma_sync_rates.md
+INT8_MMA_SYNC_TOPS = 148.8
+
 SWEEP_B = [1, 2, 4, 8, 16, 32, 64, 128]
 SWEEP_S = [1, 2]
 
@@ -66,6 +70,10 @@ class DecodeSweep:
     def weight_bytes(self):
         c = self.cfg
         return 2 * (c["hidden"] * 576 + 512 + 512 * c["num_heads"] * 256)
+
+    def flops(self, T):
+        c = self.cfg
+        return 2.0 * T * (c["hidden"] * 576 + 512 * c["num_heads"] * 256)
 
     def alg_bytes(self, T):
         # weights once + per token: hidden row, position, cos+sin rows, outputs
@@ -105,15 +113,17 @@ class DecodeSweep:
         self.m.run(p["b"], p["s"], d, self.out[i], stream)
         return self.m.last_launches
 
-    def step(self, stream, events=None):
+    def step(self, stream, events=None, intervals=None):
         """One pass over the sweep; with `events`, record one event after
-        each launch (events[0] must be recorded by the caller before)."""
+        each call (events[-1] is the event before the first call) and the
+        index pair of each call's interval in `intervals`."""
         n = 0
         for i in range(len(self.pt)):
             n += self._run(i, stream)
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record(stream)
+                intervals.append((len(events) - 2, len(events) - 1, self.pt[i]["b"] * self.pt[i]["s"]))
         return n
 
     def step_bytes(self):
@@ -153,7 +163,127 @@ class DecodeSweep:
             f"{pts} sweep points in order ({done} token rows) of the V2-Lite decode sweep, fp64 oracle, {el:.1f} s"
 
 
-WORKLOADS = {"decode_sweep": DecodeSweep}
+class SingleCall:
+    """One prolog call per step on one configuration (prefill, R1, W8A8)."""
+
+    def __init__(self, name, cfg, b, s, positions, path, seed):
+        self.name, self.cfg, self.b, self.s = name, cfg, b, s
+        self.positions, self.path, self.seed = positions, path, seed
+        self.T = b * s
+        self.points = [(b, s)]
+        self.tokens_per_step = self.T
+        self.w8 = cfg.get("quant") == "w8a8"
+
+    def describe(self):
+        c = self.cfg
+        d = {"workload": self.name, "model": c["name"], "hidden": c["hidden"], "num_heads": c["num_heads"],
+             "b": self.b, "s": self.s, "T": self.T, "dtype": c["dtype"], "positions": self.positions}
+        if self.w8:
+            d["q_lora_rank"] = c["q_lora_rank"]
+            d["quant"] = "w8a8 (int8 weights, per-token int8 activations, int32 accumulators)"
+        return d
+
+    def weight_bytes(self):
+        c = self.cfg
+        h, H, r = c["hidden"], c["num_heads"], 512
+        if self.w8:
+            rq = c["q_lora_rank"]
+            return (h * (rq + 576) + rq * H * 192 + r * H * 256) + 4 * (rq + 576 + H * 192 + H * 256) + 2 * (rq + r)
+        return 2 * (h * 576 + r + r * H * 256)
+
+    def flops(self, T):
+        c = self.cfg
+        h, H = c["hidden"], c["num_heads"]
+        if self.w8:
+            rq = c["q_lora_rank"]
+            return 2.0 * T * (h * (rq + 576) + rq * H * 192 + 512 * H * 256)
+        return 2.0 * T * (h * 576 + 512 * H * 256)
+
+    def alg_bytes(self, T):
+        c = self.cfg
+        H = c["num_heads"]
+        out = 2 * (H * 256 + 64) + (2 * H * 192 if self.w8 else 0)
+        return self.weight_bytes() + T * (2 * c["hidden"] + 4 + 2 * 64 * 4 + out)
+
+    def setup(self, dev):
+        from mla_attention_kv_gb300 import binding as B
+        self.B = B
+        gen = I.w8a8_inputs if self.w8 else I.kv_inputs
+        inp = gen(self.cfg, self.b, self.s, self.seed, self.positions)
+        self.host = inp
+        self.d = B.to_device(inp, dev)
+        self.R = 1
+        self.m = B.MLAProlog(self.cfg, self.T)
+        if not self.w8:
+            self.m.set_path(self.path)
+        self.out = self.m.alloc_outputs(self.b, self.s, dev)
+        self.hidden_h = inp["hidden"].pin_memory()
+        self.positions_h = inp["positions"].pin_memory()
+        self.out_h = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.out.items()}
+        # L2 flush buffer (2x L2), written between timed calls when the inputs fit in L2
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = None
+        if self.alg_bytes(self.T) < 2 * l2:
+            self.flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step(self, stream, events=None, intervals=None):
+        if self.flush is not None and events is not None:
+            self.flush.zero_()
+            events.append(torch.cuda.Event(enable_timing=True))
+            events[-1].record(stream)
+        self.m.run(self.b, self.s, self.d, self.out, stream)
+        if events is not None:
+            events.append(torch.cuda.Event(enable_timing=True))
+            events[-1].record(stream)
+            intervals.append((len(events) - 2, len(events) - 1, self.T))
+        return self.m.last_launches
+
+    def step_bytes(self):
+        return [self.alg_bytes(self.T)]
+
+    def e2e_step(self, stream):
+        self.d["hidden"].copy_(self.hidden_h, non_blocking=True)
+        self.d["positions"].copy_(self.positions_h, non_blocking=True)
+        self.m.run(self.b, self.s, self.d, self.out, stream)
+        d2h = 0
+        for k, v in self.out.items():
+            self.out_h[k].copy_(v, non_blocking=True)
+            d2h += v.numel() * v.element_size()
+        return self.hidden_h.numel() * 2 + self.positions_h.numel() * 4, d2h
+
+    def cpu_sample(self, seconds):
+        import oracle
+        oracle.build()
+        nt = os.cpu_count() or 1
+        rows_per = max(nt, 8)
+        done, t0, k = 0, time.perf_counter(), 0
+        fn = oracle.w8a8_prolog if self.w8 else oracle.kv_prolog
+        while True:
+            rows = [(k * rows_per + i) % self.T for i in range(rows_per)]
+            fn(self.host, rows=sorted(set(rows)), nthreads=nt)
+            done += len(set(rows))
+            k += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        el = time.perf_counter() - t0
+        return done / el, min(nt, oracle.max_threads()), \
+            f"{done} token rows of {self.name} (fp64 oracle, per-call weight promotion included), {el:.1f} s"
+
+
+def _single(name, cfg, b, s, positions, path_name, seed):
+    return lambda: SingleCall(name, cfg, b, s, positions, {"decode": 1, "prefill": 2, "auto": 0}[path_name], seed)
+
+
+WORKLOADS = {
+    "decode_sweep": DecodeSweep,
+    "v2lite_tiny": _single("v2lite_kv_prolog_tiny_b1s2", I.V2_LITE, 1, 2, [7, 8], "auto", 1000),
+    "v2lite_prefill": _single("v2lite_kv_prolog_prefill_b4s4096", I.V2_LITE, 4, 4096, "prefill", "auto", 1002),
+    "r1_decode": _single("r1_kv_prolog_decode_b64s1", I.R1, 64, 1, "decode", "auto", 1003),
+    "r1_prefill": _single("r1_kv_prolog_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1003),
+    "w8a8_t1": _single("r1_w8a8_prolog_T1", I.R1_W8A8, 1, 1, "decode", "auto", 1004),
+    "w8a8_t64": _single("r1_w8a8_prolog_T64", I.R1_W8A8, 64, 1, "decode", "auto", 1004),
+    "w8a8_t8192": _single("r1_w8a8_prolog_T8192", I.R1_W8A8, 1, 8192, "prefill", "auto", 1004),
+}
 
 
 # ------------------------------------------------------------------ clocks
@@ -215,15 +345,15 @@ def run_gpu(args, wl, rank, world, dev):
     wl.setup(dev)
     stream = torch.cuda.current_stream(dev)
 
-    # warm-up (also measures host enqueue time per step)
+    # warm-up (also measures the host enqueue time of a step)
     t0 = time.perf_counter()
     for _ in range(args.warmup):
-        launches_per_step = wl.step(stream)
+        wl.step(stream)
     torch.cuda.synchronize(dev)
     host_per_step = (time.perf_counter() - t0) / max(1, args.warmup)
 
-    # timed region
-    events = []
+    # timed region: exactly K steps between CUDA events on the launching stream
+    events, intervals = [], []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -235,20 +365,21 @@ def run_gpu(args, wl, rank, world, dev):
     events.append(start)
     total_launches = 0
     for _ in range(args.steps):
-        total_launches += wl.step(stream, events)
+        total_launches += wl.step(stream, events, intervals)
     end = events[-1]
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = start.elapsed_time(end)
-    durs = [events[i].elapsed_time(events[i + 1]) for i in range(len(events) - 1)]
+    region_ms = start.elapsed_time(end)
+    calls = [(events[a].elapsed_time(events[b]), T) for a, b, T in intervals]
+    call_ms = sum(c for c, _ in calls)
+    # with an L2 flush between calls, the flush is not part of the work
+    ms = call_ms if getattr(wl, "flush", None) is not None else region_ms
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    if durs[-1] <= 0:
-        log("warning: zero-duration events")
 
     # e2e through the public binding with host buffers
     for _ in range(2):
@@ -266,9 +397,26 @@ def run_gpu(args, wl, rank, world, dev):
         t = torch.tensor([e2e_s], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_s = float(t.item())
-    return dict(ms=ms, durs=durs, clk=clk, launches=total_launches,
-                launches_per_step=launches_per_step, e2e_s=e2e_s, e2e_steps=e2e_steps,
-                h2d=h2d, d2h=d2h, host_per_step=host_per_step)
+    return dict(ms=ms, region_ms=region_ms, calls=calls, clk=clk, launches=total_launches,
+                e2e_s=e2e_s, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h, host_per_step=host_per_step)
+
+
+def kernel_traffic(kernel: str, T: int):
+    """DRAM bytes of one call of `kernel` at T rows from the committed ncu
+    summary, or None when the summary is missing or was taken on a different
+    version of the kernel's source (its sha256 no longer matches)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        src = os.path.join(ROOT, "mla_attention_kv_gb300", "csrc", t[kernel]["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != t[kernel]["sha256_16"]:
+            return None
+        return t[kernel]["bytes_per_call"].get(str(T))
+    except Exception:
+        return None
 
 
 def main():
@@ -288,24 +436,23 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = WORKLOADS[args.workload]()
+    is_w8 = getattr(wl, "w8", False)
+    dtype = "int8/int32 (bf16 io)" if is_w8 else ("f16" if wl.cfg["dtype"] == "fp16" else "bf16")
 
     if args.impl == "reference":
         if rank != 0:
             return
-        per_step_s = None
-        # each step: the oracle over a bounded sample of the workload
         v, cores, sample = wl.cpu_sample(min(args.cpu_seconds, 20.0))
         line = {"metric": "tokens/s", "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": wl.tokens_per_step / v * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference",
                 "config": dict(wl.describe(), parallelism="none (host cores)"),
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
                                  "kind": "oracle", "sample": sample},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
-        if per_step_s:
-            line["ms_per_step"] = per_step_s * 1e3
         print(json.dumps(line), flush=True)
         return
 
@@ -318,42 +465,60 @@ def main():
     tokens = wl.tokens_per_step * args.steps * world
     value = tokens / (r["ms"] / 1e3)
     peaks, peak_kind = measured_peaks()
-    step_bytes = wl.step_bytes()
-    n_launch = len(r["durs"])
-    # algorithmic bytes of each timed launch, aligned with the events
-    per_call = []
-    for _ in range(args.steps):
-        per_call.extend(step_bytes)
-    alg = sum(per_call)
-    dur_s = sum(r["durs"]) / 1e3
-    achieved = alg / dur_s / 1e9
+    calls = r["calls"]
+    alg_bytes = sum(wl.alg_bytes(T) for _, T in calls)
+    alg_flops = sum(wl.flops(T) for _, T in calls)
+    call_s = sum(c for c, _ in calls) / 1e3
+    # roofline: the bound is the resource whose time at peak is larger
+    bw = peaks["hbm_gbs"] * 1e9
+    if is_w8:
+        tensor_peak, tensor_unit = INT8_MMA_SYNC_TOPS * 1e12, "TOPS (measured mma.sync s8)"
+    else:
+        tensor_peak, tensor_unit = peaks["bf16_tflops"] * 1e12, "TFLOP/s"
+    t_mem, t_cmp = alg_bytes / bw, alg_flops / tensor_peak
+    path = "prefill" if (not is_w8 and getattr(wl, "T", 0) >= 1024) else "decode"
+    kernel = {"prefill": "prefill_kernel", "decode": "decode_kernel"}[path] if not is_w8 else "w8a8 pipeline"
+    if t_mem >= t_cmp:
+        achieved = alg_bytes / call_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = alg_flops / call_s / 1e12
+        peak = tensor_peak / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": tensor_unit,
+                "frac": achieved / peak}
+    Ts = sorted({T for _, T in calls})
+    tr = [kernel_traffic(kernel, T) for T in Ts]
+    roof["traffic"] = None if any(x is None for x in tr) else \
+        sum(kernel_traffic(kernel, T) for _, T in calls) / len(calls)
+    roof.update({"peak_kind": peak_kind, "kernel": kernel, "calls_timed": len(calls),
+                 "mean_call_us": 1e6 * call_s / len(calls),
+                 "algorithmic_bytes_per_call": alg_bytes / len(calls),
+                 "algorithmic_flops_per_call": alg_flops / len(calls)})
     line = {
         "metric": "tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded N(0,1) hidden, N(0,0.02) weights, gamma 1+N(0,0.1))",
         "config": dict(wl.describe(), parallelism=f"replicas x{world}" if world > 1 else "none",
-                       l2="weights rotated over %d copies (> 2x L2) so every call reads them from HBM" % wl.R),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "peak_kind": peak_kind, "kernel": "decode_kernel",
-                     "launches_timed": n_launch,
-                     "mean_launch_us": 1e3 * sum(r["durs"]) / n_launch},
+                       l2=("weights rotated over %d copies (> 2x L2) so every call reads them from HBM" % wl.R
+                           if getattr(wl, "flush", None) is None else
+                           "L2 flushed (2x L2 buffer written) between timed calls; flush time excluded")),
+        "roofline": roof,
         "gpu_launches": r["launches"],
         "clocks": r["clk"],
         "e2e": {"value": wl.tokens_per_step * r["e2e_steps"] * world / r["e2e_s"], "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
-    # per-point detail: mean launch time and roofline fraction of each sweep point
-    npts = len(wl.points)
-    detail = {}
-    for j, (b, s) in enumerate(wl.points):
-        ds = [r["durs"][k] for k in range(j, n_launch, npts)]
-        us = 1e3 * statistics.mean(ds)
-        detail[f"b{b}s{s}"] = {"T": b * s, "us": round(us, 3),
-                               "tokens_per_s": b * s / (us * 1e-6),
-                               "hbm_frac": wl.alg_bytes(b * s) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
-    line["per_point"] = detail
+    if len(wl.points) > 1:
+        npts = len(wl.points)
+        detail = {}
+        for j, (b, s_) in enumerate(wl.points):
+            ds = [calls[k][0] for k in range(j, len(calls), npts)]
+            us = 1e3 * statistics.mean(ds)
+            detail[f"b{b}s{s_}"] = {"T": b * s_, "us": round(us, 3), "tokens_per_s": b * s_ / (us * 1e-6),
+                                    "hbm_frac": wl.alg_bytes(b * s_) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+        line["per_point"] = detail
     if rank == 0 and not args.no_cpu_baseline:
         v, cores, sample = wl.cpu_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
