@@ -195,9 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     };
 
     const int nb8 = warp & 3, khalf = warp >> 2;
-    float acc[kMaxMT][4];
+    // acc[m] takes the first k16 step of each stage, acc2 the second for the
+    // first two m-tiles, so that small T still has two independent chains
+    float acc[kMaxMT][4], acc2[2][4];
 #pragma unroll
     for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) acc2[m][0] = acc2[m][1] = acc2[m][2] = acc2[m][3] = 0.f;
 
 #pragma unroll 1
     for (int s = 0; s < nst - 1; ++s) {
@@ -236,12 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             uint32_t a[4];
             ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchX + (kk * 16 + (lane >> 4) * 8) * 2, a[0],
                     a[1], a[2], a[3]);
-            mma16816<E::kBf16>(acc[m], a, b0, b1);
+            if (j == 1 && m < 2) mma16816<E::kBf16>(acc2[m], a, b0, b1);
+            else mma16816<E::kBf16>(acc[m], a, b0, b1);
           }
         }
       }
       if ((i % subs) == subs - 1) {
-        // unit done: fold the two k-halves, write the fp32 partial tile
+        // unit done: fold the chains and the two k-halves, write the fp32 partial tile
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          acc[m][0] += acc2[m][0]; acc[m][1] += acc2[m][1]; acc[m][2] += acc2[m][2]; acc[m][3] += acc2[m][3];
+          acc2[m][0] = acc2[m][1] = acc2[m][2] = acc2[m][3] = 0.f;
+        }
         const int u = cta + (i / subs) * G;
         const int kc = u / kNblkA, nb = u - kc * kNblkA;
         if (khalf == 1) {

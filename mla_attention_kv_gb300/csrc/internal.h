@@ -54,7 +54,7 @@ struct DecodeParams {
 
 // Rows x split-K chunks up to which every CTA reduces all partial rows itself
 // (one grid barrier) instead of one CTA per row plus a second barrier.
-constexpr int kSingleBarrierRowsTimesChunks = 32;
+constexpr int kSingleBarrierRowsTimesChunks = 16;
 
 struct DecodePlan {
   int grid;        // CTAs (cooperative, one per SM)

@@ -11,11 +11,17 @@
 //
 // Warp roles (192 threads):
 //   warp 0   TMA producer: hidden tile [128 x 64] and W_kva / W_kvb boxes
-//            [64 x 64], 128-byte swizzled, into a 2-stage (kv_a) and a
-//            3-stage (kv_b) shared-memory ring.
+//            [64 x 64], 128-byte swizzled, into shared-memory rings: 6
+//            stages for the k_pe pass, 2 for the compressed_kv pass, 3 for
+//            kv_b (all three reuse the same 224 KB at different times).
 //   warp 1   allocates 512 TMEM columns; one thread issues every MMA.
 //   warps 2-5 epilogue; warp w owns TMEM lanes 32*(w%4) .. +31, i.e. token
 //            rows of the tile, one row per thread.
+// CTAs run in clusters of two neighbouring tiles: every weight box is
+// fetched from L2 once per cluster and multicast into both CTAs' shared
+// memory (each CTA issues half of the boxes), which halves the L2 traffic
+// of the weight stream that bounds this kernel.  A stage is refilled only
+// when both CTAs' MMAs have released it (multicast tcgen05.commit).
 // Per tile:
 //   (a) k_pe pass: C[:, 512:576] = X * W_kva[:, 512:576] (N = 64), drained
 //       by the epilogue: RoPE (de-interleave + rotate_half) -> k_pe.
@@ -39,10 +45,15 @@ namespace mla {
 namespace {
 
 constexpr int kPfThreads = 192;
+constexpr int kCl = 2;                      // CTAs per cluster sharing every weight box
+constexpr uint16_t kClMask = 0x3;
 constexpr int kBM = 128;                    // token rows per tile
 constexpr int kBK = 64;                     // K elements per TMA box / stage
 constexpr uint32_t kA2Bytes = 8 * 16384;    // normalised tile: 8 K-chunks x [128 x 64]
-constexpr uint32_t kS1Bytes = 81920;        // kv_a stage: X 16 KB + W 64 KB
+constexpr uint32_t kS1Bytes = 81920;        // compressed_kv stage: X 16 KB + W 64 KB
+constexpr uint32_t kS0Base = kS1Bytes;      // k_pe stages: [80 KB, 224 KB)
+constexpr uint32_t kS0Bytes = 24576;        // k_pe stage: X 16 KB + W 8 KB
+constexpr int kS0Stages = 6;
 constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 tile
 constexpr uint32_t kS2Bytes = 32768;        // kv_b stage: [64 K x 256 N]
 constexpr int kS2Stages = 3;
@@ -51,6 +62,7 @@ constexpr uint32_t kGamBase = kBarBase + 256;                  // gamma [512], I
 constexpr uint32_t kSmemBytes = kGamBase + 1024 + 1024;        // + alignment slack
 
 struct PfShared {
+  uint64_t full0[kS0Stages], empty0[kS0Stages];
   uint64_t full1[2], empty1[2];
   uint64_t full2[kS2Stages], empty2[kS2Stages];
   uint64_t tfull[2], tempty[2];
@@ -107,18 +119,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   auto bar = [&](uint64_t* b) { return smem_u32(b); };
 
   if (threadIdx.x == 0) {
+    // empty barriers (and a2_free) count one MMA-commit arrival from each CTA
+    // of the cluster: a stage is refilled (by multicast) only when both
+    // CTAs have consumed it
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(&sh->full1[i]), 1);
-      mbar_init(bar(&sh->empty1[i]), 1);
+      mbar_init(bar(&sh->empty1[i]), kCl);
       mbar_init(bar(&sh->tfull[i]), 1);
       mbar_init(bar(&sh->tempty[i]), 128);
     }
     for (int i = 0; i < kS2Stages; ++i) {
       mbar_init(bar(&sh->full2[i]), 1);
-      mbar_init(bar(&sh->empty2[i]), 1);
+      mbar_init(bar(&sh->empty2[i]), kCl);
+    }
+    for (int i = 0; i < kS0Stages; ++i) {
+      mbar_init(bar(&sh->full0[i]), 1);
+      mbar_init(bar(&sh->empty0[i]), kCl);
     }
     mbar_init(bar(&sh->a2_ready), 128);
-    mbar_init(bar(&sh->a2_free), 1);
+    mbar_init(bar(&sh->a2_free), kCl);
     mbar_init(bar(&sh->mma_done), 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -131,35 +150,51 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   }
   tc::fence_before_sync();
   __syncthreads();
+  tc::cluster_sync();  // the peer's barriers are initialised before any multicast
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
+  const uint32_t crank = tc::cluster_rank();
+  // every CTA of a cluster runs the same number of tiles (tiles past the end
+  // are all-padding: TMA fills zeros and the epilogue stores nothing)
+  const int iters = (ntiles + (int)gridDim.x - 1) / (int)gridDim.x;
 
   if (warp == 0) {
     // ============================================================ TMA producer
     if (lane == 0) {
-      uint32_t u1 = 0, u2 = 0;  // uses of pipeline 1 / 2
+      uint32_t u0 = 0, u1 = 0, u2 = 0;  // uses of the k_pe / compressed_kv / kv_b rings
       int tiles_done = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
-        const int m0 = tile * kBM;
+      for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
+        const int m0 = (blockIdx.x + it * gridDim.x) * kBM;
         if (tiles_done > 0 && !pf_wait(bar(&sh->a2_free), (tiles_done - 1) & 1, abort, budget, p.status)) { ok = false; break; }
-        // (a) k_pe pass then (b) compressed_kv pass over the hidden dimension
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-          for (int kc = 0; kc < nk; ++kc, ++u1) {
-            const int s = u1 & 1;
-            if (!pf_wait(bar(&sh->empty1[s]), ((u1 >> 1) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
-            const uint32_t st = sbase + s * kS1Bytes;
-            const uint32_t fb = bar(&sh->full1[s]);
-            mbar_arrive_expect_tx(fb, pass == 0 ? 16384 + 8192 : 16384 + 65536);
-            tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
-            if (pass == 0) {
-              tma_load_2d(st + 16384, &args.tm_wa, kRank, kc * kBK, fb);
-            } else {
-              for (int j = 0; j < 8; ++j) tma_load_2d(st + 16384 + j * 8192, &args.tm_wa, j * 64, kc * kBK, fb);
-            }
-          }
+        // (a) k_pe pass: 6-stage ring of [X 16 KB | W 8 KB] in [80 KB, 224 KB)
+        for (int kc = 0; kc < nk && ok; ++kc, ++u0) {
+          const int s = u0 % kS0Stages;
+          if (!pf_wait(bar(&sh->empty0[s]), ((u0 / kS0Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
+          const uint32_t st = sbase + kS0Base + s * kS0Bytes;
+          const uint32_t fb = bar(&sh->full0[s]);
+          mbar_arrive_expect_tx(fb, 16384 + 8192);
+          tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
+          if ((u0 & 1) == crank) tma_load_2d_mc(st + 16384, &args.tm_wa, kRank, kc * kBK, fb, kClMask);
         }
         if (!ok) break;
+        // (b) compressed_kv pass: 2 stages of [X 16 KB | W 64 KB] in [0, 160 KB);
+        // stage 1 overlaps k_pe stages 0-3, so it waits for their last release
+        for (int kc = 0; kc < nk && ok; ++kc, ++u1) {
+          const int s = u1 & 1;
+          if (kc == 1) {
+            for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0 && ok; ++u)
+              if ((u % kS0Stages) < 4 && !pf_wait(bar(&sh->empty0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status)) ok = false;
+            if (!ok) break;
+          }
+          if (!pf_wait(bar(&sh->empty1[s]), ((u1 >> 1) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
+          const uint32_t st = sbase + s * kS1Bytes;
+          const uint32_t fb = bar(&sh->full1[s]);
+          mbar_arrive_expect_tx(fb, 16384 + 65536);
+          tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
+          for (int j = (int)crank; j < 8; j += kCl)
+            tma_load_2d_mc(st + 16384 + j * 8192, &args.tm_wa, j * 64, kc * kBK, fb, kClMask);
+        }
         // kv_a stages overlap the kv_b ring: wait until both were released
         for (int s = 0; s < 2 && ok; ++s) {
           const uint32_t last = (u1 - 1 - s);  // uses u1-1 and u1-2 cover both stages
@@ -173,11 +208,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             const uint32_t st = sbase + kS2Base + s * kS2Bytes;
             const uint32_t fb = bar(&sh->full2[s]);
             mbar_arrive_expect_tx(fb, kS2Bytes);
-            for (int q = 0; q < 4; ++q) tma_load_2d(st + q * 8192, &args.tm_wb, j * kHeadCols + q * 64, kc * kBK, fb);
+            for (int q = (int)crank; q < 4; q += kCl)
+              tma_load_2d_mc(st + q * 8192, &args.tm_wb, j * kHeadCols + q * 64, kc * kBK, fb, kClMask);
           }
         }
       }
       // drain: every issued load has landed before the CTA may exit
+      for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0; ++u)
+        pf_wait(bar(&sh->full0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status);
       for (uint32_t u = (u1 > 2 ? u1 - 2 : 0); u < u1; ++u)
         pf_wait(bar(&sh->full1[u & 1]), (u >> 1) & 1, abort, budget, p.status);
       for (uint32_t u = (u2 > kS2Stages ? u2 - kS2Stages : 0); u < u2; ++u)
@@ -189,7 +227,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       const bool bf = E::kBf16;
       const uint32_t id64 = tc::idesc_f16(bf, 128, 64, false, true);
       const uint32_t id256 = tc::idesc_f16(bf, 128, 256, false, true);
-      uint32_t u1 = 0, u2 = 0;
+      uint32_t u0 = 0, u1 = 0, u2 = 0;
       uint32_t wcount[2] = {0, 0}, dcount[2] = {0, 0};
       int tiles_done = 0;
       bool ok = true;
@@ -200,22 +238,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
         return true;
       };
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
+      for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
         // (a) k_pe into TMEM columns [0, 64)
         if (!drain_buf(0)) { ok = false; break; }
         tc::fence_after_sync();
-        for (int kc = 0; kc < nk; ++kc, ++u1) {
-          const int s = u1 & 1;
-          if (!pf_wait(bar(&sh->full1[s]), (u1 >> 1) & 1, abort, budget, p.status)) { ok = false; break; }
+        for (int kc = 0; kc < nk; ++kc, ++u0) {
+          const int s = u0 % kS0Stages;
+          if (!pf_wait(bar(&sh->full0[s]), (u0 / kS0Stages) & 1, abort, budget, p.status)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t st = sbase + s * kS1Bytes;
+          const uint32_t st = sbase + kS0Base + s * kS0Bytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = tc::sdesc_sw128(st + k * 32, 16, 1024);
             const uint64_t bd = tc::sdesc_sw128(st + 16384 + k * 2048, 8192, 1024);
             tc::mma_f16(tmem, ad, bd, id64, kc > 0 || k > 0);
           }
-          tc::commit(bar(&sh->empty1[s]));
+          tc::commit_mc(bar(&sh->empty0[s]), kClMask);
         }
         if (!ok) break;
         tc::commit(bar(&sh->tfull[0]));
@@ -237,7 +275,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
               tc::mma_f16(tmem + half * 256, ad, bd, id256, kc > 0 || k > 0);
             }
           }
-          tc::commit(bar(&sh->empty1[s]));
+          tc::commit_mc(bar(&sh->empty1[s]), kClMask);
         }
         if (!ok) break;
         tc::commit(bar(&sh->tfull[0]));  // the epilogue drains both halves, then signals a2_ready
@@ -259,14 +297,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
               const uint64_t bd = tc::sdesc_sw128(st + k * 2048, 8192, 1024);
               tc::mma_f16(tmem + b * 256, ad, bd, id256, kc > 0 || k > 0);
             }
-            tc::commit(bar(&sh->empty2[s]));
+            tc::commit_mc(bar(&sh->empty2[s]), kClMask);
           }
           if (!ok) break;
           tc::commit(bar(&sh->tfull[b]));
           ++wcount[b];
         }
         if (!ok) break;
-        tc::commit(bar(&sh->a2_free));
+        tc::commit_mc(bar(&sh->a2_free), kClMask);
       }
       // every MMA issued so far has completed before TMEM is released
       tc::commit(bar(&sh->mma_done));
@@ -287,8 +325,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     uint32_t uf[2] = {0, 0};
     int tiles_done = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tiles_done) {
-      const int t = tile * kBM + r;
+    for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
+      const int t = (blockIdx.x + it * gridDim.x) * kBM + r;
       const bool live = t < ntok;
       const int bi = live ? t / p.s : 0, si = live ? t - bi * p.s : 0;
       // (a) k_pe: RoPE on the 64 raw columns
@@ -410,6 +448,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+  // no CTA leaves while its peer may still multicast into it or arrive on it
+  tc::cluster_sync();
 }
 
 }  // namespace
@@ -437,12 +477,21 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int ntiles = (p.T + kBM - 1) / kBM;
-  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  const int max_grid = num_sms / kCl * kCl;
+  int grid = (ntiles + kCl - 1) / kCl * kCl;
+  if (grid > max_grid) grid = max_grid;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPfThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* kargs[] = {&a};
   e = cudaLaunchKernelExC(&cfg, fn, kargs);
   if (e == cudaSuccess) *launches = 1;

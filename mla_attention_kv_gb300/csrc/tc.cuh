@@ -81,6 +81,26 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                : "memory");
 }
 
+// Arrive (once) on the mbarrier at the same shared-memory offset in every
+// CTA of `mask` (cluster) when every MMA issued so far has completed.
+__device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Whole-cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMEM loads
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
 // (quadrant base + i), columns [col, col+32).

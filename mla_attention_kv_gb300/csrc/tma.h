@@ -26,6 +26,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar)
       : "memory");
 }
+// Tiled 2-D load of one box into the same shared-memory offset of every
+// CTA in `mask` (this GPU's own memory, thread-block cluster multicast);
+// each destination CTA's mbarrier at `bar`'s offset receives the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c_inner,
+                                               int c_outer, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+      "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar), "h"(mask)
+      : "memory");
+}
 // L2 prefetch of one box (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c_inner, int c_outer) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(map),
