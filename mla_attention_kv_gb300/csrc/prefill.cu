@@ -79,6 +79,10 @@ struct PfArgs {
   PrefillParams p;
 };
 
+// (A wait on a TMA full barrier needs no tcgen05 fence: the mbarrier
+// already orders the async-proxy shared-memory writes before the MMAs that
+// read them.  tcgen05.fence::after_thread_sync is only issued where TMEM
+// written or read by another thread is reused.)
 // Bounded mbarrier wait shared by all roles; gives up on the time budget
 // or when another role has already given up.
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -227,6 +231,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       const bool bf = E::kBf16;
       const uint32_t id64 = tc::idesc_f16(bf, 128, 64, false, true);
       const uint32_t id256 = tc::idesc_f16(bf, 128, 256, false, true);
+      // base descriptors at shared-memory offset 0: K-major A (SW128, SBO
+      // 1024) and MN-major B (SW128, LBO 8192 between 64-column groups)
+      const uint64_t dA0 = tc::sdesc_sw128(sbase, 16, 1024);
+      const uint64_t dB0 = tc::sdesc_sw128(sbase, 8192, 1024);
       uint32_t u0 = 0, u1 = 0, u2 = 0;
       uint32_t wcount[2] = {0, 0}, dcount[2] = {0, 0};
       int tiles_done = 0;
@@ -245,14 +253,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         for (int kc = 0; kc < nk; ++kc, ++u0) {
           const int s = u0 % kS0Stages;
           if (!pf_wait(bar(&sh->full0[s]), (u0 / kS0Stages) & 1, abort, budget, p.status)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t st = sbase + kS0Base + s * kS0Bytes;
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = tc::sdesc_sw128(st + k * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(st + 16384 + k * 2048, 8192, 1024);
-            tc::mma_f16(tmem, ad, bd, id64, kc > 0 || k > 0);
-          }
+          // descriptors advance by constant adds (address field in 16-byte units)
+          const uint64_t ad = dA0 + (uint64_t)((kS0Base + s * kS0Bytes) >> 4);
+          const uint64_t bd = dB0 + (uint64_t)((kS0Base + s * kS0Bytes + 16384) >> 4);
+          tc::mma_f16(tmem, ad, bd, id64, kc > 0);
+          tc::mma_f16(tmem, ad + 2, bd + 128, id64, true);
+          tc::mma_f16(tmem, ad + 4, bd + 256, id64, true);
+          tc::mma_f16(tmem, ad + 6, bd + 384, id64, true);
           tc::commit_mc(bar(&sh->empty0[s]), kClMask);
         }
         if (!ok) break;
@@ -264,16 +271,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         for (int kc = 0; kc < nk; ++kc, ++u1) {
           const int s = u1 & 1;
           if (!pf_wait(bar(&sh->full1[s]), (u1 >> 1) & 1, abort, budget, p.status)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t st = sbase + s * kS1Bytes;
+          const uint64_t ad = dA0 + (uint64_t)((s * kS1Bytes) >> 4);
+          const uint64_t bd = dB0 + (uint64_t)((s * kS1Bytes + 16384) >> 4);
+          const bool acc = kc > 0;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = tc::sdesc_sw128(st + k * 32, 16, 1024);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const uint64_t bd = tc::sdesc_sw128(st + 16384 + half * 32768 + k * 2048, 8192, 1024);
-              tc::mma_f16(tmem + half * 256, ad, bd, id256, kc > 0 || k > 0);
-            }
+            tc::mma_f16(tmem, ad + 2 * k, bd + 128 * k, id256, acc || k > 0);
+            tc::mma_f16(tmem + 256, ad + 2 * k, bd + (32768 >> 4) + 128 * k, id256, acc || k > 0);
           }
           tc::commit_mc(bar(&sh->empty1[s]), kClMask);
         }
@@ -289,14 +293,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           for (int kc = 0; kc < kRank / kBK; ++kc, ++u2) {
             const int s = u2 % kS2Stages;
             if (!pf_wait(bar(&sh->full2[s]), (u2 / kS2Stages) & 1, abort, budget, p.status)) { ok = false; break; }
-            tc::fence_after_sync();
-            const uint32_t st = sbase + kS2Base + s * kS2Bytes;
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = tc::sdesc_sw128(sbase + kc * 16384 + k * 32, 16, 1024);
-              const uint64_t bd = tc::sdesc_sw128(st + k * 2048, 8192, 1024);
-              tc::mma_f16(tmem + b * 256, ad, bd, id256, kc > 0 || k > 0);
-            }
+            const uint64_t ad = dA0 + (uint64_t)((kc * 16384) >> 4);
+            const uint64_t bd = dB0 + (uint64_t)((kS2Base + s * kS2Bytes) >> 4);
+            const uint32_t d = tmem + b * 256;
+            tc::mma_f16(d, ad, bd, id256, kc > 0);
+            tc::mma_f16(d, ad + 2, bd + 128, id256, true);
+            tc::mma_f16(d, ad + 4, bd + 256, id256, true);
+            tc::mma_f16(d, ad + 6, bd + 384, id256, true);
             tc::commit_mc(bar(&sh->empty2[s]), kClMask);
           }
           if (!ok) break;
