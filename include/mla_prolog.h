@@ -202,10 +202,10 @@ mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1
  * host that owns all device memory in an arena planned up front, or a
  * latency-critical caller that cannot risk a blocking or failing
  * cudaMalloc mid-run.  It runs the fused decode kernel of
- * mla_kv_prolog_run (T = b*s rows, any T, in chunks of 64 rows) with the
+ * mla_kv_prolog_run (T = b*s rows, any T, in chunks of 64 or 128 rows) with the
  * same arguments, but needs no handle: its scratch (split-K partials,
  * latent rows, barrier counters, status word) is one fixed __device__
- * array inside the library, about 2.3 MB, held by every device that loads
+ * array inside the library, about 4.8 MB, held by every device that loads
  * the library until the process exits.  It calls no cudaMalloc, cudaFree
  * or allocating library routine.
  *   cfg            model dimensions as for create; quant must be NONE

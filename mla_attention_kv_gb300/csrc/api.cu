@@ -239,9 +239,10 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
-  for (long long t0 = 0; t0 < T; t0 += kDecodeMaxTokens) {
+  const int tt = h->dplan.tt_max;
+  for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
-    p.TT = (int)((T - t0) < kDecodeMaxTokens ? (T - t0) : kDecodeMaxTokens);
+    p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
     cudaError_t e = decode_launch(bf16, h->dplan, p, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_launches += 1;

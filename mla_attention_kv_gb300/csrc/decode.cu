@@ -15,6 +15,8 @@
 //            (b) cp.async copies of its kv_a tile and of the hidden columns
 //            that tile needs, (c) gamma and the cos/sin row of the token row
 //            it owns.
+//            (kDecodeMaxTokens is the upper bound; the plan picks 128 rows
+//            per launch when the W_kvb slice fits in shared memory, else 64)
 //   phase A  kv_a_proj split-K: tile = (KB rows x 32 columns) of W_kva;
 //            tokens are the M side of mma.sync m16n8k16 (fp32 accumulate);
 //            the CTA writes fp32 partial sums [KC, T, 576] to the workspace.
@@ -558,8 +560,10 @@ const void* kernel_for(int maxp) {
 
 }  // namespace
 
-bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
-  if (hidden % 64 != 0 || heads < 1 || num_sms < kDecodeMaxTokens) return false;
+// Shared-memory plan for `tt` token rows per launch; false if it cannot be
+// laid out (or, with `resident_only`, if W_kvb would have to be streamed).
+static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_sms,
+                     DecodePlan* plan) {
   const int G = num_sms;
   // split-K of kv_a: the smallest KB (multiple of 64 dividing hidden) with
   // at most one (KB x 32-column) tile per CTA
@@ -576,13 +580,13 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   const int ngmax = (NG + G - 1) / G;
   const int ngbox = ngmax | 1;            // odd 16-byte chunks per row: conflict-free ldmatrix
   if (ngbox * 8 > 256) return false;      // TMA box inner extent
-  const int maxp = (kMaxMT * ngmax + kWarps - 1) / kWarps;
+  const int maxp = ((tt / 16) * ngmax + kWarps - 1) / kWarps;
   if (maxp > 16) return false;
   const int pitchB = ngbox * 16;
   const int subs = KB / kSubK;
-  const int stageA = kSubK * kPitchWA + kDecodeMaxTokens * kPitchX;
+  const int stageA = kSubK * kPitchWA + tt * kPitchX;
   const int nstA = subs < 4 ? (subs < 2 ? 2 : subs) : 4;
-  const int nrm_bytes = kDecodeMaxTokens * kPitchN;
+  const int nrm_bytes = tt * kPitchN;
   const int fixed = kRedBytes + kMiscBytes + 256;
   // Region A holds the phase-A ring, later the latent rows plus (when the
   // W_kvb slice does not fit) two stream buffers; the rest of the budget
@@ -594,12 +598,14 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   if (kpre >= kRank) {
     kpre = kRank;
   } else {
+    if (resident_only) return false;
     if (regionA < nrm_bytes + 2 * kWkvbBoxRows * pitchB) regionA = nrm_bytes + 2 * kWkvbBoxRows * pitchB;
     kpre = (kSmemBudget - fixed - regionA) / pitchB / kWkvbBoxRows * kWkvbBoxRows;
     kchunk = (regionA - nrm_bytes) / (2 * pitchB) / kWkvbBoxRows * kWkvbBoxRows;
     if (kpre < 0 || kchunk < kWkvbBoxRows) return false;
   }
   plan->grid = G;
+  plan->tt_max = tt;
   plan->KB = KB;
   plan->KC = KC;
   plan->kpre = kpre;
@@ -615,6 +621,15 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   if (plan->smem > (size_t)kSmemBudget) return false;
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
   return true;
+}
+
+bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
+  if (hidden % 64 != 0 || heads < 1) return false;
+  // 128 rows per launch when the whole W_kvb slice still stays resident
+  // (V2-Lite), else 64 (R1 streams part of its slice)
+  if (num_sms >= kDecodeMaxTokens && plan_for(kDecodeMaxTokens, true, hidden, heads, num_sms, plan))
+    return true;
+  return num_sms >= 64 && plan_for(64, false, hidden, heads, num_sms, plan);
 }
 
 cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p0,

@@ -22,8 +22,9 @@ constexpr int kV = 128;            // v_head_dim
 constexpr int kHeadCols = kNope + kV;  // kv_b_proj columns per head (256)
 
 // ---------------------------------------------------------------- decode path
-// Token rows per decode launch (larger T is processed in chunks).
-constexpr int kDecodeMaxTokens = 64;
+// Upper bound of token rows per decode launch (larger T is processed in
+// chunks of the plan's tt_max); also the row stride of the workspace.
+constexpr int kDecodeMaxTokens = 128;
 
 struct DecodeParams {
   CUtensorMap tmap_wkvb;    // W_kvb [512, H*256], box = (ngbox*8 columns, 32 rows)
@@ -58,6 +59,7 @@ constexpr int kSingleBarrierRowsTimesChunks = 16;
 
 struct DecodePlan {
   int grid;        // CTAs (cooperative, one per SM)
+  int tt_max;      // token rows per launch (64 or 128)
   int KB, KC;      // split-K of kv_a
   int kpre, kchunk, nstA, ngbox, maxp;
   int off_wb, off_a, off_red, off_misc;

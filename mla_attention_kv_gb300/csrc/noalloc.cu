@@ -10,7 +10,7 @@
 // latent rows, the grid-barrier counters and the status word) lives in one
 // file-scope __device__ array that is part of the loaded library.  Every
 // device that loads the library holds this array (kScratchBytes, about
-// 2.3 MB) until the process exits.
+// 4.8 MB) until the process exits.
 //
 // Rules that follow from sharing one array:
 //   - All calls on a device share the array and see what the previous call
@@ -135,9 +135,10 @@ extern "C" mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, in
   p.hidden_dim = c.hidden; p.heads = c.num_heads; p.s = s; p.max_pos = c.max_pos;
   p.eps = c.eps; p.budget_ns = c.spin_budget_ns ? c.spin_budget_ns : 1000000000ull;
   const bool bf16 = c.dtype == MLA_BF16;
-  for (long long t0 = 0; t0 < T; t0 += kDecodeMaxTokens) {
+  const int tt = plan.tt_max;
+  for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
-    p.TT = (int)((T - t0) < kDecodeMaxTokens ? (T - t0) : kDecodeMaxTokens);
+    p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
     e = decode_launch(bf16, plan, p, stream);
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   }

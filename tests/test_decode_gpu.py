@@ -74,10 +74,24 @@ def test_r1_decode(oracle_mod):
     assert r["status"] == 0
 
 
-@pytest.mark.parametrize("T", [3, 15, 17, 63, 64, 65, 129, 200])
+def rows_per_launch(cfg):
+    """Token rows one decode launch takes: 128 when the CTA's whole W_kvb
+    slice stays resident in shared memory (V2-Lite on a GPU with at least
+    128 SMs), else 64."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 128 if (cfg["num_heads"] <= 16 and sms >= 128) else 64
+
+
+@pytest.mark.parametrize("T", [3, 15, 17, 63, 64, 65, 127, 128, 129, 200, 256, 257])
 def test_ragged_token_counts(oracle_mod, T):
     r = run_case(I.V2_LITE, T, 1, 500 + T, oracle_mod=oracle_mod)
-    assert r["launches"] == (T + 63) // 64
+    tt = rows_per_launch(I.V2_LITE)
+    assert r["status"] == 0 and r["launches"] == (T + tt - 1) // tt
+
+
+def test_r1_ragged_two_launches(oracle_mod):
+    r = run_case(I.R1, 65, 1, I.seed_for(3, 65), oracle_mod=oracle_mod)
+    assert r["status"] == 0 and r["launches"] == 2
 
 
 @pytest.mark.parametrize("H,hidden,dtype", [(1, 64, "fp16"), (3, 192, "bf16"), (5, 640, "fp16"),
