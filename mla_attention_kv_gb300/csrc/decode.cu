@@ -48,7 +48,9 @@ constexpr int kPitchN = 1040;      // smem row pitch of a 512-column latent row
 constexpr int kMaxMT = kDecodeMaxTokens / 16;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kRedBytes = 16384;   // cross-warp reduction scratch (<= 32 chains x 512 B)
-constexpr int kMiscBytes = 2048;   // gamma + cos/sin row
+constexpr int kMiscBytes = 2048;   // gamma, cos/sin row, mbarriers, flag
+constexpr int kMaxStagesA = 16;    // deepest phase-A cp.async ring
+constexpr int kMaxStreamBufs = 6;  // W_kvb chunk buffers (mbarriers at misc + 1544 ..)
 
 __device__ __forceinline__ int col_group_begin(int cta, int ngroups, int grid) {
   return (int)(((long long)cta * ngroups) / grid);
@@ -113,14 +115,17 @@ __device__ __forceinline__ void bar_exit_finish(unsigned* counters, unsigned old
   }
 }
 
-template <typename T, int MAXP>
+template <typename T, int IM, int QM>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int TT = p.TT;
-  const int MT = (TT + 15) >> 4;
+  // m-tiles of 16 rows, rounded up to a power of two so that the phase-B
+  // warp grid covers them exactly (padding rows are zero)
+  int MT = 1;
+  while (MT * 16 < TT) MT *= 2;
   const int rows_x = MT * 16;
   const int H = p.heads;
   const int NB = H * kHeadCols;      // kv_b columns
@@ -144,13 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   // ---- start: mbarriers, resident W_kvb rows (TMA), L2 prefetch of the rest
   const uint32_t bar_res = smem_u32(smem + p.off_misc + 1536);
-  const uint32_t bar_s0 = bar_res + 8;  // streamed chunk buffers 0 / 1
+  const uint32_t bar_s0 = bar_res + 8;  // streamed chunk buffers 0 .. kMaxStreamBufs-1
   int* sFlag = reinterpret_cast<int*>(smem + p.off_misc + 1600);
   if (tid == 0) {
     tma_prefetch_desc(&p.tmap_wkvb);
     mbar_init(bar_res, 1);
-    mbar_init(bar_s0, 1);
-    mbar_init(bar_s0 + 8, 1);
+    for (int i = 0; i < kMaxStreamBufs; ++i) mbar_init(bar_s0 + 8 * i, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -175,7 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int my_units = (units > cta) ? (units - cta + G - 1) / G : 0;
     const int nsub = my_units * subs;
     const int stage_bytes = kSubK * kPitchWA + rows_x * kPitchX;
-    const int nst = p.nstA;
+    // as many stages in flight as the phase-A region holds at this row
+    // count (all of them for small T), at least the plan's depth
+    int nst = (p.off_red - p.off_a) / stage_bytes;
+    if (nst > subs + 1) nst = subs + 1;
+    if (nst > kMaxStagesA) nst = kMaxStagesA;
+    if (nst < p.nstA) nst = p.nstA;
     if (nsub == 0 && tid == 0) issue_wkvb();
 
     auto load_sub = [&](int i) {
@@ -285,33 +294,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     __syncthreads();
   }
 
-  // ---- streamed W_kvb rows [kpre, 512): TMA into two chunk buffers in the
-  // freed phase-A region, behind the latent rows (they land during the barrier)
+  // ---- streamed W_kvb rows [kpre, 512): TMA into chunk buffers in the
+  // freed phase-A region, behind the latent rows (they land during the
+  // barrier); as many buffers as fit at this launch's row count
   const int nrm_bytes = rows_x * kPitchN;
   unsigned char* sN = sA;
   unsigned char* sWS = sA + nrm_bytes;
   const int nstream = kRank - p.kpre;
   const int nchunks = (ng > 0 && nstream > 0) ? (nstream + p.kchunk - 1) / p.kchunk : 0;
+  int nbuf = (p.off_red - p.off_a - nrm_bytes) / (p.kchunk * pitchB);
+  if (nbuf > kMaxStreamBufs) nbuf = kMaxStreamBufs;
+  if (nbuf < 2) nbuf = 2;  // the plan reserves two at the largest row count
   auto issue_chunk = [&](int c) {  // thread 0 only
     const int r0 = p.kpre + c * p.kchunk;
     const int nr = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
-    const uint32_t bar = bar_s0 + 8 * (c & 1);
-    const uint32_t dst = smem_u32(sWS + (c & 1) * p.kchunk * pitchB);
+    const uint32_t bar = bar_s0 + 8 * (c % nbuf);
+    const uint32_t dst = smem_u32(sWS + (c % nbuf) * p.kchunk * pitchB);
     mbar_arrive_expect_tx(bar, (uint32_t)(nr * pitchB));
     for (int r = 0; r < nr; r += kWkvbBoxRows)
       tma_load_2d(dst + r * pitchB, &p.tmap_wkvb, col0, r0 + r, bar);
   };
-  if (tid == 0) {
-    if (nchunks > 0) issue_chunk(0);
-    if (nchunks > 1) issue_chunk(1);
-  }
-  int issued = nchunks < 2 ? nchunks : 2;
-  // on an early exit, wait (bounded) for this CTA's copies still in flight
+  int issued = nchunks < nbuf ? nchunks : nbuf;
+  if (tid == 0)
+    for (int c = 0; c < issued; ++c) issue_chunk(c);
+  int waited = 0;  // chunks whose arrival this CTA has observed
+  // on an early exit, wait (bounded) for this CTA's copies still in flight:
+  // the resident rows and every issued chunk not yet observed (at most one
+  // outstanding phase per buffer)
   auto drain = [&]() {
     cp_async_wait<0>();
     if (tid == 0) {
       mbar_wait_bounded(bar_res, 0, p.budget_ns);
-      for (int c = 0; c < issued && c < 2; ++c) mbar_wait_bounded(bar_s0 + 8 * c, 0, p.budget_ns);
+      for (int c = waited; c < issued; ++c)
+        mbar_wait_bounded(bar_s0 + 8 * (c % nbuf), (c / nbuf) & 1, p.budget_ns);
     }
     __syncthreads();
   };
@@ -430,29 +445,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     bar_exit_finish(p.counters, exit_old, G);
     return;
   }
-  // Work: npairs (m-tile, 8-column group) output tiles x 32 k16 steps.  Each
-  // pair's steps are split into kslices interleaved slices so that every
-  // warp carries up to MAXP independent accumulator chains (mma.sync is
-  // latency-bound on one chain); slices are summed through shared memory.
-  const int npairs = MT * ng;
-  int kslices = 1;
-  while (kslices < 8 && npairs * kslices * 2 <= kWarps * (MAXP < 4 ? MAXP : 4)) kslices *= 2;
-  const int nchains = npairs * kslices;
-  float acc[MAXP][4];
+  // Work: MT m-tiles x ng 8-column groups x 32 k16 steps.  The warps form a
+  // (wm x wn) grid: a warp takes the IM = MT / wm m-tiles {mw, mw + wm, ...}
+  // and every wn-th of the ng * ks (group, k-slice) items, so one latent
+  // fragment per k16 step serves all of the warp's groups and each W_kvb
+  // fragment is read by wm warps only (shared-memory bandwidth, not the
+  // tensor pipe, bounds this loop).  ks divides wn, so all items of a warp
+  // share one k-slice and the warp only walks its own steps; the slices of
+  // an output tile are summed through shared memory.
+  const int wm = p.pb_wm, wn = kWarps / wm, ks = p.pb_ks;
+  const int mw = warp % wm, wr = warp / wm;
+  const int myslice = wr % ks;
+  const int nitems = ng * ks;
+  float acc[IM * QM][4];
 #pragma unroll
-  for (int q = 0; q < MAXP; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+  for (int q = 0; q < IM * QM; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
   const uint32_t nrm_u = smem_u32(sN);
-  // per chain: A-row and B-column offsets and its k-slice
-  uint32_t aoff[MAXP], boff[MAXP];
-  int kslc[MAXP];
+  uint32_t aoff[IM], boff[QM];
+  bool qv[QM];
 #pragma unroll
-  for (int q = 0; q < MAXP; ++q) {
-    const int ch = warp + q * kWarps;
-    const int pr = ch / kslices;
-    kslc[q] = ch < nchains ? ch - pr * kslices : -1;
-    const int m = pr % MT, gi = pr / MT;
-    aoff[q] = (uint32_t)(m * 16 * kPitchN);
-    boff[q] = (uint32_t)(gi * 16);
+  for (int i = 0; i < IM; ++i) aoff[i] = (uint32_t)((mw + i * wm) * 16 * kPitchN);
+#pragma unroll
+  for (int q = 0; q < QM; ++q) {
+    const int j = wr + q * wn;
+    qv[q] = j < nitems;
+    boff[q] = (uint32_t)((j / ks) * 16);
   }
 
   // K rows are consumed in chunks: the resident rows, then streamed chunks
@@ -471,91 +488,110 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (c >= 0) {
       const int r0 = p.kpre + c * p.kchunk;
       krows = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
-      wchunk = smem_u32(sWS + (c & 1) * p.kchunk * pitchB);
-      if (!mbar_wait_cta(bar_s0 + 8 * (c & 1), (c >> 1) & 1, p.budget_ns, sFlag)) {
+      wchunk = smem_u32(sWS + (c % nbuf) * p.kchunk * pitchB);
+      if (!mbar_wait_cta(bar_s0 + 8 * (c % nbuf), (c / nbuf) & 1, p.budget_ns, sFlag)) {
         if (tid == 0) atomicOr(p.status, kStatusTimeout);
         drain();
         bar_exit_finish(p.counters, exit_old, G);
         return;
       }
+      waited = c + 1;
     }
     const int steps = krows / 16;
     const int gs0 = kbase / 16;
-    // kslices divides the warp count, so all chains of a warp share one slice
-    const int myslice = warp % kslices;
-    const int st0 = ((myslice - gs0 % kslices) + kslices) % kslices;
+    const int st0 = ((myslice - gs0 % ks) + ks) % ks;
 #pragma unroll 1
-    for (int st = st0; st < steps; st += kslices) {
+    for (int st = st0; st < steps; st += ks) {
       const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchB;
       const uint32_t arow = nrm_u + (lane & 15) * kPitchN + ((kbase + st * 16) + (lane >> 4) * 8) * 2;
+      uint32_t a[IM][4];
 #pragma unroll
-      for (int q = 0; q < MAXP; ++q) {
-        if (kslc[q] >= 0) {
-          uint32_t b0, b1, a[4];
+      for (int i = 0; i < IM; ++i) ldsm_x4(arow + aoff[i], a[i][0], a[i][1], a[i][2], a[i][3]);
+#pragma unroll
+      for (int q = 0; q < QM; ++q) {
+        if (qv[q]) {
+          uint32_t b0, b1;
           ldsm_x2_trans(wrow + boff[q], b0, b1);
-          ldsm_x4(arow + aoff[q], a[0], a[1], a[2], a[3]);
-          mma16816<E::kBf16>(acc[q], a, b0, b1);
+#pragma unroll
+          for (int i = 0; i < IM; ++i) mma16816<E::kBf16>(acc[q * IM + i], a[i], b0, b1);
         }
       }
     }
     kbase += krows;
-    if (c >= 0 && c + 2 < nchunks) {
-      __syncthreads();  // every warp is done with buffer c & 1
-      if (tid == 0) issue_chunk(c + 2);
-      issued = c + 3;
+    if (c >= 0 && c + nbuf < nchunks) {
+      __syncthreads();  // every warp is done with buffer c % nbuf
+      if (tid == 0) issue_chunk(c + nbuf);
+      issued = c + nbuf + 1;
     }
   }
   bar_exit_finish(p.counters, exit_old, G);
 
-  // ---- epilogue: sum the k-slices of each pair, split + head-major stores
-  T* kn = static_cast<T*>(p.k_nope);
-  T* vv = static_cast<T*>(p.value);
-  auto store_pair = [&](int pr, const float* v) {
-    const int m = pr % MT, gi = pr / MT;
-    const int j = col0 + gi * 8 + 2 * (lane & 3);
-    const int hh = j / kHeadCols, e = j % kHeadCols;
-    T* base = (e < kNope) ? kn : vv;
-    const int ee = (e < kNope) ? e : e - kNope;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = m * 16 + (lane >> 2) + half * 8;
-      if (r < TT) {
-        const int tg = p.t0 + r;
-        const int bi = tg / p.s, si = tg - bi * p.s;
-        T* dst = base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee;
-        *reinterpret_cast<uint32_t*>(dst) = E::pack(v[2 * half], v[2 * half + 1]);
-      }
-    }
+  // ---- epilogue: the [rows_x, ng * 8] output tile goes to shared memory in
+  // the I/O dtype (the W_kvb area is free once every warp is past the loop),
+  // then out with 16-byte stores: each 8-column group lies inside one head's
+  // k_nope or value half, so consecutive threads write consecutive 16 bytes
+  // of the head-major outputs (split, step 5; assemble, step 7).
+  __syncthreads();
+  unsigned char* sO = sWB;
+  auto put = [&](int m, int gi, const float* v) {
+    const int r = m * 16 + (lane >> 2);
+    unsigned char* d = sO + r * pitchB + gi * 16 + (lane & 3) * 4;
+    *reinterpret_cast<uint32_t*>(d) = E::pack(v[0], v[1]);
+    *reinterpret_cast<uint32_t*>(d + 8 * pitchB) = E::pack(v[2], v[3]);
   };
-  if (kslices == 1) {
+  if (ks == 1) {
 #pragma unroll
-    for (int q = 0; q < MAXP; ++q)
-      if (kslc[q] >= 0) store_pair(warp + q * kWarps, acc[q]);
+    for (int q = 0; q < QM; ++q)
+      if (qv[q]) {
+#pragma unroll
+        for (int i = 0; i < IM; ++i) put(mw + i * wm, wr + q * wn, acc[q * IM + i]);
+      }
   } else {
-    // chains -> shared memory, then one warp per pair sums its slices
-    __syncthreads();
+    // tile (m, gi) is pair gi * MT + m; its ks slices are summed in order
 #pragma unroll
-    for (int q = 0; q < MAXP; ++q) {
-      const int ch = warp + q * kWarps;
-      if (ch < nchains)
-        *reinterpret_cast<float4*>(sRed + (ch * 32 + lane) * 4) = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-    }
+    for (int q = 0; q < QM; ++q)
+      if (qv[q]) {
+#pragma unroll
+        for (int i = 0; i < IM; ++i) {
+          const int pr = ((wr + q * wn) / ks) * MT + mw + i * wm;
+          *reinterpret_cast<float4*>(sRed + ((pr * ks + myslice) * 32 + lane) * 4) =
+              make_float4(acc[q * IM + i][0], acc[q * IM + i][1], acc[q * IM + i][2], acc[q * IM + i][3]);
+        }
+      }
     __syncthreads();
-    for (int pr = warp; pr < npairs; pr += kWarps) {
+    for (int pr = warp; pr < MT * ng; pr += kWarps) {
       float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ks = 0; ks < kslices; ++ks) {
-        const float4 o = *reinterpret_cast<const float4*>(sRed + ((pr * kslices + ks) * 32 + lane) * 4);
+      for (int k = 0; k < ks; ++k) {
+        const float4 o = *reinterpret_cast<const float4*>(sRed + ((pr * ks + k) * 32 + lane) * 4);
         v[0] += o.x; v[1] += o.y; v[2] += o.z; v[3] += o.w;
       }
-      store_pair(pr, v);
+      put(pr % MT, pr / MT, v);
     }
+  }
+  __syncthreads();
+  T* kn = static_cast<T*>(p.k_nope);
+  T* vv = static_cast<T*>(p.value);
+  for (int idx = tid; idx < TT * ng; idx += kThreads) {
+    const int r = idx / ng, gi = idx - r * ng;
+    const int j = col0 + gi * 8;
+    const int hh = j / kHeadCols, e = j - hh * kHeadCols;
+    T* base = (e < kNope) ? kn : vv;
+    const int ee = (e < kNope) ? e : e - kNope;
+    const int tg = p.t0 + r;
+    const int bi = tg / p.s, si = tg - bi * p.s;
+    *reinterpret_cast<uint4*>(base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee) =
+        *reinterpret_cast<const uint4*>(sO + r * pitchB + gi * 16);
   }
 }
 
+// Phase-B register tiles: IM m-tiles x QM column groups per warp.
+constexpr int kVariants[3][2] = {{1, 4}, {1, 8}, {2, 8}};
+
 template <typename T>
-const void* kernel_for(int maxp) {
-  if (maxp <= 4) return (const void*)decode_kernel<T, 4>;
-  return (const void*)decode_kernel<T, 16>;
+const void* kernel_for(int variant) {
+  if (variant == 0) return (const void*)decode_kernel<T, 1, 4>;
+  if (variant == 1) return (const void*)decode_kernel<T, 1, 8>;
+  return (const void*)decode_kernel<T, 2, 8>;
 }
 
 }  // namespace
@@ -580,8 +616,10 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   const int ngmax = (NG + G - 1) / G;
   const int ngbox = ngmax | 1;            // odd 16-byte chunks per row: conflict-free ldmatrix
   if (ngbox * 8 > 256) return false;      // TMA box inner extent
-  const int maxp = ((tt / 16) * ngmax + kWarps - 1) / kWarps;
-  if (maxp > 16) return false;
+  for (int mt = 1; mt <= tt / 16; mt *= 2) {
+    int v, wm, ks;
+    if (!decode_phase_b(mt, ngmax, &v, &wm, &ks)) return false;
+  }
   const int pitchB = ngbox * 16;
   const int subs = KB / kSubK;
   const int stageA = kSubK * kPitchWA + tt * kPitchX;
@@ -612,15 +650,43 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   plan->kchunk = kchunk;
   plan->nstA = nstA;
   plan->ngbox = ngbox;
-  plan->maxp = maxp;
+  plan->ngmax = ngmax;
   plan->off_wb = 0;
   plan->off_a = (kpre * pitchB + 127) / 128 * 128;
   plan->off_red = plan->off_a + (regionA + 127) / 128 * 128;
   plan->off_misc = plan->off_red + kRedBytes;
   plan->smem = (size_t)plan->off_misc + kMiscBytes;
   if (plan->smem > (size_t)kSmemBudget) return false;
+  if (kpre < tt) return false;  // the output tile is staged in the W_kvb area
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
   return true;
+}
+
+bool decode_phase_b(int mt, int ngmax, int* variant, int* wm_out, int* ks_out) {
+  // cost: mma.sync per warp on the critical path, with fewer than three
+  // independent chains counted as three (latency), then fewer slices
+  // (less reduction), then the smaller register tile
+  long best = -1;
+  for (int v = 0; v < 3; ++v) {
+    const int IM = kVariants[v][0], QM = kVariants[v][1];
+    if (mt % IM != 0 || mt / IM > kWarps) continue;
+    const int wm = mt / IM, wn = kWarps / wm;
+    for (int ks = 1; ks <= 8; ks *= 2) {
+      if (wn % ks != 0) continue;
+      const int per = (ngmax * ks + wn - 1) / wn;
+      if (per > QM) continue;
+      if (ks > 1 && mt * ngmax * ks > kRedBytes / 512) continue;
+      const int chains = IM * per;
+      const long cost = ((long)(32 / ks) * (chains < 3 ? 3 : chains)) * 64 + ks * 4 + v;
+      if (best < 0 || cost < best) {
+        best = cost;
+        *variant = v;
+        *wm_out = wm;
+        *ks_out = ks;
+      }
+    }
+  }
+  return best >= 0;
 }
 
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
@@ -634,7 +700,11 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
 
 cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p0,
                           cudaStream_t stream) {
-  const void* fn = bf16 ? kernel_for<__nv_bfloat16>(plan.maxp) : kernel_for<__half>(plan.maxp);
+  int mt = 1;
+  while (mt * 16 < p0.TT) mt *= 2;
+  int variant, wm, ks;
+  if (!decode_phase_b(mt, plan.ngmax, &variant, &wm, &ks)) return cudaErrorInvalidValue;
+  const void* fn = bf16 ? kernel_for<__nv_bfloat16>(variant) : kernel_for<__half>(variant);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   DecodeParams p = p0;
@@ -644,6 +714,8 @@ cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams&
   p.kchunk = plan.kchunk;
   p.nstA = plan.nstA;
   p.ngbox = plan.ngbox;
+  p.pb_wm = wm;
+  p.pb_ks = ks;
   p.off_wb = plan.off_wb;
   p.off_a = plan.off_a;
   p.off_red = plan.off_red;

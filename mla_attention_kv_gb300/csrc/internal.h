@@ -51,6 +51,7 @@ struct DecodeParams {
   int ngbox;                // 8-column groups per W_kvb box (odd; >= groups per CTA)
   int off_wb, off_a, off_red, off_misc;  // smem layout (bytes)
   int single_barrier;       // 1: every CTA reduces every row (one grid barrier)
+  int pb_wm, pb_ks;         // phase-B warp grid rows (m side) and k-slices
 };
 
 // Rows x split-K chunks up to which every CTA reduces all partial rows itself
@@ -61,7 +62,8 @@ struct DecodePlan {
   int grid;        // CTAs (cooperative, one per SM)
   int tt_max;      // token rows per launch (64 or 128)
   int KB, KC;      // split-K of kv_a
-  int kpre, kchunk, nstA, ngbox, maxp;
+  int kpre, kchunk, nstA, ngbox;
+  int ngmax;       // most 8-column W_kvb groups of one CTA
   int off_wb, off_a, off_red, off_misc;
   size_t smem;     // dynamic shared memory bytes
   size_t partial_floats;  // workspace floats needed for partials
@@ -70,6 +72,10 @@ struct DecodePlan {
 // Plan for a given model shape on the current device; returns false if the
 // shape cannot be handled (shared memory or register budget).
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan);
+// Phase-B work split for mt m-tiles (a power of two <= 8) and at most ngmax
+// column groups per CTA: register-tile variant, warp-grid rows, k-slices.
+// False if no variant holds the tile.
+bool decode_phase_b(int mt, int ngmax, int* variant, int* wm, int* ks);
 // Rows of W_kvb per TMA box of the decode kernel.
 constexpr int kWkvbBoxRows = 32;
 cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p,
