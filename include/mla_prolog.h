@@ -44,7 +44,9 @@
  *   - The caller owns every tensor.  Device pointers must be 16-byte
  *     aligned (else MLA_ERR_MISALIGNED) and the tensors dense row-major in
  *     the layouts given.  Weights use the pre-transposed [in, out] layout of
- *     [MIG] §"源码级原理" step 1; nothing is pre-packed.
+ *     [MIG] §"源码级原理" step 1.  Optionally a handle keeps a re-laid-out
+ *     copy of W_kva / W_kvb for the decode kernel
+ *     (mla_kv_prolog_prepare_weights).
  *   - A handle owns only its device workspace (allocated by create, freed
  *     by destroy).  run never allocates and never synchronises: it enqueues
  *     its kernels on `stream` and returns.  Launch failures come back as
@@ -134,6 +136,27 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const int32_t* positions, const void* W_kva, const void* gamma_kv,
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream);
+
+/* Take a snapshot of W_kva [hidden, 576] and W_kvb [512, H*256] (layouts
+ * as for mla_kv_prolog_run) in the decode kernel's own layout: every CTA's
+ * kv_a tile and kv_b column slice become one contiguous block, with the
+ * 16-byte chunks of each row permuted so that the kernel's shared-memory
+ * reads meet no bank conflict.  The kernel then fetches them with a few
+ * large bulk copies instead of many narrow strided rows (the tile rows of
+ * W_kva are 64 bytes wide).  The layout is a property of this library
+ * only: the pages ([MIG] §"源码级原理" step 1) use the plain [in, out]
+ * layout, and the arithmetic is unchanged (same products, same order).
+ *   Later mla_kv_prolog_run calls on this handle whose W_kva and W_kvb
+ *   pointers equal these two take the snapshot on the decode path; other
+ *   pointers (and the prefill path) read the weights as passed.  The copy
+ *   is made on `stream` (two kernels); call again after changing the
+ *   weights in place.  Passing NULL for both forgets the snapshot.
+ *   The first call allocates hidden*576*2 + 512*H*256*2 bytes of device
+ *   memory owned by the handle (freed by destroy); later calls reuse it.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_MISALIGNED, MLA_ERR_WRONG_MODE
+ * (W8A8 handle), MLA_ERR_NO_MEMORY, MLA_ERR_CUDA. */
+mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,
+                                         cudaStream_t stream);
 
 /* Enqueue the W8A8 full MLA prolog (Q side + KV side) of T = b*s rows on a
  * handle created with quant = MLA_QUANT_W8A8 and dtype = MLA_BF16.

@@ -27,7 +27,8 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
             "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
-            "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc"]
+            "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
+            "mla_kv_prolog_prepare_weights"]
 
 
 class MLAError(RuntimeError):
@@ -75,6 +76,7 @@ def load(path: str | None = None):
     L.mla_w8a8_gemm_s32.argtypes = [P, P, I, I, I, P, P]
     L.mla_prolog_w8a8_operands.argtypes = [H, I, P, P, P, P, P]
     L.mla_kv_prolog_run_noalloc.argtypes = [ctypes.POINTER(Config), I, I] + [P] * 11 + [P]
+    L.mla_kv_prolog_prepare_weights.argtypes = [H, P, P, P]
     for fn in ("mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
                "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
                "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
@@ -152,6 +154,17 @@ def mla_kv_prolog_run(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, W_kvb, c
             _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
             _dev(k_nope, dt, "k_nope"), _dev(value, dt, "value"), _dev(k_pe, dt, "k_pe")]
     _check(load().mla_kv_prolog_run(h, b, s, *args, _stream(stream)), "mla_kv_prolog_run")
+
+
+def mla_kv_prolog_prepare_weights(h, cfg, W_kva, W_kvb, stream=None):
+    """Snapshot W_kva / W_kvb in the decode kernel's packed layout (None, None forgets it)."""
+    if W_kva is None and W_kvb is None:
+        _check(load().mla_kv_prolog_prepare_weights(h, None, None, _stream(stream)),
+               "mla_kv_prolog_prepare_weights")
+        return
+    dt = _tdt(cfg)
+    _check(load().mla_kv_prolog_prepare_weights(h, _dev(W_kva, dt, "W_kva"), _dev(W_kvb, dt, "W_kvb"),
+                                                _stream(stream)), "mla_kv_prolog_prepare_weights")
 
 
 def mla_prolog_w8a8_run(h, b, s, hidden, positions, W_qa, sW_qa, gamma_q, W_qb, sW_qb, W_kva,
@@ -241,6 +254,10 @@ class MLAProlog:
 
     def status(self, stream=None) -> int:
         return mla_kv_prolog_status(self.h, stream)
+
+    def prepare_weights(self, d: dict, stream=None):
+        """Packed snapshot of d["W_kva"], d["W_kvb"]; runs passing these tensors use it."""
+        mla_kv_prolog_prepare_weights(self.h, self.cfg, d["W_kva"], d["W_kvb"], stream)
 
     def alloc_outputs(self, b: int, s: int, device="cuda"):
         c = self.cfg

@@ -30,6 +30,12 @@ struct mla_prolog_s {
   void* nrm;
   DecodePlan dplan;
   bool decode_ok;
+  // packed weight snapshot (mla_kv_prolog_prepare_weights): W_kva tiles then
+  // W_kvb slices, and the caller pointers they were taken from
+  void* pk;
+  size_t pk_kva_bytes, pk_bytes;
+  const void* pk_src_kva;
+  const void* pk_src_kvb;
   // W8A8 workspace (see w8a8.cu)
   W8Workspace w8;
   // tensor maps of recently seen W_kvb pointers (decode kernel)
@@ -158,6 +164,7 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
 
 mla_status mla_kv_prolog_destroy(mla_prolog_t h) {
   if (!h) return MLA_ERR_INVALID_ARG;
+  if (h->pk) cudaFree(h->pk);
   cudaError_t e = cudaFree(h->ws);
   delete h;
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "cudaFree workspace");
@@ -226,27 +233,67 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
     return MLA_OK;
   }
 
-  const CUtensorMap* tm = wkvb_map(h, W_kvb);
-  if (!tm) {
-    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed for W_kvb");
-    return MLA_ERR_CUDA;
-  }
+  // the packed snapshot serves runs that pass the weights it was taken from
+  const bool packed = h->pk && W_kva == h->pk_src_kva && W_kvb == h->pk_src_kvb;
   DecodeParams p = {};
-  p.tmap_wkvb = *tm;
+  if (packed) {
+    W_kva = h->pk;
+    W_kvb = static_cast<const unsigned char*>(h->pk) + h->pk_kva_bytes;
+  } else {
+    const CUtensorMap* tm = wkvb_map(h, W_kvb);
+    if (!tm) {
+      snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed for W_kvb");
+      return MLA_ERR_CUDA;
+    }
+    p.tmap_wkvb = *tm;
+  }
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
   p.k_pe = k_pe; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
+  p.ntok = (int)T;
   const int tt = h->dplan.tt_max;
   for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
     p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
-    cudaError_t e = decode_launch(bf16, h->dplan, p, stream);
+    cudaError_t e = decode_launch(bf16, packed, h->dplan, p, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_launches += 1;
   }
+  return MLA_OK;
+}
+
+mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,
+                                         cudaStream_t stream) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
+  if (!W_kva && !W_kvb) {  // forget the snapshot
+    h->pk_src_kva = h->pk_src_kvb = nullptr;
+    return MLA_OK;
+  }
+  if (!W_kva || !W_kvb) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(W_kva) || !aligned16(W_kvb)) return MLA_ERR_MISALIGNED;
+  const size_t kva_bytes = (size_t)h->cfg.hidden * kNa * 2;
+  const size_t kvb_bytes = (size_t)kRank * h->cfg.num_heads * kHeadCols * 2;
+  if (!h->pk) {
+    cudaError_t e = cudaMalloc(&h->pk, kva_bytes + kvb_bytes);
+    if (e != cudaSuccess) {
+      h->pk = nullptr;
+      cuda_fail(e, "cudaMalloc packed weights");
+      return MLA_ERR_NO_MEMORY;
+    }
+    h->pk_kva_bytes = kva_bytes;
+    h->pk_bytes = kva_bytes + kvb_bytes;
+  }
+  h->pk_src_kva = h->pk_src_kvb = nullptr;
+  unsigned char* base = static_cast<unsigned char*>(h->pk);
+  cudaError_t e = decode_pack_weights(h->dplan, h->cfg.hidden, h->cfg.num_heads, W_kva, W_kvb, base,
+                                      base + kva_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pack weights");
+  h->pk_src_kva = W_kva;
+  h->pk_src_kvb = W_kvb;
   return MLA_OK;
 }
 

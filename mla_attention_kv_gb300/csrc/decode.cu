@@ -30,6 +30,9 @@
 //   phase B  kv_b_proj split-N over the resident W_kvb slice; the epilogue
 //            does the reshape/split (step 5) and the head-major stores
 //            (step 7) straight from the accumulators.
+#include <type_traits>
+#include <utility>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tma.h"
@@ -89,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait_cta(uint32_t bar, uint32_t parity,
   __syncthreads();
   const bool ok = *reinterpret_cast<volatile int*>(flag) != 0;
   if (ok) {
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_test_wait(bar, parity)) {
     }
   }
   return ok;
@@ -115,10 +118,19 @@ __device__ __forceinline__ void bar_exit_finish(unsigned* counters, unsigned old
   }
 }
 
-template <typename T, int IM, int QM>
+// f(std::integral_constant<int, c>) for c = 0 .. sizeof...(Cs) - 1, in order
+template <int... Cs, typename F>
+__device__ __forceinline__ void for_each_c(std::integer_sequence<int, Cs...>, F&& f) {
+  (f(std::integral_constant<int, Cs>{}), ...);
+}
+
+template <typename T, int IM, int QM, bool PK>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // 1024-byte aligned base (the hidden-state boxes use the 128-byte swizzle)
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, cta = blockIdx.x;
   const int TT = p.TT;
@@ -151,8 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const uint32_t bar_res = smem_u32(smem + p.off_misc + 1536);
   const uint32_t bar_s0 = bar_res + 8;  // streamed chunk buffers 0 .. kMaxStreamBufs-1
   int* sFlag = reinterpret_cast<int*>(smem + p.off_misc + 1600);
+  const uint32_t bar_a0 = bar_res + 128;  // phase-A stages 0 .. kMaxStagesA-1 (packed weights)
   if (tid == 0) {
-    tma_prefetch_desc(&p.tmap_wkvb);
+    if constexpr (PK) {
+      tma_prefetch_desc(&p.tmap_x);
+      for (int i = 0; i < kMaxStagesA; ++i) mbar_init(bar_a0 + 8 * i, 1);
+    } else {
+      tma_prefetch_desc(&p.tmap_wkvb);
+    }
     mbar_init(bar_res, 1);
     for (int i = 0; i < kMaxStreamBufs; ++i) mbar_init(bar_s0 + 8 * i, 1);
     fence_mbar_init();
@@ -161,38 +179,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // The W_kvb slice is only needed after the grid barrier: its TMA copies
   // are issued once this CTA's first kv_a stage has landed, so the kv_a
   // loads (on the critical path) are not queued behind them in DRAM.
+  // Packed weights: this CTA's W_kvb slice is one contiguous block of 512
+  // rows x ng 16-byte chunks (chunk order swizzled per row), copied with
+  // 1-D bulk copies; otherwise TMA boxes of the [512, H*256] matrix.
+  const unsigned char* wkvb_blk = static_cast<const unsigned char*>(p.W_kvb) + (size_t)g0 * (kRank * 16);
+  const int pitchW = PK ? ng * 16 : pitchB;  // smem row pitch of the W_kvb rows
   auto issue_wkvb = [&]() {
-    mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchB : 0));
+    mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchW : 0));
     if (ng > 0) {
-      for (int r = 0; r < p.kpre; r += kWkvbBoxRows)
-        tma_load_2d(smem_u32(sWB + r * pitchB), &p.tmap_wkvb, col0, r, bar_res);
-      for (int r = p.kpre; r < kRank; r += kWkvbBoxRows)
-        tma_prefetch_2d(&p.tmap_wkvb, col0, r);
+      if constexpr (PK) {
+        for (int r = 0; r < p.kpre; r += kWkvbBoxRows)
+          bulk_g2s(smem_u32(sWB + r * pitchW), wkvb_blk + (size_t)r * pitchW, kWkvbBoxRows * pitchW, bar_res);
+        if (p.kpre < kRank)
+          prefetch_l2_bulk(wkvb_blk + (size_t)p.kpre * pitchW, (uint32_t)((kRank - p.kpre) * pitchW));
+      } else {
+        for (int r = 0; r < p.kpre; r += kWkvbBoxRows)
+          tma_load_2d(smem_u32(sWB + r * pitchB), &p.tmap_wkvb, col0, r, bar_res);
+        for (int r = p.kpre; r < kRank; r += kWkvbBoxRows)
+          tma_prefetch_2d(&p.tmap_wkvb, col0, r);
+      }
     }
   };
   if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
 
   // ================================================================ phase A
+  bool wkvb_on = false;  // resident W_kvb copies issued (thread 0's view; uniform)
   {
     const int units = p.KC * kNblkA;
     const int subs = p.KB / kSubK;
     const int my_units = (units > cta) ? (units - cta + G - 1) / G : 0;
     const int nsub = my_units * subs;
-    const int stage_bytes = kSubK * kPitchWA + rows_x * kPitchX;
+    // raw weights: cp.async ring, W rows padded to kPitchWA, hidden rows to
+    // kPitchX.  Packed weights: TMA box of the hidden rows (64 columns,
+    // 128-byte swizzle) + one 1-D bulk copy of the pre-swizzled W tile per
+    // stage, completion on a per-stage mbarrier.
+    const int xbytes = PK ? rows_x * 128 : rows_x * kPitchX;
+    const int stage_bytes = PK ? xbytes + kSubK * 64 : kSubK * kPitchWA + rows_x * kPitchX;
     // as many stages in flight as the phase-A region holds at this row
     // count (all of them for small T), at least the plan's depth
     int nst = (p.off_red - p.off_a) / stage_bytes;
     if (nst > subs + 1) nst = subs + 1;
     if (nst > kMaxStagesA) nst = kMaxStagesA;
     if (nst < p.nstA) nst = p.nstA;
-    if (nsub == 0 && tid == 0) issue_wkvb();
+    if (nsub == 0) {
+      if (tid == 0) issue_wkvb();
+      wkvb_on = true;
+    }
 
-    auto load_sub = [&](int i) {
+    auto load_sub = [&](int i) {  // raw weights: every thread
       const int u = cta + (i / subs) * G;
       const int kc = u / kNblkA, nb = u - kc * kNblkA;
       const int k0 = kc * p.KB + (i % subs) * kSubK;
       unsigned char* st = sA + (i % nst) * stage_bytes;
-      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + kSubK * kPitchWA);
+      const uint32_t w_s = smem_u32(st + xbytes), x_s = smem_u32(st);
       if (tid < kSubK * 4) {
         const int r = tid >> 2, ch = tid & 3;
         cp_async16(w_s + r * kPitchWA + ch * 16, Wa + (size_t)(k0 + r) * kNa + nb * kNbA + ch * 8);
@@ -204,90 +243,222 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
                    r < TT ? 16 : 0);
       }
     };
+    const unsigned char* Wpk = static_cast<const unsigned char*>(p.W_kva);
+    auto issue_stage = [&](int i, int slot) {  // packed weights: thread 0
+      const int u = cta + (i / subs) * G;
+      const int kc = u / kNblkA;
+      const int sub = i % subs;
+      const uint32_t bar = bar_a0 + 8 * slot;
+      const uint32_t dst = smem_u32(sA + slot * stage_bytes);
+      mbar_arrive_expect_tx(bar, (uint32_t)(p.xrows * 128 + kSubK * 64));
+      tma_load_2d(dst, &p.tmap_x, kc * p.KB + sub * kSubK, p.t0, bar);
+      bulk_g2s(dst + xbytes, Wpk + ((size_t)u * p.KB + sub * kSubK) * 64, kSubK * 64, bar);
+    };
 
     const int nb8 = warp & 3, khalf = warp >> 2;
     // acc[m] takes the first k16 step of each stage, acc2 the second for the
     // first two m-tiles, so that small T still has two independent chains
-    float acc[kMaxMT][4], acc2[2][4];
+    // Accumulator slots: for M m-tiles (compile time) stage i and k16 step j
+    // add into acc[((i % SC) * JC + j) * M + m], JC = 2 while M <= 4 and SC =
+    // 8 / (M * JC) -- eight independent mma chains whatever M is (one chain
+    // per accumulator would be bound by the mma.sync latency).  The slots of
+    // each m-tile are folded in a fixed order when the unit is done.
+    float acc[kMaxMT][4];
 #pragma unroll
     for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 2; ++m) acc2[m][0] = acc2[m][1] = acc2[m][2] = acc2[m][3] = 0.f;
 
-#pragma unroll 1
-    for (int s = 0; s < nst - 1; ++s) {
-      if (s < nsub) load_sub(s);
-      cp_async_commit();
-    }
-    // cos/sin row of the owned token (position arrived by now or soon)
-    if (owner) {
-      if (tid == 0) reinterpret_cast<volatile int*>(sRed)[0] = pos;
-      __syncthreads();
-      int pp = reinterpret_cast<volatile int*>(sRed)[0];
-      if (pp < 0 || pp >= p.max_pos) {
-        if (tid == 0) atomicOr(p.status, kStatusBadPosition);
-        pp = pp < 0 ? 0 : p.max_pos - 1;
-      }
-      if (tid < 16) cp_async16(smem_u32(sCos) + tid * 16, p.cos_t + (size_t)pp * kRope + tid * 4);
-      else if (tid < 32) cp_async16(smem_u32(sSin) + (tid - 16) * 16, p.sin_t + (size_t)pp * kRope + (tid - 16) * 4);
-    }
-#pragma unroll 1
-    for (int i = 0; i < nsub; ++i) {
-      cp_async_wait_dyn(nst - 2);
-      __syncthreads();
-      if (i == 0 && tid == 0) issue_wkvb();
-      if (i + nst - 1 < nsub) load_sub(i + nst - 1);
-      cp_async_commit();
-      const unsigned char* st = sA + (i % nst) * stage_bytes;
-      const uint32_t w_s = smem_u32(st), x_s = smem_u32(st + kSubK * kPitchWA);
+    // one stage (64 k rows) in smem slot `slot`, accumulator chain C, for M
+    // m-tiles (compile time, so only real tiles are issued): each warp takes
+    // two of the four k16 steps (khalf) of its 8-column group nb8
+    auto stage_mma = [&](auto mt_c, auto ch_c, int slot) {
+      constexpr int M = decltype(mt_c)::value;
+      constexpr int C = decltype(ch_c)::value;
+      constexpr int JC = M <= 4 ? 2 : 1;
+      const unsigned char* st = sA + slot * stage_bytes;
+      const uint32_t x_s = smem_u32(st), w_s = smem_u32(st + xbytes);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int kk = khalf + 2 * j;
         uint32_t b0, b1;
-        ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * kPitchWA + nb8 * 16, b0, b1);
+        if constexpr (PK)  // packed W rows: 64 bytes, chunk c stored at c ^ ((row >> 1) & 3)
+          ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * 64 + ((nb8 ^ ((lane >> 1) & 3)) * 16), b0, b1);
+        else
+          ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * kPitchWA + nb8 * 16, b0, b1);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          uint32_t a[4];
+          if constexpr (PK)  // 128-byte swizzle: chunk c of row r at c ^ (r & 7)
+            ldsm_x4(x_s + (m * 16 + (lane & 15)) * 128 + (((kk * 2 + (lane >> 4)) ^ (lane & 7)) * 16),
+                    a[0], a[1], a[2], a[3]);
+          else
+            ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchX + (kk * 16 + (lane >> 4) * 8) * 2, a[0],
+                    a[1], a[2], a[3]);
+          mma16816<E::kBf16>(acc[(C * JC + (JC == 2 ? j : 0)) * M + m], a, b0, b1);
+        }
+      }
+    };
+    // stages [i0, i1), stage i in smem slot slot0 + i - i0 and chain i % SC
+    auto stages_mma = [&](int i0, int i1, int slot0) {
+      auto run = [&](auto mt_c) {
+        constexpr int M = decltype(mt_c)::value;
+        constexpr int SC = 8 / (M * (M <= 4 ? 2 : 1));
+#pragma unroll 1
+        for (int q = i0 - i0 % SC; q < i1; q += SC) {
+          for_each_c(std::make_integer_sequence<int, SC>{}, [&](auto ch_c) {
+            const int i = q + decltype(ch_c)::value;
+            if (i >= i0 && i < i1) stage_mma(mt_c, ch_c, slot0 + i - i0);
+          });
+        }
+      };
+      switch (MT) {
+        case 1: run(std::integral_constant<int, 1>{}); break;
+        case 2: run(std::integral_constant<int, 2>{}); break;
+        case 4: run(std::integral_constant<int, 4>{}); break;
+        default: run(std::integral_constant<int, 8>{}); break;
+      }
+    };
+    // fold the chain slots of each m-tile into acc[m] (fixed order)
+    auto fold = [&]() {
+      auto run = [&](auto mt_c) {
+        constexpr int M = decltype(mt_c)::value;
+#pragma unroll
+        for (int sl = 1; sl < 8 / M; ++sl)
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            acc[m][0] += acc[sl * M + m][0]; acc[m][1] += acc[sl * M + m][1];
+            acc[m][2] += acc[sl * M + m][2]; acc[m][3] += acc[sl * M + m][3];
+          }
+      };
+      switch (MT) {
+        case 1: run(std::integral_constant<int, 1>{}); break;
+        case 2: run(std::integral_constant<int, 2>{}); break;
+        case 4: run(std::integral_constant<int, 4>{}); break;
+        default: break;
+      }
+    };
+    auto unit_done = [&](int i) {
+      // unit done: fold the chains and the two k-halves, write the fp32 partial tile
+      fold();
+      const int u = cta + (i / subs) * G;
+      const int kc = u / kNblkA, nb = u - kc * kNblkA;
+      if (khalf == 1) {
+#pragma unroll
+        for (int m = 0; m < kMaxMT; ++m)
+          if (m < MT)
+            *reinterpret_cast<float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4) =
+                make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      }
+      __syncthreads();
+      if (khalf == 0) {
+        float* P = p.partials + (size_t)kc * kDecodeMaxTokens * kNa;
+        const int col = nb * kNbA + nb8 * 8 + 2 * (lane & 3);
 #pragma unroll
         for (int m = 0; m < kMaxMT; ++m) {
           if (m < MT) {
-            uint32_t a[4];
-            ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchX + (kk * 16 + (lane >> 4) * 8) * 2, a[0],
-                    a[1], a[2], a[3]);
-            if (j == 1 && m < 2) mma16816<E::kBf16>(acc2[m], a, b0, b1);
-            else mma16816<E::kBf16>(acc[m], a, b0, b1);
+            const float4 o = *reinterpret_cast<const float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4);
+            const int r0 = m * 16 + (lane >> 2);
+            if (r0 < TT) *reinterpret_cast<float2*>(P + (size_t)r0 * kNa + col) = make_float2(acc[m][0] + o.x, acc[m][1] + o.y);
+            if (r0 + 8 < TT) *reinterpret_cast<float2*>(P + (size_t)(r0 + 8) * kNa + col) = make_float2(acc[m][2] + o.z, acc[m][3] + o.w);
           }
         }
       }
-      if ((i % subs) == subs - 1) {
-        // unit done: fold the chains and the two k-halves, write the fp32 partial tile
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          acc[m][0] += acc2[m][0]; acc[m][1] += acc2[m][1]; acc[m][2] += acc2[m][2]; acc[m][3] += acc2[m][3];
-          acc2[m][0] = acc2[m][1] = acc2[m][2] = acc2[m][3] = 0.f;
-        }
-        const int u = cta + (i / subs) * G;
-        const int kc = u / kNblkA, nb = u - kc * kNblkA;
-        if (khalf == 1) {
-#pragma unroll
-          for (int m = 0; m < kMaxMT; ++m)
-            if (m < MT)
-              *reinterpret_cast<float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4) =
-                  make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-        }
+      for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    };
+    // cos/sin row of the owned token (position arrived by now or soon)
+    auto load_rope_row = [&]() {
+      if (owner) {
+        if (tid == 0) reinterpret_cast<volatile int*>(sRed)[0] = pos;
         __syncthreads();
-        if (khalf == 0) {
-          float* P = p.partials + (size_t)kc * kDecodeMaxTokens * kNa;
-          const int col = nb * kNbA + nb8 * 8 + 2 * (lane & 3);
-#pragma unroll
-          for (int m = 0; m < kMaxMT; ++m) {
-            if (m < MT) {
-              const float4 o = *reinterpret_cast<const float4*>(sRed + ((nb8 * kMaxMT + m) * 32 + lane) * 4);
-              const int r0 = m * 16 + (lane >> 2);
-              if (r0 < TT) *reinterpret_cast<float2*>(P + (size_t)r0 * kNa + col) = make_float2(acc[m][0] + o.x, acc[m][1] + o.y);
-              if (r0 + 8 < TT) *reinterpret_cast<float2*>(P + (size_t)(r0 + 8) * kNa + col) = make_float2(acc[m][2] + o.z, acc[m][3] + o.w);
+        int pp = reinterpret_cast<volatile int*>(sRed)[0];
+        if (pp < 0 || pp >= p.max_pos) {
+          if (tid == 0) atomicOr(p.status, kStatusBadPosition);
+          pp = pp < 0 ? 0 : p.max_pos - 1;
+        }
+        if (tid < 16) cp_async16(smem_u32(sCos) + tid * 16, p.cos_t + (size_t)pp * kRope + tid * 4);
+        else if (tid < 32) cp_async16(smem_u32(sSin) + (tid - 16) * 16, p.sin_t + (size_t)pp * kRope + (tid - 16) * 4);
+      }
+    };
+
+    if constexpr (PK) {
+      // Stages are consumed in groups, one CTA barrier per group: all of
+      // them at once when the ring holds them (small T), else groups of
+      // nst / 2 in two halves of the ring (one loads while one computes).
+      // The CTA owns at most one unit, so unit_done runs once, at the end.
+      const int gsz = nsub <= nst ? (nsub > 0 ? nsub : 1) : nst / 2;
+      const int ngroups = (nsub + gsz - 1) / gsz;
+      auto issue_group = [&](int k) {  // thread 0
+        for (int i = k * gsz; i < (k + 1) * gsz && i < nsub; ++i) issue_stage(i, (k & 1) * gsz + i - k * gsz);
+      };
+      if (tid == 0) {
+        if (ngroups > 0) issue_group(0);
+        if (ngroups > 1) issue_group(1);
+      }
+      int issuedG = ngroups < 2 ? ngroups : 2;
+      load_rope_row();
+      cp_async_commit();
+#pragma unroll 1
+      for (int k = 0; k < ngroups; ++k) {
+        const int i0 = k * gsz, i1 = (i0 + gsz) < nsub ? i0 + gsz : nsub;
+        const int slot0 = (k & 1) * gsz;
+        const uint32_t par = (k >> 1) & 1;
+        if (tid == 0) {
+          int ok = 1;
+          for (int i = i0; i < i1 && ok; ++i) {
+            ok = mbar_wait_bounded(bar_a0 + 8 * (slot0 + i - i0), par, p.budget_ns) ? 1 : 0;
+            // the W_kvb slice goes out once the first kv_a stage is in
+            if (ok && k == 0 && i == 0) {
+              issue_wkvb();
+              wkvb_on = true;
             }
           }
+          *sFlag = ok;
         }
-#pragma unroll
-        for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+        __syncthreads();
+        if (*reinterpret_cast<volatile int*>(sFlag) == 0) {
+          // a copy never completed: wait (bounded) for the rest in flight, then leave;
+          // the other CTAs give up at the grid barrier
+          if (tid == 0) {
+            atomicOr(p.status, kStatusTimeout);
+            for (int kk = k; kk < issuedG; ++kk)
+              for (int i = kk * gsz; i < (kk + 1) * gsz && i < nsub; ++i)
+                mbar_wait_bounded(bar_a0 + 8 * ((kk & 1) * gsz + i - kk * gsz), (kk >> 1) & 1, p.budget_ns);
+            if (wkvb_on) mbar_wait_bounded(bar_res, 0, p.budget_ns);
+          }
+          cp_async_wait<0>();
+          __syncthreads();
+          return;
+        }
+        for (int i = i0; i < i1; ++i)  // every thread observes the completed phases
+          while (!mbar_test_wait(bar_a0 + 8 * (slot0 + i - i0), par)) {
+          }
+        stages_mma(i0, i1, slot0);
+        if (k + 2 < ngroups) {
+          __syncthreads();  // every warp is done with these slots
+          if (tid == 0) issue_group(k + 2);
+          issuedG = k + 3;
+        }
+      }
+      if (nsub > 0) unit_done(nsub - 1);
+    } else {
+#pragma unroll 1
+      for (int s = 0; s < nst - 1; ++s) {
+        if (s < nsub) load_sub(s);
+        cp_async_commit();
+      }
+      load_rope_row();
+#pragma unroll 1
+      for (int i = 0; i < nsub; ++i) {
+        cp_async_wait_dyn(nst - 2);
+        __syncthreads();
+        if (i == 0) {
+          if (tid == 0) issue_wkvb();
+          wkvb_on = true;
+        }
+        if (i + nst - 1 < nsub) load_sub(i + nst - 1);
+        cp_async_commit();
+        stages_mma(i, i + 1, i % nst);
+        if ((i % subs) == subs - 1) unit_done(i);
       }
     }
     cp_async_wait<0>();
@@ -302,17 +473,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   unsigned char* sWS = sA + nrm_bytes;
   const int nstream = kRank - p.kpre;
   const int nchunks = (ng > 0 && nstream > 0) ? (nstream + p.kchunk - 1) / p.kchunk : 0;
-  int nbuf = (p.off_red - p.off_a - nrm_bytes) / (p.kchunk * pitchB);
+  const int cstride = p.kchunk * pitchW;  // bytes per chunk buffer
+  int nbuf = (p.off_red - p.off_a - nrm_bytes) / cstride;
   if (nbuf > kMaxStreamBufs) nbuf = kMaxStreamBufs;
   if (nbuf < 2) nbuf = 2;  // the plan reserves two at the largest row count
   auto issue_chunk = [&](int c) {  // thread 0 only
     const int r0 = p.kpre + c * p.kchunk;
     const int nr = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
     const uint32_t bar = bar_s0 + 8 * (c % nbuf);
-    const uint32_t dst = smem_u32(sWS + (c % nbuf) * p.kchunk * pitchB);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nr * pitchB));
-    for (int r = 0; r < nr; r += kWkvbBoxRows)
-      tma_load_2d(dst + r * pitchB, &p.tmap_wkvb, col0, r0 + r, bar);
+    const uint32_t dst = smem_u32(sWS + (c % nbuf) * cstride);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nr * pitchW));
+    if constexpr (PK) {
+      bulk_g2s(dst, wkvb_blk + (size_t)r0 * pitchW, (uint32_t)(nr * pitchW), bar);
+    } else {
+      for (int r = 0; r < nr; r += kWkvbBoxRows)
+        tma_load_2d(dst + r * pitchB, &p.tmap_wkvb, col0, r0 + r, bar);
+    }
   };
   int issued = nchunks < nbuf ? nchunks : nbuf;
   if (tid == 0)
@@ -465,11 +641,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   bool qv[QM];
 #pragma unroll
   for (int i = 0; i < IM; ++i) aoff[i] = (uint32_t)((mw + i * wm) * 16 * kPitchN);
+  // packed slices store chunk g of row r at g ^ pack_swizzle(ng, r); the
+  // rows a lane addresses are congruent to lane mod 8
+  const int xm = PK ? pack_swizzle(ng, lane & 7) : 0;
 #pragma unroll
   for (int q = 0; q < QM; ++q) {
     const int j = wr + q * wn;
     qv[q] = j < nitems;
-    boff[q] = (uint32_t)((j / ks) * 16);
+    boff[q] = (uint32_t)((qv[q] ? ((j / ks) ^ xm) : 0) * 16);
   }
 
   // K rows are consumed in chunks: the resident rows, then streamed chunks
@@ -488,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (c >= 0) {
       const int r0 = p.kpre + c * p.kchunk;
       krows = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
-      wchunk = smem_u32(sWS + (c % nbuf) * p.kchunk * pitchB);
+      wchunk = smem_u32(sWS + (c % nbuf) * cstride);
       if (!mbar_wait_cta(bar_s0 + 8 * (c % nbuf), (c / nbuf) & 1, p.budget_ns, sFlag)) {
         if (tid == 0) atomicOr(p.status, kStatusTimeout);
         drain();
@@ -502,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int st0 = ((myslice - gs0 % ks) + ks) % ks;
 #pragma unroll 1
     for (int st = st0; st < steps; st += ks) {
-      const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchB;
+      const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchW;
       const uint32_t arow = nrm_u + (lane & 15) * kPitchN + ((kbase + st * 16) + (lane >> 4) * 8) * 2;
       uint32_t a[IM][4];
 #pragma unroll
@@ -587,14 +766,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // Phase-B register tiles: IM m-tiles x QM column groups per warp.
 constexpr int kVariants[3][2] = {{1, 4}, {1, 8}, {2, 8}};
 
-template <typename T>
+template <typename T, bool PK>
 const void* kernel_for(int variant) {
-  if (variant == 0) return (const void*)decode_kernel<T, 1, 4>;
-  if (variant == 1) return (const void*)decode_kernel<T, 1, 8>;
-  return (const void*)decode_kernel<T, 2, 8>;
+  if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK>;
+  if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK>;
+  return (const void*)decode_kernel<T, 2, 8, PK>;
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------- weight packing
+// W_kva [hidden, 576] -> one contiguous tile per phase-A unit u = kc * 18 + nb
+// (the unit CTA u computes): KB rows of 32 columns (64 bytes), the four
+// 16-byte chunks of row r stored at c ^ ((r >> 1) & 3) so that ldmatrix of
+// 16 consecutive rows meets no bank conflict.
+__global__ void pack_wkva_kernel(const uint4* __restrict__ W, uint4* __restrict__ out, int hidden,
+                                 int KB) {
+  const long n = (long)hidden * (kNa / 8);
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int row = (int)(i / (kNa / 8)), cc = (int)(i % (kNa / 8));
+    const int nb = cc >> 2, c = cc & 3;
+    const int kc = row / KB, r = row - kc * KB;
+    const long u = (long)kc * kNblkA + nb;
+    out[(u * KB + r) * 4 + (c ^ ((r >> 1) & 3))] = W[i];
+  }
+}
+
+// W_kvb [512, NG*8] -> per CTA c one contiguous block of its column groups
+// [g0(c), g0(c+1)): 512 rows x ng 16-byte chunks, chunk j of row r stored at
+// j ^ pack_swizzle(ng, r).  Block c starts at g0(c) * 512 chunks.
+__global__ void pack_wkvb_kernel(const uint4* __restrict__ W, uint4* __restrict__ out, int NG,
+                                 int G) {
+  const long n = (long)kRank * NG;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / NG), g = (int)(i % NG);
+    // owner: the CTA c with g0(c) <= g < g0(c + 1), g0(c) = floor(c * NG / G)
+    const int c = (int)(((long)(g + 1) * G + NG - 1) / NG) - 1;
+    const int g0 = col_group_begin(c, NG, G), ng = col_group_begin(c + 1, NG, G) - g0;
+    const int j = g - g0;
+    out[(long)g0 * kRank + (long)r * ng + (j ^ pack_swizzle(ng, r))] = W[i];
+  }
+}
+
+cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, const void* W_kva,
+                                const void* W_kvb, void* pk_kva, void* pk_kvb, cudaStream_t stream) {
+  const int NG = heads * kHeadCols / 8;
+  pack_wkva_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kva),
+                                                     static_cast<uint4*>(pk_kva), hidden, plan.KB);
+  pack_wkvb_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kvb),
+                                                     static_cast<uint4*>(pk_kvb), NG, plan.grid);
+  return cudaGetLastError();
+}
 
 // Shared-memory plan for `tt` token rows per launch; false if it cannot be
 // laid out (or, with `resident_only`, if W_kvb would have to be streamed).
@@ -625,7 +847,8 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   const int stageA = kSubK * kPitchWA + tt * kPitchX;
   const int nstA = subs < 4 ? (subs < 2 ? 2 : subs) : 4;
   const int nrm_bytes = tt * kPitchN;
-  const int fixed = kRedBytes + kMiscBytes + 256;
+  // + 1024 to align the dynamic shared memory base, + up to 1023 to align region A
+  const int fixed = kRedBytes + kMiscBytes + 256 + 2048;
   // Region A holds the phase-A ring, later the latent rows plus (when the
   // W_kvb slice does not fit) two stream buffers; the rest of the budget
   // keeps W_kvb rows resident from kernel start.
@@ -652,10 +875,10 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   plan->ngbox = ngbox;
   plan->ngmax = ngmax;
   plan->off_wb = 0;
-  plan->off_a = (kpre * pitchB + 127) / 128 * 128;
+  plan->off_a = (kpre * pitchB + 1023) / 1024 * 1024;
   plan->off_red = plan->off_a + (regionA + 127) / 128 * 128;
   plan->off_misc = plan->off_red + kRedBytes;
-  plan->smem = (size_t)plan->off_misc + kMiscBytes;
+  plan->smem = (size_t)plan->off_misc + kMiscBytes + 1024;  // + base alignment slack
   if (plan->smem > (size_t)kSmemBudget) return false;
   if (kpre < tt) return false;  // the output tile is staged in the W_kvb area
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
@@ -698,13 +921,14 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   return num_sms >= 64 && plan_for(64, false, hidden, heads, num_sms, plan);
 }
 
-cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p0,
+cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p0,
                           cudaStream_t stream) {
   int mt = 1;
   while (mt * 16 < p0.TT) mt *= 2;
   int variant, wm, ks;
   if (!decode_phase_b(mt, plan.ngmax, &variant, &wm, &ks)) return cudaErrorInvalidValue;
-  const void* fn = bf16 ? kernel_for<__nv_bfloat16>(variant) : kernel_for<__half>(variant);
+  const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant) : kernel_for<__half, true>(variant))
+                          : (bf16 ? kernel_for<__nv_bfloat16, false>(variant) : kernel_for<__half, false>(variant));
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   DecodeParams p = p0;
@@ -720,6 +944,16 @@ cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams&
   p.off_a = plan.off_a;
   p.off_red = plan.off_red;
   p.off_misc = plan.off_misc;
+  if (packed) {
+    // hidden rows [ntok, hidden]: boxes of 64 columns x xrows rows, 128-byte
+    // swizzle; rows past ntok read as zero.  The box is at most the tensor's
+    // height; smem rows past it only feed output rows that are not stored.
+    p.xrows = 16 * mt < p.ntok ? 16 * mt : p.ntok;
+    if (!encode_tmap_2d(&p.tmap_x, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        p.hidden, (uint64_t)p.hidden_dim, (uint64_t)p.ntok, (uint64_t)p.hidden_dim * 2, 64,
+                        (uint32_t)p.xrows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   // one barrier when every CTA can afford to reduce all rows itself
   p.single_barrier = (p.TT * plan.KC <= kSingleBarrierRowsTimesChunks) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};

@@ -28,6 +28,7 @@ constexpr int kDecodeMaxTokens = 128;
 
 struct DecodeParams {
   CUtensorMap tmap_wkvb;    // W_kvb [512, H*256], box = (ngbox*8 columns, 32 rows)
+  CUtensorMap tmap_x;       // packed path: hidden [ntok, hidden], box = (64 columns, 16*mt rows)
   const void* hidden;       // [T, hidden]
   const int32_t* positions; // [T]
   const void* W_kva;        // [hidden, 576]
@@ -43,6 +44,8 @@ struct DecodeParams {
   unsigned* counters;       // workspace: grid barrier {arrivals, generation}
   unsigned* status;         // workspace: device status word
   int hidden_dim, heads, s, t0, TT, max_pos;
+  int ntok;                 // rows of `hidden` (b*s)
+  int xrows;                // packed path: rows of one hidden-state box
   float eps;
   unsigned long long budget_ns;
   // filled from the plan by decode_launch
@@ -76,9 +79,26 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan);
 // column groups per CTA: register-tile variant, warp-grid rows, k-slices.
 // False if no variant holds the tile.
 bool decode_phase_b(int mt, int ngmax, int* variant, int* wm, int* ks);
+
+// XOR applied to the 16-byte chunk index within row r of a packed W_kvb
+// slice of ng chunks per row: the rows of one 8x8 ldmatrix tile then fall
+// in distinct banks (odd ng needs none; ng even swaps within aligned pairs,
+// quads or octets, so the index stays below ng).
+__host__ __device__ inline int pack_swizzle(int ng, int r) {
+  if (ng & 1) return 0;
+  if (ng & 2) return (r >> 2) & 1;
+  if (ng & 4) return (r >> 1) & 3;
+  return r & 7;
+}
+// Pack W_kva / W_kvb (raw [in, out] layouts) into the decode kernel's
+// per-CTA contiguous layouts (same byte counts) on `stream`.
+cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, const void* W_kva,
+                                const void* W_kvb, void* pk_kva, void* pk_kvb, cudaStream_t stream);
 // Rows of W_kvb per TMA box of the decode kernel.
 constexpr int kWkvbBoxRows = 32;
-cudaError_t decode_launch(bool bf16, const DecodePlan& plan, const DecodeParams& p,
+// Packed weights (decode_pack_weights): W_kva / W_kvb point at the packed
+// copies, which the kernel reads with 1-D bulk copies.
+cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p,
                           cudaStream_t stream);
 
 }  // namespace mla

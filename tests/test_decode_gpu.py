@@ -27,11 +27,13 @@ def _lib():
 
 
 def run_case(cfg, b, s, seed, positions="decode", path=B.PATH_DECODE, max_tokens=None,
-             rows=None, oracle_mod=None, nan_fill=True):
+             rows=None, oracle_mod=None, nan_fill=True, packed=False):
     inp = I.kv_inputs(cfg, b, s, seed, positions)
     d = B.to_device(inp)
     m = B.MLAProlog(cfg, max_tokens or max(1, b * s))
     m.set_path(path)
+    if packed:
+        m.prepare_weights(d)
     out = m.alloc_outputs(b, s)
     if nan_fill:
         for t in out.values():
@@ -155,4 +157,81 @@ def test_host_errors_on_device_buffers():
     assert e.value.code == 4
     m.run(0, 2, d, out)  # T = 0 is a no-op
     assert m.last_launches == 0
+    m.close()
+
+
+# ---------------------------------------------------------------- packed weights
+# mla_kv_prolog_prepare_weights: the decode kernel reads a re-laid-out copy
+# of W_kva / W_kvb (bulk copies + TMA boxes of the hidden rows); same
+# arithmetic, same tolerance against the oracle.
+
+@pytest.mark.parametrize("b,s", [(1, 1), (1, 2), (4, 1), (8, 2), (32, 1), (64, 1), (64, 2), (128, 1)])
+def test_packed_decode_v2lite(oracle_mod, b, s):
+    r = run_case(I.V2_LITE, b, s, 700 + b * s, oracle_mod=oracle_mod, packed=True)
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("T", [1, 17, 64])
+def test_packed_decode_r1(oracle_mod, T):
+    r = run_case(I.R1, T, 1, 800 + T, oracle_mod=oracle_mod, packed=True)
+    assert r["status"] == 0
+
+
+@pytest.mark.parametrize("T", [3, 33, 127, 129, 200, 257])
+def test_packed_ragged(oracle_mod, T):
+    r = run_case(I.V2_LITE, T, 1, 900 + T, oracle_mod=oracle_mod, packed=True)
+    tt = rows_per_launch(I.V2_LITE)
+    assert r["status"] == 0 and r["launches"] == (T + tt - 1) // tt
+
+
+@pytest.mark.parametrize("H,hidden,dtype", [(1, 64, "fp16"), (3, 192, "bf16"), (5, 640, "fp16"),
+                                            (2, 2048, "bf16"), (16, 2048, "bf16"), (128, 2048, "fp16")])
+def test_packed_small_shapes(oracle_mod, H, hidden, dtype):
+    cfg = I.small_config(I.V2_LITE, hidden=hidden, num_heads=H, dtype=dtype)
+    r = run_case(cfg, 3, 2, 950 + H, oracle_mod=oracle_mod, packed=True)
+    assert r["status"] == 0
+
+
+def test_packed_matches_raw_bitwise():
+    """Same products in the same order: the packed and raw layouts give
+    identical outputs."""
+    a = run_case(I.V2_LITE, 16, 2, 4242)
+    b = run_case(I.V2_LITE, 16, 2, 4242, packed=True)
+    for k in ("k_nope", "value", "k_pe"):
+        assert torch.equal(a["out"][k].view(torch.int16), b["out"][k].view(torch.int16)), k
+
+
+def test_packed_snapshot_only_serves_its_own_weights(oracle_mod):
+    """A run with other weight tensors reads them as passed; changing the
+    snapshotted weights in place needs a new prepare; (None, None) forgets."""
+    cfg = I.V2_LITE
+    inp1 = I.kv_inputs(cfg, 4, 1, 11)
+    inp2 = I.kv_inputs(cfg, 4, 1, 12)
+    d1, d2 = B.to_device(inp1), B.to_device(inp2)
+    m = B.MLAProlog(cfg, 4)
+    m.set_path(B.PATH_DECODE)
+    m.prepare_weights(d1)
+    out = m.alloc_outputs(4, 1)
+    m.run(4, 1, d2, out)  # other weights: raw path
+    torch.cuda.synchronize()
+    ref2 = oracle_mod.kv_prolog(inp2)
+    for name, r in zip(("k_nope", "value", "k_pe"), ref2):
+        compare(name, out[name], r, oracle_mod)
+    m.run(4, 1, d1, out)  # snapshot
+    torch.cuda.synchronize()
+    ref1 = oracle_mod.kv_prolog(inp1)
+    for name, r in zip(("k_nope", "value", "k_pe"), ref1):
+        compare(name, out[name], r, oracle_mod)
+    # in-place change of the snapshotted tensors, then a new snapshot
+    d1["W_kva"].copy_(d2["W_kva"])
+    d1["W_kvb"].copy_(d2["W_kvb"])
+    m.prepare_weights(d1)
+    m.run(4, 1, dict(d2, W_kva=d1["W_kva"], W_kvb=d1["W_kvb"]), out)
+    torch.cuda.synchronize()
+    for name, r in zip(("k_nope", "value", "k_pe"), ref2):
+        compare(name, out[name], r, oracle_mod)
+    B.mla_kv_prolog_prepare_weights(m.h, cfg, None, None)
+    m.run(4, 1, d2, out)
+    torch.cuda.synchronize()
+    assert m.status() == 0
     m.close()
