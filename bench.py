@@ -65,7 +65,9 @@ class DecodeSweep:
         return {"workload": self.name, "model": "DeepSeek-V2-Lite KV prolog", "hidden": 2048,
                 "kv_lora_rank": 512, "rope_dim": 64, "num_heads": 16, "nope_dim": 128,
                 "v_dim": 128, "points": [f"b{b}s{s}" for b, s in self.points],
-                "tokens_per_step": self.tokens_per_step, "positions": "uniform per sequence in [0,4095]"}
+                "tokens_per_step": self.tokens_per_step, "positions": "uniform per sequence in [0,4095]",
+                "weights": "one handle per weight copy, packed once by mla_kv_prolog_prepare_weights "
+                           "outside the timed region"}
 
     def weight_bytes(self):
         c = self.cfg
@@ -99,7 +101,16 @@ class DecodeSweep:
                                 positions=inp["positions"].to(dev),
                                 hidden_h=inp["hidden"].pin_memory(),
                                 positions_h=inp["positions"].pin_memory()))
-        self.m = B.MLAProlog(self.cfg, max(b * s for b, s in self.points))
+        # one handle per weight copy, each with its packed snapshot (a serving
+        # engine packs every layer's weights once at load time)
+        tmax = max(b * s for b, s in self.points)
+        self.ms = []
+        for w in self.wcopies:
+            m = B.MLAProlog(self.cfg, tmax)
+            m.prepare_weights(w)
+            self.ms.append(m)
+        torch.cuda.synchronize(dev)
+        self.m = self.ms[0]
         self.out = [self.m.alloc_outputs(p["b"], p["s"], dev) for p in self.pt]
         self.out_h = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in o.items()}
                       for o in self.out]
@@ -108,10 +119,11 @@ class DecodeSweep:
     def _run(self, i, stream):
         p = self.pt[i]
         w = self.wcopies[self.calls % self.R]
+        m = self.ms[self.calls % self.R]
         self.calls += 1
         d = dict(hidden=p["hidden"], positions=p["positions"], cos=self.cos, sin=self.sin, **w)
-        self.m.run(p["b"], p["s"], d, self.out[i], stream)
-        return self.m.last_launches
+        m.run(p["b"], p["s"], d, self.out[i], stream)
+        return m.last_launches
 
     def step(self, stream, events=None, intervals=None):
         """One pass over the sweep; with `events`, record one event after
@@ -216,6 +228,8 @@ class SingleCall:
         self.m = B.MLAProlog(self.cfg, self.T)
         if not self.w8:
             self.m.set_path(self.path)
+            self.m.prepare_weights(self.d)  # packed snapshot for the decode path
+            torch.cuda.synchronize(dev)
         self.out = self.m.alloc_outputs(self.b, self.s, dev)
         self.hidden_h = inp["hidden"].pin_memory()
         self.positions_h = inp["positions"].pin_memory()
