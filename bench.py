@@ -135,11 +135,40 @@ class DecodeSweep:
             if events is not None:
                 events.append(torch.cuda.Event(enable_timing=True))
                 events[-1].record(stream)
-                intervals.append((len(events) - 2, len(events) - 1, self.pt[i]["b"] * self.pt[i]["s"]))
+                intervals.append((len(events) - 2, len(events) - 1, [self.pt[i]["b"] * self.pt[i]["s"]]))
         return n
 
     def step_bytes(self):
         return [self.alg_bytes(b * s) for b, s in self.points]
+
+    def capture(self, dev):
+        """One CUDA graph per rotation offset: graph p holds the 16 calls of a
+        step that starts at weight copy 16p (mod R)."""
+        st = torch.cuda.Stream(dev)
+        graphs = []
+        saved = self.calls
+        for gi in range(self.R):
+            self.calls = (gi * len(self.pt)) % self.R
+            g = torch.cuda.CUDAGraph()
+            n = 0
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(g, stream=st):
+                    for i in range(len(self.pt)):
+                        n += self._run(i, st)
+            graphs.append(g)
+            self.graph_launches = n
+        self.calls = saved
+        torch.cuda.synchronize(dev)
+        return graphs
+
+    def graph_step(self, k, graphs, stream, events, intervals):
+        events.append(torch.cuda.Event(enable_timing=True))
+        events[-1].record(stream)
+        graphs[k % len(graphs)].replay()
+        events.append(torch.cuda.Event(enable_timing=True))
+        events[-1].record(stream)
+        intervals.append((len(events) - 2, len(events) - 1, [b * s for b, s in self.points]))
+        return self.graph_launches
 
     def e2e_step(self, stream):
         h2d = d2h = 0
@@ -249,11 +278,32 @@ class SingleCall:
         if events is not None:
             events.append(torch.cuda.Event(enable_timing=True))
             events[-1].record(stream)
-            intervals.append((len(events) - 2, len(events) - 1, self.T))
+            intervals.append((len(events) - 2, len(events) - 1, [self.T]))
         return self.m.last_launches
 
     def step_bytes(self):
         return [self.alg_bytes(self.T)]
+
+    def capture(self, dev):
+        st = torch.cuda.Stream(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(g, stream=st):
+                self.m.run(self.b, self.s, self.d, self.out, st)
+        self.graph_launches = self.m.last_launches
+        torch.cuda.synchronize(dev)
+        return [g]
+
+    def graph_step(self, k, graphs, stream, events, intervals):
+        if self.flush is not None:
+            self.flush.zero_()
+        events.append(torch.cuda.Event(enable_timing=True))
+        events[-1].record(stream)
+        graphs[0].replay()
+        events.append(torch.cuda.Event(enable_timing=True))
+        events[-1].record(stream)
+        intervals.append((len(events) - 2, len(events) - 1, [self.T]))
+        return self.graph_launches
 
     def e2e_step(self, stream):
         self.d["hidden"].copy_(self.hidden_h, non_blocking=True)
@@ -366,34 +416,47 @@ def run_gpu(args, wl, rank, world, dev):
     torch.cuda.synchronize(dev)
     host_per_step = (time.perf_counter() - t0) / max(1, args.warmup)
 
-    # timed region: exactly K steps between CUDA events on the launching stream
-    events, intervals = [], []
-    if world > 1:
-        torch.distributed.barrier()
+    # CUDA graphs of the steps (how a serving engine issues repeated decode
+    # steps): captured once, replayed in the timed region
+    graphs = wl.capture(dev)
+    for k in range(min(len(graphs), 3)):
+        graphs[k].replay()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    sleep_s = min(5.0, 1.5 * host_per_step * args.steps + 0.05)
-    torch.cuda._sleep(int(sleep_s * 2.0e9))
-    start = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    events.append(start)
-    total_launches = 0
-    for _ in range(args.steps):
-        total_launches += wl.step(stream, events, intervals)
-    end = events[-1]
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    region_ms = start.elapsed_time(end)
-    calls = [(events[a].elapsed_time(events[b]), T) for a, b, T in intervals]
-    call_ms = sum(c for c, _ in calls)
-    # with an L2 flush between calls, the flush is not part of the work
-    ms = call_ms if getattr(wl, "flush", None) is not None else region_ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+
+    def timed(run_step):
+        events, intervals = [], []
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        clocks = ClockSampler(dev.index if dev.index is not None else 0)
+        sleep_s = min(5.0, 1.5 * host_per_step * args.steps + 0.05)
+        torch.cuda._sleep(int(sleep_s * 2.0e9))
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        events.append(start)
+        launches = 0
+        for k in range(args.steps):
+            launches += run_step(k, events, intervals)
+        end = events[-1]
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop()
+        region_ms = start.elapsed_time(end)
+        calls = [(events[a].elapsed_time(events[b]), Ts) for a, b, Ts in intervals]
+        # with an L2 flush between calls, the flush is not part of the work
+        ms = sum(c for c, _ in calls) if getattr(wl, "flush", None) is not None else region_ms
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, region_ms, calls, clk, launches
+
+    # timed region: exactly K steps (graph replays) between CUDA events on the launching stream
+    ms, region_ms, calls, clk, total_launches = timed(
+        lambda k, ev, iv: wl.graph_step(k, graphs, stream, ev, iv))
+    # the same K steps launched eagerly through the binding, call by call
+    ms_e, _, calls_e, clk_e, _ = timed(lambda k, ev, iv: wl.step(stream, ev, iv))
 
     # e2e through the public binding with host buffers
     for _ in range(2):
@@ -412,7 +475,8 @@ def run_gpu(args, wl, rank, world, dev):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_s = float(t.item())
     return dict(ms=ms, region_ms=region_ms, calls=calls, clk=clk, launches=total_launches,
-                e2e_s=e2e_s, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h, host_per_step=host_per_step)
+                e2e_s=e2e_s, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h, host_per_step=host_per_step,
+                ms_eager=ms_e, calls_eager=calls_e, clk_eager=clk_e)
 
 
 def kernel_traffic(kernel: str, T: int):
@@ -480,8 +544,9 @@ def main():
     value = tokens / (r["ms"] / 1e3)
     peaks, peak_kind = measured_peaks()
     calls = r["calls"]
-    alg_bytes = sum(wl.alg_bytes(T) for _, T in calls)
-    alg_flops = sum(wl.flops(T) for _, T in calls)
+    Tlist = [T for _, Ts in calls for T in Ts]
+    alg_bytes = sum(wl.alg_bytes(T) for T in Tlist)
+    alg_flops = sum(wl.flops(T) for T in Tlist)
     call_s = sum(c for c, _ in calls) / 1e3
     # roofline: the bound is the resource whose time at peak is larger
     bw = peaks["hbm_gbs"] * 1e9
@@ -501,14 +566,15 @@ def main():
         peak = tensor_peak / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": tensor_unit,
                 "frac": achieved / peak}
-    Ts = sorted({T for _, T in calls})
+    Ts = sorted(set(Tlist))
     tr = [kernel_traffic(kernel, T) for T in Ts]
     roof["traffic"] = None if any(x is None for x in tr) else \
-        sum(kernel_traffic(kernel, T) for _, T in calls) / len(calls)
-    roof.update({"peak_kind": peak_kind, "kernel": kernel, "calls_timed": len(calls),
-                 "mean_call_us": 1e6 * call_s / len(calls),
-                 "algorithmic_bytes_per_call": alg_bytes / len(calls),
-                 "algorithmic_flops_per_call": alg_flops / len(calls)})
+        sum(kernel_traffic(kernel, T) for T in Tlist) / len(Tlist)
+    roof.update({"peak_kind": peak_kind, "kernel": kernel, "calls_timed": len(Tlist),
+                 "mean_call_us": 1e6 * call_s / len(Tlist),
+                 "algorithmic_bytes_per_call": alg_bytes / len(Tlist),
+                 "algorithmic_flops_per_call": alg_flops / len(Tlist),
+                 "timing": "CUDA events around each CUDA-graph replay of a step"})
     line = {
         "metric": "tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
@@ -524,15 +590,20 @@ def main():
         "e2e": {"value": wl.tokens_per_step * r["e2e_steps"] * world / r["e2e_s"], "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
+    ce = r["calls_eager"]
+    line["eager"] = {"value": tokens / (r["ms_eager"] / 1e3), "ms_per_step": r["ms_eager"] / args.steps,
+                     "mean_call_us": 1e3 * sum(c for c, _ in ce) / len(ce), "clocks": r["clk_eager"],
+                     "note": "the same steps launched call by call through the binding (no CUDA graph)"}
     if len(wl.points) > 1:
         npts = len(wl.points)
         detail = {}
         for j, (b, s_) in enumerate(wl.points):
-            ds = [calls[k][0] for k in range(j, len(calls), npts)]
+            ds = [ce[k][0] for k in range(j, len(ce), npts)]
             us = 1e3 * statistics.mean(ds)
             detail[f"b{b}s{s_}"] = {"T": b * s_, "us": round(us, 3), "tokens_per_s": b * s_ / (us * 1e-6),
                                     "hbm_frac": wl.alg_bytes(b * s_) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
         line["per_point"] = detail
+        line["per_point_timing"] = "CUDA events around each call of the eager pass"
     if rank == 0 and not args.no_cpu_baseline:
         v, cores, sample = wl.cpu_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",

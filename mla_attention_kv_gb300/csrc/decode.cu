@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(bar_res, 1);
     for (int i = 0; i < kMaxStreamBufs; ++i) mbar_init(bar_s0 + 8 * i, 1);
     fence_mbar_init();
+    sFlag[1] = 0;  // resident W_kvb copies not issued yet (packed path)
   }
   __syncthreads();
   // The W_kvb slice is only needed after the grid barrier: its TMA copies
@@ -200,10 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
   };
+  // packed weights: warp 1 issues the resident rows, one 32-row bulk copy per
+  // lane (thread 0 alone spends ~40 ns per copy instruction), and records
+  // that it did in *sWkvbOn for the drains
+  int* sWkvbOn = sFlag + 1;
+  auto issue_wkvb_warp = [&]() {  // warp 1
+    if (lane == 0) mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchW : 0));
+    __syncwarp();
+    if (ng > 0) {
+      for (int r = lane * kWkvbBoxRows; r < p.kpre; r += 32 * kWkvbBoxRows)
+        bulk_g2s(smem_u32(sWB + r * pitchW), wkvb_blk + (size_t)r * pitchW, kWkvbBoxRows * pitchW, bar_res);
+      if (lane == 0 && p.kpre < kRank)
+        prefetch_l2_bulk(wkvb_blk + (size_t)p.kpre * pitchW, (uint32_t)((kRank - p.kpre) * pitchW));
+    }
+    if (lane == 0) *reinterpret_cast<volatile int*>(sWkvbOn) = 1;
+  };
   if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
 
   // ================================================================ phase A
-  bool wkvb_on = false;  // resident W_kvb copies issued (thread 0's view; uniform)
+  bool wkvb_on = false;  // resident W_kvb copies issued (raw path: thread 0's view)
   {
     const int units = p.KC * kNblkA;
     const int subs = p.KB / kSubK;
@@ -222,7 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (nst > kMaxStagesA) nst = kMaxStagesA;
     if (nst < p.nstA) nst = p.nstA;
     if (nsub == 0) {
-      if (tid == 0) issue_wkvb();
+      if constexpr (PK) {
+        if (warp == 1) issue_wkvb_warp();
+      } else if (tid == 0) {
+        issue_wkvb();
+      }
       wkvb_on = true;
     }
 
@@ -387,12 +407,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // The CTA owns at most one unit, so unit_done runs once, at the end.
       const int gsz = nsub <= nst ? (nsub > 0 ? nsub : 1) : nst / 2;
       const int ngroups = (nsub + gsz - 1) / gsz;
-      auto issue_group = [&](int k) {  // thread 0
-        for (int i = k * gsz; i < (k + 1) * gsz && i < nsub; ++i) issue_stage(i, (k & 1) * gsz + i - k * gsz);
+      auto issue_group = [&](int k) {  // warp 0: lane L issues stage k * gsz + L (gsz <= 16)
+        const int i = k * gsz + lane;
+        if (lane < gsz && i < nsub) issue_stage(i, (k & 1) * gsz + lane);
       };
-      if (tid == 0) {
+      if (warp == 0) {
         if (ngroups > 0) issue_group(0);
         if (ngroups > 1) issue_group(1);
+      }
+      // warp 1: the W_kvb slice goes out once the first kv_a stage is in
+      if (warp == 1 && nsub > 0) {
+        int ok = 0;
+        if (lane == 0) ok = mbar_wait_bounded(bar_a0, 0, p.budget_ns) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) issue_wkvb_warp();
       }
       int issuedG = ngroups < 2 ? ngroups : 2;
       load_rope_row();
@@ -404,14 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         const uint32_t par = (k >> 1) & 1;
         if (tid == 0) {
           int ok = 1;
-          for (int i = i0; i < i1 && ok; ++i) {
+          for (int i = i0; i < i1 && ok; ++i)
             ok = mbar_wait_bounded(bar_a0 + 8 * (slot0 + i - i0), par, p.budget_ns) ? 1 : 0;
-            // the W_kvb slice goes out once the first kv_a stage is in
-            if (ok && k == 0 && i == 0) {
-              issue_wkvb();
-              wkvb_on = true;
-            }
-          }
           *sFlag = ok;
         }
         __syncthreads();
@@ -423,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             for (int kk = k; kk < issuedG; ++kk)
               for (int i = kk * gsz; i < (kk + 1) * gsz && i < nsub; ++i)
                 mbar_wait_bounded(bar_a0 + 8 * ((kk & 1) * gsz + i - kk * gsz), (kk >> 1) & 1, p.budget_ns);
-            if (wkvb_on) mbar_wait_bounded(bar_res, 0, p.budget_ns);
+            if (*reinterpret_cast<volatile int*>(sWkvbOn)) mbar_wait_bounded(bar_res, 0, p.budget_ns);
           }
           cp_async_wait<0>();
           __syncthreads();
@@ -435,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         stages_mma(i0, i1, slot0);
         if (k + 2 < ngroups) {
           __syncthreads();  // every warp is done with these slots
-          if (tid == 0) issue_group(k + 2);
+          if (warp == 0) issue_group(k + 2);
           issuedG = k + 3;
         }
       }
