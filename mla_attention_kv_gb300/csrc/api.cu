@@ -135,7 +135,7 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
   off += h->decode_ok ? h->dplan.partial_floats * sizeof(float) : 0;
   off = (off + 255) & ~(size_t)255;
   const size_t nrm_off = off;
-  off += (size_t)kDecodeMaxTokens * kRank * 2;
+  off += kDecodeNrmBytes;
   off = (off + 255) & ~(size_t)255;
   size_t w8_off = off;
   if (c.quant == MLA_QUANT_W8A8) off += w8_workspace_bytes(c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens);

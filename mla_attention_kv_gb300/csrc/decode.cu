@@ -47,7 +47,7 @@ constexpr int kNbA = 32;           // kv_a columns per split-K tile
 constexpr int kNblkA = kNa / kNbA; // 18 column blocks
 constexpr int kPitchWA = 80;       // smem row pitch of a 32-column tile (odd multiple of 16)
 constexpr int kPitchX = 144;       // smem row pitch of a 64-column hidden tile
-constexpr int kPitchN = 1040;      // smem row pitch of a 512-column latent row
+constexpr int kPitchN = kNrmPitch; // smem row pitch of a 512-column latent row (= workspace pitch)
 constexpr int kMaxMT = kDecodeMaxTokens / 16;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kRedBytes = 16384;   // cross-warp reduction scratch (<= 32 chains x 512 B)
@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const uint32_t bar_s0 = bar_res + 8;  // streamed chunk buffers 0 .. kMaxStreamBufs-1
   int* sFlag = reinterpret_cast<int*>(smem + p.off_misc + 1600);
   const uint32_t bar_a0 = bar_res + 128;  // phase-A stages 0 .. kMaxStagesA-1 (packed weights)
+  const uint32_t bar_lat = bar_res + 256; // latent rows from the workspace (two-barrier mode)
+  const uint32_t bar_r0 = bar_res + 272;  // streamed W_kvb chunk batches 0 .. 15 (one use each)
   if (tid == 0) {
     if constexpr (PK) {
       tma_prefetch_desc(&p.tmap_x);
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     for (int i = 0; i < kMaxStreamBufs; ++i) mbar_init(bar_s0 + 8 * i, 1);
     fence_mbar_init();
     sFlag[1] = 0;  // resident W_kvb copies not issued yet (packed path)
+    mbar_init(bar_lat, 1);
+    for (int i = 0; i < kRank / kWkvbBoxRows; ++i) mbar_init(bar_r0 + 8 * i, 1);
   }
   __syncthreads();
   // The W_kvb slice is only needed after the grid barrier: its TMA copies
@@ -211,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (ng > 0) {
       for (int r = lane * kWkvbBoxRows; r < p.kpre; r += 32 * kWkvbBoxRows)
         bulk_g2s(smem_u32(sWB + r * pitchW), wkvb_blk + (size_t)r * pitchW, kWkvbBoxRows * pitchW, bar_res);
-      if (lane == 0 && p.kpre < kRank)
-        prefetch_l2_bulk(wkvb_blk + (size_t)p.kpre * pitchW, (uint32_t)((kRank - p.kpre) * pitchW));
+      // (no L2 prefetch of the streamed rows: a bulk prefetch occupies the
+      // SM's copy engine and the chunk copies would queue behind it)
     }
     if (lane == 0) *reinterpret_cast<volatile int*>(sWkvbOn) = 1;
   };
@@ -487,44 +491,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     __syncthreads();
   }
 
-  // ---- streamed W_kvb rows [kpre, 512): TMA into chunk buffers in the
-  // freed phase-A region, behind the latent rows (they land during the
-  // barrier); as many buffers as fit at this launch's row count
+  // ---- W_kvb rows as a ring of 32-row chunks: chunks [0, nres) were copied
+  // into the resident slots at the start; when the slice is larger than that
+  // (R1 shapes), chunks nres, nres+1, ... follow into nbuf buffers in the
+  // freed phase-A region (behind the latent rows) and then into whichever
+  // slot, resident or buffer, the consumer has just finished with, so the
+  // stream stays nslots chunks ahead of the MMAs.
   const int nrm_bytes = rows_x * kPitchN;
   unsigned char* sN = sA;
   unsigned char* sWS = sA + nrm_bytes;
-  const int nstream = kRank - p.kpre;
-  const int nchunks = (ng > 0 && nstream > 0) ? (nstream + p.kchunk - 1) / p.kchunk : 0;
-  const int cstride = p.kchunk * pitchW;  // bytes per chunk buffer
-  int nbuf = (p.off_red - p.off_a - nrm_bytes) / cstride;
+  constexpr int CR = kWkvbBoxRows;
+  constexpr int nch = kRank / CR;
+  const int nres = p.kpre / CR;
+  const bool ring = ng > 0 && nres < nch;
+  int nbuf = (p.off_red - p.off_a - nrm_bytes) / (CR * pitchW);
   if (nbuf > kMaxStreamBufs) nbuf = kMaxStreamBufs;
   if (nbuf < 2) nbuf = 2;  // the plan reserves two at the largest row count
-  auto issue_chunk = [&](int c) {  // thread 0 only
-    const int r0 = p.kpre + c * p.kchunk;
-    const int nr = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
-    const uint32_t bar = bar_s0 + 8 * (c % nbuf);
-    const uint32_t dst = smem_u32(sWS + (c % nbuf) * cstride);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nr * pitchW));
-    if constexpr (PK) {
-      bulk_g2s(dst, wkvb_blk + (size_t)r0 * pitchW, (uint32_t)(nr * pitchW), bar);
-    } else {
-      for (int r = 0; r < nr; r += kWkvbBoxRows)
-        tma_load_2d(dst + r * pitchB, &p.tmap_wkvb, col0, r0 + r, bar);
+  const int nslots = nres + nbuf;
+  auto slot_ptr = [&](int sl) -> unsigned char* {
+    return sl < nres ? sWB + sl * CR * pitchW : sWS + (sl - nres) * CR * pitchW;
+  };
+  // Streamed chunks go out in batches -- the buffer chunks at the end of
+  // phase A, then the refills after each run of chunks -- and each batch
+  // completes on a barrier of its own (bar_r0 + 8 * batch, used once per
+  // launch, so its phase is always 0).  sBatch[c] records the batch of
+  // chunk c for the consumers.
+  unsigned char* sBatch = reinterpret_cast<unsigned char*>(sFlag + 2);
+  int nbatch = 0;  // batches issued (thread 0's count; every thread tracks it)
+  auto issue_batch = [&](int c0, int c1) {  // thread 0 only: chunks [c0, c1), c0 >= nres
+    const uint32_t bar = bar_r0 + 8 * nbatch;
+    mbar_arrive_expect_tx(bar, (uint32_t)((c1 - c0) * CR * pitchW));
+    for (int c = c0; c < c1; ++c) {
+      sBatch[c] = (unsigned char)nbatch;
+      const uint32_t dst = smem_u32(slot_ptr(c % nslots));
+      if constexpr (PK) {
+        bulk_g2s(dst, wkvb_blk + (size_t)c * CR * pitchW, (uint32_t)(CR * pitchW), bar);
+      } else {
+        tma_load_2d(dst, &p.tmap_wkvb, col0, c * CR, bar);
+      }
     }
   };
-  int issued = nchunks < nbuf ? nchunks : nbuf;
-  if (tid == 0)
-    for (int c = 0; c < issued; ++c) issue_chunk(c);
-  int waited = 0;  // chunks whose arrival this CTA has observed
+  int issued = ring ? (nslots < nch ? nslots : nch) : nres;  // chunks issued so far
+  if (ring) {
+    if (tid == 0) issue_batch(nres, issued);
+    nbatch = 1;
+  }
   // on an early exit, wait (bounded) for this CTA's copies still in flight:
   // the resident rows and every issued chunk not yet observed (at most one
-  // outstanding phase per buffer)
+  // outstanding phase per slot)
+  bool lat_issued = false;  // thread 0: latent-row bulk copy in flight
   auto drain = [&]() {
     cp_async_wait<0>();
     if (tid == 0) {
       mbar_wait_bounded(bar_res, 0, p.budget_ns);
-      for (int c = waited; c < issued; ++c)
-        mbar_wait_bounded(bar_s0 + 8 * (c % nbuf), (c / nbuf) & 1, p.budget_ns);
+      if (lat_issued) mbar_wait_bounded(bar_lat, 0, p.budget_ns);
+      for (int b = 0; b < nbatch; ++b) mbar_wait_bounded(bar_r0 + 8 * b, 0, p.budget_ns);
     }
     __syncthreads();
   };
@@ -612,7 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         const int c = tid * 4;
         uint2 pk = make_uint2(E::pack(v.x * inv * E::to_f(sGam[c]), v.y * inv * E::to_f(sGam[c + 1])),
                               E::pack(v.z * inv * E::to_f(sGam[c + 2]), v.w * inv * E::to_f(sGam[c + 3])));
-        *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * kRank + c) = pk;
+        *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * (kNrmPitch / 2) + c) = pk;
+        // the row is read back by bulk copies (async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
       } else if (tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
         T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
@@ -626,15 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       drain();
       return;
     }
-    // latent rows (zero rows past TT) -> shared memory
-    const T* nrm = static_cast<const T*>(p.nrm);
-    const uint32_t nu = smem_u32(sN);
-    for (int c = tid; c < rows_x * 64; c += kThreads) {
-      const int r = c >> 6, ch = c & 63;
-      const int rr = r < TT ? r : 0;
-      cp_async16(nu + r * kPitchN + ch * 16, nrm + (size_t)rr * kRank + ch * 8, r < TT ? 16 : 0);
+    // latent rows -> shared memory: the workspace rows have the shared-memory
+    // pitch, so one bulk copy moves all TT of them; rows past TT are zeroed
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(bar_lat, (uint32_t)(TT * kNrmPitch));
+      bulk_g2s(smem_u32(sN), p.nrm, (uint32_t)(TT * kNrmPitch), bar_lat);
+      lat_issued = true;
     }
-    cp_async_commit();
+    for (int c = tid; c < (rows_x - TT) * (kPitchN / 16); c += kThreads)
+      *reinterpret_cast<uint4*>(sN + TT * kPitchN + c * 16) = make_uint4(0, 0, 0, 0);
   }
   const unsigned exit_old = bar_exit_arrive(p.counters);
 
@@ -670,59 +694,88 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   for (int q = 0; q < QM; ++q) {
     const int j = wr + q * wn;
     qv[q] = j < nitems;
-    boff[q] = (uint32_t)((qv[q] ? ((j / ks) ^ xm) : 0) * 16);
+    boff[q] = (uint32_t)((qv[q] ? ((j / ks) ^ xm) : 0) * 16);  // unused items: group 0 (read, not used)
   }
 
   // K rows are consumed in chunks: the resident rows, then streamed chunks
   cp_async_wait<0>();
   __syncthreads();
-  if (!mbar_wait_cta(bar_res, 0, p.budget_ns, sFlag)) {
+  if (!mbar_wait_cta(bar_res, 0, p.budget_ns, sFlag) ||
+      (!p.single_barrier && !mbar_wait_cta(bar_lat, 0, p.budget_ns, sFlag))) {
     if (tid == 0) atomicOr(p.status, kStatusTimeout);
     drain();
     bar_exit_finish(p.counters, exit_old, G);
     return;
   }
-  int kbase = 0, krows = p.kpre;
-  uint32_t wchunk = smem_u32(sWB);
-#pragma unroll 1
-  for (int c = -1; c < nchunks; ++c) {
-    if (c >= 0) {
-      const int r0 = p.kpre + c * p.kchunk;
-      krows = (kRank - r0) < p.kchunk ? (kRank - r0) : p.kchunk;
-      wchunk = smem_u32(sWS + (c % nbuf) * cstride);
-      if (!mbar_wait_cta(bar_s0 + 8 * (c % nbuf), (c / nbuf) & 1, p.budget_ns, sFlag)) {
-        if (tid == 0) atomicOr(p.status, kStatusTimeout);
-        drain();
-        bar_exit_finish(p.counters, exit_old, G);
-        return;
-      }
-      waited = c + 1;
-    }
+  // k16 steps of rows [kbase, kbase + krows) whose W_kvb rows start at
+  // shared address wbase; a warp walks only the steps of its k-slice
+  auto mma_rows = [&](uint32_t wbase, int kbase, int krows) {
     const int steps = krows / 16;
     const int gs0 = kbase / 16;
     const int st0 = ((myslice - gs0 % ks) + ks) % ks;
 #pragma unroll 1
     for (int st = st0; st < steps; st += ks) {
-      const uint32_t wrow = wchunk + (st * 16 + (lane & 15)) * pitchW;
+      const uint32_t wrow = wbase + (st * 16 + (lane & 15)) * pitchW;
       const uint32_t arow = nrm_u + (lane & 15) * kPitchN + ((kbase + st * 16) + (lane >> 4) * 8) * 2;
-      uint32_t a[IM][4];
+      // every fragment of the step is loaded before the first MMA (unused
+      // items read a valid address), so the ldmatrix latencies overlap
+      uint32_t a[IM][4], b[QM][2];
 #pragma unroll
       for (int i = 0; i < IM; ++i) ldsm_x4(arow + aoff[i], a[i][0], a[i][1], a[i][2], a[i][3]);
 #pragma unroll
+      for (int q = 0; q < QM; ++q) ldsm_x2_trans(wrow + boff[q], b[q][0], b[q][1]);
+#pragma unroll
       for (int q = 0; q < QM; ++q) {
         if (qv[q]) {
-          uint32_t b0, b1;
-          ldsm_x2_trans(wrow + boff[q], b0, b1);
 #pragma unroll
-          for (int i = 0; i < IM; ++i) mma16816<E::kBf16>(acc[q * IM + i], a[i], b0, b1);
+          for (int i = 0; i < IM; ++i) mma16816<E::kBf16>(acc[q * IM + i], a[i], b[q][0], b[q][1]);
         }
       }
     }
-    kbase += krows;
-    if (c >= 0 && c + nbuf < nchunks) {
-      __syncthreads();  // every warp is done with buffer c % nbuf
-      if (tid == 0) issue_chunk(c + nbuf);
-      issued = c + nbuf + 1;
+  };
+  if (!ring) {
+    mma_rows(smem_u32(sWB), 0, p.kpre);
+  } else {
+    // Chunks are consumed in runs that are contiguous in shared memory (same
+    // region, consecutive slots), one MMA sweep and at most one CTA barrier
+    // per run; a run ends where the chunks whose slots feed a refill end, so
+    // those refills go out as early as possible.
+#pragma unroll 1
+    for (int c = 0; c < nch;) {
+      const int sl = c % nslots;
+      const bool refill = c + nslots < nch;
+      int e = c + 1;
+      while (e < nch && e % nslots == sl + (e - c) && ((e % nslots) < nres) == (sl < nres) &&
+             (e + nslots < nch) == refill)
+        ++e;
+      if (e > nres) {  // some chunks of the run are streamed: wait for their batches
+        const int k0 = c > nres ? c : nres;
+        const int b0 = sBatch[k0], b1 = sBatch[e - 1];
+        if (tid == 0) {
+          int ok = 1;
+          for (int b = b0; b <= b1 && ok; ++b) ok = mbar_wait_bounded(bar_r0 + 8 * b, 0, p.budget_ns) ? 1 : 0;
+          *sFlag = ok;
+        }
+        __syncthreads();
+        if (*reinterpret_cast<volatile int*>(sFlag) == 0) {
+          if (tid == 0) atomicOr(p.status, kStatusTimeout);
+          drain();
+          bar_exit_finish(p.counters, exit_old, G);
+          return;
+        }
+        for (int b = b0; b <= b1; ++b)  // every thread observes the phases
+          while (!mbar_test_wait(bar_r0 + 8 * b, 0)) {
+          }
+      }
+      mma_rows(smem_u32(slot_ptr(sl)), c * CR, (e - c) * CR);
+      if (refill) {
+        __syncthreads();  // every warp is done with these slots
+        if (tid == 0) issue_batch(c + nslots, e + nslots);
+        ++nbatch;
+        issued = e + nslots;
+        __syncthreads();  // sBatch of the new chunks is visible
+      }
+      c = e;
     }
   }
   bar_exit_finish(p.counters, exit_old, G);

@@ -25,6 +25,11 @@ constexpr int kHeadCols = kNope + kV;  // kv_b_proj columns per head (256)
 // Upper bound of token rows per decode launch (larger T is processed in
 // chunks of the plan's tt_max); also the row stride of the workspace.
 constexpr int kDecodeMaxTokens = 128;
+// Bytes per normalised latent row in the workspace: the decode kernel's
+// shared-memory pitch (512 values + 16 bytes of padding), so one bulk copy
+// moves all rows of a launch.
+constexpr int kNrmPitch = 1040;
+constexpr size_t kDecodeNrmBytes = (size_t)kDecodeMaxTokens * kNrmPitch;
 
 struct DecodeParams {
   CUtensorMap tmap_wkvb;    // W_kvb [512, H*256], box = (ngbox*8 columns, 32 rows)

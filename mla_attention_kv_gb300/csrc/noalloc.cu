@@ -41,7 +41,7 @@ namespace {
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kMaxSplitK = 16;
 constexpr size_t kPartialBytes = kMaxSplitK * kDecodeMaxTokens * kNa * sizeof(float);
-constexpr size_t kNrmBytes = (size_t)kDecodeMaxTokens * kRank * 2;
+constexpr size_t kNrmBytes = kDecodeNrmBytes;
 constexpr size_t kScratchBytes = kHeaderBytes + kPartialBytes + kNrmBytes;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
