@@ -514,15 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // Streamed chunks go out in batches -- the buffer chunks at the end of
   // phase A, then the refills after each run of chunks -- and each batch
   // completes on a barrier of its own (bar_r0 + 8 * batch, used once per
-  // launch, so its phase is always 0).  sBatch[c] records the batch of
-  // chunk c for the consumers.
-  unsigned char* sBatch = reinterpret_cast<unsigned char*>(sFlag + 2);
-  int nbatch = 0;  // batches issued (thread 0's count; every thread tracks it)
-  auto issue_batch = [&](int c0, int c1) {  // thread 0 only: chunks [c0, c1), c0 >= nres
+  // launch, so its phase is always 0).  Every thread keeps the batch of
+  // each chunk (4 bits per chunk) in `bmap`, computed identically.
+  int nbatch = 0;       // batches issued
+  uint64_t bmap = 0;    // batch of chunk c in bits [4c, 4c + 4)
+  auto batch_of = [&](int c) { return (int)((bmap >> (4 * c)) & 15u); };
+  auto issue_batch = [&](int c0, int c1) {  // whole warp 0: lane L copies chunk c0 + L
     const uint32_t bar = bar_r0 + 8 * nbatch;
-    mbar_arrive_expect_tx(bar, (uint32_t)((c1 - c0) * CR * pitchW));
-    for (int c = c0; c < c1; ++c) {
-      sBatch[c] = (unsigned char)nbatch;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)((c1 - c0) * CR * pitchW));
+    __syncwarp();
+    const int c = c0 + lane;
+    if (c < c1) {
       const uint32_t dst = smem_u32(slot_ptr(c % nslots));
       if constexpr (PK) {
         bulk_g2s(dst, wkvb_blk + (size_t)c * CR * pitchW, (uint32_t)(CR * pitchW), bar);
@@ -531,10 +533,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
   };
+  auto note_batch = [&](int c0, int c1) {  // every thread
+    for (int c = c0; c < c1; ++c) bmap |= (uint64_t)nbatch << (4 * c);
+    ++nbatch;
+  };
   int issued = ring ? (nslots < nch ? nslots : nch) : nres;  // chunks issued so far
   if (ring) {
-    if (tid == 0) issue_batch(nres, issued);
-    nbatch = 1;
+    if (warp == 0) issue_batch(nres, issued);
+    note_batch(nres, issued);
   }
   // on an early exit, wait (bounded) for this CTA's copies still in flight:
   // the resident rows and every issued chunk not yet observed (at most one
@@ -750,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         ++e;
       if (e > nres) {  // some chunks of the run are streamed: wait for their batches
         const int k0 = c > nres ? c : nres;
-        const int b0 = sBatch[k0], b1 = sBatch[e - 1];
+        const int b0 = batch_of(k0), b1 = batch_of(e - 1);
         if (tid == 0) {
           int ok = 1;
           for (int b = b0; b <= b1 && ok; ++b) ok = mbar_wait_bounded(bar_r0 + 8 * b, 0, p.budget_ns) ? 1 : 0;
@@ -770,10 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mma_rows(smem_u32(slot_ptr(sl)), c * CR, (e - c) * CR);
       if (refill) {
         __syncthreads();  // every warp is done with these slots
-        if (tid == 0) issue_batch(c + nslots, e + nslots);
-        ++nbatch;
+        if (warp == 0) issue_batch(c + nslots, e + nslots);
+        note_batch(c + nslots, e + nslots);
         issued = e + nslots;
-        __syncthreads();  // sBatch of the new chunks is visible
       }
       c = e;
     }
