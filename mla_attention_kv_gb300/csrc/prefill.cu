@@ -74,8 +74,9 @@ static_assert(sizeof(PfShared) <= 256, "barrier block");
 
 struct PfArgs {
   CUtensorMap tm_x;    // hidden [T, hidden], box {64, 128}, SW128
-  CUtensorMap tm_wa;   // W_kva [hidden, 576], box {64, 64}, SW128
-  CUtensorMap tm_wb;   // W_kvb [512, H*256], box {64, 64}, SW128
+  CUtensorMap tm_wa;   // W_kva [hidden, 576], box {64, 64}, SW128 (k_pe pass)
+  CUtensorMap tm_wa3;  // W_kva as [hidden][9][64], box {64, 64, 4}: half a compressed_kv stage
+  CUtensorMap tm_wb3;  // W_kvb as [512][H*4][64], box {64, 64, 2}: half a kv_b stage
   PrefillParams p;
 };
 
@@ -150,7 +151,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&args.tm_x);
     tma_prefetch_desc(&args.tm_wa);
-    tma_prefetch_desc(&args.tm_wb);
+    tma_prefetch_desc(&args.tm_wa3);
+    tma_prefetch_desc(&args.tm_wb3);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -196,8 +198,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           const uint32_t fb = bar(&sh->full1[s]);
           mbar_arrive_expect_tx(fb, 16384 + 65536);
           tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
-          for (int j = (int)crank; j < 8; j += kCl)
-            tma_load_2d_mc(st + 16384 + j * 8192, &args.tm_wa, j * 64, kc * kBK, fb, kClMask);
+          // this CTA's half: column groups 4*crank .. 4*crank+3, one 32 KB box
+          tma_load_3d_mc(st + 16384 + crank * 4 * 8192, &args.tm_wa3, 0, kc * kBK, (int)crank * 4, fb, kClMask);
         }
         // kv_a stages overlap the kv_b ring: wait until both were released
         for (int s = 0; s < 2 && ok; ++s) {
@@ -212,8 +214,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             const uint32_t st = sbase + kS2Base + s * kS2Bytes;
             const uint32_t fb = bar(&sh->full2[s]);
             mbar_arrive_expect_tx(fb, kS2Bytes);
-            for (int q = (int)crank; q < 4; q += kCl)
-              tma_load_2d_mc(st + q * 8192, &args.tm_wb, j * kHeadCols + q * 64, kc * kBK, fb, kClMask);
+            // this CTA's half of head j's 4 column groups, one 16 KB box
+            tma_load_3d_mc(st + crank * 2 * 8192, &args.tm_wb3, 0, kc * kBK, j * 4 + (int)crank * 2, fb, kClMask);
           }
         }
       }
@@ -474,7 +476,8 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   const uint64_t h = (uint64_t)p.hidden_dim, NB = (uint64_t)p.heads * kHeadCols;
   if (!encode_tmap_2d(&a.tm_x, dt, p.hidden, h, (uint64_t)p.T, h * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&a.tm_wa, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&a.tm_wb, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tmap_3d_colblocks(&a.tm_wa3, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, 4, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_3d_colblocks(&a.tm_wb3, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const void* fn = bf16 ? (const void*)prefill_kernel<__nv_bfloat16> : (const void*)prefill_kernel<__half>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

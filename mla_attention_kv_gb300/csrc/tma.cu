@@ -35,4 +35,20 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_3d_colblocks(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t cols, uint64_t rows, uint64_t row_stride, uint32_t inner,
+                              uint32_t box_rows, uint32_t box_blocks, uint32_t elem_bytes,
+                              CUtensorMapSwizzle swizzle) {
+  auto fn = get_encode();
+  if (!fn || cols % inner != 0) return false;
+  cuuint64_t dims[3] = {inner, rows, cols / inner};
+  cuuint64_t strides[2] = {row_stride, (cuuint64_t)inner * elem_bytes};
+  cuuint32_t box[3] = {inner, box_rows, box_blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mla

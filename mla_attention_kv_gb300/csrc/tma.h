@@ -15,6 +15,17 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t inner, uint64_t outer, uint64_t row_stride, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// Encode a 3-D view of a row-major matrix [rows, cols] (cols a multiple of
+// `inner`): element (x, y, z) = M[y][z * inner + x], i.e. dims {inner, rows,
+// cols / inner} with strides {row_stride, inner * element size}.  A box
+// {inner, box_rows, box_blocks} lands in shared memory as box_blocks
+// consecutive [box_rows x inner] blocks -- the MN-major layout of a tensor-core
+// operand made of inner-wide column groups.
+bool encode_tmap_3d_colblocks(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t cols, uint64_t rows, uint64_t row_stride, uint32_t inner,
+                              uint32_t box_rows, uint32_t box_blocks, uint32_t elem_bytes,
+                              CUtensorMapSwizzle swizzle);
+
 #ifdef __CUDACC__
 // Tiled 2-D load of one box into shared memory; completion is counted in
 // bytes on `bar`.  c_inner * element size must be a multiple of 16 bytes.
@@ -35,6 +46,16 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
       "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar), "h"(mask)
+      : "memory");
+}
+// 3-D tiled load of one box into the same shared-memory offset of every CTA
+// in `mask` (cluster multicast); x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
       : "memory");
 }
 // L2 prefetch of one box (no shared-memory destination).
