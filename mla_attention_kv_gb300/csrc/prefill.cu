@@ -45,38 +45,40 @@ namespace mla {
 namespace {
 
 constexpr int kPfThreads = 192;
-constexpr int kCl = 2;                      // CTAs per cluster sharing every weight box
-constexpr uint16_t kClMask = 0x3;
-constexpr int kBM = 128;                    // token rows per tile
+constexpr int kCl = 2;                      // CTAs per cluster: one 2-SM MMA pair
+constexpr int kBM = 128;                    // token rows per CTA tile (256 per pair)
 constexpr int kBK = 64;                     // K elements per TMA box / stage
-constexpr uint32_t kA2Bytes = 8 * 16384;    // normalised tile: 8 K-chunks x [128 x 64]
-constexpr uint32_t kS1Bytes = 81920;        // compressed_kv stage: X 16 KB + W 64 KB
-constexpr uint32_t kS0Base = kS1Bytes;      // k_pe stages: [80 KB, 224 KB)
-constexpr uint32_t kS0Bytes = 24576;        // k_pe stage: X 16 KB + W 8 KB
-constexpr int kS0Stages = 6;
-constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 tile
-constexpr uint32_t kS2Bytes = 32768;        // kv_b stage: [64 K x 256 N]
-constexpr int kS2Stages = 3;
+constexpr uint32_t kA2Bytes = 8 * 16384;    // normalised tile: 8 K-chunks x [128 x 64], [0, 128 KB)
+constexpr uint32_t kS0Base = 0;             // k_pe stages: [0, 120 KB)
+constexpr uint32_t kS0Bytes = 24576;        // k_pe stage: X 16 KB + the 64 k_pe columns of W 8 KB
+constexpr int kS0Stages = 5;
+constexpr uint32_t kS1Bytes = 49152;        // compressed_kv stage: X 16 KB + this CTA's half of two N = 256 tiles
+constexpr int kS1Stages = 2;                // [0, 96 KB)
+constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 tile: [128 KB, 224 KB)
+constexpr uint32_t kS2Bytes = 16384;        // kv_b stage: this CTA's half of [64 K x 256 N]
+constexpr int kS2Stages = 6;
 constexpr uint32_t kBarBase = kS2Base + kS2Stages * kS2Bytes;  // 229376
-constexpr uint32_t kGamBase = kBarBase + 256;                  // gamma [512], I/O dtype
+constexpr uint32_t kGamBase = kBarBase + 512;                  // gamma [512], I/O dtype
 constexpr uint32_t kSmemBytes = kGamBase + 1024 + 1024;        // + alignment slack
+static_assert(kS0Base + kS0Stages * kS0Bytes <= kA2Bytes, "k_pe ring inside the A2 area");
+static_assert(kS1Stages * kS1Bytes <= kA2Bytes, "compressed_kv ring inside the A2 area");
 
 struct PfShared {
   uint64_t full0[kS0Stages], empty0[kS0Stages];
-  uint64_t full1[2], empty1[2];
+  uint64_t full1[kS1Stages], empty1[kS1Stages];
   uint64_t full2[kS2Stages], empty2[kS2Stages];
   uint64_t tfull[2], tempty[2];
   uint64_t a2_ready, a2_free, mma_done;
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(PfShared) <= 256, "barrier block");
+static_assert(sizeof(PfShared) <= 512, "barrier block");
 
 struct PfArgs {
   CUtensorMap tm_x;    // hidden [T, hidden], box {64, 128}, SW128
-  CUtensorMap tm_wa;   // W_kva [hidden, 576], box {64, 64}, SW128 (k_pe pass)
-  CUtensorMap tm_wa3;  // W_kva as [hidden][9][64], box {64, 64, 4}: half a compressed_kv stage
-  CUtensorMap tm_wb3;  // W_kvb as [512][H*4][64], box {64, 64, 2}: half a kv_b stage
+  CUtensorMap tm_wa;   // W_kva [hidden, 576], box {64, 64}, SW128 (the k_pe columns)
+  CUtensorMap tm_wa3;  // W_kva as [hidden][9][64], box {64, 64, 2}: one CTA's half of an N = 256 tile
+  CUtensorMap tm_wb3;  // W_kvb as [512][H*4][64], box {64, 64, 2}: one CTA's half of a head
   PrefillParams p;
 };
 
@@ -85,13 +87,16 @@ struct PfArgs {
 // read them.  tcgen05.fence::after_thread_sync is only issued where TMEM
 // written or read by another thread is reused.)
 // Bounded mbarrier wait shared by all roles; gives up on the time budget
-// or when another role has already given up.
+// or when another role has already given up.  `cluster`: the phase is
+// completed by arrivals from the peer CTA (acquire at cluster scope).
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                        unsigned long long budget, unsigned* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                        unsigned long long budget, unsigned* status,
+                                        bool cluster = false) {
+  auto test = [&]() { return cluster ? tc::test_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!test()) {
     if (((++n) & 63) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > budget) {
@@ -122,32 +127,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const unsigned long long budget = p.budget_ns;
 
   auto bar = [&](uint64_t* b) { return smem_u32(b); };
+  // the leader's (cluster rank 0) copy of a barrier, as a cluster address
+  auto lead = [&](uint64_t* b) { return tc::mapa(smem_u32(b), 0); };
 
   if (threadIdx.x == 0) {
-    // empty barriers (and a2_free) count one MMA-commit arrival from each CTA
-    // of the cluster: a stage is refilled (by multicast) only when both
-    // CTAs have consumed it
-    for (int i = 0; i < 2; ++i) {
+    // full barriers: one arrival (the leader's expect_tx for both CTAs'
+    // bytes); empty / tfull / a2_free / mma_done: one pair-commit arrival;
+    // tempty / a2_ready: one arrival per epilogue warp of both CTAs
+    for (int i = 0; i < kS0Stages; ++i) {
+      mbar_init(bar(&sh->full0[i]), 1);
+      mbar_init(bar(&sh->empty0[i]), 1);
+    }
+    for (int i = 0; i < kS1Stages; ++i) {
       mbar_init(bar(&sh->full1[i]), 1);
-      mbar_init(bar(&sh->empty1[i]), kCl);
-      mbar_init(bar(&sh->tfull[i]), 1);
-      mbar_init(bar(&sh->tempty[i]), 128);
+      mbar_init(bar(&sh->empty1[i]), 1);
     }
     for (int i = 0; i < kS2Stages; ++i) {
       mbar_init(bar(&sh->full2[i]), 1);
-      mbar_init(bar(&sh->empty2[i]), kCl);
+      mbar_init(bar(&sh->empty2[i]), 1);
     }
-    for (int i = 0; i < kS0Stages; ++i) {
-      mbar_init(bar(&sh->full0[i]), 1);
-      mbar_init(bar(&sh->empty0[i]), kCl);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(&sh->tfull[i]), 1);
+      mbar_init(bar(&sh->tempty[i]), 4 * kCl);
     }
-    mbar_init(bar(&sh->a2_ready), 128);
-    mbar_init(bar(&sh->a2_free), kCl);
+    mbar_init(bar(&sh->a2_ready), 4 * kCl);
+    mbar_init(bar(&sh->a2_free), 1);
     mbar_init(bar(&sh->mma_done), 1);
     sh->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(smem_u32(&sh->tmem_base), 512);
+  if (warp == 1) tc::tmem_alloc2(smem_u32(&sh->tmem_base), 512);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&args.tm_x);
     tma_prefetch_desc(&args.tm_wa);
@@ -156,100 +165,103 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   }
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync();  // the peer's barriers are initialised before any multicast
+  tc::cluster_sync();  // both CTAs' barriers are initialised before any copy or commit reaches them
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
   const uint32_t crank = tc::cluster_rank();
+  const bool leader = crank == 0;
   // every CTA of a cluster runs the same number of tiles (tiles past the end
   // are all-padding: TMA fills zeros and the epilogue stores nothing)
   const int iters = (ntiles + (int)gridDim.x - 1) / (int)gridDim.x;
 
   if (warp == 0) {
     // ============================================================ TMA producer
+    // Each CTA loads its own token rows (A) and its half of every weight
+    // tile (B) into its own shared memory; the bytes of both CTAs complete
+    // on the leader's full barrier, whose expect_tx the leader posts.
     if (lane == 0) {
       uint32_t u0 = 0, u1 = 0, u2 = 0;  // uses of the k_pe / compressed_kv / kv_b rings
       int tiles_done = 0;
       bool ok = true;
       for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
         const int m0 = (blockIdx.x + it * gridDim.x) * kBM;
+        // the rings of this tile overlap the previous tile's A2 area
         if (tiles_done > 0 && !pf_wait(bar(&sh->a2_free), (tiles_done - 1) & 1, abort, budget, p.status)) { ok = false; break; }
-        // (a) k_pe pass: 6-stage ring of [X 16 KB | W 8 KB] in [80 KB, 224 KB)
+        // (a) k_pe pass
         for (int kc = 0; kc < nk && ok; ++kc, ++u0) {
           const int s = u0 % kS0Stages;
           if (!pf_wait(bar(&sh->empty0[s]), ((u0 / kS0Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
           const uint32_t st = sbase + kS0Base + s * kS0Bytes;
-          const uint32_t fb = bar(&sh->full0[s]);
-          mbar_arrive_expect_tx(fb, 16384 + 8192);
-          tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
-          if ((u0 & 1) == crank) tma_load_2d_mc(st + 16384, &args.tm_wa, kRank, kc * kBK, fb, kClMask);
+          const uint32_t fb = lead(&sh->full0[s]);
+          if (leader) mbar_arrive_expect_tx(bar(&sh->full0[s]), kCl * kS0Bytes);
+          tma_load_2d_pair(st, &args.tm_x, kc * kBK, m0, fb);
+          tma_load_2d_pair(st + 16384, &args.tm_wa, kRank, kc * kBK, fb);
         }
         if (!ok) break;
-        // (b) compressed_kv pass: 2 stages of [X 16 KB | W 64 KB] in [0, 160 KB);
-        // stage 1 overlaps k_pe stages 0-3, so it waits for their last release
+        // (b) compressed_kv pass: its ring overlaps the k_pe ring, so it
+        // starts once every k_pe stage of this tile has been released
+        for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0 && ok; ++u)
+          if (!pf_wait(bar(&sh->empty0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status)) ok = false;
         for (int kc = 0; kc < nk && ok; ++kc, ++u1) {
-          const int s = u1 & 1;
-          if (kc == 1) {
-            for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0 && ok; ++u)
-              if ((u % kS0Stages) < 4 && !pf_wait(bar(&sh->empty0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status)) ok = false;
-            if (!ok) break;
-          }
-          if (!pf_wait(bar(&sh->empty1[s]), ((u1 >> 1) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
+          const int s = u1 % kS1Stages;
+          if (!pf_wait(bar(&sh->empty1[s]), ((u1 / kS1Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
           const uint32_t st = sbase + s * kS1Bytes;
-          const uint32_t fb = bar(&sh->full1[s]);
-          mbar_arrive_expect_tx(fb, 16384 + 65536);
-          tma_load_2d(st, &args.tm_x, kc * kBK, m0, fb);
-          // this CTA's half: column groups 4*crank .. 4*crank+3, one 32 KB box
-          tma_load_3d_mc(st + 16384 + crank * 4 * 8192, &args.tm_wa3, 0, kc * kBK, (int)crank * 4, fb, kClMask);
+          const uint32_t fb = lead(&sh->full1[s]);
+          if (leader) mbar_arrive_expect_tx(bar(&sh->full1[s]), kCl * kS1Bytes);
+          tma_load_2d_pair(st, &args.tm_x, kc * kBK, m0, fb);
+          // this CTA's 128 columns of each N = 256 tile: groups 2r, 2r+1 and 4+2r, 5+2r
+          tma_load_3d_pair(st + 16384, &args.tm_wa3, 0, kc * kBK, (int)crank * 2, fb);
+          tma_load_3d_pair(st + 32768, &args.tm_wa3, 0, kc * kBK, 4 + (int)crank * 2, fb);
         }
-        // kv_a stages overlap the kv_b ring: wait until both were released
-        for (int s = 0; s < 2 && ok; ++s) {
-          const uint32_t last = (u1 - 1 - s);  // uses u1-1 and u1-2 cover both stages
-          if (!pf_wait(bar(&sh->empty1[last & 1]), (last >> 1) & 1, abort, budget, p.status)) ok = false;
-        }
-        // (c) kv_b: per head, 8 K-chunks of [64 x 256]
+        // (c) kv_b: per head, 8 K-chunks; this CTA's 128 of the head's 256 columns
         for (int j = 0; j < H && ok; ++j) {
           for (int kc = 0; kc < kRank / kBK; ++kc, ++u2) {
             const int s = u2 % kS2Stages;
             if (!pf_wait(bar(&sh->empty2[s]), ((u2 / kS2Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
             const uint32_t st = sbase + kS2Base + s * kS2Bytes;
-            const uint32_t fb = bar(&sh->full2[s]);
-            mbar_arrive_expect_tx(fb, kS2Bytes);
-            // this CTA's half of head j's 4 column groups, one 16 KB box
-            tma_load_3d_mc(st + crank * 2 * 8192, &args.tm_wb3, 0, kc * kBK, j * 4 + (int)crank * 2, fb, kClMask);
+            const uint32_t fb = lead(&sh->full2[s]);
+            if (leader) mbar_arrive_expect_tx(bar(&sh->full2[s]), kCl * kS2Bytes);
+            tma_load_3d_pair(st, &args.tm_wb3, 0, kc * kBK, j * 4 + (int)crank * 2, fb);
           }
         }
       }
-      // drain: every issued load has landed before the CTA may exit
-      for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0; ++u)
-        pf_wait(bar(&sh->full0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status);
-      for (uint32_t u = (u1 > 2 ? u1 - 2 : 0); u < u1; ++u)
-        pf_wait(bar(&sh->full1[u & 1]), (u >> 1) & 1, abort, budget, p.status);
-      for (uint32_t u = (u2 > kS2Stages ? u2 - kS2Stages : 0); u < u2; ++u)
-        pf_wait(bar(&sh->full2[u % kS2Stages]), (u / kS2Stages) & 1, abort, budget, p.status);
+      // drain: on the leader every issued copy of both CTAs has landed (the
+      // leader's full barriers count them) before the pair may exit
+      if (leader) {
+        for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0; ++u)
+          pf_wait(bar(&sh->full0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status);
+        for (uint32_t u = (u1 > (uint32_t)kS1Stages ? u1 - kS1Stages : 0); u < u1; ++u)
+          pf_wait(bar(&sh->full1[u % kS1Stages]), (u / kS1Stages) & 1, abort, budget, p.status);
+        for (uint32_t u = (u2 > (uint32_t)kS2Stages ? u2 - kS2Stages : 0); u < u2; ++u)
+          pf_wait(bar(&sh->full2[u % kS2Stages]), (u / kS2Stages) & 1, abort, budget, p.status);
+      }
     }
   } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    if (lane == 0) {
+    // ============================================================ MMA issuer (leader only)
+    if (lane == 0 && leader) {
       const bool bf = E::kBf16;
-      const uint32_t id64 = tc::idesc_f16(bf, 128, 64, false, true);
-      const uint32_t id256 = tc::idesc_f16(bf, 128, 256, false, true);
-      // base descriptors at shared-memory offset 0: K-major A (SW128, SBO
-      // 1024) and MN-major B (SW128, LBO 8192 between 64-column groups)
+      const uint32_t id128 = tc::idesc_f16(bf, 256, 128, false, true);
+      const uint32_t id256 = tc::idesc_f16(bf, 256, 256, false, true);
+      // base descriptors at shared-memory offset 0 (the same offsets in both
+      // CTAs): K-major A (SW128, SBO 1024) and MN-major B (SW128, LBO 8192
+      // between 64-column groups)
       const uint64_t dA0 = tc::sdesc_sw128(sbase, 16, 1024);
       const uint64_t dB0 = tc::sdesc_sw128(sbase, 8192, 1024);
       uint32_t u0 = 0, u1 = 0, u2 = 0;
       uint32_t wcount[2] = {0, 0}, dcount[2] = {0, 0};
       int tiles_done = 0;
       bool ok = true;
+      // TMEM buffer b is free once both CTAs' epilogues have drained it
       auto drain_buf = [&](int b) -> bool {
         while (dcount[b] < wcount[b]) {
-          if (!pf_wait(bar(&sh->tempty[b]), dcount[b] & 1, abort, budget, p.status)) return false;
+          if (!pf_wait(bar(&sh->tempty[b]), dcount[b] & 1, abort, budget, p.status, true)) return false;
           ++dcount[b];
         }
         return true;
       };
       for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
-        // (a) k_pe into TMEM columns [0, 64)
+        // (a) k_pe into TMEM columns [0, 128): N = 128, each CTA holding the same
+        // 64 k_pe columns, so columns 64..127 repeat 0..63 and are not read
         if (!drain_buf(0)) { ok = false; break; }
         tc::fence_after_sync();
         for (int kc = 0; kc < nk; ++kc, ++u0) {
@@ -258,35 +270,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           // descriptors advance by constant adds (address field in 16-byte units)
           const uint64_t ad = dA0 + (uint64_t)((kS0Base + s * kS0Bytes) >> 4);
           const uint64_t bd = dB0 + (uint64_t)((kS0Base + s * kS0Bytes + 16384) >> 4);
-          tc::mma_f16(tmem, ad, bd, id64, kc > 0);
-          tc::mma_f16(tmem, ad + 2, bd + 128, id64, true);
-          tc::mma_f16(tmem, ad + 4, bd + 256, id64, true);
-          tc::mma_f16(tmem, ad + 6, bd + 384, id64, true);
-          tc::commit_mc(bar(&sh->empty0[s]), kClMask);
+          tc::mma2_f16(tmem, ad, bd, id128, kc > 0);
+          tc::mma2_f16(tmem, ad + 2, bd + 128, id128, true);
+          tc::mma2_f16(tmem, ad + 4, bd + 256, id128, true);
+          tc::mma2_f16(tmem, ad + 6, bd + 384, id128, true);
+          tc::commit2_both(bar(&sh->empty0[s]));
         }
         if (!ok) break;
-        tc::commit(bar(&sh->tfull[0]));
+        tc::commit2_both(bar(&sh->tfull[0]));
         ++wcount[0];
-        // (b) compressed_kv into TMEM columns [0, 512)
+        // (b) compressed_kv into TMEM columns [0, 512): two N = 256 tiles per K step
         if (!drain_buf(0) || !drain_buf(1)) { ok = false; break; }
         tc::fence_after_sync();
         for (int kc = 0; kc < nk; ++kc, ++u1) {
-          const int s = u1 & 1;
-          if (!pf_wait(bar(&sh->full1[s]), (u1 >> 1) & 1, abort, budget, p.status)) { ok = false; break; }
+          const int s = u1 % kS1Stages;
+          if (!pf_wait(bar(&sh->full1[s]), (u1 / kS1Stages) & 1, abort, budget, p.status)) { ok = false; break; }
           const uint64_t ad = dA0 + (uint64_t)((s * kS1Bytes) >> 4);
           const uint64_t bd = dB0 + (uint64_t)((s * kS1Bytes + 16384) >> 4);
           const bool acc = kc > 0;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            tc::mma_f16(tmem, ad + 2 * k, bd + 128 * k, id256, acc || k > 0);
-            tc::mma_f16(tmem + 256, ad + 2 * k, bd + (32768 >> 4) + 128 * k, id256, acc || k > 0);
+            tc::mma2_f16(tmem, ad + 2 * k, bd + 128 * k, id256, acc || k > 0);
+            tc::mma2_f16(tmem + 256, ad + 2 * k, bd + (16384 >> 4) + 128 * k, id256, acc || k > 0);
           }
-          tc::commit_mc(bar(&sh->empty1[s]), kClMask);
+          tc::commit2_both(bar(&sh->empty1[s]));
         }
         if (!ok) break;
-        tc::commit(bar(&sh->tfull[0]));  // the epilogue drains both halves, then signals a2_ready
+        tc::commit2_both(bar(&sh->tfull[0]));  // the epilogues drain both halves, then signal a2_ready
         // (c) kv_b, one head per N = 256 tile
-        if (!pf_wait(bar(&sh->a2_ready), tiles_done & 1, abort, budget, p.status)) { ok = false; break; }
+        if (!pf_wait(bar(&sh->a2_ready), tiles_done & 1, abort, budget, p.status, true)) { ok = false; break; }
         tc::fence_after_sync();
         for (int j = 0; j < H && ok; ++j) {
           const int b = j & 1;
@@ -298,24 +310,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             const uint64_t ad = dA0 + (uint64_t)((kc * 16384) >> 4);
             const uint64_t bd = dB0 + (uint64_t)((kS2Base + s * kS2Bytes) >> 4);
             const uint32_t d = tmem + b * 256;
-            tc::mma_f16(d, ad, bd, id256, kc > 0);
-            tc::mma_f16(d, ad + 2, bd + 128, id256, true);
-            tc::mma_f16(d, ad + 4, bd + 256, id256, true);
-            tc::mma_f16(d, ad + 6, bd + 384, id256, true);
-            tc::commit_mc(bar(&sh->empty2[s]), kClMask);
+            tc::mma2_f16(d, ad, bd, id256, kc > 0);
+            tc::mma2_f16(d, ad + 2, bd + 128, id256, true);
+            tc::mma2_f16(d, ad + 4, bd + 256, id256, true);
+            tc::mma2_f16(d, ad + 6, bd + 384, id256, true);
+            tc::commit2_both(bar(&sh->empty2[s]));
           }
           if (!ok) break;
-          tc::commit(bar(&sh->tfull[b]));
+          tc::commit2_both(bar(&sh->tfull[b]));
           ++wcount[b];
         }
         if (!ok) break;
-        tc::commit_mc(bar(&sh->a2_free), kClMask);
+        tc::commit2_both(bar(&sh->a2_free));
       }
-      // every MMA issued so far has completed before TMEM is released
-      tc::commit(bar(&sh->mma_done));
+      // every MMA issued so far has completed (in both CTAs) before TMEM is released
+      tc::commit2_both(bar(&sh->mma_done));
+      pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
+    } else if (lane == 0) {
+      // the peer CTA releases its tensor memory only after the pair's last MMA
       pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
     }
   } else {
+
     // ============================================================ epilogue
     const int q = warp & 3;                // TMEM lane quadrant
     const int r = q * 32 + lane;           // row within the tile
@@ -373,8 +389,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
+      // release TMEM buffer 0 to the leader's MMA thread (one arrival per warp)
       tc::fence_before_sync();
-      mbar_arrive(bar(&sh->tempty[0]));
+      __syncwarp();
+      if (lane == 0) tc::arrive_cluster_relaxed(lead(&sh->tempty[0]));
       // (b) RMSNorm of compressed_kv -> normalised A tile in shared memory
       if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
       ++uf[0];
@@ -414,9 +432,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           }
         }
       }
+      // the leader's kv_b MMAs read this CTA's A2 rows through the async proxy
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      mbar_arrive(bar(&sh->a2_ready));
+      __syncwarp();
+      if (lane == 0) tc::arrive_cluster(lead(&sh->a2_ready));
       // (c) per head: split into k_nope / value, head-major stores
       T* kn = static_cast<T*>(p.k_nope);
       T* vv = static_cast<T*>(p.value);
@@ -442,19 +462,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           }
         }
         tc::fence_before_sync();
-        mbar_arrive(bar(&sh->tempty[b]));
+        __syncwarp();
+        if (lane == 0) tc::arrive_cluster_relaxed(lead(&sh->tempty[b]));
       }
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
+  // neither CTA leaves, or releases the pair's tensor memory, while its peer
+  // may still copy into it, read it, or arrive on its barriers
+  tc::cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_dealloc2(tmem, 512);
   }
-  // no CTA leaves while its peer may still multicast into it or arrive on it
-  tc::cluster_sync();
 }
 
 }  // namespace
@@ -476,7 +498,7 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   const uint64_t h = (uint64_t)p.hidden_dim, NB = (uint64_t)p.heads * kHeadCols;
   if (!encode_tmap_2d(&a.tm_x, dt, p.hidden, h, (uint64_t)p.T, h * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&a.tm_wa, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_3d_colblocks(&a.tm_wa3, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, 4, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_3d_colblocks(&a.tm_wa3, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_3d_colblocks(&a.tm_wb3, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const void* fn = bf16 ? (const void*)prefill_kernel<__nv_bfloat16> : (const void*)prefill_kernel<__half>;
