@@ -53,15 +53,15 @@ constexpr uint32_t kS0Base = 0;             // k_pe stages: [0, 120 KB)
 constexpr uint32_t kS0Bytes = 24576;        // k_pe stage: X 16 KB + the 64 k_pe columns of W 8 KB
 constexpr int kS0Stages = 5;
 constexpr uint32_t kS1Bytes = 49152;        // compressed_kv stage: X 16 KB + this CTA's half of two N = 256 tiles
-constexpr int kS1Stages = 2;                // [0, 96 KB)
-constexpr uint32_t kS2Base = kA2Bytes;      // kv_b stages live after the A2 tile: [128 KB, 224 KB)
+constexpr int kS1Stages = 3;                // [0, 144 KB): the last stage reaches past the A2 tile
+constexpr uint32_t kS2Base = kS1Stages * kS1Bytes;  // kv_b stages after both: [144 KB, 224 KB)
 constexpr uint32_t kS2Bytes = 16384;        // kv_b stage: this CTA's half of [64 K x 256 N]
-constexpr int kS2Stages = 6;
+constexpr int kS2Stages = 5;
 constexpr uint32_t kBarBase = kS2Base + kS2Stages * kS2Bytes;  // 229376
 constexpr uint32_t kGamBase = kBarBase + 512;                  // gamma [512], I/O dtype
 constexpr uint32_t kSmemBytes = kGamBase + 1024 + 1024;        // + alignment slack
 static_assert(kS0Base + kS0Stages * kS0Bytes <= kA2Bytes, "k_pe ring inside the A2 area");
-static_assert(kS1Stages * kS1Bytes <= kA2Bytes, "compressed_kv ring inside the A2 area");
+static_assert(kS2Base >= kA2Bytes, "kv_b ring clear of the A2 tile");
 
 struct PfShared {
   uint64_t full0[kS0Stages], empty0[kS0Stages];
@@ -331,7 +331,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
     }
   } else {
-
     // ============================================================ epilogue
     const int q = warp & 3;                // TMEM lane quadrant
     const int r = q * 32 + lane;           // row within the tile
@@ -447,18 +446,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         tc::fence_after_sync();
         const size_t orow = (((size_t)bi * H + j) * p.s + si) * kNope;
 #pragma unroll 1
-        for (int c = 0; c < kHeadCols / 32; ++c) {
-          uint32_t x[32];
-          tc::ld32(lane_addr + b * 256 + c * 32, x);
+        for (int c = 0; c < kHeadCols / 32; c += 2) {  // two TMEM loads in flight
+          uint32_t x[2][32];
+          tc::ld32(lane_addr + b * 256 + c * 32, x[0]);
+          tc::ld32(lane_addr + b * 256 + (c + 1) * 32, x[1]);
           tc::wait_ld();
           if (live) {
-            uint32_t o[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = E::pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
-            T* dst = (c < 4 ? kn : vv) + orow + (c & 3) * 32;
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t o[16];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+              for (int i = 0; i < 16; ++i) o[i] = E::pack(__uint_as_float(x[h2][2 * i]), __uint_as_float(x[h2][2 * i + 1]));
+              const int cc = c + h2;
+              T* dst = (cc < 4 ? kn : vv) + orow + (cc & 3) * 32;
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            }
           }
         }
         tc::fence_before_sync();
