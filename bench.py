@@ -419,8 +419,9 @@ def run_gpu(args, wl, rank, world, dev):
     # CUDA graphs of the steps (how a serving engine issues repeated decode
     # steps): captured once, replayed in the timed region
     graphs = wl.capture(dev)
-    for k in range(min(len(graphs), 3)):
-        graphs[k].replay()
+    for _ in range(2):  # upload and warm every graph before the timed region
+        for g in graphs:
+            g.replay()
     torch.cuda.synchronize(dev)
 
     def timed(run_step):
