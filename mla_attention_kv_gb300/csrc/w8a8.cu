@@ -30,6 +30,7 @@ namespace mla {
 namespace {
 
 constexpr int kGThreads = 128;  // 4 warps, 2 x 2 over a 64 x 64 tile
+constexpr int kGemvMaxRows = 8; // M up to this takes the dp4a weight-streaming path
 constexpr int kGBM = 64, kGBN = 64, kGBK = 32;
 constexpr int kPitchA8 = 48;    // smem row pitch (bytes) of a [64 x 32] int8 tile: odd multiple of 16
 constexpr int kPitchBt = 48;    // smem row pitch of the transposed [64 n x 32 k] tile
@@ -151,6 +152,87 @@ __global__ void __launch_bounds__(kGThreads) gemm_s8_kernel(const int8_t* __rest
           } else {
             *reinterpret_cast<int2*>(c) = make_int2(acc[i][j][2 * hf], acc[i][j][2 * hf + 1]);
           }
+        }
+      }
+    }
+  }
+}
+
+// Small-M path (decode sizes): C[m, n] (+)= sum_k A[m, k] * W[k, n] for the
+// M <= MT rows.  The weight stream is the cost, so a lane owns 8 consecutive
+// columns (a warp 256) and walks K 4 rows at a time with 8-byte coalesced
+// loads of each row; the 4 x 8 bytes are transposed with byte permutes into
+// 8 words of 4 K-consecutive weights and accumulated with dp4a (int8 x int8
+// -> int32).  The 4 warps of a CTA take interleaved 4-row groups of the
+// CTA's K range and are summed through shared memory; blockIdx.y splits K
+// across CTAs, whose partials are added with atomics (exact).
+template <int MT>
+__global__ void __launch_bounds__(128) gemv_s8_kernel(const int8_t* __restrict__ A,
+                                                      const int8_t* __restrict__ W, int M, int K,
+                                                      int N, int32_t* __restrict__ C, int ldc,
+                                                      int kchunk, int atomic) {
+  __shared__ int red[3][MT][8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * 256 + lane * 8;
+  const int kb = blockIdx.y * kchunk;
+  const int ke = min(K, kb + kchunk);
+  const bool live = n0 < N;
+  int acc[MT][8];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[m][c] = 0;
+  if (live) {
+    const int8_t* wp = W + (size_t)(kb + 4 * warp) * N + n0;
+#pragma unroll 4
+    for (int k = kb + 4 * warp; k < ke; k += 16) {
+      const uint2 r0 = __ldg(reinterpret_cast<const uint2*>(wp));
+      const uint2 r1 = __ldg(reinterpret_cast<const uint2*>(wp + N));
+      const uint2 r2 = __ldg(reinterpret_cast<const uint2*>(wp + 2 * (size_t)N));
+      const uint2 r3 = __ldg(reinterpret_cast<const uint2*>(wp + 3 * (size_t)N));
+      wp += 16 * (size_t)N;
+      uint32_t w[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // columns 4h .. 4h+3
+        const uint32_t x0 = h ? r0.y : r0.x, x1 = h ? r1.y : r1.x;
+        const uint32_t x2 = h ? r2.y : r2.x, x3 = h ? r3.y : r3.x;
+        const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), lo23 = __byte_perm(x2, x3, 0x5140);
+        const uint32_t hi01 = __byte_perm(x0, x1, 0x7362), hi23 = __byte_perm(x2, x3, 0x7362);
+        w[4 * h + 0] = __byte_perm(lo01, lo23, 0x5410);
+        w[4 * h + 1] = __byte_perm(lo01, lo23, 0x7632);
+        w[4 * h + 2] = __byte_perm(hi01, hi23, 0x5410);
+        w[4 * h + 3] = __byte_perm(hi01, hi23, 0x7632);
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+          const int a = __ldg(reinterpret_cast<const int*>(A + (size_t)m * K + k));
+#pragma unroll
+          for (int c = 0; c < 8; ++c) acc[m][c] = __dp4a((int)w[c], a, acc[m][c]);
+        }
+      }
+    }
+  }
+  if (warp > 0) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) red[warp - 1][m][c][lane] = acc[m][c];
+  }
+  __syncthreads();
+  if (warp == 0 && live) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m < M) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[m][c] += red[0][m][c][lane] + red[1][m][c][lane] + red[2][m][c][lane];
+        int32_t* cp = C + (size_t)m * ldc + n0;
+        if (atomic) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) atomicAdd(cp + j, acc[m][j]);
+        } else {
+          *reinterpret_cast<int4*>(cp) = make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+          *reinterpret_cast<int4*>(cp + 4) = make_int4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
         }
       }
     }
@@ -328,8 +410,36 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int g_num_sms = 148;
 
+// Small-M launch: 256-column blocks x K splits of at least 128 rows (32 per
+// warp), aiming at about 4 CTAs per SM.
+cudaError_t gemv(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
+                 cudaStream_t st, int* launches) {
+  const int tn = (N + 255) / 256;
+  long per = ((long)K * tn + 4L * g_num_sms - 1) / (4L * g_num_sms);
+  int kchunk = (int)((per + 63) / 64 * 64);
+  if (kchunk < 128) kchunk = 128;
+  if (kchunk > K) kchunk = (K + 15) / 16 * 16;
+  const int splits = (K + kchunk - 1) / kchunk;
+  if (splits > 1) {
+    cudaError_t e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, M, st);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  }
+  dim3 grid(tn, splits);
+  const int atomic = splits > 1 ? 1 : 0;
+  if (M <= 1) gemv_s8_kernel<1><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
+  else if (M <= 2) gemv_s8_kernel<2><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
+  else if (M <= 4) gemv_s8_kernel<4><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
+  else gemv_s8_kernel<8><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
+  ++*launches;
+  return cudaGetLastError();
+}
+
 cudaError_t gemm(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
                  cudaStream_t st, int* launches) {
+  // decode sizes stream the weights; the 64 x 64 tensor-core tiles would be
+  // mostly padding rows
+  if (M <= kGemvMaxRows && K % 16 == 0 && N % 8 == 0) return gemv(A, W, M, K, N, C, ldc, st, launches);
   const int tn = N / kGBN, tm = (M + kGBM - 1) / kGBM;
   int splits = 1;
   const int tiles = tn * tm;
