@@ -36,8 +36,10 @@ struct mla_prolog_s {
   size_t pk_kva_bytes, pk_bytes;
   const void* pk_src_kva;
   const void* pk_src_kvb;
-  // W8A8 workspace (see w8a8.cu)
+  // W8A8 workspace, decode-size launch plan and tensor maps (see w8a8.cu)
   W8Workspace w8;
+  W8SmallPlan w8plan;
+  W8Maps w8maps;
   // tensor maps of recently seen W_kvb pointers (decode kernel)
   static constexpr int kMapCache = 64;
   const void* map_ptr[kMapCache];
@@ -138,7 +140,8 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
   off += kDecodeNrmBytes;
   off = (off + 255) & ~(size_t)255;
   size_t w8_off = off;
-  if (c.quant == MLA_QUANT_W8A8) off += w8_workspace_bytes(c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens);
+  if (c.quant == MLA_QUANT_W8A8)
+    off += w8_workspace_bytes(c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens, h->num_sms);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -157,7 +160,17 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
   h->counters = reinterpret_cast<unsigned*>(base + 64);
   h->partials = reinterpret_cast<float*>(base + part_off);
   h->nrm = base + nrm_off;
-  if (c.quant == MLA_QUANT_W8A8) w8_workspace_carve(base + w8_off, c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens, &h->w8);
+  if (c.quant == MLA_QUANT_W8A8) {
+    w8_workspace_carve(base + w8_off, c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens,
+                       h->num_sms, &h->w8, &h->w8plan);
+    e = w8_workspace_init(h->w8, h->w8plan, c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens,
+                          h->num_sms);
+    if (e != cudaSuccess) {
+      cudaFree(h->ws);
+      delete h;
+      return cuda_fail(e, "W8A8 workspace init");
+    }
+  }
   *out = h;
   return MLA_OK;
 }
@@ -325,9 +338,18 @@ mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_
   p.sin_t = sin_table; p.q_nope = q_nope; p.q_pe = q_pe; p.k_nope = k_nope; p.value = value;
   p.k_pe = k_pe; p.status = h->status; p.hidden_dim = h->cfg.hidden;
   p.q_rank = h->cfg.q_lora_rank; p.heads = h->cfg.num_heads; p.s = s; p.T = (int)T;
-  p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
+  p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps; p.budget_ns = h->budget_ns;
+  // tensor maps of the decode-size chain, re-encoded when a weight pointer changes
+  const W8Maps* maps = nullptr;
+  if (T <= kW8SmallRows) {
+    W8Maps& m = h->w8maps;
+    if (!m.valid || m.src[0] != W_qa || m.src[1] != W_kva || m.src[2] != W_qb || m.src[3] != W_kvb)
+      w8_encode_maps(p, h->w8plan, &m);
+    if (!m.valid) return cuda_fail(cudaErrorInvalidValue, "W8A8 tensor maps");
+    maps = &m;
+  }
   int launches = 0;
-  cudaError_t e = w8a8_launch(p, h->w8, h->num_sms, stream, &launches);
+  cudaError_t e = w8a8_launch(p, h->w8, h->w8plan, maps, h->num_sms, stream, &launches);
   h->last_launches = launches;
   h->last_path = MLA_PATH_AUTO;
   if (e != cudaSuccess) return cuda_fail(e, "w8a8 launch");

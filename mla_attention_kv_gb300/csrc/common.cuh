@@ -188,6 +188,16 @@ __device__ __forceinline__ void mma16832_s8(int* d, const uint32_t* a, uint32_t 
 // ---------------------------------------------------------------- timing / sync
 __device__ __forceinline__ uint64_t globaltimer_ns() { return globaltimer_ns_(); }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel in
+// the stream (launched with programmatic stream serialisation) start while
+// this one runs; grid_dep_wait blocks until the kernel before this one has
+// completed and its memory operations are visible.  Both are no-ops when the
+// launches carry no programmatic dependency.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -149,6 +149,24 @@ struct W8Workspace {
   int32_t* acc2;  // [max_tokens, max(H*192, H*256)]
 };
 
+// Decode-size W8A8 chain (T <= kW8SmallRows): tensor maps of the four int8
+// weight matrices and the per-handle launch plan.
+constexpr int kW8SmallRows = 8;
+struct W8Maps {
+  CUtensorMap qa, kva;  // W_qa [hidden, q_rank], W_kva [hidden, 576]: box 256 columns x kchunk rows
+  CUtensorMap qb, kvb;  // W_qb [q_rank, H*192], W_kvb [512, H*256]: box 128 columns x 256 rows
+  const void* src[4];   // the pointers they describe
+  bool valid;
+};
+struct W8SmallPlan {
+  int kchunk, splits;   // kv_a/q_a split-K: rows per chunk (multiple of 16, <= 256), chunk count
+  int nblk_a1, nblk_a;  // 256-column blocks of q_a, of q_a + kv_a
+  int nblk_b1, nblk_b;  // 128-column blocks of q_b, of q_b + kv_b
+  int grid_b;           // CTAs of the q_b / kv_b kernel
+  int* units;           // device: [grid_b + 1] offsets, then block ids (workspace)
+  int max_units;        // longest per-CTA list
+};
+
 struct W8Params {
   const void* hidden;
   const int32_t* positions;
@@ -172,13 +190,21 @@ struct W8Params {
   unsigned* status;
   int hidden_dim, q_rank, heads, s, T, max_pos;
   float eps;
+  unsigned long long budget_ns;
 };
 
-size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens);
+size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens, int num_sms);
 void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,
-                        W8Workspace* w);
-cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, int num_sms,
-                        cudaStream_t stream, int* launches);
+                        int num_sms, W8Workspace* w, W8SmallPlan* plan);
+// Zero the q_a/kv_a accumulator rows and upload the q_b/kv_b work lists
+// (once, when the handle is created; synchronous).
+cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int hidden,
+                              int q_rank, int heads, int max_tokens, int num_sms);
+// Tensor maps of the decode-size chain for these weight pointers (false if
+// the driver rejects one).
+bool w8_encode_maps(const W8Params& p, const W8SmallPlan& plan, W8Maps* maps);
+cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPlan& plan,
+                        const W8Maps* maps, int num_sms, cudaStream_t stream, int* launches);
 cudaError_t w8a8_quant_rows_launch(const void* x_bf16, int rows, int cols, int8_t* q,
                                    float* scale, cudaStream_t stream);
 cudaError_t w8a8_gemm_s32_launch(const int8_t* A, const int8_t* W, int M, int K, int N,

@@ -23,8 +23,12 @@
 // few output tiles to fill the GPU the K range is split across CTAs and
 // the int32 partials are added with atomics, which is exact and
 // order-independent.
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tma.h"
 
 namespace mla {
 namespace {
@@ -158,87 +162,6 @@ __global__ void __launch_bounds__(kGThreads) gemm_s8_kernel(const int8_t* __rest
   }
 }
 
-// Small-M path (decode sizes): C[m, n] (+)= sum_k A[m, k] * W[k, n] for the
-// M <= MT rows.  The weight stream is the cost, so a lane owns 8 consecutive
-// columns (a warp 256) and walks K 4 rows at a time with 8-byte coalesced
-// loads of each row; the 4 x 8 bytes are transposed with byte permutes into
-// 8 words of 4 K-consecutive weights and accumulated with dp4a (int8 x int8
-// -> int32).  The 4 warps of a CTA take interleaved 4-row groups of the
-// CTA's K range and are summed through shared memory; blockIdx.y splits K
-// across CTAs, whose partials are added with atomics (exact).
-template <int MT>
-__global__ void __launch_bounds__(128) gemv_s8_kernel(const int8_t* __restrict__ A,
-                                                      const int8_t* __restrict__ W, int M, int K,
-                                                      int N, int32_t* __restrict__ C, int ldc,
-                                                      int kchunk, int atomic) {
-  __shared__ int red[3][MT][8][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * 256 + lane * 8;
-  const int kb = blockIdx.y * kchunk;
-  const int ke = min(K, kb + kchunk);
-  const bool live = n0 < N;
-  int acc[MT][8];
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int c = 0; c < 8; ++c) acc[m][c] = 0;
-  if (live) {
-    const int8_t* wp = W + (size_t)(kb + 4 * warp) * N + n0;
-#pragma unroll 4
-    for (int k = kb + 4 * warp; k < ke; k += 16) {
-      const uint2 r0 = __ldg(reinterpret_cast<const uint2*>(wp));
-      const uint2 r1 = __ldg(reinterpret_cast<const uint2*>(wp + N));
-      const uint2 r2 = __ldg(reinterpret_cast<const uint2*>(wp + 2 * (size_t)N));
-      const uint2 r3 = __ldg(reinterpret_cast<const uint2*>(wp + 3 * (size_t)N));
-      wp += 16 * (size_t)N;
-      uint32_t w[8];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // columns 4h .. 4h+3
-        const uint32_t x0 = h ? r0.y : r0.x, x1 = h ? r1.y : r1.x;
-        const uint32_t x2 = h ? r2.y : r2.x, x3 = h ? r3.y : r3.x;
-        const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), lo23 = __byte_perm(x2, x3, 0x5140);
-        const uint32_t hi01 = __byte_perm(x0, x1, 0x7362), hi23 = __byte_perm(x2, x3, 0x7362);
-        w[4 * h + 0] = __byte_perm(lo01, lo23, 0x5410);
-        w[4 * h + 1] = __byte_perm(lo01, lo23, 0x7632);
-        w[4 * h + 2] = __byte_perm(hi01, hi23, 0x5410);
-        w[4 * h + 3] = __byte_perm(hi01, hi23, 0x7632);
-      }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m < M) {
-          const int a = __ldg(reinterpret_cast<const int*>(A + (size_t)m * K + k));
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[m][c] = __dp4a((int)w[c], a, acc[m][c]);
-        }
-      }
-    }
-  }
-  if (warp > 0) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) red[warp - 1][m][c][lane] = acc[m][c];
-  }
-  __syncthreads();
-  if (warp == 0 && live) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[m][c] += red[0][m][c][lane] + red[1][m][c][lane] + red[2][m][c][lane];
-        int32_t* cp = C + (size_t)m * ldc + n0;
-        if (atomic) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) atomicAdd(cp + j, acc[m][j]);
-        } else {
-          *reinterpret_cast<int4*>(cp) = make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-          *reinterpret_cast<int4*>(cp + 4) = make_int4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
-        }
-      }
-    }
-  }
-}
-
 // Block-wide max / sum over 256 threads.
 template <bool kMax>
 __device__ __forceinline__ float block_reduce(float v, float* scratch) {
@@ -294,20 +217,27 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
 
 // Per token: dequantise the [q_rank + 576] accumulator row, RMSNorm of the
 // q latent and of compressed_kv, requantise both, RoPE of k_pe.
-__global__ void __launch_bounds__(256) norm_quant_kernel(const int32_t* __restrict__ acc1,
+__global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ acc1,
                                                          const float* __restrict__ sx,
                                                          W8Params p, W8Workspace w) {
   extern __shared__ float yrow[];  // [q_rank + 576]
   __shared__ float scratch[8];
+  // in the decode-size chain this kernel is launched while the GEMV that
+  // produces acc1 still runs: let the next kernel start, then wait for acc1
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   const int t = blockIdx.x;
   const int rq = p.q_rank, na = rq + kNa;
   const float s = sx[t];
-  const int32_t* a = acc1 + (size_t)t * na;
+  int32_t* a = acc1 + (size_t)t * na;
   for (int c = threadIdx.x; c < na; c += 256) {
     const float sw = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
     yrow[c] = __fmul_rn(__fmul_rn((float)a[c], s), sw);
   }
   __syncthreads();
+  // leave the accumulator row zeroed: the decode-size chain adds its split-K
+  // partials into it atomically without clearing it first
+  for (int c = threadIdx.x; c < na; c += 256) a[c] = 0;
   // q latent
   float ss = 0.f;
   for (int c = threadIdx.x; c < rq; c += 256) ss += yrow[c] * yrow[c];
@@ -406,40 +336,643 @@ __global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __rest
   }
 }
 
+// ---------------------------------------------------------------- decode-size chain (T <= 8)
+// Three launches instead of about ten, chained with programmatic dependent
+// launch so that each kernel is resident, with its weight copies in flight,
+// before its predecessor finishes:
+//   front  q_a / kv_a split-K GEMV.  A TMA copy of the CTA's weight tile is
+//          issued at entry; meanwhile the CTA quantises the hidden rows
+//          itself (every CTA finds the same amax, so the codes are those of
+//          step 1); int32 partials are added atomically into the accumulator
+//          rows, which the norm kernel leaves zeroed after reading them.  The
+//          CTA also prefetches its share of W_qb and W_kvb into L2, so that
+//          the whole weight stream is requested in the first microsecond.
+//   norm   RMSNorms, requantisation, RoPE(k_pe) (norm_quant_kernel).
+//   back   q_b and kv_b, full K per 128-column block, each CTA walking a
+//          fixed list of blocks through a ring of TMA boxes; dequantisation,
+//          RoPE(q_pe) and the head-major stores happen in the epilogue, so no
+//          int32 accumulator goes back to memory.
+// The two GEMV kernels also serve the plain int8 GEMM entry for M <= 8 (no
+// quantisation, int32 results stored), which is how their integer sums are
+// checked bit for bit.
+
+struct W8FrontParams {
+  CUtensorMap tm[2];               // W_qa, W_kva (or the one matrix of a plain GEMM)
+  const void* x;                   // QUANT: bf16 hidden rows [M, K]; else int8 A [M, K]
+  int32_t* acc;                    // [M, ldc]
+  float* sx;                       // QUANT: [M] per-row scales
+  const unsigned char* pf[2];      // L2 prefetch ranges (W_qb, W_kvb)
+  unsigned long long pf_bytes[2];
+  unsigned* status;
+  unsigned long long budget_ns;
+  int M, K, ldc;
+  int n[2];                        // columns of each matrix
+  int bw[2];                       // box width (bytes = columns) of each matrix, <= 256
+  int nblk1;                       // 256-column blocks of matrix 0
+  int kchunk;                      // K rows per CTA (box height), multiple of 16
+  int atomic;                      // add into acc (split K) instead of storing
+};
+
+// Grid (column blocks of matrix 0 then of matrix 1, K chunks); 128 threads.
+// Shared memory: weight box [kchunk][bw] | codes [MT][kchunk] | reduction
+// [3][MT][8][32] int | per-warp amax [4][MT] | mbarrier | flag.
+template <int MT, bool QUANT>
+__global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W8FrontParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kc = p.kchunk, k4n = kc >> 2;
+  const int bx = blockIdx.x, kb = blockIdx.y * kc;
+  const int sel = bx < p.nblk1 ? 0 : 1;
+  const int col0 = (sel ? bx - p.nblk1 : bx) * 256;
+  const int N = p.n[sel], bw = p.bw[sel];
+  const int coff = sel ? p.n[0] : 0;
+  unsigned char* sW = sm;
+  uint32_t* sX = reinterpret_cast<uint32_t*>(sm + 256 * kc);
+  int* red = reinterpret_cast<int*>(sm + 256 * kc + MT * kc);
+  float* s_amax = reinterpret_cast<float*>(red + 3 * MT * 256);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_amax + 4 * MT);
+  int* s_flag = reinterpret_cast<int*>(s_bar + 1);
+  const uint32_t bar = smem_u32(s_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, (uint32_t)(bw * kc));
+    tma_load_2d(smem_u32(sW), &p.tm[sel], col0, kb, bar);
+  } else if (tid == 32) {
+    // this CTA's share of the q_b / kv_b weight bytes, prefetched into L2
+    const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y;
+    const unsigned long long id = (unsigned long long)blockIdx.y * gridDim.x + bx;
+    const unsigned long long tot = p.pf_bytes[0] + p.pf_bytes[1];
+    const unsigned long long per = ((tot + nct - 1) / nct + 15) & ~15ull;
+    const unsigned long long b0 = id * per, b1 = b0 + per < tot ? b0 + per : tot;
+    unsigned long long base = 0;
+    for (int r = 0; r < 2; ++r) {
+      const unsigned long long lo = b0 > base ? b0 : base;
+      const unsigned long long end = base + p.pf_bytes[r];
+      const unsigned long long hi = b1 < end ? b1 : end;
+      for (unsigned long long o = lo; o < hi; o += 65536ull) {
+        const unsigned long long len = hi - o < 65536ull ? hi - o : 65536ull;
+        prefetch_l2_bulk(p.pf[r] + (o - base), (uint32_t)len);
+      }
+      base = end;
+    }
+  }
+  grid_dep_launch_dependents();
+  // activation codes of rows [kb, kb + kc), four per word, zero past K
+  if constexpr (QUANT) {
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+    float am[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) am[m] = 0.f;
+    for (int i = tid; i < (p.K >> 3); i += 128) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * p.K) + i);
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) am[m] = fmaxf(am[m], fabsf(__bfloat162float(e[j])));
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) am[m] = fmaxf(am[m], __shfl_xor_sync(0xffffffffu, am[m], o));
+      if (lane == 0) s_amax[warp * MT + m] = am[m];
+    }
+    __syncthreads();
+    for (int i = tid; i < MT * k4n; i += 128) {
+      const int m = i / k4n, k = kb + 4 * (i - m * k4n);
+      uint32_t word = 0;
+      if (m < p.M && k < p.K) {
+        const float amax = fmaxf(fmaxf(s_amax[m], s_amax[MT + m]), fmaxf(s_amax[2 * MT + m], s_amax[3 * MT + m]));
+        const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)m * p.K + k));
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          word |= (uint32_t)(uint8_t)q8(__bfloat162float(e[j]), inv) << (8 * j);
+      }
+      sX[i] = word;
+    }
+    if (bx == 0 && blockIdx.y == 0 && tid < p.M) {
+      const float amax = fmaxf(fmaxf(s_amax[tid], s_amax[MT + tid]), fmaxf(s_amax[2 * MT + tid], s_amax[3 * MT + tid]));
+      p.sx[tid] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    }
+  } else {
+    const int8_t* A = static_cast<const int8_t*>(p.x);
+    for (int i = tid; i < MT * k4n; i += 128) {
+      const int m = i / k4n, k = kb + 4 * (i - m * k4n);
+      sX[i] = (m < p.M && k < p.K) ? __ldg(reinterpret_cast<const uint32_t*>(A + (size_t)m * p.K + k)) : 0u;
+    }
+  }
+  __syncthreads();
+  // the weight tile (bounded wait; on expiry record it, let the copy land, leave)
+  if (tid == 0) *s_flag = mbar_wait_bounded(bar, 0, p.budget_ns) ? 1 : 0;
+  __syncthreads();
+  if (*reinterpret_cast<volatile int*>(s_flag) == 0) {
+    if (tid == 0) {
+      if (p.status) atomicOr(p.status, kStatusTimeout);
+      mbar_wait_bounded(bar, 0, p.budget_ns);
+    }
+    return;
+  }
+  while (!mbar_test_wait(bar, 0)) {
+  }
+  // a lane owns 8 columns; warp w takes the 4-row groups w, w + 4, ...
+  int acc[MT][8];
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[m][c] = 0;
+  const bool live = lane * 8 < bw && col0 + lane * 8 < N;
+  if (live) {
+    for (int g = warp; g < k4n; g += 4) {
+      const unsigned char* wr = sW + (size_t)(4 * g) * bw + lane * 8;
+      const uint2 r0 = *reinterpret_cast<const uint2*>(wr);
+      const uint2 r1 = *reinterpret_cast<const uint2*>(wr + bw);
+      const uint2 r2 = *reinterpret_cast<const uint2*>(wr + 2 * bw);
+      const uint2 r3 = *reinterpret_cast<const uint2*>(wr + 3 * bw);
+      uint32_t w[8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // columns 4h .. 4h+3
+        const uint32_t x0 = h ? r0.y : r0.x, x1 = h ? r1.y : r1.x;
+        const uint32_t x2 = h ? r2.y : r2.x, x3 = h ? r3.y : r3.x;
+        const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), lo23 = __byte_perm(x2, x3, 0x5140);
+        const uint32_t hi01 = __byte_perm(x0, x1, 0x7362), hi23 = __byte_perm(x2, x3, 0x7362);
+        w[4 * h + 0] = __byte_perm(lo01, lo23, 0x5410);
+        w[4 * h + 1] = __byte_perm(lo01, lo23, 0x7632);
+        w[4 * h + 2] = __byte_perm(hi01, hi23, 0x5410);
+        w[4 * h + 3] = __byte_perm(hi01, hi23, 0x7632);
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+          const int a = (int)sX[m * k4n + g];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) acc[m][c] = __dp4a((int)w[c], a, acc[m][c]);
+        }
+      }
+    }
+  }
+  if (warp > 0) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) red[((warp - 1) * MT + m) * 256 + c * 32 + lane] = acc[m][c];
+  }
+  __syncthreads();
+  if (warp == 0 && live) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m < p.M) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          acc[m][c] += red[m * 256 + c * 32 + lane] + red[(MT + m) * 256 + c * 32 + lane] +
+                       red[(2 * MT + m) * 256 + c * 32 + lane];
+        int32_t* cp = p.acc + (size_t)m * p.ldc + coff + col0 + lane * 8;
+        if (p.atomic) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) atomicAdd(cp + j, acc[m][j]);
+        } else {
+          *reinterpret_cast<int4*>(cp) = make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+          *reinterpret_cast<int4*>(cp + 4) = make_int4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+        }
+      }
+    }
+  }
+}
+
+__host__ __device__ constexpr size_t w8_front_smem(int MT, int kc) {
+  return 128 + 256 * (size_t)kc + (size_t)MT * kc + 3 * (size_t)MT * 1024 + 16 * (size_t)MT + 64;
+}
+
+constexpr int kBackStages = 3;      // TMA boxes in flight per CTA
+constexpr int kBackBox = 32768;     // bytes per ring slot (128 columns x 256 rows)
+
+struct W8BackParams {
+  CUtensorMap tm[2];               // W_qb, W_kvb (or one matrix): box bw x brows
+  const int8_t* act[2];            // int8 rows [M, K] feeding each matrix
+  const float* srow[2];            // [M] row scales (prolog mode)
+  const float* scol[2];            // [N] column scales (prolog mode)
+  const int* units;                // [grid + 1] offsets, then block ids; null: block b -> CTA b % grid
+  int32_t* raw;                    // raw mode: C [M, raw_ld]
+  void* q_nope;
+  void* q_pe;
+  void* k_nope;
+  void* value;
+  const int32_t* positions;
+  const float* cos_t;
+  const float* sin_t;
+  unsigned* status;
+  unsigned long long budget_ns;
+  int M, s, heads, max_pos, raw_ld, raw_mode;
+  int K[2], N[2];
+  int bw[2];                       // box width in columns (128, or N when N < 128)
+  int brows[2];                    // box height in rows (256, or K when K < 256)
+  int nbox[2];                     // boxes per block: ceil(K / brows)
+  int kpad[2];                     // nbox * brows: activation row length in shared memory
+  int nblk1, nblk;                 // blocks of matrix 0, of both
+};
+
+// Persistent over the CTA's blocks; 256 threads.  Warp w takes rows
+// [32w, 32w + 32) of each box, a lane 4 columns (one 4-byte load per row, a
+// warp one 128-byte row).  Shared memory: ring [kBackStages][32 KB] |
+// activations [MT][kpad0] then [MT][kpad1] | reduction [8][MT][128] int |
+// mbarriers.
+template <int MT>
+__global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8BackParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  unsigned char* ring = sm;
+  int8_t* sAct0 = reinterpret_cast<int8_t*>(sm + kBackStages * kBackBox);
+  int8_t* sAct1 = sAct0 + MT * p.kpad[0];
+  int* red = reinterpret_cast<int*>(sAct1 + MT * p.kpad[1]);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(red + 8 * MT * 128);
+  // this CTA's blocks
+  int u0, nu;
+  const int* ulist = nullptr;
+  if (p.units) {
+    u0 = p.units[cta];
+    nu = p.units[cta + 1] - u0;
+    ulist = p.units + G + 1 + u0;
+  } else {
+    u0 = cta;
+    nu = cta < p.nblk ? (p.nblk - 1 - cta) / G + 1 : 0;
+  }
+  if (nu == 0) return;
+  auto block_of = [&](int i) { return ulist ? ulist[i] : u0 + i * G; };
+  // producer state (thread 0): next box to issue
+  int iss_u = 0, iss_j = 0, issued = 0;
+  auto issue_next = [&]() {
+    if (iss_u >= nu) return;
+    const int b = block_of(iss_u);
+    const int sel = b < p.nblk1 ? 0 : 1;
+    const int x = (sel ? b - p.nblk1 : b) * 128;
+    const int slot = issued % kBackStages;
+    const uint32_t bar = smem_u32(s_bar + slot);
+    mbar_arrive_expect_tx(bar, (uint32_t)(p.bw[sel] * p.brows[sel]));
+    tma_load_2d(smem_u32(ring + slot * kBackBox), &p.tm[sel], x, iss_j * p.brows[sel], bar);
+    ++issued;
+    if (++iss_j == p.nbox[sel]) {
+      iss_j = 0;
+      ++iss_u;
+    }
+  };
+  if (tid == 0) {
+    for (int i = 0; i < kBackStages; ++i) mbar_init(smem_u32(s_bar + i), 1);
+    fence_mbar_init();
+    // weights are read-only inputs: their copies may start before the
+    // kernel that produces the activations has finished
+    for (int i = 0; i < kBackStages; ++i) issue_next();
+  }
+  grid_dep_wait();
+  // activation rows (zero past K) -- written by the previous kernel
+  for (int sel = 0; sel < 2; ++sel) {
+    const int kp = p.kpad[sel], K = p.K[sel];
+    int8_t* dst = sel ? sAct1 : sAct0;
+    if (p.raw_mode && sel == 1) break;
+    for (int i = tid; i < MT * (kp >> 4); i += 256) {
+      const int m = i / (kp >> 4), k = 16 * (i - m * (kp >> 4));
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m < p.M && k < K) v = *reinterpret_cast<const uint4*>(p.act[sel] + (size_t)m * K + k);
+      *reinterpret_cast<uint4*>(dst + m * kp + k) = v;
+    }
+  }
+  __syncthreads();
+  int consumed = 0;
+  for (int ui = 0; ui < nu; ++ui) {
+    const int b = block_of(ui);
+    const int sel = b < p.nblk1 ? 0 : 1;
+    const int bw = p.bw[sel], kp = p.kpad[sel];
+    const int8_t* act = sel ? sAct1 : sAct0;
+    int acc[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[m][c] = 0;
+    for (int j = 0; j < p.nbox[sel]; ++j) {
+      const int slot = consumed % kBackStages;
+      const uint32_t bar = smem_u32(s_bar + slot);
+      const uint32_t par = (uint32_t)(consumed / kBackStages) & 1u;
+      const bool ok = mbar_wait_bounded(bar, par, p.budget_ns);
+      if (!__syncthreads_and(ok ? 1 : 0)) {
+        if (tid == 0) {
+          if (p.status) atomicOr(p.status, kStatusTimeout);
+          for (int q = consumed; q < issued; ++q)
+            mbar_wait_bounded(smem_u32(s_bar + q % kBackStages), (uint32_t)(q / kBackStages) & 1u,
+                              p.budget_ns);
+        }
+        return;
+      }
+      const int r0 = 32 * warp;
+      if (lane * 4 < bw && r0 < p.brows[sel]) {
+        const unsigned char* wb = ring + slot * kBackBox + (size_t)r0 * bw + lane * 4;
+        const int8_t* ab = act + j * p.brows[sel] + r0;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          if (r0 + 4 * g < p.brows[sel]) {
+            const uint32_t x0 = *reinterpret_cast<const uint32_t*>(wb + (4 * g) * bw);
+            const uint32_t x1 = *reinterpret_cast<const uint32_t*>(wb + (4 * g + 1) * bw);
+            const uint32_t x2 = *reinterpret_cast<const uint32_t*>(wb + (4 * g + 2) * bw);
+            const uint32_t x3 = *reinterpret_cast<const uint32_t*>(wb + (4 * g + 3) * bw);
+            const uint32_t lo01 = __byte_perm(x0, x1, 0x5140), lo23 = __byte_perm(x2, x3, 0x5140);
+            const uint32_t hi01 = __byte_perm(x0, x1, 0x7362), hi23 = __byte_perm(x2, x3, 0x7362);
+            const uint32_t w0 = __byte_perm(lo01, lo23, 0x5410), w1 = __byte_perm(lo01, lo23, 0x7632);
+            const uint32_t w2 = __byte_perm(hi01, hi23, 0x5410), w3 = __byte_perm(hi01, hi23, 0x7632);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              if (m < p.M) {
+                const int a = *reinterpret_cast<const int*>(ab + m * kp + 4 * g);
+                acc[m][0] = __dp4a((int)w0, a, acc[m][0]);
+                acc[m][1] = __dp4a((int)w1, a, acc[m][1]);
+                acc[m][2] = __dp4a((int)w2, a, acc[m][2]);
+                acc[m][3] = __dp4a((int)w3, a, acc[m][3]);
+              }
+            }
+          }
+        }
+      }
+      ++consumed;
+      __syncthreads();  // every warp is done with the slot
+      if (tid == 0) issue_next();
+    }
+    // sum the 8 warps' partials, then the epilogue (two adjacent columns per item)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      *reinterpret_cast<int4*>(red + (warp * MT + m) * 128 + lane * 4) =
+          make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    __syncthreads();
+    const int cb = (sel ? b - p.nblk1 : b) * 128;
+    for (int idx = tid; idx < p.M * 64; idx += 256) {
+      const int m = idx >> 6, col = 2 * (idx & 63);
+      const int gc = cb + col;
+      if (col >= bw || gc >= p.N[sel]) continue;
+      int v0 = 0, v1 = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const int2 r = *reinterpret_cast<const int2*>(red + (w * MT + m) * 128 + col);
+        v0 += r.x;
+        v1 += r.y;
+      }
+      if (p.raw_mode) {
+        *reinterpret_cast<int2*>(p.raw + (size_t)m * p.raw_ld + gc) = make_int2(v0, v1);
+        continue;
+      }
+      const float sr = p.srow[sel][m];
+      const float y0 = __fmul_rn(__fmul_rn((float)v0, sr), p.scol[sel][gc]);
+      const float y1 = __fmul_rn(__fmul_rn((float)v1, sr), p.scol[sel][gc + 1]);
+      const int bi = m / p.s, si = m - bi * p.s;
+      if (sel == 0) {
+        const int h = gc / (kNope + kRope), e = gc - h * (kNope + kRope);
+        const size_t orow = ((size_t)bi * p.heads + h) * p.s + si;
+        if (e < kNope) {
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.q_nope) + orow * kNope + e) =
+              __floats2bfloat162_rn(y0, y1);
+        } else {
+          const int j = (e - kNope) >> 1;
+          int pos = p.positions[m];
+          pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
+          const float* cr = p.cos_t + (size_t)pos * kRope;
+          const float* sn = p.sin_t + (size_t)pos * kRope;
+          __nv_bfloat16* qp = static_cast<__nv_bfloat16*>(p.q_pe) + orow * kRope;
+          qp[j] = __float2bfloat16_rn(y0 * cr[j] - y1 * sn[j]);
+          qp[j + 32] = __float2bfloat16_rn(y1 * cr[j + 32] + y0 * sn[j + 32]);
+        }
+      } else {
+        const int h = gc / kHeadCols, e = gc - h * kHeadCols;
+        const size_t orow = ((size_t)bi * p.heads + h) * p.s + si;
+        __nv_bfloat16* dst = e < kNope ? static_cast<__nv_bfloat16*>(p.k_nope) + orow * kNope + e
+                                       : static_cast<__nv_bfloat16*>(p.value) + orow * kV + (e - kNope);
+        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(y0, y1);
+      }
+    }
+    __syncthreads();  // the reduction area is reused by the next block
+  }
+}
+
+__host__ __device__ constexpr size_t w8_back_smem(int MT, int kp0, int kp1) {
+  return 128 + (size_t)kBackStages * kBackBox + (size_t)MT * (kp0 + kp1) + 8 * (size_t)MT * 512 +
+         8 * kBackStages + 16;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int g_num_sms = 148;
 
-// Small-M launch: 256-column blocks x K splits of at least 128 rows (32 per
-// warp), aiming at about 4 CTAs per SM.
-cudaError_t gemv(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
-                 cudaStream_t st, int* launches) {
-  const int tn = (N + 255) / 256;
-  long per = ((long)K * tn + 4L * g_num_sms - 1) / (4L * g_num_sms);
-  int kchunk = (int)((per + 63) / 64 * 64);
-  if (kchunk < 128) kchunk = 128;
-  if (kchunk > K) kchunk = (K + 15) / 16 * 16;
-  const int splits = (K + kchunk - 1) / kchunk;
+// Launch with or without programmatic stream serialisation (the kernel may
+// start before the previous kernel in the stream has finished; it calls
+// grid_dep_wait before touching that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? at : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int MT, bool QUANT>
+cudaError_t launch_front(const W8FrontParams& f, int nblk, int splits, cudaStream_t st) {
+  const size_t smem = w8_front_smem(MT, f.kchunk);
+  cudaError_t e = cudaFuncSetAttribute(w8_front_kernel<MT, QUANT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_k(w8_front_kernel<MT, QUANT>, dim3(nblk, splits), dim3(128), smem, st, false, f);
+}
+
+template <bool QUANT>
+cudaError_t launch_front_m(const W8FrontParams& f, int nblk, int splits, cudaStream_t st) {
+  if (f.M <= 1) return launch_front<1, QUANT>(f, nblk, splits, st);
+  if (f.M <= 2) return launch_front<2, QUANT>(f, nblk, splits, st);
+  if (f.M <= 4) return launch_front<4, QUANT>(f, nblk, splits, st);
+  return launch_front<8, QUANT>(f, nblk, splits, st);
+}
+
+template <int MT>
+cudaError_t launch_back(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
+  const size_t smem = w8_back_smem(MT, b.kpad[0], b.kpad[1]);
+  cudaError_t e = cudaFuncSetAttribute(w8_back_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_k(w8_back_kernel<MT>, dim3(grid), dim3(256), smem, st, pdl, b);
+}
+
+cudaError_t launch_back_m(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
+  if (b.M <= 1) return launch_back<1>(b, grid, st, pdl);
+  if (b.M <= 2) return launch_back<2>(b, grid, st, pdl);
+  if (b.M <= 4) return launch_back<4>(b, grid, st, pdl);
+  return launch_back<8>(b, grid, st, pdl);
+}
+
+// Box geometry of one matrix of the back kernel.
+void back_geometry(int K, int N, int* bw, int* brows, int* nbox, int* kpad) {
+  *bw = N < 128 ? N : 128;
+  *brows = K < 256 ? K : 256;
+  *nbox = (K + *brows - 1) / *brows;
+  *kpad = *nbox * *brows;
+}
+
+// K rows per front-kernel CTA: about three CTAs per SM over `nblk` column
+// blocks, a multiple of 16 rows, at most one 256-row box.
+int front_kchunk(int K, int nblk, int num_sms) {
+  const int target = (3 * num_sms + nblk - 1) / nblk;
+  int kc = (K + target - 1) / target;
+  kc = (kc + 15) / 16 * 16;
+  if (kc < 16) kc = 16;
+  if (kc > 256) kc = 256;
+  return kc;
+}
+
+bool encode_i8(CUtensorMap* m, const void* base, int rows, int cols, int box_cols, int box_rows) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, (uint64_t)cols, (uint64_t)rows,
+                        (uint64_t)cols, (uint32_t)box_cols, (uint32_t)box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Plain int8 GEMM for M <= 8 through the two GEMV kernels: full K per CTA
+// when K is short, else split K with atomics into a cleared C.
+cudaError_t gemv_tma(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
+                     cudaStream_t st, int* launches) {
+  if (K <= 2048) {
+    W8BackParams b = {};
+    int bw, brows, nbox, kpad;
+    back_geometry(K, N, &bw, &brows, &nbox, &kpad);
+    if (!encode_i8(&b.tm[0], W, K, N, bw, brows)) return cudaErrorInvalidValue;
+    b.tm[1] = b.tm[0];
+    b.act[0] = A;
+    b.raw = C;
+    b.raw_ld = ldc;
+    b.raw_mode = 1;
+    b.M = M;
+    b.s = 1;
+    b.K[0] = K;
+    b.N[0] = N;
+    b.bw[0] = bw;
+    b.brows[0] = brows;
+    b.nbox[0] = nbox;
+    b.kpad[0] = kpad;
+    b.nblk1 = b.nblk = (N + 127) / 128;
+    b.status = nullptr;
+    b.budget_ns = 1000000000ull;
+    const int grid = b.nblk < g_num_sms ? b.nblk : g_num_sms;
+    ++*launches;
+    return launch_back_m(b, grid, st, false);
+  }
+  W8FrontParams f = {};
+  const int nblk = (N + 255) / 256;
+  f.kchunk = front_kchunk(K, nblk, g_num_sms);
+  const int splits = (K + f.kchunk - 1) / f.kchunk;
+  f.bw[0] = f.bw[1] = N < 256 ? N : 256;
+  if (!encode_i8(&f.tm[0], W, K, N, f.bw[0], f.kchunk)) return cudaErrorInvalidValue;
+  f.tm[1] = f.tm[0];
+  f.x = A;
+  f.acc = C;
+  f.M = M;
+  f.K = K;
+  f.ldc = ldc;
+  f.n[0] = N;
+  f.n[1] = 0;
+  f.nblk1 = nblk;
+  f.atomic = splits > 1 ? 1 : 0;
+  f.budget_ns = 1000000000ull;
   if (splits > 1) {
     cudaError_t e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, M, st);
     if (e != cudaSuccess) return e;
     ++*launches;
   }
-  dim3 grid(tn, splits);
-  const int atomic = splits > 1 ? 1 : 0;
-  if (M <= 1) gemv_s8_kernel<1><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
-  else if (M <= 2) gemv_s8_kernel<2><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
-  else if (M <= 4) gemv_s8_kernel<4><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
-  else gemv_s8_kernel<8><<<grid, 128, 0, st>>>(A, W, M, K, N, C, ldc, kchunk, atomic);
   ++*launches;
-  return cudaGetLastError();
+  return launch_front_m<false>(f, nblk, splits, st);
+}
+
+// Decode-size chain: front (normal launch) -> norm -> back (both launched
+// with programmatic stream serialisation).
+cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8SmallPlan& pl,
+                               const W8Maps& mp, cudaStream_t st, int* launches) {
+  const int T = p.T, rq = p.q_rank, H = p.heads;
+  W8FrontParams f = {};
+  f.tm[0] = mp.qa;
+  f.tm[1] = mp.kva;
+  f.x = p.hidden;
+  f.acc = w.acc1;
+  f.sx = w.sx;
+  f.pf[0] = reinterpret_cast<const unsigned char*>(p.W_qb);
+  f.pf_bytes[0] = (unsigned long long)rq * H * (kNope + kRope);
+  f.pf[1] = reinterpret_cast<const unsigned char*>(p.W_kvb);
+  f.pf_bytes[1] = (unsigned long long)kRank * H * kHeadCols;
+  f.status = p.status;
+  f.budget_ns = p.budget_ns;
+  f.M = T;
+  f.K = p.hidden_dim;
+  f.ldc = rq + kNa;
+  f.n[0] = rq;
+  f.n[1] = kNa;
+  f.bw[0] = rq < 256 ? rq : 256;
+  f.bw[1] = 256;
+  f.nblk1 = pl.nblk_a1;
+  f.kchunk = pl.kchunk;
+  f.atomic = pl.splits > 1 ? 1 : 0;
+  cudaError_t e = launch_front_m<true>(f, pl.nblk_a, pl.splits, st);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+  const size_t nsmem = (size_t)(rq + kNa) * sizeof(float);
+  e = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)nsmem);
+  if (e == cudaSuccess) e = launch_k(norm_quant_kernel, dim3(T), dim3(256), nsmem, st, true, w.acc1, (const float*)w.sx, p, w);
+  ++*launches;
+  if (e != cudaSuccess) return e;
+  W8BackParams b = {};
+  b.tm[0] = mp.qb;
+  b.tm[1] = mp.kvb;
+  b.act[0] = w.q1;
+  b.act[1] = w.c1;
+  b.srow[0] = w.s1;
+  b.srow[1] = w.s2;
+  b.scol[0] = p.sW_qb;
+  b.scol[1] = p.sW_kvb;
+  b.units = pl.units;
+  b.q_nope = p.q_nope;
+  b.q_pe = p.q_pe;
+  b.k_nope = p.k_nope;
+  b.value = p.value;
+  b.positions = p.positions;
+  b.cos_t = p.cos_t;
+  b.sin_t = p.sin_t;
+  b.status = p.status;
+  b.budget_ns = p.budget_ns;
+  b.M = T;
+  b.s = p.s;
+  b.heads = H;
+  b.max_pos = p.max_pos;
+  b.K[0] = rq;
+  b.K[1] = kRank;
+  b.N[0] = H * (kNope + kRope);
+  b.N[1] = H * kHeadCols;
+  for (int i = 0; i < 2; ++i) back_geometry(b.K[i], b.N[i], &b.bw[i], &b.brows[i], &b.nbox[i], &b.kpad[i]);
+  b.nblk1 = pl.nblk_b1;
+  b.nblk = pl.nblk_b;
+  e = launch_back_m(b, pl.grid_b, st, true);
+  ++*launches;
+  return e;
 }
 
 cudaError_t gemm(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
                  cudaStream_t st, int* launches) {
   // decode sizes stream the weights; the 64 x 64 tensor-core tiles would be
   // mostly padding rows
-  if (M <= kGemvMaxRows && K % 16 == 0 && N % 8 == 0) return gemv(A, W, M, K, N, C, ldc, st, launches);
+  if (M <= kGemvMaxRows && K % 16 == 0 && N % 16 == 0) return gemv_tma(A, W, M, K, N, C, ldc, st, launches);
   const int tn = N / kGBN, tm = (M + kGBM - 1) / kGBM;
   int splits = 1;
   const int tiles = tn * tm;
@@ -466,18 +999,73 @@ cudaError_t gemm(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t*
 
 }  // namespace
 
-size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens) {
+namespace {
+
+int small_nblk_b(int q_rank, int heads) {
+  (void)q_rank;
+  return (heads * (kNope + kRope) + 127) / 128 + (heads * kHeadCols + 127) / 128;
+}
+
+void small_plan(int hidden, int q_rank, int heads, int num_sms, W8SmallPlan* pl) {
+  pl->nblk_a1 = (q_rank + 255) / 256;
+  pl->nblk_a = pl->nblk_a1 + (kNa + 255) / 256;
+  pl->kchunk = front_kchunk(hidden, pl->nblk_a, num_sms);
+  pl->splits = (hidden + pl->kchunk - 1) / pl->kchunk;
+  pl->nblk_b1 = (heads * (kNope + kRope) + 127) / 128;
+  pl->nblk_b = small_nblk_b(q_rank, heads);
+  pl->grid_b = pl->nblk_b < num_sms ? pl->nblk_b : num_sms;
+}
+
+// Longest-processing-time-first assignment of the q_b / kv_b blocks (cost:
+// boxes per block) to the back kernel's CTAs: [grid + 1] offsets, then ids.
+std::vector<int> small_units(int q_rank, int heads, const W8SmallPlan& pl, int* max_units) {
+  int bw, brows, nbox0, nbox1, kpad;
+  back_geometry(q_rank, heads * (kNope + kRope), &bw, &brows, &nbox0, &kpad);
+  back_geometry(kRank, heads * kHeadCols, &bw, &brows, &nbox1, &kpad);
+  const int G = pl.grid_b;
+  std::vector<long> load(G, 0);
+  std::vector<std::vector<int>> lists(G);
+  // blocks in decreasing cost (ids of the costlier matrix first; stable)
+  std::vector<int> order;
+  const bool qfirst = nbox0 >= nbox1;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool q = (pass == 0) == qfirst;
+    const int lo = q ? 0 : pl.nblk_b1, hi = q ? pl.nblk_b1 : pl.nblk_b;
+    for (int b = lo; b < hi; ++b) order.push_back(b);
+  }
+  for (int b : order) {
+    int best = 0;
+    for (int c = 1; c < G; ++c)
+      if (load[c] < load[best]) best = c;
+    load[best] += b < pl.nblk_b1 ? nbox0 : nbox1;
+    lists[best].push_back(b);
+  }
+  std::vector<int> t(G + 1 + pl.nblk_b);
+  int off = 0;
+  *max_units = 0;
+  for (int c = 0; c < G; ++c) {
+    t[c] = off;
+    for (int b : lists[c]) t[G + 1 + off++] = b;
+    if ((int)lists[c].size() > *max_units) *max_units = (int)lists[c].size();
+  }
+  t[G] = off;
+  return t;
+}
+
+}  // namespace
+
+size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens, int num_sms) {
   const size_t T = (size_t)max_tokens;
   const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
   return align256(T * hidden) + align256(T * 4) + align256(T * (q_rank + kNa) * 4) +
          align256(T * q_rank) + align256(T * 4) + align256(T * kRank) + align256(T * 4) +
-         align256(T * nb * 4);
+         align256(T * nb * 4) + align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4);
 }
 
 void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,
-                        W8Workspace* w) {
+                        int num_sms, W8Workspace* w, W8SmallPlan* plan) {
   const size_t T = (size_t)max_tokens;
-  (void)heads;
+  const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
   unsigned char* b = static_cast<unsigned char*>(base);
   w->xq = reinterpret_cast<int8_t*>(b); b += align256(T * hidden);
   w->sx = reinterpret_cast<float*>(b); b += align256(T * 4);
@@ -486,7 +1074,38 @@ void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_t
   w->s1 = reinterpret_cast<float*>(b); b += align256(T * 4);
   w->c1 = reinterpret_cast<int8_t*>(b); b += align256(T * kRank);
   w->s2 = reinterpret_cast<float*>(b); b += align256(T * 4);
-  w->acc2 = reinterpret_cast<int32_t*>(b);
+  w->acc2 = reinterpret_cast<int32_t*>(b); b += align256(T * nb * 4);
+  small_plan(hidden, q_rank, heads, num_sms, plan);
+  plan->units = reinterpret_cast<int*>(b);
+}
+
+cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int hidden,
+                              int q_rank, int heads, int max_tokens, int num_sms) {
+  (void)hidden;
+  (void)num_sms;
+  cudaError_t e = cudaMemset(w.acc1, 0, (size_t)max_tokens * (q_rank + kNa) * 4);
+  if (e != cudaSuccess) return e;
+  int mu = 0;
+  const std::vector<int> t = small_units(q_rank, heads, plan, &mu);
+  return cudaMemcpy(plan.units, t.data(), t.size() * sizeof(int), cudaMemcpyHostToDevice);
+}
+
+bool w8_encode_maps(const W8Params& p, const W8SmallPlan& pl, W8Maps* m) {
+  const int rq = p.q_rank, H = p.heads, h = p.hidden_dim;
+  int bw, brows, nbox, kpad;
+  m->valid = false;
+  if (!encode_i8(&m->qa, p.W_qa, h, rq, rq < 256 ? rq : 256, pl.kchunk)) return false;
+  if (!encode_i8(&m->kva, p.W_kva, h, kNa, 256, pl.kchunk)) return false;
+  back_geometry(rq, H * (kNope + kRope), &bw, &brows, &nbox, &kpad);
+  if (!encode_i8(&m->qb, p.W_qb, rq, H * (kNope + kRope), bw, brows)) return false;
+  back_geometry(kRank, H * kHeadCols, &bw, &brows, &nbox, &kpad);
+  if (!encode_i8(&m->kvb, p.W_kvb, kRank, H * kHeadCols, bw, brows)) return false;
+  m->src[0] = p.W_qa;
+  m->src[1] = p.W_kva;
+  m->src[2] = p.W_qb;
+  m->src[3] = p.W_kvb;
+  m->valid = true;
+  return true;
 }
 
 cudaError_t w8a8_quant_rows_launch(const void* x_bf16, int rows, int cols, int8_t* q,
@@ -514,13 +1133,22 @@ cudaError_t w8a8_copy_operands(const W8Workspace& w, int T, int q_rank, int8_t* 
   return e;
 }
 
-cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, int num_sms, cudaStream_t st,
-                        int* launches) {
+cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPlan& plan,
+                        const W8Maps* maps, int num_sms, cudaStream_t st, int* launches) {
   g_num_sms = num_sms;
   *launches = 0;
   const int T = p.T, h = p.hidden_dim, rq = p.q_rank, H = p.heads;
   const int na = rq + kNa;
   cudaError_t e;
+  if (T <= kW8SmallRows && maps && maps->valid) {
+    e = launch_small_chain(p, w, plan, *maps, st, launches);
+    if (e != cudaSuccess) {
+      // the accumulator rows must be zero when the next chain starts
+      cudaGetLastError();
+      cudaMemsetAsync(w.acc1, 0, (size_t)T * na * 4, st);
+    }
+    return e;
+  }
   // 1. quantise hidden rows
   quant_rows_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(p.hidden), h, w.xq, w.sx);
   ++*launches;

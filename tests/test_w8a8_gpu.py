@@ -45,7 +45,10 @@ def test_quant_rows_bit_exact(oracle_mod, rows, cols):
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 7168, 1536), (1, 7168, 576), (64, 1536, 2048), (5, 512, 64),
-                                   (130, 256, 192), (8192, 64, 64)])
+                                   (130, 256, 192), (8192, 64, 64),
+                                   # M <= 8: full-K TMA GEMV (K <= 2048) and split-K TMA GEMV
+                                   (1, 1536, 24576), (8, 512, 32768), (3, 192, 384), (2, 64, 128),
+                                   (7, 4096, 2112), (4, 2048, 320), (6, 2080, 64)])
 def test_gemm_s32_bit_exact(oracle_mod, M, K, N):
     g = torch.Generator().manual_seed(M + K + N)
     A = torch.randint(-127, 128, (M, K), generator=g, dtype=torch.int8)
@@ -83,7 +86,7 @@ def test_w8a8_tiny(oracle_mod):
     assert r["status"] == 0
 
 
-@pytest.mark.parametrize("b,s", [(1, 1), (64, 1)])
+@pytest.mark.parametrize("b,s", [(1, 1), (64, 1), (2, 1), (1, 2), (5, 1), (4, 2)])
 def test_w8a8_r1_decode(oracle_mod, b, s):
     r = run_w8(I.R1_W8A8, b, s, I.seed_for(4) + b, oracle_mod=oracle_mod)
     assert r["status"] == 0
@@ -96,12 +99,14 @@ def test_w8a8_r1_prefill_sampled(oracle_mod):
     assert r["status"] == 0
 
 
-def test_w8a8_operands_and_accumulators(oracle_mod):
+@pytest.mark.parametrize("b", [16, 4])
+def test_w8a8_operands_and_accumulators(oracle_mod, b):
     """The int8 operands the GPU fed to q_b / kv_b agree with the oracle's
     requantisation (>= 99.9 % equal, never off by more than 1), and the
-    int32 accumulators the GPU GEMM forms from them are bit-exact."""
+    int32 accumulators the GPU GEMM forms from them are bit-exact.  b = 4
+    runs the decode-size chain (fused quantisation, split-K GEMV)."""
     cfg = I.R1_W8A8
-    b, s = 16, 1
+    s = 1
     r = run_w8(cfg, b, s, 4242, keep=True)
     m, T = r["m"], b * s
     rq = cfg["q_lora_rank"]
@@ -130,3 +135,34 @@ def test_w8a8_operands_and_accumulators(oracle_mod):
         torch.cuda.synchronize()
         ref = oracle_mod.int_gemm(A.cpu().numpy()[:4], W.cpu().numpy())
         assert np.array_equal(acc.cpu().numpy()[:4].astype(np.int64), ref)
+
+
+def test_w8a8_small_chain_repeats_and_alternates(oracle_mod):
+    """The decode-size chain adds split-K partials into accumulator rows that
+    the previous call left zeroed: repeated calls, and a prefill-size call in
+    between, give the same outputs."""
+    cfg = I.small_config(I.R1_W8A8, hidden=512, q_lora_rank=256, num_heads=4, max_pos=64)
+    inp = I.w8a8_inputs(cfg, 3, 1, 77, "decode")
+    d = B.to_device(inp)
+    big = I.w8a8_inputs(cfg, 2, 16, 78, "prefill")
+    db = B.to_device(big)
+    m = B.MLAProlog(cfg, 64)
+    try:
+        outs = []
+        for i in range(3):
+            out = m.alloc_outputs(3, 1)
+            m.run(3, 1, d, out)
+            torch.cuda.synchronize()
+            outs.append({k: v.clone() for k, v in out.items()})
+            ob = m.alloc_outputs(2, 16)
+            m.run(2, 16, db, ob)
+            torch.cuda.synchronize()
+        assert m.status() == 0
+        for o in outs[1:]:
+            for k in NAMES:
+                assert torch.equal(o[k], outs[0][k]), k
+        ref = oracle_mod.w8a8_prolog(inp)
+        for n, r in zip(NAMES, ref):
+            compare(n, outs[0][n], r, oracle_mod)
+    finally:
+        m.close()
