@@ -159,7 +159,7 @@ struct W8Maps {
   bool valid;
 };
 struct W8SmallPlan {
-  int kchunk, splits;   // kv_a/q_a split-K: rows per chunk (multiple of 16, <= 256), chunk count
+  int kchunk, splits;   // kv_a/q_a split-K: rows per chunk (multiple of 32, <= 512), chunk count
   int nblk_a1, nblk_a;  // 256-column blocks of q_a, of q_a + kv_a
   int nblk_b1, nblk_b;  // 128-column blocks of q_b, of q_b + kv_b
   int grid_b;           // CTAs of the q_b / kv_b kernel

@@ -216,24 +216,46 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
 }
 
 // Per token: dequantise the [q_rank + 576] accumulator row, RMSNorm of the
-// q latent and of compressed_kv, requantise both, RoPE of k_pe.
+// q latent and of compressed_kv, requantise both, RoPE of k_pe.  Shared
+// memory: the row [q_rank + 576] | its weight scales [q_rank + 576] | gamma_q
+// [q_rank] | gamma_kv [512] | cos, sin of the token's position [2][64].
+__host__ __device__ constexpr size_t norm_smem(int q_rank) {
+  return (size_t)(2 * (q_rank + kNa) + q_rank + kRank + 2 * kRope) * sizeof(float);
+}
+
 __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ acc1,
                                                          const float* __restrict__ sx,
                                                          W8Params p, W8Workspace w) {
-  extern __shared__ float yrow[];  // [q_rank + 576]
+  extern __shared__ float yrow[];
   __shared__ float scratch[8];
+  const int t = blockIdx.x;
+  const int rq = p.q_rank, na = rq + kNa;
+  float* colsc = yrow + na;
+  float* gq = colsc + na;
+  float* gk = gq + rq;
+  float* rope = gk + kRank;
+  // inputs that do not come from the previous kernel are read while it runs
+  const __nv_bfloat16* gqp = static_cast<const __nv_bfloat16*>(p.gamma_q);
+  const __nv_bfloat16* gkp = static_cast<const __nv_bfloat16*>(p.gamma_kv);
+  for (int c = threadIdx.x; c < na; c += 256) colsc[c] = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
+  for (int c = threadIdx.x; c < rq; c += 256) gq[c] = __bfloat162float(gqp[c]);
+  for (int c = threadIdx.x; c < kRank; c += 256) gk[c] = __bfloat162float(gkp[c]);
+  if (threadIdx.x < 2 * kRope) {
+    int pos = p.positions[t];
+    if (pos < 0 || pos >= p.max_pos) {
+      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPosition);
+      pos = pos < 0 ? 0 : p.max_pos - 1;
+    }
+    const int j = threadIdx.x & (kRope - 1);
+    rope[threadIdx.x] = (threadIdx.x < kRope ? p.cos_t : p.sin_t)[(size_t)pos * kRope + j];
+  }
   // in the decode-size chain this kernel is launched while the GEMV that
   // produces acc1 still runs: let the next kernel start, then wait for acc1
   grid_dep_launch_dependents();
   grid_dep_wait();
-  const int t = blockIdx.x;
-  const int rq = p.q_rank, na = rq + kNa;
   const float s = sx[t];
   int32_t* a = acc1 + (size_t)t * na;
-  for (int c = threadIdx.x; c < na; c += 256) {
-    const float sw = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
-    yrow[c] = __fmul_rn(__fmul_rn((float)a[c], s), sw);
-  }
+  for (int c = threadIdx.x; c < na; c += 256) yrow[c] = __fmul_rn(__fmul_rn((float)a[c], s), colsc[c]);
   __syncthreads();
   // leave the accumulator row zeroed: the decode-size chain adds its split-K
   // partials into it atomically without clearing it first
@@ -244,9 +266,8 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   ss = block_reduce<false>(ss, scratch);
   const float invq = 1.0f / sqrtf(ss / (float)rq + p.eps);
   float amax = 0.f;
-  const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(p.gamma_q);
   for (int c = threadIdx.x; c < rq; c += 256) {
-    const float v = yrow[c] * invq * __bfloat162float(gq[c]);
+    const float v = yrow[c] * invq * gq[c];
     yrow[c] = v;
     amax = fmaxf(amax, fabsf(v));
   }
@@ -263,11 +284,10 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   ss = block_reduce<false>(ss, scratch);
   const float invk = 1.0f / sqrtf(ss / (float)kRank + p.eps);
   amax = 0.f;
-  const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(p.gamma_kv);
   float nv[2];
   for (int i = 0; i < 2; ++i) {
     const int c = threadIdx.x + i * 256;
-    nv[i] = ck[c] * invk * __bfloat162float(gk[c]);
+    nv[i] = ck[c] * invk * gk[c];
     amax = fmaxf(amax, fabsf(nv[i]));
   }
   amax = block_reduce<true>(amax, scratch);
@@ -278,16 +298,11 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   }
   // RoPE of k_pe (raw columns 512..575 of the kv_a output)
   if (threadIdx.x < 32) {
-    int pos = p.positions[t];
-    if (pos < 0 || pos >= p.max_pos) {
-      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPosition);
-      pos = pos < 0 ? 0 : p.max_pos - 1;
-    }
     const float* kp = ck + kRank;
     const int j = threadIdx.x;
     const float a0 = kp[2 * j], b0 = kp[2 * j + 1];
-    const float* cr = p.cos_t + (size_t)pos * kRope;
-    const float* sr = p.sin_t + (size_t)pos * kRope;
+    const float* cr = rope;
+    const float* sr = rope + kRope;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope;
     out[j] = __float2bfloat16_rn(a0 * cr[j] - b0 * sr[j]);
     out[j + 32] = __float2bfloat16_rn(b0 * cr[j + 32] + a0 * sr[j + 32]);
@@ -369,15 +384,21 @@ struct W8FrontParams {
   int n[2];                        // columns of each matrix
   int bw[2];                       // box width (bytes = columns) of each matrix, <= 256
   int nblk1;                       // 256-column blocks of matrix 0
-  int kchunk;                      // K rows per CTA (box height), multiple of 16
+  int kchunk;                      // K rows per CTA: multiple of 32, <= 512
+  int nbox;                        // TMA boxes per CTA (1, or 2 when kchunk > 256)
   int atomic;                      // add into acc (split K) instead of storing
 };
 
-// Grid (column blocks of matrix 0 then of matrix 1, K chunks); 128 threads.
-// Shared memory: weight box [kchunk][bw] | codes [MT][kchunk] | reduction
-// [3][MT][8][32] int | per-warp amax [4][MT] | mbarrier | flag.
+__host__ __device__ constexpr size_t w8_front_region(int MT, int kc) {
+  return 256 * (size_t)kc > 8192 * (size_t)MT ? 256 * (size_t)kc : 8192 * (size_t)MT;
+}
+
+// Grid (column blocks of matrix 0 then of matrix 1, K chunks); 256 threads.
+// Shared memory: weight boxes [kchunk][bw], reused for the cross-warp
+// reduction [8][MT][256] | codes [MT][kchunk] | per-warp amax [8][MT] |
+// mbarrier | flag.
 template <int MT, bool QUANT>
-__global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W8FrontParams p) {
+__global__ void __launch_bounds__(256) w8_front_kernel(const __grid_constant__ W8FrontParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
@@ -388,52 +409,59 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
   const int col0 = (sel ? bx - p.nblk1 : bx) * 256;
   const int N = p.n[sel], bw = p.bw[sel];
   const int coff = sel ? p.n[0] : 0;
+  const size_t region = w8_front_region(MT, kc);
   unsigned char* sW = sm;
-  uint32_t* sX = reinterpret_cast<uint32_t*>(sm + 256 * kc);
-  int* red = reinterpret_cast<int*>(sm + 256 * kc + MT * kc);
-  float* s_amax = reinterpret_cast<float*>(red + 3 * MT * 256);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_amax + 4 * MT);
+  int* red = reinterpret_cast<int*>(sm);
+  uint32_t* sX = reinterpret_cast<uint32_t*>(sm + region);
+  float* s_amax = reinterpret_cast<float*>(sm + region + (size_t)MT * kc);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_amax + 8 * MT);
   int* s_flag = reinterpret_cast<int*>(s_bar + 1);
   const uint32_t bar = smem_u32(s_bar);
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, (uint32_t)(bw * kc));
-    tma_load_2d(smem_u32(sW), &p.tm[sel], col0, kb, bar);
-  } else if (tid == 32) {
-    // this CTA's share of the q_b / kv_b weight bytes, prefetched into L2
-    const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y;
-    const unsigned long long id = (unsigned long long)blockIdx.y * gridDim.x + bx;
-    const unsigned long long tot = p.pf_bytes[0] + p.pf_bytes[1];
-    const unsigned long long per = ((tot + nct - 1) / nct + 15) & ~15ull;
-    const unsigned long long b0 = id * per, b1 = b0 + per < tot ? b0 + per : tot;
-    unsigned long long base = 0;
-    for (int r = 0; r < 2; ++r) {
-      const unsigned long long lo = b0 > base ? b0 : base;
-      const unsigned long long end = base + p.pf_bytes[r];
-      const unsigned long long hi = b1 < end ? b1 : end;
-      for (unsigned long long o = lo; o < hi; o += 65536ull) {
-        const unsigned long long len = hi - o < 65536ull ? hi - o : 65536ull;
-        prefetch_l2_bulk(p.pf[r] + (o - base), (uint32_t)len);
-      }
-      base = end;
-    }
+    // boxes that start past K are not loaded: their rows meet zero codes
+    const int brows = kc / p.nbox;
+    int nload = 0;
+    for (int i = 0; i < p.nbox; ++i) nload += kb + i * brows < p.K ? 1 : 0;
+    mbar_arrive_expect_tx(bar, (uint32_t)(bw * brows * nload));
+    for (int i = 0; i < nload; ++i)
+      tma_load_2d(smem_u32(sW + (size_t)i * brows * bw), &p.tm[sel], col0, kb + i * brows, bar);
   }
   grid_dep_launch_dependents();
   // activation codes of rows [kb, kb + kc), four per word, zero past K
   if constexpr (QUANT) {
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
+    const int nv = p.K >> 3;  // 16-byte vectors per row
     float am[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) am[m] = 0.f;
-    for (int i = tid; i < (p.K >> 3); i += 128) {
+    // all loads of two rows in flight at once (one round trip per row pair)
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        if (m < p.M) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)m * p.K) + i);
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+    for (int m0 = 0; m0 < MT; m0 += 2) {
+      if (m0 < p.M) {
+        for (int base = 0; base < nv; base += 256 * 4) {
+          uint4 v[2][4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) am[m] = fmaxf(am[m], fabsf(__bfloat162float(e[j])));
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i = base + tid + 256 * j;
+              v[r][j] = make_uint4(0u, 0u, 0u, 0u);
+              if (m0 + r < MT && m0 + r < p.M && i < nv)
+                v[r][j] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(m0 + r) * p.K) + i);
+            }
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            if (m0 + r < MT) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[r][j]);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) am[m0 + r] = fmaxf(am[m0 + r], fabsf(__bfloat162float(e[q])));
+              }
+            }
+          }
         }
       }
     }
@@ -444,11 +472,17 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
       if (lane == 0) s_amax[warp * MT + m] = am[m];
     }
     __syncthreads();
-    for (int i = tid; i < MT * k4n; i += 128) {
+    auto row_amax = [&](int m) {
+      float a = s_amax[m];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) a = fmaxf(a, s_amax[w * MT + m]);
+      return a;
+    };
+    for (int i = tid; i < MT * k4n; i += 256) {
       const int m = i / k4n, k = kb + 4 * (i - m * k4n);
       uint32_t word = 0;
       if (m < p.M && k < p.K) {
-        const float amax = fmaxf(fmaxf(s_amax[m], s_amax[MT + m]), fmaxf(s_amax[2 * MT + m], s_amax[3 * MT + m]));
+        const float amax = row_amax(m);
         const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)m * p.K + k));
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
@@ -459,12 +493,12 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
       sX[i] = word;
     }
     if (bx == 0 && blockIdx.y == 0 && tid < p.M) {
-      const float amax = fmaxf(fmaxf(s_amax[tid], s_amax[MT + tid]), fmaxf(s_amax[2 * MT + tid], s_amax[3 * MT + tid]));
+      const float amax = row_amax(tid);
       p.sx[tid] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
     }
   } else {
     const int8_t* A = static_cast<const int8_t*>(p.x);
-    for (int i = tid; i < MT * k4n; i += 128) {
+    for (int i = tid; i < MT * k4n; i += 256) {
       const int m = i / k4n, k = kb + 4 * (i - m * k4n);
       sX[i] = (m < p.M && k < p.K) ? __ldg(reinterpret_cast<const uint32_t*>(A + (size_t)m * p.K + k)) : 0u;
     }
@@ -482,7 +516,27 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
   }
   while (!mbar_test_wait(bar, 0)) {
   }
-  // a lane owns 8 columns; warp w takes the 4-row groups w, w + 4, ...
+  if (tid == 32) {
+    // this CTA's share of the q_b / kv_b weight bytes, prefetched into L2
+    // once its own tile is in (the q_a / kv_a stream goes first)
+    const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y;
+    const unsigned long long id = (unsigned long long)blockIdx.y * gridDim.x + bx;
+    const unsigned long long tot = p.pf_bytes[0] + p.pf_bytes[1];
+    const unsigned long long per = ((tot + nct - 1) / nct + 15) & ~15ull;
+    const unsigned long long b0 = id * per, b1 = b0 + per < tot ? b0 + per : tot;
+    unsigned long long base = 0;
+    for (int r = 0; r < 2; ++r) {
+      const unsigned long long lo = b0 > base ? b0 : base;
+      const unsigned long long end = base + p.pf_bytes[r];
+      const unsigned long long hi = b1 < end ? b1 : end;
+      for (unsigned long long o = lo; o < hi; o += 65536ull) {
+        const unsigned long long len = hi - o < 65536ull ? hi - o : 65536ull;
+        prefetch_l2_bulk(p.pf[r] + (o - base), (uint32_t)len);
+      }
+      base = end;
+    }
+  }
+  // a lane owns 8 columns; warp w takes the 4-row groups w, w + 8, ...
   int acc[MT][8];
 #pragma unroll
   for (int m = 0; m < MT; ++m)
@@ -490,7 +544,7 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
     for (int c = 0; c < 8; ++c) acc[m][c] = 0;
   const bool live = lane * 8 < bw && col0 + lane * 8 < N;
   if (live) {
-    for (int g = warp; g < k4n; g += 4) {
+    for (int g = warp; g < k4n; g += 8) {
       const unsigned char* wr = sW + (size_t)(4 * g) * bw + lane * 8;
       const uint2 r0 = *reinterpret_cast<const uint2*>(wr);
       const uint2 r1 = *reinterpret_cast<const uint2*>(wr + bw);
@@ -518,39 +572,35 @@ __global__ void __launch_bounds__(128) w8_front_kernel(const __grid_constant__ W
       }
     }
   }
-  if (warp > 0) {
+  // the 8 warps' partials through shared memory (the weight area is free
+  // now), then one coalesced add or store per column and row
+  __syncthreads();
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) red[((warp - 1) * MT + m) * 256 + c * 32 + lane] = acc[m][c];
+  for (int m = 0; m < MT; ++m) {
+    int* rp = red + (warp * MT + m) * 256 + lane * 8;
+    *reinterpret_cast<int4*>(rp) = make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    *reinterpret_cast<int4*>(rp + 4) = make_int4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
   }
   __syncthreads();
-  if (warp == 0 && live) {
+  for (int i = tid; i < p.M * 256; i += 256) {
+    const int m = i >> 8, col = i & 255;
+    if (col >= bw || col0 + col >= N) continue;
+    int v = 0;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < p.M) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          acc[m][c] += red[m * 256 + c * 32 + lane] + red[(MT + m) * 256 + c * 32 + lane] +
-                       red[(2 * MT + m) * 256 + c * 32 + lane];
-        int32_t* cp = p.acc + (size_t)m * p.ldc + coff + col0 + lane * 8;
-        if (p.atomic) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) atomicAdd(cp + j, acc[m][j]);
-        } else {
-          *reinterpret_cast<int4*>(cp) = make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
-          *reinterpret_cast<int4*>(cp + 4) = make_int4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
-        }
-      }
-    }
+    for (int w = 0; w < 8; ++w) v += red[(w * MT + m) * 256 + col];
+    int32_t* cp = p.acc + (size_t)m * p.ldc + coff + col0 + col;
+    if (p.atomic)
+      atomicAdd(cp, v);
+    else
+      *cp = v;
   }
 }
 
 __host__ __device__ constexpr size_t w8_front_smem(int MT, int kc) {
-  return 128 + 256 * (size_t)kc + (size_t)MT * kc + 3 * (size_t)MT * 1024 + 16 * (size_t)MT + 64;
+  return 128 + w8_front_region(MT, kc) + (size_t)MT * kc + 32 * (size_t)MT + 64;
 }
 
-constexpr int kBackStages = 3;      // TMA boxes in flight per CTA
+constexpr int kBackStages = 8;      // most TMA boxes in flight per CTA
 constexpr int kBackBox = 32768;     // bytes per ring slot (128 columns x 256 rows)
 
 struct W8BackParams {
@@ -576,11 +626,12 @@ struct W8BackParams {
   int nbox[2];                     // boxes per block: ceil(K / brows)
   int kpad[2];                     // nbox * brows: activation row length in shared memory
   int nblk1, nblk;                 // blocks of matrix 0, of both
+  int nst;                         // ring slots (<= kBackStages)
 };
 
 // Persistent over the CTA's blocks; 256 threads.  Warp w takes rows
 // [32w, 32w + 32) of each box, a lane 4 columns (one 4-byte load per row, a
-// warp one 128-byte row).  Shared memory: ring [kBackStages][32 KB] |
+// warp one 128-byte row).  Shared memory: ring [nst][32 KB] |
 // activations [MT][kpad0] then [MT][kpad1] | reduction [8][MT][128] int |
 // mbarriers.
 template <int MT>
@@ -591,7 +642,8 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   unsigned char* ring = sm;
-  int8_t* sAct0 = reinterpret_cast<int8_t*>(sm + kBackStages * kBackBox);
+  const int nst = p.nst;
+  int8_t* sAct0 = reinterpret_cast<int8_t*>(sm + (size_t)nst * kBackBox);
   int8_t* sAct1 = sAct0 + MT * p.kpad[0];
   int* red = reinterpret_cast<int*>(sAct1 + MT * p.kpad[1]);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(red + 8 * MT * 128);
@@ -615,7 +667,7 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     const int b = block_of(iss_u);
     const int sel = b < p.nblk1 ? 0 : 1;
     const int x = (sel ? b - p.nblk1 : b) * 128;
-    const int slot = issued % kBackStages;
+    const int slot = issued % nst;
     const uint32_t bar = smem_u32(s_bar + slot);
     mbar_arrive_expect_tx(bar, (uint32_t)(p.bw[sel] * p.brows[sel]));
     tma_load_2d(smem_u32(ring + slot * kBackBox), &p.tm[sel], x, iss_j * p.brows[sel], bar);
@@ -626,11 +678,11 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     }
   };
   if (tid == 0) {
-    for (int i = 0; i < kBackStages; ++i) mbar_init(smem_u32(s_bar + i), 1);
+    for (int i = 0; i < nst; ++i) mbar_init(smem_u32(s_bar + i), 1);
     fence_mbar_init();
     // weights are read-only inputs: their copies may start before the
     // kernel that produces the activations has finished
-    for (int i = 0; i < kBackStages; ++i) issue_next();
+    for (int i = 0; i < nst; ++i) issue_next();
   }
   grid_dep_wait();
   // activation rows (zero past K) -- written by the previous kernel
@@ -658,15 +710,15 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[m][c] = 0;
     for (int j = 0; j < p.nbox[sel]; ++j) {
-      const int slot = consumed % kBackStages;
+      const int slot = consumed % nst;
       const uint32_t bar = smem_u32(s_bar + slot);
-      const uint32_t par = (uint32_t)(consumed / kBackStages) & 1u;
+      const uint32_t par = (uint32_t)(consumed / nst) & 1u;
       const bool ok = mbar_wait_bounded(bar, par, p.budget_ns);
       if (!__syncthreads_and(ok ? 1 : 0)) {
         if (tid == 0) {
           if (p.status) atomicOr(p.status, kStatusTimeout);
           for (int q = consumed; q < issued; ++q)
-            mbar_wait_bounded(smem_u32(s_bar + q % kBackStages), (uint32_t)(q / kBackStages) & 1u,
+            mbar_wait_bounded(smem_u32(s_bar + q % nst), (uint32_t)(q / nst) & 1u,
                               p.budget_ns);
         }
         return;
@@ -757,9 +809,16 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
   }
 }
 
-__host__ __device__ constexpr size_t w8_back_smem(int MT, int kp0, int kp1) {
-  return 128 + (size_t)kBackStages * kBackBox + (size_t)MT * (kp0 + kp1) + 8 * (size_t)MT * 512 +
+__host__ __device__ constexpr size_t w8_back_smem(int MT, int nst, int kp0, int kp1) {
+  return 128 + (size_t)nst * kBackBox + (size_t)MT * (kp0 + kp1) + 8 * (size_t)MT * 512 +
          8 * kBackStages + 16;
+}
+
+// Ring slots that fit next to the activations and the reduction area.
+int back_stages(int MT, int kp0, int kp1) {
+  int n = kBackStages;
+  while (n > 2 && w8_back_smem(MT, n, kp0, kp1) > 227 * 1024) --n;
+  return n;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -791,7 +850,7 @@ cudaError_t launch_front(const W8FrontParams& f, int nblk, int splits, cudaStrea
   cudaError_t e = cudaFuncSetAttribute(w8_front_kernel<MT, QUANT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_k(w8_front_kernel<MT, QUANT>, dim3(nblk, splits), dim3(128), smem, st, false, f);
+  return launch_k(w8_front_kernel<MT, QUANT>, dim3(nblk, splits), dim3(256), smem, st, false, f);
 }
 
 template <bool QUANT>
@@ -804,11 +863,13 @@ cudaError_t launch_front_m(const W8FrontParams& f, int nblk, int splits, cudaStr
 
 template <int MT>
 cudaError_t launch_back(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
-  const size_t smem = w8_back_smem(MT, b.kpad[0], b.kpad[1]);
+  W8BackParams bb = b;
+  bb.nst = back_stages(MT, b.kpad[0], b.kpad[1]);
+  const size_t smem = w8_back_smem(MT, bb.nst, b.kpad[0], b.kpad[1]);
   cudaError_t e = cudaFuncSetAttribute(w8_back_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_k(w8_back_kernel<MT>, dim3(grid), dim3(256), smem, st, pdl, b);
+  return launch_k(w8_back_kernel<MT>, dim3(grid), dim3(256), smem, st, pdl, bb);
 }
 
 cudaError_t launch_back_m(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
@@ -826,14 +887,14 @@ void back_geometry(int K, int N, int* bw, int* brows, int* nbox, int* kpad) {
   *kpad = *nbox * *brows;
 }
 
-// K rows per front-kernel CTA: about three CTAs per SM over `nblk` column
-// blocks, a multiple of 16 rows, at most one 256-row box.
+// K rows per front-kernel CTA: about one CTA per SM over `nblk` column
+// blocks, a multiple of 32 rows, at most two 256-row boxes.
 int front_kchunk(int K, int nblk, int num_sms) {
-  const int target = (3 * num_sms + nblk - 1) / nblk;
+  int target = num_sms / nblk;
+  if (target < 1) target = 1;
   int kc = (K + target - 1) / target;
-  kc = (kc + 15) / 16 * 16;
-  if (kc < 16) kc = 16;
-  if (kc > 256) kc = 256;
+  kc = (kc + 31) / 32 * 32;
+  if (kc > 512) kc = 512;
   return kc;
 }
 
@@ -877,7 +938,8 @@ cudaError_t gemv_tma(const int8_t* A, const int8_t* W, int M, int K, int N, int3
   f.kchunk = front_kchunk(K, nblk, g_num_sms);
   const int splits = (K + f.kchunk - 1) / f.kchunk;
   f.bw[0] = f.bw[1] = N < 256 ? N : 256;
-  if (!encode_i8(&f.tm[0], W, K, N, f.bw[0], f.kchunk)) return cudaErrorInvalidValue;
+  f.nbox = f.kchunk > 256 ? 2 : 1;
+  if (!encode_i8(&f.tm[0], W, K, N, f.bw[0], f.kchunk / f.nbox)) return cudaErrorInvalidValue;
   f.tm[1] = f.tm[0];
   f.x = A;
   f.acc = C;
@@ -924,11 +986,12 @@ cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8
   f.bw[1] = 256;
   f.nblk1 = pl.nblk_a1;
   f.kchunk = pl.kchunk;
+  f.nbox = pl.kchunk > 256 ? 2 : 1;
   f.atomic = pl.splits > 1 ? 1 : 0;
   cudaError_t e = launch_front_m<true>(f, pl.nblk_a, pl.splits, st);
   ++*launches;
   if (e != cudaSuccess) return e;
-  const size_t nsmem = (size_t)(rq + kNa) * sizeof(float);
+  const size_t nsmem = norm_smem(rq);
   e = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)nsmem);
   if (e == cudaSuccess) e = launch_k(norm_quant_kernel, dim3(T), dim3(256), nsmem, st, true, w.acc1, (const float*)w.sx, p, w);
   ++*launches;
@@ -1094,8 +1157,9 @@ bool w8_encode_maps(const W8Params& p, const W8SmallPlan& pl, W8Maps* m) {
   const int rq = p.q_rank, H = p.heads, h = p.hidden_dim;
   int bw, brows, nbox, kpad;
   m->valid = false;
-  if (!encode_i8(&m->qa, p.W_qa, h, rq, rq < 256 ? rq : 256, pl.kchunk)) return false;
-  if (!encode_i8(&m->kva, p.W_kva, h, kNa, 256, pl.kchunk)) return false;
+  const int arows = pl.kchunk > 256 ? pl.kchunk / 2 : pl.kchunk;
+  if (!encode_i8(&m->qa, p.W_qa, h, rq, rq < 256 ? rq : 256, arows)) return false;
+  if (!encode_i8(&m->kva, p.W_kva, h, kNa, 256, arows)) return false;
   back_geometry(rq, H * (kNope + kRope), &bw, &brows, &nbox, &kpad);
   if (!encode_i8(&m->qb, p.W_qb, rq, H * (kNope + kRope), bw, brows)) return false;
   back_geometry(kRank, H * kHeadCols, &bw, &brows, &nbox, &kpad);
@@ -1157,7 +1221,7 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
   if ((e = gemm(w.xq, p.W_qa, T, h, rq, w.acc1, na, st, launches)) != cudaSuccess) return e;
   if ((e = gemm(w.xq, p.W_kva, T, h, kNa, w.acc1 + rq, na, st, launches)) != cudaSuccess) return e;
   // 3-4. RMSNorms, requantisation, RoPE(k_pe)
-  const size_t smem = (size_t)na * sizeof(float);
+  const size_t smem = norm_smem(rq);
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
