@@ -147,6 +147,7 @@ struct W8Workspace {
   int8_t* c1;     // [max_tokens, 512]
   float* s2;      // [max_tokens]
   int32_t* acc2;  // [max_tokens, max(H*192, H*256)]
+  unsigned* readers;  // decode-size chain: CTAs done reading acc1
 };
 
 // Decode-size W8A8 chain (T <= kW8SmallRows): tensor maps of the four int8

@@ -215,31 +215,21 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 }
 
-// Per token: dequantise the [q_rank + 576] accumulator row, RMSNorm of the
-// q latent and of compressed_kv, requantise both, RoPE of k_pe.  Shared
-// memory: the row [q_rank + 576] | its weight scales [q_rank + 576] | gamma_q
-// [q_rank] | gamma_kv [512] | cos, sin of the token's position [2][64].
-__host__ __device__ constexpr size_t norm_smem(int q_rank) {
-  return (size_t)(2 * (q_rank + kNa) + q_rank + kRank + 2 * kRope) * sizeof(float);
-}
-
-__global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ acc1,
-                                                         const float* __restrict__ sx,
-                                                         W8Params p, W8Workspace w) {
-  extern __shared__ float yrow[];
-  __shared__ float scratch[8];
-  const int t = blockIdx.x;
+// Per-token normalisation inputs that do not depend on the GEMM: the
+// weight scales of the q_a / kv_a columns, gamma_q, gamma_kv (as floats).
+__device__ __forceinline__ void norm_load_inputs(const W8Params& p, float* colsc, float* gq,
+                                                 float* gk) {
   const int rq = p.q_rank, na = rq + kNa;
-  float* colsc = yrow + na;
-  float* gq = colsc + na;
-  float* gk = gq + rq;
-  float* rope = gk + kRank;
-  // inputs that do not come from the previous kernel are read while it runs
   const __nv_bfloat16* gqp = static_cast<const __nv_bfloat16*>(p.gamma_q);
   const __nv_bfloat16* gkp = static_cast<const __nv_bfloat16*>(p.gamma_kv);
-  for (int c = threadIdx.x; c < na; c += 256) colsc[c] = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
-  for (int c = threadIdx.x; c < rq; c += 256) gq[c] = __bfloat162float(gqp[c]);
-  for (int c = threadIdx.x; c < kRank; c += 256) gk[c] = __bfloat162float(gkp[c]);
+  for (int c = threadIdx.x; c < na; c += blockDim.x) colsc[c] = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
+  for (int c = threadIdx.x; c < rq; c += blockDim.x) gq[c] = __bfloat162float(gqp[c]);
+  for (int c = threadIdx.x; c < kRank; c += blockDim.x) gk[c] = __bfloat162float(gkp[c]);
+}
+
+// cos / sin of token t's position into rope[0, 64) / rope[64, 128) (threads
+// 0..127); an out-of-range position is clamped and recorded.
+__device__ __forceinline__ void rope_load(const W8Params& p, int t, float* rope) {
   if (threadIdx.x < 2 * kRope) {
     int pos = p.positions[t];
     if (pos < 0 || pos >= p.max_pos) {
@@ -249,17 +239,19 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
     const int j = threadIdx.x & (kRope - 1);
     rope[threadIdx.x] = (threadIdx.x < kRope ? p.cos_t : p.sin_t)[(size_t)pos * kRope + j];
   }
-  // in the decode-size chain this kernel is launched while the GEMV that
-  // produces acc1 still runs: let the next kernel start, then wait for acc1
-  grid_dep_launch_dependents();
-  grid_dep_wait();
-  const float s = sx[t];
-  int32_t* a = acc1 + (size_t)t * na;
+}
+
+// One token row (all 256 threads of the CTA): dequantise the [q_rank + 576]
+// accumulator row a (scale s), RMSNorm of the q latent and of compressed_kv,
+// requantise both (codes to q_out / c_out, scales to *s1_out / *s2_out, any
+// address space), RoPE of k_pe to kpe_out (skipped when null).
+__device__ void norm_row(const int32_t* a, float s, const W8Params& p, float* yrow,
+                         const float* colsc, const float* gq, const float* gk, const float* rope,
+                         float* scratch, int8_t* q_out, float* s1_out, int8_t* c_out, float* s2_out,
+                         __nv_bfloat16* kpe_out) {
+  const int rq = p.q_rank, na = rq + kNa;
   for (int c = threadIdx.x; c < na; c += 256) yrow[c] = __fmul_rn(__fmul_rn((float)a[c], s), colsc[c]);
   __syncthreads();
-  // leave the accumulator row zeroed: the decode-size chain adds its split-K
-  // partials into it atomically without clearing it first
-  for (int c = threadIdx.x; c < na; c += 256) a[c] = 0;
   // q latent
   float ss = 0.f;
   for (int c = threadIdx.x; c < rq; c += 256) ss += yrow[c] * yrow[c];
@@ -274,8 +266,8 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   amax = block_reduce<true>(amax, scratch);
   {
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    for (int c = threadIdx.x; c < rq; c += 256) w.q1[(size_t)t * rq + c] = q8(yrow[c], inv);
-    if (threadIdx.x == 0) w.s1[t] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    for (int c = threadIdx.x; c < rq; c += 256) q_out[c] = q8(yrow[c], inv);
+    if (threadIdx.x == 0) *s1_out = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
   }
   // compressed_kv
   float* ck = yrow + rq;
@@ -293,20 +285,48 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   amax = block_reduce<true>(amax, scratch);
   {
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    for (int i = 0; i < 2; ++i) w.c1[(size_t)t * kRank + threadIdx.x + i * 256] = q8(nv[i], inv);
-    if (threadIdx.x == 0) w.s2[t] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    for (int i = 0; i < 2; ++i) c_out[threadIdx.x + i * 256] = q8(nv[i], inv);
+    if (threadIdx.x == 0) *s2_out = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
   }
   // RoPE of k_pe (raw columns 512..575 of the kv_a output)
-  if (threadIdx.x < 32) {
+  if (kpe_out && threadIdx.x < 32) {
     const float* kp = ck + kRank;
     const int j = threadIdx.x;
     const float a0 = kp[2 * j], b0 = kp[2 * j + 1];
     const float* cr = rope;
     const float* sr = rope + kRope;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope;
-    out[j] = __float2bfloat16_rn(a0 * cr[j] - b0 * sr[j]);
-    out[j + 32] = __float2bfloat16_rn(b0 * cr[j + 32] + a0 * sr[j + 32]);
+    kpe_out[j] = __float2bfloat16_rn(a0 * cr[j] - b0 * sr[j]);
+    kpe_out[j + 32] = __float2bfloat16_rn(b0 * cr[j + 32] + a0 * sr[j + 32]);
   }
+  __syncthreads();  // yrow is reused by the next row
+}
+
+// Per token (prefill sizes): norm_row on one accumulator row per CTA, which
+// it leaves zeroed.  Shared memory: the row [q_rank + 576] | its weight
+// scales [q_rank + 576] | gamma_q [q_rank] | gamma_kv [512] | cos, sin [2][64].
+__host__ __device__ constexpr size_t norm_smem(int q_rank) {
+  return (size_t)(2 * (q_rank + kNa) + q_rank + kRank + 2 * kRope) * sizeof(float);
+}
+
+__global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ acc1,
+                                                         const float* __restrict__ sx,
+                                                         W8Params p, W8Workspace w) {
+  extern __shared__ float yrow[];
+  __shared__ float scratch[8];
+  const int t = blockIdx.x;
+  const int rq = p.q_rank, na = rq + kNa;
+  float* colsc = yrow + na;
+  float* gq = colsc + na;
+  float* gk = gq + rq;
+  float* rope = gk + kRank;
+  norm_load_inputs(p, colsc, gq, gk);
+  rope_load(p, t, rope);
+  int32_t* a = acc1 + (size_t)t * na;
+  norm_row(a, sx[t], p, yrow, colsc, gq, gk, rope, scratch, w.q1 + (size_t)t * rq, w.s1 + t,
+           w.c1 + (size_t)t * kRank, w.s2 + t,
+           static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope);
+  // leave the accumulator row zeroed (the decode-size chain adds into it)
+  for (int c = threadIdx.x; c < na; c += 256) a[c] = 0;
 }
 
 // Dequantise q_b / kv_b accumulators and write the head-major outputs.
@@ -352,21 +372,22 @@ __global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __rest
 }
 
 // ---------------------------------------------------------------- decode-size chain (T <= 8)
-// Three launches instead of about ten, chained with programmatic dependent
-// launch so that each kernel is resident, with its weight copies in flight,
-// before its predecessor finishes:
-//   front  q_a / kv_a split-K GEMV.  A TMA copy of the CTA's weight tile is
-//          issued at entry; meanwhile the CTA quantises the hidden rows
-//          itself (every CTA finds the same amax, so the codes are those of
-//          step 1); int32 partials are added atomically into the accumulator
-//          rows, which the norm kernel leaves zeroed after reading them.  The
-//          CTA also prefetches its share of W_qb and W_kvb into L2, so that
-//          the whole weight stream is requested in the first microsecond.
-//   norm   RMSNorms, requantisation, RoPE(k_pe) (norm_quant_kernel).
+// Two launches instead of about ten, the second launched with programmatic
+// stream serialisation so that it is resident, with its weight copies in
+// flight, before the first finishes:
+//   front  q_a / kv_a split-K GEMV, about one CTA per SM.  TMA copies of the
+//          CTA's weight tile are issued at entry; meanwhile the CTA
+//          quantises the hidden rows itself (every CTA finds the same amax,
+//          so the codes are those of step 1); int32 partials are summed
+//          across the CTA's warps and added atomically into the accumulator
+//          rows, which the back kernel leaves zeroed after reading them.
 //   back   q_b and kv_b, full K per 128-column block, each CTA walking a
-//          fixed list of blocks through a ring of TMA boxes; dequantisation,
-//          RoPE(q_pe) and the head-major stores happen in the epilogue, so no
-//          int32 accumulator goes back to memory.
+//          fixed list of blocks through a ring of TMA boxes (the rest of its
+//          boxes prefetched into L2 at entry).  After the dependency wait
+//          every CTA forms the requantised q_b / kv_b operands itself
+//          (RMSNorms, step 4); dequantisation, RoPE(q_pe) and the head-major
+//          stores happen in the epilogue, so no int32 accumulator of the
+//          second stage goes back to memory.
 // The two GEMV kernels also serve the plain int8 GEMM entry for M <= 8 (no
 // quantisation, int32 results stored), which is how their integer sums are
 // checked bit for bit.
@@ -376,8 +397,6 @@ struct W8FrontParams {
   const void* x;                   // QUANT: bf16 hidden rows [M, K]; else int8 A [M, K]
   int32_t* acc;                    // [M, ldc]
   float* sx;                       // QUANT: [M] per-row scales
-  const unsigned char* pf[2];      // L2 prefetch ranges (W_qb, W_kvb)
-  unsigned long long pf_bytes[2];
   unsigned* status;
   unsigned long long budget_ns;
   int M, K, ldc;
@@ -516,26 +535,6 @@ __global__ void __launch_bounds__(256) w8_front_kernel(const __grid_constant__ W
   }
   while (!mbar_test_wait(bar, 0)) {
   }
-  if (tid == 32) {
-    // this CTA's share of the q_b / kv_b weight bytes, prefetched into L2
-    // once its own tile is in (the q_a / kv_a stream goes first)
-    const unsigned long long nct = (unsigned long long)gridDim.x * gridDim.y;
-    const unsigned long long id = (unsigned long long)blockIdx.y * gridDim.x + bx;
-    const unsigned long long tot = p.pf_bytes[0] + p.pf_bytes[1];
-    const unsigned long long per = ((tot + nct - 1) / nct + 15) & ~15ull;
-    const unsigned long long b0 = id * per, b1 = b0 + per < tot ? b0 + per : tot;
-    unsigned long long base = 0;
-    for (int r = 0; r < 2; ++r) {
-      const unsigned long long lo = b0 > base ? b0 : base;
-      const unsigned long long end = base + p.pf_bytes[r];
-      const unsigned long long hi = b1 < end ? b1 : end;
-      for (unsigned long long o = lo; o < hi; o += 65536ull) {
-        const unsigned long long len = hi - o < 65536ull ? hi - o : 65536ull;
-        prefetch_l2_bulk(p.pf[r] + (o - base), (uint32_t)len);
-      }
-      base = end;
-    }
-  }
   // a lane owns 8 columns; warp w takes the 4-row groups w, w + 8, ...
   int acc[MT][8];
 #pragma unroll
@@ -605,21 +604,18 @@ constexpr int kBackBox = 32768;     // bytes per ring slot (128 columns x 256 ro
 
 struct W8BackParams {
   CUtensorMap tm[2];               // W_qb, W_kvb (or one matrix): box bw x brows
-  const int8_t* act[2];            // int8 rows [M, K] feeding each matrix
-  const float* srow[2];            // [M] row scales (prolog mode)
+  const int8_t* act[2];            // raw mode: int8 rows [M, K] of matrix 0
   const float* scol[2];            // [N] column scales (prolog mode)
+  W8Params pr;                     // prolog mode: the call's inputs and outputs
+  int32_t* acc1;                   // prolog mode: q_a / kv_a accumulator rows [M, q_rank + 576]
+  const float* sx;                 // [M] hidden-row scales
+  W8Workspace ws;                  // operand copies (q1, s1, c1, s2) written by CTA 0
+  unsigned* readers;               // CTAs done reading acc1 (the last one clears it)
   const int* units;                // [grid + 1] offsets, then block ids; null: block b -> CTA b % grid
   int32_t* raw;                    // raw mode: C [M, raw_ld]
-  void* q_nope;
-  void* q_pe;
-  void* k_nope;
-  void* value;
-  const int32_t* positions;
-  const float* cos_t;
-  const float* sin_t;
   unsigned* status;
   unsigned long long budget_ns;
-  int M, s, heads, max_pos, raw_ld, raw_mode;
+  int M, raw_ld, raw_mode;
   int K[2], N[2];
   int bw[2];                       // box width in columns (128, or N when N < 128)
   int brows[2];                    // box height in rows (256, or K when K < 256)
@@ -629,11 +625,13 @@ struct W8BackParams {
   int nst;                         // ring slots (<= kBackStages)
 };
 
-// Persistent over the CTA's blocks; 256 threads.  Warp w takes rows
-// [32w, 32w + 32) of each box, a lane 4 columns (one 4-byte load per row, a
-// warp one 128-byte row).  Shared memory: ring [nst][32 KB] |
-// activations [MT][kpad0] then [MT][kpad1] | reduction [8][MT][128] int |
-// mbarriers.
+// Persistent over the CTA's blocks; 256 threads.  In prolog mode every CTA
+// first forms the q_b / kv_b operands itself (norm_row on the M accumulator
+// rows: cheaper than one more kernel boundary); CTA 0 also writes k_pe and
+// the operand copies.  Warp w takes rows [32w, 32w + 32) of each box, a lane
+// 4 columns (one 4-byte load per row, a warp one 128-byte row).  Shared
+// memory: ring [nst][32 KB] | codes [MT][kpad0] then [MT][kpad1] |
+// reduction [8][MT][128] int | norm scratch (prolog mode) | mbarriers.
 template <int MT>
 __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8BackParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -646,7 +644,17 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
   int8_t* sAct0 = reinterpret_cast<int8_t*>(sm + (size_t)nst * kBackBox);
   int8_t* sAct1 = sAct0 + MT * p.kpad[0];
   int* red = reinterpret_cast<int*>(sAct1 + MT * p.kpad[1]);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(red + 8 * MT * 128);
+  const bool prolog = !p.raw_mode;
+  const int rq = p.pr.q_rank, na = rq + kNa;
+  float* yrow = reinterpret_cast<float*>(red + 8 * MT * 128);
+  float* colsc = yrow + (prolog ? na : 0);
+  float* gq = colsc + (prolog ? na : 0);
+  float* gk = gq + (prolog ? rq : 0);
+  float* rope = gk + (prolog ? kRank : 0);      // [MT][128]
+  float* srow = rope + (prolog ? MT * 2 * kRope : 0);  // [2][MT]
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(srow + (prolog ? 2 * MT : 0));
+  __shared__ float scratch[8];
+  __shared__ int s_last;
   // this CTA's blocks
   int u0, nu;
   const int* ulist = nullptr;
@@ -658,7 +666,18 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     u0 = cta;
     nu = cta < p.nblk ? (p.nblk - 1 - cta) / G + 1 : 0;
   }
-  if (nu == 0) return;
+  if (nu == 0) {
+    // no blocks (only when the grid has more CTAs than blocks): still one
+    // of the acc1 readers to count
+    if (prolog) {
+      grid_dep_wait();
+      if (tid == 0 && atomicAdd(p.readers, 1u) == (unsigned)G - 1) {
+        for (int i = 0; i < p.M * na; ++i) p.acc1[i] = 0;
+        *p.readers = 0u;
+      }
+    }
+    return;
+  }
   auto block_of = [&](int i) { return ulist ? ulist[i] : u0 + i * G; };
   // producer state (thread 0): next box to issue
   int iss_u = 0, iss_j = 0, issued = 0;
@@ -683,18 +702,55 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     // weights are read-only inputs: their copies may start before the
     // kernel that produces the activations has finished
     for (int i = 0; i < nst; ++i) issue_next();
+    // the rest of this CTA's boxes into L2 now, so that the weight stream
+    // runs while the operands are formed
+    int u = iss_u, j = iss_j;
+    while (u < nu) {
+      const int b = block_of(u);
+      const int sel = b < p.nblk1 ? 0 : 1;
+      tma_prefetch_2d(&p.tm[sel], (sel ? b - p.nblk1 : b) * 128, j * p.brows[sel]);
+      if (++j == p.nbox[sel]) {
+        j = 0;
+        ++u;
+      }
+    }
   }
-  grid_dep_wait();
-  // activation rows (zero past K) -- written by the previous kernel
-  for (int sel = 0; sel < 2; ++sel) {
-    const int kp = p.kpad[sel], K = p.K[sel];
-    int8_t* dst = sel ? sAct1 : sAct0;
-    if (p.raw_mode && sel == 1) break;
+  if (prolog) {
+    // inputs that do not come from the previous kernel, read while it runs
+    norm_load_inputs(p.pr, colsc, gq, gk);
+    for (int m = 0; m < p.M; ++m) rope_load(p.pr, m, rope + m * 2 * kRope);
+    // codes are written up to K; the padding rows of the last box read zeros
+    for (int i = tid; i < MT * p.kpad[0]; i += 256) sAct0[i] = 0;
+    for (int i = tid; i < MT * p.kpad[1]; i += 256) sAct1[i] = 0;
+    __syncthreads();
+    grid_dep_wait();
+    for (int m = 0; m < p.M; ++m)
+      norm_row(p.acc1 + (size_t)m * na, p.sx[m], p.pr, yrow, colsc, gq, gk, rope + m * 2 * kRope,
+               scratch, sAct0 + m * p.kpad[0], srow + m, sAct1 + m * p.kpad[1], srow + MT + m,
+               cta == 0 ? static_cast<__nv_bfloat16*>(p.pr.k_pe) + (size_t)m * kRope : nullptr);
+    // the last CTA to finish reading acc1 clears it for the next call
+    if (tid == 0) s_last = atomicAdd(p.readers, 1u) == (unsigned)G - 1 ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+      for (int i = tid; i < p.M * na; i += 256) p.acc1[i] = 0;
+      if (tid == 0) *p.readers = 0u;
+    }
+    if (cta == 0) {  // operand copies for inspection
+      for (int i = tid; i < p.M * rq; i += 256) p.ws.q1[i] = sAct0[(i / rq) * p.kpad[0] + i % rq];
+      for (int i = tid; i < p.M * kRank; i += 256) p.ws.c1[i] = sAct1[(i / kRank) * p.kpad[1] + i % kRank];
+      if (tid < p.M) {
+        p.ws.s1[tid] = srow[tid];
+        p.ws.s2[tid] = srow[MT + tid];
+      }
+    }
+  } else {
+    // raw mode: int8 rows of matrix 0 (zero past K)
+    const int kp = p.kpad[0], K = p.K[0];
     for (int i = tid; i < MT * (kp >> 4); i += 256) {
       const int m = i / (kp >> 4), k = 16 * (i - m * (kp >> 4));
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (m < p.M && k < K) v = *reinterpret_cast<const uint4*>(p.act[sel] + (size_t)m * K + k);
-      *reinterpret_cast<uint4*>(dst + m * kp + k) = v;
+      if (m < p.M && k < K) v = *reinterpret_cast<const uint4*>(p.act[0] + (size_t)m * K + k);
+      *reinterpret_cast<uint4*>(sAct0 + m * kp + k) = v;
     }
   }
   __syncthreads();
@@ -777,31 +833,29 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
         *reinterpret_cast<int2*>(p.raw + (size_t)m * p.raw_ld + gc) = make_int2(v0, v1);
         continue;
       }
-      const float sr = p.srow[sel][m];
+      const float sr = srow[sel * MT + m];
       const float y0 = __fmul_rn(__fmul_rn((float)v0, sr), p.scol[sel][gc]);
       const float y1 = __fmul_rn(__fmul_rn((float)v1, sr), p.scol[sel][gc + 1]);
-      const int bi = m / p.s, si = m - bi * p.s;
+      const int bi = m / p.pr.s, si = m - bi * p.pr.s;
       if (sel == 0) {
         const int h = gc / (kNope + kRope), e = gc - h * (kNope + kRope);
-        const size_t orow = ((size_t)bi * p.heads + h) * p.s + si;
+        const size_t orow = ((size_t)bi * p.pr.heads + h) * p.pr.s + si;
         if (e < kNope) {
-          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.q_nope) + orow * kNope + e) =
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.pr.q_nope) + orow * kNope + e) =
               __floats2bfloat162_rn(y0, y1);
         } else {
           const int j = (e - kNope) >> 1;
-          int pos = p.positions[m];
-          pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-          const float* cr = p.cos_t + (size_t)pos * kRope;
-          const float* sn = p.sin_t + (size_t)pos * kRope;
-          __nv_bfloat16* qp = static_cast<__nv_bfloat16*>(p.q_pe) + orow * kRope;
+          const float* cr = rope + m * 2 * kRope;
+          const float* sn = cr + kRope;
+          __nv_bfloat16* qp = static_cast<__nv_bfloat16*>(p.pr.q_pe) + orow * kRope;
           qp[j] = __float2bfloat16_rn(y0 * cr[j] - y1 * sn[j]);
           qp[j + 32] = __float2bfloat16_rn(y1 * cr[j + 32] + y0 * sn[j + 32]);
         }
       } else {
         const int h = gc / kHeadCols, e = gc - h * kHeadCols;
-        const size_t orow = ((size_t)bi * p.heads + h) * p.s + si;
-        __nv_bfloat16* dst = e < kNope ? static_cast<__nv_bfloat16*>(p.k_nope) + orow * kNope + e
-                                       : static_cast<__nv_bfloat16*>(p.value) + orow * kV + (e - kNope);
+        const size_t orow = ((size_t)bi * p.pr.heads + h) * p.pr.s + si;
+        __nv_bfloat16* dst = e < kNope ? static_cast<__nv_bfloat16*>(p.pr.k_nope) + orow * kNope + e
+                                       : static_cast<__nv_bfloat16*>(p.pr.value) + orow * kV + (e - kNope);
         *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(y0, y1);
       }
     }
@@ -809,15 +863,19 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
   }
 }
 
-__host__ __device__ constexpr size_t w8_back_smem(int MT, int nst, int kp0, int kp1) {
+// nrm_floats: the prolog-mode norm scratch (0 in raw mode).
+__host__ __device__ constexpr size_t w8_back_smem(int MT, int nst, int kp0, int kp1, int nrm_floats) {
   return 128 + (size_t)nst * kBackBox + (size_t)MT * (kp0 + kp1) + 8 * (size_t)MT * 512 +
-         8 * kBackStages + 16;
+         4 * (size_t)nrm_floats + 8 * kBackStages + 16;
+}
+__host__ __device__ constexpr int back_norm_floats(int MT, int q_rank) {
+  return 2 * (q_rank + kNa) + q_rank + kRank + MT * 2 * kRope + 2 * MT;
 }
 
-// Ring slots that fit next to the activations and the reduction area.
-int back_stages(int MT, int kp0, int kp1) {
+// Ring slots that fit next to the codes, the reduction area and the scratch.
+int back_stages(int MT, int kp0, int kp1, int nrm_floats) {
   int n = kBackStages;
-  while (n > 2 && w8_back_smem(MT, n, kp0, kp1) > 227 * 1024) --n;
+  while (n > 2 && w8_back_smem(MT, n, kp0, kp1, nrm_floats) > 227 * 1024) --n;
   return n;
 }
 
@@ -864,8 +922,9 @@ cudaError_t launch_front_m(const W8FrontParams& f, int nblk, int splits, cudaStr
 template <int MT>
 cudaError_t launch_back(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
   W8BackParams bb = b;
-  bb.nst = back_stages(MT, b.kpad[0], b.kpad[1]);
-  const size_t smem = w8_back_smem(MT, bb.nst, b.kpad[0], b.kpad[1]);
+  const int nf = b.raw_mode ? 0 : back_norm_floats(MT, b.pr.q_rank);
+  bb.nst = back_stages(MT, b.kpad[0], b.kpad[1], nf);
+  const size_t smem = w8_back_smem(MT, bb.nst, b.kpad[0], b.kpad[1], nf);
   cudaError_t e = cudaFuncSetAttribute(w8_back_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -919,7 +978,6 @@ cudaError_t gemv_tma(const int8_t* A, const int8_t* W, int M, int K, int N, int3
     b.raw_ld = ldc;
     b.raw_mode = 1;
     b.M = M;
-    b.s = 1;
     b.K[0] = K;
     b.N[0] = N;
     b.bw[0] = bw;
@@ -960,8 +1018,8 @@ cudaError_t gemv_tma(const int8_t* A, const int8_t* W, int M, int K, int N, int3
   return launch_front_m<false>(f, nblk, splits, st);
 }
 
-// Decode-size chain: front (normal launch) -> norm -> back (both launched
-// with programmatic stream serialisation).
+// Decode-size chain: front (normal launch) -> back (launched with
+// programmatic stream serialisation; it forms the q_b / kv_b operands itself).
 cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8SmallPlan& pl,
                                const W8Maps& mp, cudaStream_t st, int* launches) {
   const int T = p.T, rq = p.q_rank, H = p.heads;
@@ -971,10 +1029,6 @@ cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8
   f.x = p.hidden;
   f.acc = w.acc1;
   f.sx = w.sx;
-  f.pf[0] = reinterpret_cast<const unsigned char*>(p.W_qb);
-  f.pf_bytes[0] = (unsigned long long)rq * H * (kNope + kRope);
-  f.pf[1] = reinterpret_cast<const unsigned char*>(p.W_kvb);
-  f.pf_bytes[1] = (unsigned long long)kRank * H * kHeadCols;
   f.status = p.status;
   f.budget_ns = p.budget_ns;
   f.M = T;
@@ -991,34 +1045,20 @@ cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8
   cudaError_t e = launch_front_m<true>(f, pl.nblk_a, pl.splits, st);
   ++*launches;
   if (e != cudaSuccess) return e;
-  const size_t nsmem = norm_smem(rq);
-  e = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)nsmem);
-  if (e == cudaSuccess) e = launch_k(norm_quant_kernel, dim3(T), dim3(256), nsmem, st, true, w.acc1, (const float*)w.sx, p, w);
-  ++*launches;
-  if (e != cudaSuccess) return e;
   W8BackParams b = {};
   b.tm[0] = mp.qb;
   b.tm[1] = mp.kvb;
-  b.act[0] = w.q1;
-  b.act[1] = w.c1;
-  b.srow[0] = w.s1;
-  b.srow[1] = w.s2;
   b.scol[0] = p.sW_qb;
   b.scol[1] = p.sW_kvb;
+  b.pr = p;
+  b.acc1 = w.acc1;
+  b.sx = w.sx;
+  b.ws = w;
+  b.readers = w.readers;
   b.units = pl.units;
-  b.q_nope = p.q_nope;
-  b.q_pe = p.q_pe;
-  b.k_nope = p.k_nope;
-  b.value = p.value;
-  b.positions = p.positions;
-  b.cos_t = p.cos_t;
-  b.sin_t = p.sin_t;
   b.status = p.status;
   b.budget_ns = p.budget_ns;
   b.M = T;
-  b.s = p.s;
-  b.heads = H;
-  b.max_pos = p.max_pos;
   b.K[0] = rq;
   b.K[1] = kRank;
   b.N[0] = H * (kNope + kRope);
@@ -1122,7 +1162,7 @@ size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens, int
   const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
   return align256(T * hidden) + align256(T * 4) + align256(T * (q_rank + kNa) * 4) +
          align256(T * q_rank) + align256(T * 4) + align256(T * kRank) + align256(T * 4) +
-         align256(T * nb * 4) + align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4);
+         align256(T * nb * 4) + align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4) + 256;
 }
 
 void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,
@@ -1140,6 +1180,8 @@ void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_t
   w->acc2 = reinterpret_cast<int32_t*>(b); b += align256(T * nb * 4);
   small_plan(hidden, q_rank, heads, num_sms, plan);
   plan->units = reinterpret_cast<int*>(b);
+  b += align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4);
+  w->readers = reinterpret_cast<unsigned*>(b);
 }
 
 cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int hidden,
@@ -1147,6 +1189,7 @@ cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int
   (void)hidden;
   (void)num_sms;
   cudaError_t e = cudaMemset(w.acc1, 0, (size_t)max_tokens * (q_rank + kNa) * 4);
+  if (e == cudaSuccess) e = cudaMemset(w.readers, 0, 256);
   if (e != cudaSuccess) return e;
   int mu = 0;
   const std::vector<int> t = small_units(q_rank, heads, plan, &mu);
