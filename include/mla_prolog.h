@@ -104,7 +104,7 @@ typedef struct mla_prolog_config {
   int max_tokens;   /* largest b*s any run on this handle will pass (sizes workspace)  */
   int max_pos;      /* rows of the cos/sin tables                                       */
   int quant;        /* mla_quant                                                        */
-  int q_lora_rank;  /* W8A8 only: q latent width (1536); multiple of 64                 */
+  int q_lora_rank;  /* W8A8 only: q latent width (1536); multiple of 64, <= 3520        */
   unsigned long long spin_budget_ns; /* device wait limit; 0 selects 1 s               */
 } mla_prolog_config;
 
@@ -114,8 +114,8 @@ typedef struct mla_prolog_s* mla_prolog_t;
  * latent rows, barrier counters, status word) on the current device and
  * return a handle in *out.  Errors: MLA_ERR_INVALID_ARG (null, non-positive
  * sizes, eps < 0), MLA_ERR_UNSUPPORTED (kv_lora_rank != 512, rope_dim != 64,
- * nope/v != 128, hidden % 64 != 0, W8A8 with dtype != BF16 or
- * q_lora_rank % 64 != 0), MLA_ERR_NO_MEMORY, MLA_ERR_CUDA. */
+ * nope/v != 128, hidden % 64 != 0, W8A8 with dtype != BF16, q_lora_rank
+ * % 64 != 0 or q_lora_rank > 3520), MLA_ERR_NO_MEMORY, MLA_ERR_CUDA. */
 mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out);
 
 /* Enqueue one KV prolog (steps 1-7 above) of T = b*s token rows on `stream`.

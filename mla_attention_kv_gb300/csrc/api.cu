@@ -111,7 +111,8 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
       c.hidden % 64 != 0)
     return MLA_ERR_UNSUPPORTED;
   if (c.quant == MLA_QUANT_W8A8 &&
-      (c.dtype != MLA_BF16 || c.q_lora_rank <= 0 || c.q_lora_rank % 64 != 0))
+      (c.dtype != MLA_BF16 || c.q_lora_rank <= 0 || c.q_lora_rank % 64 != 0 ||
+       c.q_lora_rank + kNa > kW8MaxNormCols))
     return MLA_ERR_UNSUPPORTED;
 
   mla_prolog_s* h = new (std::nothrow) mla_prolog_s();

@@ -153,6 +153,8 @@ struct W8Workspace {
 // Decode-size W8A8 chain (T <= kW8SmallRows): tensor maps of the four int8
 // weight matrices and the per-handle launch plan.
 constexpr int kW8SmallRows = 8;
+// Longest q_rank + 576 row the W8A8 normalisation handles (q_rank <= 3520).
+constexpr int kW8MaxNormCols = 4096;
 struct W8Maps {
   CUtensorMap qa, kva;  // W_qa [hidden, q_rank], W_kva [hidden, 576]: box 256 columns x kchunk rows
   CUtensorMap qb, kvb;  // W_qb [q_rank, H*192], W_kvb [512, H*256]: box 128 columns x 256 rows

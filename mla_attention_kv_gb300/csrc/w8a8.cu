@@ -215,16 +215,46 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 }
 
+// 16-byte vectors of a [q_rank + 576] row per thread of a 256-thread CTA:
+// every global load of a row is issued before the first one is used.
+constexpr int kNormVec = kW8MaxNormCols / 4 / 256;
+
 // Per-token normalisation inputs that do not depend on the GEMM: the
 // weight scales of the q_a / kv_a columns, gamma_q, gamma_kv (as floats).
+// q_rank % 64 == 0, so every piece is a whole number of 16-byte vectors.
 __device__ __forceinline__ void norm_load_inputs(const W8Params& p, float* colsc, float* gq,
                                                  float* gk) {
-  const int rq = p.q_rank, na = rq + kNa;
-  const __nv_bfloat16* gqp = static_cast<const __nv_bfloat16*>(p.gamma_q);
-  const __nv_bfloat16* gkp = static_cast<const __nv_bfloat16*>(p.gamma_kv);
-  for (int c = threadIdx.x; c < na; c += blockDim.x) colsc[c] = c < rq ? p.sW_qa[c] : p.sW_kva[c - rq];
-  for (int c = threadIdx.x; c < rq; c += blockDim.x) gq[c] = __bfloat162float(gqp[c]);
-  for (int c = threadIdx.x; c < kRank; c += blockDim.x) gk[c] = __bfloat162float(gkp[c]);
+  const int rq = p.q_rank, nq4 = rq / 4, na4 = (rq + kNa) / 4;
+  const int nq8 = rq / 8, ng8 = (rq + kRank) / 8;
+  float4 v[kNormVec];
+  uint4 g[kNormVec / 2];
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    v[k] = i < nq4 ? reinterpret_cast<const float4*>(p.sW_qa)[i]
+                   : (i < na4 ? reinterpret_cast<const float4*>(p.sW_kva)[i - nq4] : make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+#pragma unroll
+  for (int k = 0; k < kNormVec / 2; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    g[k] = i < nq8 ? reinterpret_cast<const uint4*>(p.gamma_q)[i]
+                   : (i < ng8 ? reinterpret_cast<const uint4*>(p.gamma_kv)[i - nq8] : make_uint4(0u, 0u, 0u, 0u));
+  }
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    if (i < na4) reinterpret_cast<float4*>(colsc)[i] = v[k];
+  }
+#pragma unroll
+  for (int k = 0; k < kNormVec / 2; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    if (i < ng8) {
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&g[k]);
+      float* d = i < nq8 ? gq + 8 * i : gk + 8 * (i - nq8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) d[j] = __bfloat162float(e[j]);
+    }
+  }
 }
 
 // cos / sin of token t's position into rope[0, 64) / rope[64, 128) (threads
@@ -249,8 +279,26 @@ __device__ void norm_row(const int32_t* a, float s, const W8Params& p, float* yr
                          const float* colsc, const float* gq, const float* gk, const float* rope,
                          float* scratch, int8_t* q_out, float* s1_out, int8_t* c_out, float* s2_out,
                          __nv_bfloat16* kpe_out) {
-  const int rq = p.q_rank, na = rq + kNa;
-  for (int c = threadIdx.x; c < na; c += 256) yrow[c] = __fmul_rn(__fmul_rn((float)a[c], s), colsc[c]);
+  const int rq = p.q_rank, na4 = (rq + kNa) / 4;
+  int4 av[kNormVec];
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    av[k] = i < na4 ? reinterpret_cast<const int4*>(a)[i] : make_int4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int k = 0; k < kNormVec; ++k) {
+    const int i = threadIdx.x + 256 * k;
+    if (i < na4) {
+      const float4 c = reinterpret_cast<const float4*>(colsc)[i];
+      float4 y;
+      y.x = __fmul_rn(__fmul_rn((float)av[k].x, s), c.x);
+      y.y = __fmul_rn(__fmul_rn((float)av[k].y, s), c.y);
+      y.z = __fmul_rn(__fmul_rn((float)av[k].z, s), c.z);
+      y.w = __fmul_rn(__fmul_rn((float)av[k].w, s), c.w);
+      reinterpret_cast<float4*>(yrow)[i] = y;
+    }
+  }
   __syncthreads();
   // q latent
   float ss = 0.f;
@@ -382,8 +430,8 @@ __global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __rest
 //          across the CTA's warps and added atomically into the accumulator
 //          rows, which the back kernel leaves zeroed after reading them.
 //   back   q_b and kv_b, full K per 128-column block, each CTA walking a
-//          fixed list of blocks through a ring of TMA boxes (the rest of its
-//          boxes prefetched into L2 at entry).  After the dependency wait
+//          fixed list of blocks through a ring of TMA boxes (the first ones
+//          issued while the front kernel runs).  After the dependency wait
 //          every CTA forms the requantised q_b / kv_b operands itself
 //          (RMSNorms, step 4); dequantisation, RoPE(q_pe) and the head-major
 //          stores happen in the epilogue, so no int32 accumulator of the
@@ -623,6 +671,7 @@ struct W8BackParams {
   int kpad[2];                     // nbox * brows: activation row length in shared memory
   int nblk1, nblk;                 // blocks of matrix 0, of both
   int nst;                         // ring slots (<= kBackStages)
+  int npre;                        // boxes issued before the dependency wait (<= nst)
 };
 
 // Persistent over the CTA's blocks; 256 threads.  In prolog mode every CTA
@@ -701,19 +750,9 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     fence_mbar_init();
     // weights are read-only inputs: their copies may start before the
     // kernel that produces the activations has finished
-    for (int i = 0; i < nst; ++i) issue_next();
-    // the rest of this CTA's boxes into L2 now, so that the weight stream
-    // runs while the operands are formed
-    int u = iss_u, j = iss_j;
-    while (u < nu) {
-      const int b = block_of(u);
-      const int sel = b < p.nblk1 ? 0 : 1;
-      tma_prefetch_2d(&p.tm[sel], (sel ? b - p.nblk1 : b) * 128, j * p.brows[sel]);
-      if (++j == p.nbox[sel]) {
-        j = 0;
-        ++u;
-      }
-    }
+    // weights are read-only: their copies may start before the previous
+    // kernel has finished
+    for (int i = 0; i < p.npre; ++i) issue_next();
   }
   if (prolog) {
     // inputs that do not come from the previous kernel, read while it runs
@@ -724,6 +763,8 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     for (int i = tid; i < MT * p.kpad[1]; i += 256) sAct1[i] = 0;
     __syncthreads();
     grid_dep_wait();
+    if (tid == 0)
+      for (int i = p.npre; i < nst; ++i) issue_next();
     for (int m = 0; m < p.M; ++m)
       norm_row(p.acc1 + (size_t)m * na, p.sx[m], p.pr, yrow, colsc, gq, gk, rope + m * 2 * kRope,
                scratch, sAct0 + m * p.kpad[0], srow + m, sAct1 + m * p.kpad[1], srow + MT + m,
@@ -744,6 +785,8 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
       }
     }
   } else {
+    if (tid == 0)
+      for (int i = p.npre; i < nst; ++i) issue_next();
     // raw mode: int8 rows of matrix 0 (zero past K)
     const int kp = p.kpad[0], K = p.K[0];
     for (int i = tid; i < MT * (kp >> 4); i += 256) {
@@ -765,6 +808,14 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
     for (int m = 0; m < MT; ++m)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[m][c] = 0;
+    // the epilogue's column scales, loaded now (thread t always handles the
+    // column pair t % 64 of the block)
+    const int cb = (sel ? b - p.nblk1 : b) * 128;
+    float sc0 = 0.f, sc1 = 0.f;
+    if (!p.raw_mode && cb + 2 * (tid & 63) < p.N[sel] && 2 * (tid & 63) < bw) {
+      sc0 = p.scol[sel][cb + 2 * (tid & 63)];
+      sc1 = p.scol[sel][cb + 2 * (tid & 63) + 1];
+    }
     for (int j = 0; j < p.nbox[sel]; ++j) {
       const int slot = consumed % nst;
       const uint32_t bar = smem_u32(s_bar + slot);
@@ -817,7 +868,6 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
       *reinterpret_cast<int4*>(red + (warp * MT + m) * 128 + lane * 4) =
           make_int4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
     __syncthreads();
-    const int cb = (sel ? b - p.nblk1 : b) * 128;
     for (int idx = tid; idx < p.M * 64; idx += 256) {
       const int m = idx >> 6, col = 2 * (idx & 63);
       const int gc = cb + col;
@@ -834,8 +884,8 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
         continue;
       }
       const float sr = srow[sel * MT + m];
-      const float y0 = __fmul_rn(__fmul_rn((float)v0, sr), p.scol[sel][gc]);
-      const float y1 = __fmul_rn(__fmul_rn((float)v1, sr), p.scol[sel][gc + 1]);
+      const float y0 = __fmul_rn(__fmul_rn((float)v0, sr), sc0);
+      const float y1 = __fmul_rn(__fmul_rn((float)v1, sr), sc1);
       const int bi = m / p.pr.s, si = m - bi * p.pr.s;
       if (sel == 0) {
         const int h = gc / (kNope + kRope), e = gc - h * (kNope + kRope);
@@ -923,7 +973,11 @@ template <int MT>
 cudaError_t launch_back(const W8BackParams& b, int grid, cudaStream_t st, bool pdl) {
   W8BackParams bb = b;
   const int nf = b.raw_mode ? 0 : back_norm_floats(MT, b.pr.q_rank);
-  bb.nst = back_stages(MT, b.kpad[0], b.kpad[1], nf);
+  // prolog mode: two slots, so that the CTAs fit next to the front kernel's
+  // and start their copies while it runs (a deeper ring that has to wait
+  // for the front kernel to leave measured no faster)
+  bb.nst = b.raw_mode ? back_stages(MT, b.kpad[0], b.kpad[1], nf) : 2;
+  if (bb.npre > bb.nst) bb.npre = bb.nst;
   const size_t smem = w8_back_smem(MT, bb.nst, b.kpad[0], b.kpad[1], nf);
   cudaError_t e = cudaFuncSetAttribute(w8_back_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -1056,6 +1110,7 @@ cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8
   b.ws = w;
   b.readers = w.readers;
   b.units = pl.units;
+  b.npre = 2;
   b.status = p.status;
   b.budget_ns = p.budget_ns;
   b.M = T;
