@@ -36,6 +36,9 @@ struct mla_prolog_s {
   size_t pk_kva_bytes, pk_bytes;
   const void* pk_src_kva;
   const void* pk_src_kvb;
+  // the snapshot was just written: the next decode launch must not read it
+  // before its dependency wait (launched without programmatic serialisation)
+  bool pk_fresh;
   // W8A8 workspace, decode-size launch plan and tensor maps (see w8a8.cu)
   W8Workspace w8;
   W8SmallPlan w8plan;
@@ -272,8 +275,9 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
   for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
     p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
-    cudaError_t e = decode_launch(bf16, packed, h->dplan, p, stream);
+    cudaError_t e = decode_launch(bf16, packed, h->dplan, p, !(packed && h->pk_fresh), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (packed) h->pk_fresh = false;
     h->last_launches += 1;
   }
   return MLA_OK;
@@ -308,6 +312,7 @@ mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, cons
   if (e != cudaSuccess) return cuda_fail(e, "pack weights");
   h->pk_src_kva = W_kva;
   h->pk_src_kvb = W_kvb;
+  h->pk_fresh = true;
   return MLA_OK;
 }
 

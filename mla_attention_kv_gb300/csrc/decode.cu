@@ -155,9 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   float* sCos = reinterpret_cast<float*>(smem + p.off_misc + 1024);
   float* sSin = sCos + kRope;
   const bool owner = cta < TT;           // this CTA ropes / normalises token row `cta`
-  int pos = 0;
-  if (owner && tid == 0) pos = p.positions[p.t0 + cta];
-  const unsigned st0 = *reinterpret_cast<volatile unsigned*>(p.status);
 
   // ---- start: mbarriers, resident W_kvb rows (TMA), L2 prefetch of the rest
   const uint32_t bar_res = smem_u32(smem + p.off_misc + 1536);
@@ -220,10 +217,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     if (lane == 0) *reinterpret_cast<volatile int*>(sWkvbOn) = 1;
   };
-  if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
+  // The next kernel in the stream may launch now (it waits for this one
+  // before it reads anything this one writes).
+  grid_dep_launch_dependents();
+  // Everything that may come from the previous kernel in the stream -- hidden
+  // rows, positions, gamma, the raw weights, the workspace -- is read after
+  // prologue_inputs (every thread calls it once); the packed weight snapshot
+  // is read-only and may be copied before.
+  int pos = 0;
+  unsigned st0 = 0;
+  auto prologue_inputs = [&]() {
+    grid_dep_wait();
+    if (owner && tid == 0) pos = p.positions[p.t0 + cta];
+    st0 = *reinterpret_cast<volatile unsigned*>(p.status);
+    if (tid < kRank / 8) cp_async16(smem_u32(sGam) + tid * 16, static_cast<const T*>(p.gamma) + tid * 8);
+  };
 
   // ================================================================ phase A
   bool wkvb_on = false;  // resident W_kvb copies issued (raw path: thread 0's view)
+  if constexpr (!PK) prologue_inputs();
   {
     const int units = p.KC * kNblkA;
     const int subs = p.KB / kSubK;
@@ -268,15 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     };
     const unsigned char* Wpk = static_cast<const unsigned char*>(p.W_kva);
-    auto issue_stage = [&](int i, int slot) {  // packed weights: thread 0
+    // a stage's weight part (the packed snapshot: read-only, so it may be
+    // copied before the previous kernel in the stream has finished) and its
+    // hidden-row part (after the dependency wait); one mbarrier phase covers both
+    auto issue_stage_w = [&](int i, int slot) {
       const int u = cta + (i / subs) * G;
-      const int kc = u / kNblkA;
       const int sub = i % subs;
       const uint32_t bar = bar_a0 + 8 * slot;
       const uint32_t dst = smem_u32(sA + slot * stage_bytes);
       mbar_arrive_expect_tx(bar, (uint32_t)(p.xrows * 128 + kSubK * 64));
-      tma_load_2d(dst, &p.tmap_x, kc * p.KB + sub * kSubK, p.t0, bar);
       bulk_g2s(dst + xbytes, Wpk + ((size_t)u * p.KB + sub * kSubK) * 64, kSubK * 64, bar);
+    };
+    auto issue_stage_x = [&](int i, int slot) {
+      const int u = cta + (i / subs) * G;
+      const int kc = u / kNblkA;
+      const int sub = i % subs;
+      tma_load_2d(smem_u32(sA + slot * stage_bytes), &p.tmap_x, kc * p.KB + sub * kSubK, p.t0,
+                  bar_a0 + 8 * slot);
+    };
+    auto issue_stage = [&](int i, int slot) {  // packed weights: one lane
+      issue_stage_w(i, slot);
+      issue_stage_x(i, slot);
     };
 
     const int nb8 = warp & 3, khalf = warp >> 2;
@@ -416,8 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         if (lane < gsz && i < nsub) issue_stage(i, (k & 1) * gsz + lane);
       };
       if (warp == 0) {
-        if (ngroups > 0) issue_group(0);
-        if (ngroups > 1) issue_group(1);
+        for (int k = 0; k < 2 && k < ngroups; ++k) {
+          const int i = k * gsz + lane;
+          if (lane < gsz && i < nsub) issue_stage_w(i, (k & 1) * gsz + lane);
+        }
+      }
+      prologue_inputs();
+      if (warp == 0) {
+        for (int k = 0; k < 2 && k < ngroups; ++k) {
+          const int i = k * gsz + lane;
+          if (lane < gsz && i < nsub) issue_stage_x(i, (k & 1) * gsz + lane);
+        }
       }
       // warp 1: the W_kvb slice goes out once the first kv_a stage is in
       if (warp == 1 && nsub > 0) {
@@ -1002,7 +1035,7 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
 }
 
 cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p0,
-                          cudaStream_t stream) {
+                          bool pdl, cudaStream_t stream) {
   int mt = 1;
   while (mt * 16 < p0.TT) mt *= 2;
   int variant, wm, ks;
@@ -1041,12 +1074,25 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   void* args[] = {&p};
+  // programmatic serialisation together with a cooperative launch: if the
+  // runtime refuses the pair, launch cooperatively alone from then on
+  static int pdl_ok = 1;
+  if (pdl && pdl_ok) {
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported && e != cudaErrorInvalidConfiguration)
+      return e;
+    cudaGetLastError();
+    pdl_ok = 0;
+  }
+  cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -102,9 +102,13 @@ cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, c
 // Rows of W_kvb per TMA box of the decode kernel.
 constexpr int kWkvbBoxRows = 32;
 // Packed weights (decode_pack_weights): W_kva / W_kvb point at the packed
-// copies, which the kernel reads with 1-D bulk copies.
+// copies, which the kernel reads with 1-D bulk copies.  pdl: launch with
+// programmatic stream serialisation (the kernel may start before the
+// previous kernel in the stream ends; it reads only the packed snapshot
+// before its dependency wait, so the snapshot must not be the previous
+// kernel's output).
 cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p,
-                          cudaStream_t stream);
+                          bool pdl, cudaStream_t stream);
 
 }  // namespace mla
 

@@ -139,7 +139,7 @@ extern "C" mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, in
   for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
     p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
-    e = decode_launch(bf16, false, plan, p, stream);
+    e = decode_launch(bf16, false, plan, p, true, stream);
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   }
   if (device_status) {
