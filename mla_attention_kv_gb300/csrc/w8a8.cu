@@ -51,10 +51,7 @@ __global__ void __launch_bounds__(kGThreads) gemm_s8_kernel(const int8_t* __rest
   const int n0 = blockIdx.x * kGBN, m0 = blockIdx.y * kGBM;
   const int kb = blockIdx.z * kchunk;
   const int ke = min(K, kb + kchunk);
-  // chained launches: let the next kernel start, wait for this one's inputs
-  grid_dep_launch_dependents();
   if (kb >= ke) return;
-  grid_dep_wait();
   const int nsteps = (ke - kb) / kGBK;
   const int wm = warp >> 1, wn = warp & 1;  // warp tile rows wm*32, cols wn*32
 
@@ -193,8 +190,6 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
                                                          int8_t* __restrict__ q,
                                                          float* __restrict__ scale) {
   __shared__ float scratch[8];
-  grid_dep_launch_dependents();
-  grid_dep_wait();
   const int row = blockIdx.x;
   const __nv_bfloat16* xr = x + (size_t)row * cols;
   float amax = 0.f;
@@ -374,8 +369,6 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   float* rope = gk + kRank;
   norm_load_inputs(p, colsc, gq, gk);
   rope_load(p, t, rope);
-  grid_dep_launch_dependents();
-  grid_dep_wait();
   int32_t* a = acc1 + (size_t)t * na;
   norm_row(a, sx[t], p, yrow, colsc, gq, gk, rope, scratch, w.q1 + (size_t)t * rq, w.s1 + t,
            w.c1 + (size_t)t * kRank, w.s2 + t,
@@ -392,8 +385,6 @@ __global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __rest
                                                            const float* __restrict__ srow,
                                                            const float* __restrict__ scol,
                                                            W8Params p, int mode) {
-  grid_dep_launch_dependents();
-  grid_dep_wait();
   const int t = blockIdx.x, hh = blockIdx.y, H = p.heads;
   const int bi = t / p.s, si = t - bi * p.s;
   const int width = mode == 0 ? kNope + kRope : kHeadCols;
@@ -1135,10 +1126,9 @@ cudaError_t launch_small_chain(const W8Params& p, const W8Workspace& w, const W8
   return e;
 }
 
-// c_zero: C is known to hold zeros (no clearing before split-K adds);
-// pdl: launch with programmatic stream serialisation.
+// c_zero: C is known to hold zeros (no clearing before split-K adds).
 cudaError_t gemm(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t* C, int ldc,
-                 cudaStream_t st, int* launches, bool c_zero = false, bool pdl = false) {
+                 cudaStream_t st, int* launches, bool c_zero = false) {
   // decode sizes stream the weights; the 64 x 64 tensor-core tiles would be
   // mostly padding rows
   if (M <= kGemvMaxRows && K % 16 == 0 && N % 16 == 0) return gemv_tma(A, W, M, K, N, C, ldc, st, launches);
@@ -1159,10 +1149,9 @@ cudaError_t gemm(const int8_t* A, const int8_t* W, int M, int K, int N, int32_t*
     cudaError_t e = cudaMemset2DAsync(C, (size_t)ldc * 4, 0, (size_t)N * 4, M, st);
     if (e != cudaSuccess) return e;
     ++*launches;
-    pdl = false;  // (a memset node between the kernels)
   }
   ++*launches;
-  return launch_k(gemm_s8_kernel, dim3(tn, tm, splits), dim3(kGThreads), 0, st, pdl, A, W, M, K, N, C,
+  return launch_k(gemm_s8_kernel, dim3(tn, tm, splits), dim3(kGThreads), 0, st, false, A, W, M, K, N, C,
                   ldc, kchunk, splits > 1 ? 1 : 0);
 }
 
@@ -1326,32 +1315,32 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
   quant_rows_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(p.hidden), h, w.xq, w.sx);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // Every launch after the first is chained with programmatic stream
-  // serialisation (each kernel waits for its predecessor before reading).
   // The accumulator rows are left zeroed by every call (norm_quant_kernel,
   // or the decode-size chain), so the q_a / kv_a split-K adds need no clear.
+  // (Programmatic dependent launch measured slower here: the early
+  // dependents share the SMs with the compute-bound GEMM CTAs.)
   auto chain = [&]() -> cudaError_t {
     // 2. q_a_proj and kv_a_proj into one [T, q_rank + 576] accumulator
-    cudaError_t e2 = gemm(w.xq, p.W_qa, T, h, rq, w.acc1, na, st, launches, true, true);
-    if (e2 == cudaSuccess) e2 = gemm(w.xq, p.W_kva, T, h, kNa, w.acc1 + rq, na, st, launches, true, true);
+    cudaError_t e2 = gemm(w.xq, p.W_qa, T, h, rq, w.acc1, na, st, launches, true);
+    if (e2 == cudaSuccess) e2 = gemm(w.xq, p.W_kva, T, h, kNa, w.acc1 + rq, na, st, launches, true);
     if (e2 != cudaSuccess) return e2;
     // 3-4. RMSNorms, requantisation, RoPE(k_pe)
     const size_t smem = norm_smem(rq);
     e2 = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e2 == cudaSuccess) e2 = launch_k(norm_quant_kernel, dim3(T), dim3(256), smem, st, true, w.acc1, (const float*)w.sx, p, w);
+    if (e2 == cudaSuccess) e2 = launch_k(norm_quant_kernel, dim3(T), dim3(256), smem, st, false, w.acc1, (const float*)w.sx, p, w);
     ++*launches;
     if (e2 != cudaSuccess) return e2;
     // 5. q_b_proj -> q_nope, RoPE(q_pe)
-    e2 = gemm(w.q1, p.W_qb, T, rq, H * (kNope + kRope), w.acc2, H * (kNope + kRope), st, launches, false, true);
+    e2 = gemm(w.q1, p.W_qb, T, rq, H * (kNope + kRope), w.acc2, H * (kNope + kRope), st, launches);
     if (e2 == cudaSuccess)
-      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, true, (const int32_t*)w.acc2,
+      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, false, (const int32_t*)w.acc2,
                     (const float*)w.s1, p.sW_qb, p, 0);
     ++*launches;
     if (e2 != cudaSuccess) return e2;
     // 6. kv_b_proj -> k_nope, value
-    e2 = gemm(w.c1, p.W_kvb, T, kRank, H * kHeadCols, w.acc2, H * kHeadCols, st, launches, false, true);
+    e2 = gemm(w.c1, p.W_kvb, T, kRank, H * kHeadCols, w.acc2, H * kHeadCols, st, launches);
     if (e2 == cudaSuccess)
-      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, true, (const int32_t*)w.acc2,
+      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, false, (const int32_t*)w.acc2,
                     (const float*)w.s2, p.sW_kvb, p, 1);
     ++*launches;
     return e2;
