@@ -489,10 +489,11 @@ def run_gpu(args, wl, rank, world, dev):
                 ms_eager=ms_e, calls_eager=calls_e, clk_eager=clk_e)
 
 
-def kernel_traffic(kernel: str, T: int):
-    """DRAM bytes of one call of `kernel` at T rows from the committed ncu
-    summary, or None when the summary is missing or was taken on a different
-    version of the kernel's source (its sha256 no longer matches)."""
+def kernel_traffic(kernel: str, T: int, model: str = ""):
+    """DRAM bytes of one call of `kernel` at T rows (entry "<model>:<T>", else
+    "<T>") from the committed ncu summary, or None when the summary is missing
+    or was taken on a different version of the kernel's source (its sha256 no
+    longer matches)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -502,7 +503,8 @@ def kernel_traffic(kernel: str, T: int):
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if h != t[kernel]["sha256_16"]:
             return None
-        return t[kernel]["bytes_per_call"].get(str(T))
+        b = t[kernel]["bytes_per_call"]
+        return b.get("%s:%d" % (model, T), b.get(str(T)))
     except Exception:
         return None
 
@@ -577,9 +579,10 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": tensor_unit,
                 "frac": achieved / peak}
     Ts = sorted(set(Tlist))
-    tr = [kernel_traffic(kernel, T) for T in Ts]
+    model = wl.cfg["name"]
+    tr = [kernel_traffic(kernel, T, model) for T in Ts]
     roof["traffic"] = None if any(x is None for x in tr) else \
-        sum(kernel_traffic(kernel, T) for T in Tlist) / len(Tlist)
+        sum(kernel_traffic(kernel, T, model) for T in Tlist) / len(Tlist)
     roof.update({"peak_kind": peak_kind, "kernel": kernel, "calls_timed": len(Tlist),
                  "mean_call_us": 1e6 * call_s / len(Tlist),
                  "algorithmic_bytes_per_call": alg_bytes / len(Tlist),
