@@ -130,6 +130,9 @@ struct PrefillParams {
   int hidden_dim, heads, s, T, max_pos;
   float eps;
   unsigned long long budget_ns;
+  // filled by prefill_launch
+  int main_ctas;   // CTAs that own tiles
+  int kpe_split;   // 1: the CTAs past main_ctas run the k_pe pass of every tile
 };
 
 // Token count from which AUTO selects the tensor-core prefill kernel.

@@ -170,9 +170,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const uint32_t tmem = sh->tmem_base;
   const uint32_t crank = tc::cluster_rank();
   const bool leader = crank == 0;
-  // every CTA of a cluster runs the same number of tiles (tiles past the end
-  // are all-padding: TMA fills zeros and the epilogue stores nothing)
-  const int iters = (ntiles + (int)gridDim.x - 1) / (int)gridDim.x;
+  // Main CTAs [0, main_ctas) take tiles blockIdx.x + it * main_ctas.  With
+  // kpe_split, the CTA pairs past them are k_pe workers: pair w runs only
+  // pass (a) for the tile pairs w, w + nwp, ... (its two CTAs on the two
+  // tiles of a pair), and the main CTAs skip pass (a).  Every CTA of a
+  // cluster runs the same number of tiles (tiles past the end are
+  // all-padding: TMA fills zeros and the epilogue stores nothing).
+  const bool worker = p.kpe_split && (int)blockIdx.x >= p.main_ctas;
+  const bool do_kpe = !p.kpe_split || worker;
+  const bool do_main = !worker;
+  const int nwp = ((int)gridDim.x - p.main_ctas) / kCl, wp = ((int)blockIdx.x - p.main_ctas) / kCl;
+  const int npairs = (ntiles + kCl - 1) / kCl;
+  const int iters = worker ? (wp < npairs ? (npairs - wp + nwp - 1) / nwp : 0)
+                           : (ntiles + p.main_ctas - 1) / p.main_ctas;
+  auto tile_of = [&](int it) {
+    return worker ? kCl * (wp + it * nwp) + (int)crank : (int)blockIdx.x + it * p.main_ctas;
+  };
 
   if (warp == 0) {
     // ============================================================ TMA producer
@@ -184,11 +197,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       int tiles_done = 0;
       bool ok = true;
       for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
-        const int m0 = (blockIdx.x + it * gridDim.x) * kBM;
+        const int m0 = tile_of(it) * kBM;
         // the rings of this tile overlap the previous tile's A2 area
-        if (tiles_done > 0 && !pf_wait(bar(&sh->a2_free), (tiles_done - 1) & 1, abort, budget, p.status)) { ok = false; break; }
+        if (do_main && tiles_done > 0 && !pf_wait(bar(&sh->a2_free), (tiles_done - 1) & 1, abort, budget, p.status)) { ok = false; break; }
         // (a) k_pe pass
-        for (int kc = 0; kc < nk && ok; ++kc, ++u0) {
+        for (int kc = 0; kc < nk && ok && do_kpe; ++kc, ++u0) {
           const int s = u0 % kS0Stages;
           if (!pf_wait(bar(&sh->empty0[s]), ((u0 / kS0Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
           const uint32_t st = sbase + kS0Base + s * kS0Bytes;
@@ -198,6 +211,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           tma_load_2d_pair(st + 16384, &args.tm_wa, kRank, kc * kBK, fb);
         }
         if (!ok) break;
+        if (!do_main) continue;
         // (b) compressed_kv pass: its ring overlaps the k_pe ring, so it
         // starts once every k_pe stage of this tile has been released
         for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0 && ok; ++u)
@@ -262,6 +276,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
         // (a) k_pe into TMEM columns [0, 128): N = 128, each CTA holding the same
         // 64 k_pe columns, so columns 64..127 repeat 0..63 and are not read
+        if (do_kpe) {
         if (!drain_buf(0)) { ok = false; break; }
         tc::fence_after_sync();
         for (int kc = 0; kc < nk; ++kc, ++u0) {
@@ -279,6 +294,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         if (!ok) break;
         tc::commit2_both(bar(&sh->tfull[0]));
         ++wcount[0];
+        }
+        if (!do_main) continue;
         // (b) compressed_kv into TMEM columns [0, 512): two N = 256 tiles per K step
         if (!drain_buf(0) || !drain_buf(1)) { ok = false; break; }
         tc::fence_after_sync();
@@ -346,10 +363,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     int tiles_done = 0;
     bool ok = true;
     for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
-      const int t = (blockIdx.x + it * gridDim.x) * kBM + r;
+      const int t = tile_of(it) * kBM + r;
       const bool live = t < ntok;
       const int bi = live ? t / p.s : 0, si = live ? t - bi * p.s : 0;
       // (a) k_pe: RoPE on the 64 raw columns
+      if (do_kpe) {
       if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
       ++uf[0];
       tc::fence_after_sync();
@@ -392,6 +410,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::arrive_cluster_relaxed(lead(&sh->tempty[0]));
+      }
+      if (!do_main) continue;
       // (b) RMSNorm of compressed_kv -> normalised A tile in shared memory
       if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
       ++uf[0];
@@ -508,12 +528,7 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   const void* fn = bf16 ? (const void*)prefill_kernel<__nv_bfloat16> : (const void*)prefill_kernel<__half>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int ntiles = (p.T + kBM - 1) / kBM;
-  const int max_grid = num_sms / kCl * kCl;
-  int grid = (ntiles + kCl - 1) / kCl * kCl;
-  if (grid > max_grid) grid = max_grid;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPfThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
@@ -524,6 +539,34 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // CTA pairs that fit on the GPU at once (two per cluster, one CTA per SM)
+  static int max_clusters[2] = {0, 0};
+  int& mc = max_clusters[bf16 ? 1 : 0];
+  if (mc == 0) {
+    cfg.gridDim = dim3(num_sms / kCl * kCl);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / kCl;
+    }
+    mc = n;
+  }
+  const int ntiles = (p.T + kBM - 1) / kBM;
+  const int max_grid = mc * kCl;
+  int grid = (ntiles + kCl - 1) / kCl * kCl;
+  if (grid > max_grid) grid = max_grid;
+  // Pairs left over when every tile has its own CTA take the k_pe pass of
+  // all tiles (it re-reads the hidden tile, so the main CTAs save one full
+  // read of their rows): used when they are at least one per eight tiles.
+  const int spare = max_grid - grid;
+  a.p.main_ctas = grid;
+  a.p.kpe_split = 0;
+  if (grid >= ntiles && spare >= kCl && spare * 8 >= ntiles) {
+    const int workers = (spare < grid ? spare : grid) / kCl * kCl;
+    a.p.kpe_split = 1;
+    grid += workers;
+  }
+  cfg.gridDim = dim3(grid);
   void* kargs[] = {&a};
   e = cudaLaunchKernelExC(&cfg, fn, kargs);
   if (e == cudaSuccess) *launches = 1;
