@@ -86,6 +86,9 @@ def lib():
             L.oracle_kv_prolog.argtypes = [ctypes.POINTER(_Dims), ctypes.c_int64, ctypes.c_int64,
                                            P, P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int,
                                            P, P, P]
+            L.oracle_kv_latent.restype = ctypes.c_int
+            L.oracle_kv_latent.argtypes = [ctypes.POINTER(_Dims), ctypes.c_int64, ctypes.c_int64,
+                                           P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int, P, P]
             L.oracle_quant_row_f32.restype = None
             L.oracle_quant_row_f32.argtypes = [P, ctypes.c_int64, P, P]
             L.oracle_int_gemm.restype = None
@@ -240,6 +243,34 @@ def kv_prolog(inp: dict, rows=None, nthreads: int = 0):
     if bad:
         raise ValueError(f"{bad} token rows have positions outside [0, max_pos)")
     return k_nope, value, k_pe
+
+
+def kv_latent(inp: dict, rows=None, nthreads: int = 0):
+    """fp64 latent-cache variant (steps 1, 2, 3, 6 of the prolog) on the dict
+    made by the input generator: (latent [b*s, 512], k_pe [b,1,s,64]) as
+    float64; rows not listed in ``rows`` are NaN."""
+    cfg = inp["cfg"]
+    b, s = inp["b"], inp["s"]
+    T = b * s
+    r, dr = cfg["kv_lora_rank"], cfg["rope_dim"]
+    d = _Dims(cfg["hidden"], r, dr, cfg["num_heads"], cfg["nope_dim"], cfg["v_dim"],
+              inp["cos"].shape[0], cfg["eps"], 0 if cfg["dtype"] == "fp16" else 1)
+    hid = _bits16(inp["hidden"])
+    pos = _np(inp["positions"], np.int32)
+    wa = _bits16(inp["W_kva"])
+    g = _bits16(inp["gamma_kv"])
+    cos = _np(inp["cos"], np.float32)
+    sin = _np(inp["sin"], np.float32)
+    rows = np.arange(T, dtype=np.int64) if rows is None else _np(rows, np.int64)
+    latent = np.full((T, r), np.nan)
+    k_pe = np.full((b, 1, s, dr), np.nan)
+    nt = nthreads if nthreads > 0 else (os.cpu_count() or 1)
+    bad = lib().oracle_kv_latent(ctypes.byref(d), b, s, _ptr(hid), _ptr(pos), _ptr(wa), _ptr(g),
+                                 _ptr(cos), _ptr(sin), _ptr(rows), rows.size, nt, _ptr(latent),
+                                 _ptr(k_pe))
+    if bad:
+        raise ValueError(f"{bad} token rows have positions outside [0, max_pos)")
+    return latent, k_pe
 
 
 def _w8_dims(inp):

@@ -267,6 +267,46 @@ int oracle_kv_prolog(const oracle_dims* d, int64_t b, int64_t s, const uint16_t*
   return bad;
 }
 
+/* Latent-cache variant: steps 1, 2, 3 and 6 only -- the normalised
+ * compressed_kv row that a weight-absorbed attention caches instead of
+ * k_nope / value, and the roped k_pe.  latent [T, rank] (row t = bi*s + si),
+ * k_pe [b, 1, s, rope].  Same row selection, threads and return value as
+ * oracle_kv_prolog.                                                        */
+int oracle_kv_latent(const oracle_dims* d, int64_t b, int64_t s, const uint16_t* hidden,
+                     const int32_t* positions, const uint16_t* W_kva, const uint16_t* gamma,
+                     const float* cosb, const float* sinb, const int64_t* rows, int64_t n_rows,
+                     int nthreads, double* latent, double* k_pe) {
+  const int64_t h = d->hidden, r = d->rank, dr = d->rope, na = r + dr;
+  int bad = 0;
+  (void)b;
+  (void)nthreads;
+  double* Wa = (double*)malloc(sizeof(double) * h * na);
+  double* g = (double*)malloc(sizeof(double) * r);
+  oracle_promote16(W_kva, h * na, d->dtype, Wa);
+  oracle_promote16(gamma, r, d->dtype, g);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1) reduction(+ : bad)
+#endif
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t t = rows[i];
+    int32_t p = positions[t];
+    if (p < 0 || p >= d->max_pos) {
+      bad += 1;
+      continue;
+    }
+    double* x = (double*)malloc(sizeof(double) * h);
+    double* C = (double*)malloc(sizeof(double) * na);
+    oracle_promote16(hidden + t * h, h, d->dtype, x);
+    oracle_vec_matmul(x, Wa, h, na, C);                 /* step 1 */
+    oracle_rmsnorm(C, r, g, d->eps, latent + t * r);    /* steps 2, 3 */
+    oracle_rope(C + r, (int)dr, cosb + (int64_t)p * dr, sinb + (int64_t)p * dr,
+                k_pe + t * dr);                         /* step 6 */
+    free(x); free(C);
+  }
+  free(Wa); free(g);
+  return bad;
+}
+
 /* ------------------------------------------------------------------ */
 /* W8A8 full MLA prolog (Q side + KV side), int8 weights                */
 /* ------------------------------------------------------------------ */

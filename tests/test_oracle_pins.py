@@ -309,6 +309,44 @@ def test_kv_prolog_bad_position(oracle_mod):
         oracle_mod.kv_prolog(inp, nthreads=1)
 
 
+# ------------------------------------------------------------ latent-cache variant
+@pytest.mark.parametrize("b,s", [(2, 3), (6, 1)])
+def test_kv_latent_routing_closed_form(oracle_mod, b, s):
+    """Identity routing: the latent row is RMSNorm of c_t * sign in closed
+    form, and k_pe is the same roped row as the full prolog's."""
+    T = b * s
+    positions = [0, 5, 0, 99, 4095, 1][:T]
+    inp, hid, sign, cvals, gam, src, wj = _routing_case(b, s, 2, positions)
+    latent, k_pe = oracle_mod.kv_latent(inp, nthreads=1)
+    assert latent.shape == (T, 512) and k_pe.shape == (b, 1, s, 64)
+    full_kpe = oracle_mod.kv_prolog(inp, nthreads=1)[2]
+    assert np.array_equal(k_pe, full_kpe)
+    for t in range(T):
+        c = cvals[t]
+        np.testing.assert_allclose(latent[t], c * sign / math.sqrt(c * c + 1e-6) * gam, rtol=1e-14)
+
+
+def test_kv_latent_feeds_kv_b(oracle_mod):
+    """latent x W_kvb (a library matmul in fp64), reshaped per head, is the
+    full prolog's k_nope / value; rows not asked for stay NaN."""
+    cfg = I.small_config(I.V2_LITE, hidden=192, num_heads=3)
+    b, s = 2, 3
+    inp = I.kv_inputs(cfg, b, s, seed=21, positions="decode")
+    latent, k_pe = oracle_mod.kv_latent(inp, nthreads=2)
+    k_nope, value, kpe_full = oracle_mod.kv_prolog(inp, nthreads=2)
+    Wb = inp["W_kvb"].double().numpy()
+    kv = latent @ Wb
+    for t in range(b * s):
+        bi, si = divmod(t, s)
+        for hh in range(3):
+            np.testing.assert_allclose(kv[t, hh * 256:hh * 256 + 128], k_nope[bi, hh, si], rtol=1e-9, atol=1e-12)
+            np.testing.assert_allclose(kv[t, hh * 256 + 128:hh * 256 + 256], value[bi, hh, si], rtol=1e-9, atol=1e-12)
+    assert np.array_equal(k_pe, kpe_full)
+    part, kp2 = oracle_mod.kv_latent(inp, rows=[1, 4], nthreads=1)
+    assert np.array_equal(part[[1, 4]], latent[[1, 4]])
+    assert np.all(np.isnan(part[[0, 2, 3, 5]])) and np.all(np.isnan(kp2[0, 0, 0]))
+
+
 # ------------------------------------------------------------ W8A8
 def test_quant_hand_values(oracle_mod):
     for c in _gold("quant_hand.json")["cases"]:
