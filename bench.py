@@ -205,15 +205,17 @@ class DecodeSweep:
 
 
 class SingleCall:
-    """One prolog call per step on one configuration (prefill, R1, W8A8)."""
+    """One prolog call per step on one configuration (prefill, R1, W8A8, or
+    the latent-cache variant: kv_a_proj + RMSNorm + RoPE(k_pe), no kv_b_proj)."""
 
-    def __init__(self, name, cfg, b, s, positions, path, seed):
+    def __init__(self, name, cfg, b, s, positions, path, seed, latent=False):
         self.name, self.cfg, self.b, self.s = name, cfg, b, s
         self.positions, self.path, self.seed = positions, path, seed
         self.T = b * s
         self.points = [(b, s)]
         self.tokens_per_step = self.T
         self.w8 = cfg.get("quant") == "w8a8"
+        self.latent = latent
 
     def describe(self):
         c = self.cfg
@@ -222,6 +224,8 @@ class SingleCall:
         if self.w8:
             d["q_lora_rank"] = c["q_lora_rank"]
             d["quant"] = "w8a8 (int8 weights, per-token int8 activations, int32 accumulators)"
+        if self.latent:
+            d["variant"] = "latent cache: normalised compressed_kv [T, 512] + k_pe, no kv_b_proj"
         return d
 
     def weight_bytes(self):
@@ -230,6 +234,8 @@ class SingleCall:
         if self.w8:
             rq = c["q_lora_rank"]
             return (h * (rq + 576) + rq * H * 192 + r * H * 256) + 4 * (rq + 576 + H * 192 + H * 256) + 2 * (rq + r)
+        if self.latent:
+            return 2 * (h * 576 + r)
         return 2 * (h * 576 + r + r * H * 256)
 
     def flops(self, T):
@@ -238,12 +244,14 @@ class SingleCall:
         if self.w8:
             rq = c["q_lora_rank"]
             return 2.0 * T * (h * (rq + 576) + rq * H * 192 + 512 * H * 256)
+        if self.latent:
+            return 2.0 * T * h * 576
         return 2.0 * T * (h * 576 + 512 * H * 256)
 
     def alg_bytes(self, T):
         c = self.cfg
         H = c["num_heads"]
-        out = 2 * (H * 256 + 64) + (2 * H * 192 if self.w8 else 0)
+        out = 2 * (512 + 64) if self.latent else 2 * (H * 256 + 64) + (2 * H * 192 if self.w8 else 0)
         return self.weight_bytes() + T * (2 * c["hidden"] + 4 + 2 * 64 * 4 + out)
 
     def setup(self, dev):
@@ -259,7 +267,8 @@ class SingleCall:
             self.m.set_path(self.path)
             self.m.prepare_weights(self.d)  # packed snapshot for the decode path
             torch.cuda.synchronize(dev)
-        self.out = self.m.alloc_outputs(self.b, self.s, dev)
+        self.out = (self.m.alloc_latent_outputs(self.b, self.s, dev) if self.latent
+                    else self.m.alloc_outputs(self.b, self.s, dev))
         self.hidden_h = inp["hidden"].pin_memory()
         self.positions_h = inp["positions"].pin_memory()
         self.out_h = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.out.items()}
@@ -274,6 +283,12 @@ class SingleCall:
             self.flush_rd = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
             self.flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
+    def call(self, stream):
+        if self.latent:
+            self.m.run_latent(self.b, self.s, self.d, self.out, stream)
+        else:
+            self.m.run(self.b, self.s, self.d, self.out, stream)
+
     def flush_l2(self):
         self.flush.zero_()
         torch.sum(self.flush_rd, dim=0, out=self.flush_sink)
@@ -283,7 +298,7 @@ class SingleCall:
             self.flush_l2()
             events.append(torch.cuda.Event(enable_timing=True))
             events[-1].record(stream)
-        self.m.run(self.b, self.s, self.d, self.out, stream)
+        self.call(stream)
         if events is not None:
             events.append(torch.cuda.Event(enable_timing=True))
             events[-1].record(stream)
@@ -298,7 +313,7 @@ class SingleCall:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(st):
             with torch.cuda.graph(g, stream=st):
-                self.m.run(self.b, self.s, self.d, self.out, st)
+                self.call(st)
         self.graph_launches = self.m.last_launches
         torch.cuda.synchronize(dev)
         return [g]
@@ -317,7 +332,7 @@ class SingleCall:
     def e2e_step(self, stream):
         self.d["hidden"].copy_(self.hidden_h, non_blocking=True)
         self.d["positions"].copy_(self.positions_h, non_blocking=True)
-        self.m.run(self.b, self.s, self.d, self.out, stream)
+        self.call(stream)
         d2h = 0
         for k, v in self.out.items():
             self.out_h[k].copy_(v, non_blocking=True)
@@ -330,7 +345,7 @@ class SingleCall:
         nt = os.cpu_count() or 1
         rows_per = max(nt, 8)
         done, t0, k = 0, time.perf_counter(), 0
-        fn = oracle.w8a8_prolog if self.w8 else oracle.kv_prolog
+        fn = oracle.w8a8_prolog if self.w8 else (oracle.kv_latent if self.latent else oracle.kv_prolog)
         while True:
             rows = [(k * rows_per + i) % self.T for i in range(rows_per)]
             fn(self.host, rows=sorted(set(rows)), nthreads=nt)
@@ -343,8 +358,9 @@ class SingleCall:
             f"{done} token rows of {self.name} (fp64 oracle, per-call weight promotion included), {el:.1f} s"
 
 
-def _single(name, cfg, b, s, positions, path_name, seed):
-    return lambda: SingleCall(name, cfg, b, s, positions, {"decode": 1, "prefill": 2, "auto": 0}[path_name], seed)
+def _single(name, cfg, b, s, positions, path_name, seed, latent=False):
+    return lambda: SingleCall(name, cfg, b, s, positions, {"decode": 1, "prefill": 2, "auto": 0}[path_name],
+                              seed, latent)
 
 
 WORKLOADS = {
@@ -356,6 +372,10 @@ WORKLOADS = {
     "w8a8_t1": _single("r1_w8a8_prolog_T1", I.R1_W8A8, 1, 1, "decode", "auto", 1004),
     "w8a8_t64": _single("r1_w8a8_prolog_T64", I.R1_W8A8, 64, 1, "decode", "auto", 1004),
     "w8a8_t8192": _single("r1_w8a8_prolog_T8192", I.R1_W8A8, 1, 8192, "prefill", "auto", 1004),
+    "v2lite_latent_decode": _single("v2lite_kv_latent_decode_b64s1", I.V2_LITE, 64, 1, "decode", "auto",
+                                    1005, latent=True),
+    "r1_latent_prefill": _single("r1_kv_latent_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1005,
+                                 latent=True),
 }
 
 
@@ -569,6 +589,8 @@ def main():
     t_mem, t_cmp = alg_bytes / bw, alg_flops / tensor_peak
     path = "prefill" if (not is_w8 and getattr(wl, "T", 0) >= 1024) else "decode"
     kernel = {"prefill": "prefill_kernel", "decode": "decode_kernel"}[path] if not is_w8 else "w8a8 pipeline"
+    if getattr(wl, "latent", False):
+        kernel += " (latent variant)"
     if t_mem >= t_cmp:
         achieved = alg_bytes / call_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -137,6 +137,23 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream);
 
+/* Latent-cache variant: enqueue steps 1, 2, 3 and 6 of the prolog only --
+ * kv_a_proj, split, RMSNorm of compressed_kv and RoPE of k_pe -- for an
+ * attention that absorbs kv_b_proj into its query / output projections and
+ * caches the normalised latent instead of k_nope / value.  The pages'
+ * prolog ([MIG] §背景) ends with kv_b_proj; this entry stops before it.
+ *   hidden_states, positions, W_kva, gamma_kv, cos_table, sin_table as for
+ *   mla_kv_prolog_run
+ *   latent        [b*s, 512]           dtype      output: RMSNorm(compressed_kv) * gamma
+ *   k_pe          [b, 1, s, 64]        dtype      output (identical to mla_kv_prolog_run's)
+ * Same path selection, packed W_kva snapshot (matched on W_kva alone),
+ * errors and device status as mla_kv_prolog_run. */
+mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                    const int32_t* positions, const void* W_kva,
+                                    const void* gamma_kv, const float* cos_table,
+                                    const float* sin_table, void* latent, void* k_pe,
+                                    cudaStream_t stream);
+
 /* Take a snapshot of W_kva [hidden, 576] and W_kvb [512, H*256] (layouts
  * as for mla_kv_prolog_run) in the decode kernel's own layout: every CTA's
  * kv_a tile and kv_b column slice become one contiguous block, with the

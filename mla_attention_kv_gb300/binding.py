@@ -28,7 +28,7 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
             "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
-            "mla_kv_prolog_prepare_weights"]
+            "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent"]
 
 
 class MLAError(RuntimeError):
@@ -66,6 +66,7 @@ def load(path: str | None = None):
     P, I, H = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
     L.mla_kv_prolog_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_void_p)]
     L.mla_kv_prolog_run.argtypes = [H, I, I] + [P] * 10 + [P]
+    L.mla_kv_prolog_run_latent.argtypes = [H, I, I] + [P] * 8 + [P]
     L.mla_prolog_w8a8_run.argtypes = [H, I, I] + [P] * 19 + [P]
     L.mla_kv_prolog_status.argtypes = [H, P]
     L.mla_kv_prolog_destroy.argtypes = [H]
@@ -154,6 +155,16 @@ def mla_kv_prolog_run(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, W_kvb, c
             _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
             _dev(k_nope, dt, "k_nope"), _dev(value, dt, "value"), _dev(k_pe, dt, "k_pe")]
     _check(load().mla_kv_prolog_run(h, b, s, *args, _stream(stream)), "mla_kv_prolog_run")
+
+
+def mla_kv_prolog_run_latent(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, cos, sin, latent,
+                             k_pe, stream=None):
+    dt = _tdt(cfg)
+    args = [_dev(hidden, dt, "hidden_states"), _dev(positions, torch.int32, "positions"),
+            _dev(W_kva, dt, "W_kva"), _dev(gamma_kv, dt, "gamma_kv"),
+            _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
+            _dev(latent, dt, "latent"), _dev(k_pe, dt, "k_pe")]
+    _check(load().mla_kv_prolog_run_latent(h, b, s, *args, _stream(stream)), "mla_kv_prolog_run_latent")
 
 
 def mla_kv_prolog_prepare_weights(h, cfg, W_kva, W_kvb, stream=None):
@@ -269,6 +280,18 @@ class MLAProlog:
         if c.get("quant") == "w8a8":
             out["q_nope"] = torch.empty(b, H, s, c["nope_dim"], dtype=dt, device=device)
             out["q_pe"] = torch.empty(b, H, s, c["rope_dim"], dtype=dt, device=device)
+        return out
+
+    def alloc_latent_outputs(self, b: int, s: int, device="cuda"):
+        c = self.cfg
+        dt = _tdt(c)
+        return dict(latent=torch.empty(b * s, c["kv_lora_rank"], dtype=dt, device=device),
+                    k_pe=torch.empty(b, 1, s, c["rope_dim"], dtype=dt, device=device))
+
+    def run_latent(self, b, s, d: dict, out: dict, stream=None):
+        """Latent-cache variant: out["latent"] [b*s, 512] and out["k_pe"]."""
+        mla_kv_prolog_run_latent(self.h, self.cfg, b, s, d["hidden"], d["positions"], d["W_kva"],
+                                 d["gamma_kv"], d["cos"], d["sin"], out["latent"], out["k_pe"], stream)
         return out
 
     def run(self, b, s, d: dict, out: dict, stream=None):

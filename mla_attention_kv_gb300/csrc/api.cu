@@ -213,18 +213,20 @@ mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
   return MLA_OK;
 }
 
-mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_states,
-                             const int32_t* positions, const void* W_kva, const void* gamma_kv,
-                             const void* W_kvb, const float* cos_table, const float* sin_table,
-                             void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
+// The KV prolog (latent == null) or its latent-cache variant (latent [T, 512]
+// written instead of k_nope / value; W_kvb, k_nope and value unused).
+static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states,
+                         const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                         const void* W_kvb, const float* cos_table, const float* sin_table,
+                         void* k_nope, void* value, void* k_pe, void* latent, cudaStream_t stream) {
   if (!h || b < 0 || s < 0) return MLA_ERR_INVALID_ARG;
   if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
   const long long T = (long long)b * s;
   h->last_launches = 0;
   if (T == 0) return MLA_OK;
   if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
-  const void* ptrs[] = {hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
-                        k_nope, value, k_pe};
+  const void* ptrs[] = {hidden_states, positions, W_kva, gamma_kv, cos_table, sin_table, k_pe,
+                        latent ? latent : W_kvb, latent ? latent : k_nope, latent ? latent : value};
   for (const void* q : ptrs)
     if (!q) return MLA_ERR_INVALID_ARG;
   for (const void* q : ptrs)
@@ -239,7 +241,7 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
     PrefillParams pp = {};
     pp.hidden = hidden_states; pp.positions = positions; pp.W_kva = W_kva; pp.gamma = gamma_kv;
     pp.W_kvb = W_kvb; pp.cos_t = cos_table; pp.sin_t = sin_table; pp.k_nope = k_nope;
-    pp.value = value; pp.k_pe = k_pe; pp.status = h->status;
+    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.status = h->status;
     pp.hidden_dim = h->cfg.hidden; pp.heads = h->cfg.num_heads; pp.s = s; pp.T = (int)T;
     pp.max_pos = h->cfg.max_pos; pp.eps = h->cfg.eps; pp.budget_ns = h->budget_ns;
     int launches = 0;
@@ -251,12 +253,13 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
   }
 
   // the packed snapshot serves runs that pass the weights it was taken from
-  const bool packed = h->pk && W_kva == h->pk_src_kva && W_kvb == h->pk_src_kvb;
+  // (the latent-cache variant needs only its W_kva part)
+  const bool packed = h->pk && W_kva == h->pk_src_kva && (latent || W_kvb == h->pk_src_kvb);
   DecodeParams p = {};
   if (packed) {
     W_kva = h->pk;
     W_kvb = static_cast<const unsigned char*>(h->pk) + h->pk_kva_bytes;
-  } else {
+  } else if (!latent) {
     const CUtensorMap* tm = wkvb_map(h, W_kvb);
     if (!tm) {
       snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed for W_kvb");
@@ -266,7 +269,7 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
   }
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
-  p.k_pe = k_pe; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
+  p.k_pe = k_pe; p.latent = latent; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
@@ -281,6 +284,24 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
     h->last_launches += 1;
   }
   return MLA_OK;
+}
+
+mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_states,
+                             const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                             const void* W_kvb, const float* cos_table, const float* sin_table,
+                             void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
+  return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
+                k_nope, value, k_pe, nullptr, stream);
+}
+
+mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                    const int32_t* positions, const void* W_kva,
+                                    const void* gamma_kv, const float* cos_table,
+                                    const float* sin_table, void* latent, void* k_pe,
+                                    cudaStream_t stream) {
+  if (!latent) return MLA_ERR_INVALID_ARG;
+  return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, nullptr, cos_table, sin_table,
+                nullptr, nullptr, k_pe, latent, stream);
 }
 
 mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int NB = H * kHeadCols;      // kv_b columns
   const int NG = NB / 8;             // 8-column groups
   const int g0 = col_group_begin(cta, NG, G), g1 = col_group_begin(cta + 1, NG, G);
-  const int ng = g1 - g0;
+  const int ng = p.latent ? 0 : g1 - g0;  // latent-cache variant: no kv_b columns
   const int col0 = g0 * 8;
   const int pitchB = p.ngbox * 16;   // odd multiple of 16: conflict-free ldmatrix
   const T* __restrict__ hid = static_cast<const T*>(p.hidden) + (size_t)p.t0 * p.hidden_dim;
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if constexpr (PK) {
       tma_prefetch_desc(&p.tmap_x);
       for (int i = 0; i < kMaxStagesA; ++i) mbar_init(bar_a0 + 8 * i, 1);
-    } else {
+    } else if (!p.latent) {
       tma_prefetch_desc(&p.tmap_wkvb);
     }
     mbar_init(bar_res, 1);
@@ -672,9 +672,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         const int c = tid * 4;
         uint2 pk = make_uint2(E::pack(v.x * inv * E::to_f(sGam[c]), v.y * inv * E::to_f(sGam[c + 1])),
                               E::pack(v.z * inv * E::to_f(sGam[c + 2]), v.w * inv * E::to_f(sGam[c + 3])));
-        *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * (kNrmPitch / 2) + c) = pk;
-        // the row is read back by bulk copies (async proxy)
-        asm volatile("fence.proxy.async.global;" ::: "memory");
+        if (p.latent) {  // latent-cache variant: the row is an output
+          *reinterpret_cast<uint2*>(static_cast<T*>(p.latent) + (size_t)(p.t0 + t) * kRank + c) = pk;
+        } else {
+          *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * (kNrmPitch / 2) + c) = pk;
+          // the row is read back by bulk copies (async proxy)
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
       } else if (tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
         T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
@@ -684,13 +688,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
       }
     }
-    if (!bar_arrive_wait(p.counters + 1, G, p.budget_ns, p.status)) {
+    if (!p.latent && !bar_arrive_wait(p.counters + 1, G, p.budget_ns, p.status)) {
       drain();
       return;
     }
     // latent rows -> shared memory: the workspace rows have the shared-memory
     // pitch, so one bulk copy moves all TT of them; rows past TT are zeroed
-    if (tid == 0) {
+    if (tid == 0 && !p.latent) {
       asm volatile("fence.proxy.async.global;" ::: "memory");
       mbar_arrive_expect_tx(bar_lat, (uint32_t)(TT * kNrmPitch));
       bulk_g2s(smem_u32(sN), p.nrm, (uint32_t)(TT * kNrmPitch), bar_lat);
@@ -703,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   // ================================================================ phase B
   if (ng == 0) {
+    drain();  // (the latent rows' bulk copy may still be landing)
     bar_exit_finish(p.counters, exit_old, G);
     return;
   }
@@ -1068,7 +1073,8 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
       return cudaErrorInvalidValue;
   }
   // one barrier when every CTA can afford to reduce all rows itself
-  p.single_barrier = (p.TT * plan.KC <= kSingleBarrierRowsTimesChunks) ? 1 : 0;
+  // (the latent-cache variant has no phase B: the owners write the rows out)
+  p.single_barrier = (!p.latent && p.TT * plan.KC <= kSingleBarrierRowsTimesChunks) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(kThreads);

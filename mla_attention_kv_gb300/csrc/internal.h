@@ -44,6 +44,7 @@ struct DecodeParams {
   void* k_nope;             // [b, H, s, 128]
   void* value;              // [b, H, s, 128]
   void* k_pe;               // [b, 1, s, 64]
+  void* latent;             // latent-cache variant: normalised compressed_kv [T, 512]; null: full prolog
   float* partials;          // workspace [KC][kDecodeMaxTokens][576] fp32
   void* nrm;                // workspace [kDecodeMaxTokens][512] dtype
   unsigned* counters;       // workspace: grid barrier {arrivals, generation}
@@ -126,6 +127,7 @@ struct PrefillParams {
   void* k_nope;
   void* value;
   void* k_pe;
+  void* latent;    // latent-cache variant: normalised compressed_kv [T, 512] (no kv_b); null: full prolog
   unsigned* status;
   int hidden_dim, heads, s, T, max_pos;
   float eps;

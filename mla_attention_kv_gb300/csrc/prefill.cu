@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     tma_prefetch_desc(&args.tm_x);
     tma_prefetch_desc(&args.tm_wa);
     tma_prefetch_desc(&args.tm_wa3);
-    tma_prefetch_desc(&args.tm_wb3);
+    if (!p.latent) tma_prefetch_desc(&args.tm_wb3);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           tma_load_3d_pair(st + 32768, &args.tm_wa3, 0, kc * kBK, 4 + (int)crank * 2, fb);
         }
         // (c) kv_b: per head, 8 K-chunks; this CTA's 128 of the head's 256 columns
-        for (int j = 0; j < H && ok; ++j) {
+        for (int j = 0; j < H && ok && !p.latent; ++j) {
           for (int kc = 0; kc < kRank / kBK; ++kc, ++u2) {
             const int s = u2 % kS2Stages;
             if (!pf_wait(bar(&sh->empty2[s]), ((u2 / kS2Stages) & 1) ^ 1, abort, budget, p.status)) { ok = false; break; }
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         // (c) kv_b, one head per N = 256 tile
         if (!pf_wait(bar(&sh->a2_ready), tiles_done & 1, abort, budget, p.status, true)) { ok = false; break; }
         tc::fence_after_sync();
-        for (int j = 0; j < H && ok; ++j) {
+        for (int j = 0; j < H && ok && !p.latent; ++j) {
           const int b = j & 1;
           if (j >= 2 && !drain_buf(b)) { ok = false; break; }
           tc::fence_after_sync();
@@ -441,6 +441,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             o[j / 2] = E::pack(__uint_as_float(x[j]) * inv * E::to_f(gam[col]),
                                __uint_as_float(x[j + 1]) * inv * E::to_f(gam[col + 1]));
           }
+          if (p.latent) {  // latent-cache variant: the normalised row is an output
+            if (live) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.latent) + (size_t)t * kRank + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            }
+            continue;
+          }
           // K-chunk c/2 (64 columns), 16-byte chunks (c%2)*4 .. +3 of this row
           unsigned char* chunk = a2row + (c >> 1) * 16384;
 #pragma unroll
@@ -456,6 +464,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::arrive_cluster(lead(&sh->a2_ready));
+      if (p.latent) continue;
       // (c) per head: split into k_nope / value, head-major stores
       T* kn = static_cast<T*>(p.k_nope);
       T* vv = static_cast<T*>(p.value);
@@ -522,9 +531,15 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   const uint64_t h = (uint64_t)p.hidden_dim, NB = (uint64_t)p.heads * kHeadCols;
   if (!encode_tmap_2d(&a.tm_x, dt, p.hidden, h, (uint64_t)p.T, h * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&a.tm_wa, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_3d_colblocks(&a.tm_wa3, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_3d_colblocks(&a.tm_wb3, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tmap_3d_colblocks(&a.tm_wa3, dt, p.W_kva, kNa, h, kNa * 2, kBK, kBK, 2, 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // (the latent-cache variant reads no W_kvb)
+  if (p.latent) {
+    a.tm_wb3 = a.tm_wa3;
+  } else if (!encode_tmap_3d_colblocks(&a.tm_wb3, dt, p.W_kvb, NB, kRank, NB * 2, kBK, kBK, 2, 2,
+                                       CU_TENSOR_MAP_SWIZZLE_128B)) {
+    return cudaErrorInvalidValue;
+  }
   const void* fn = bf16 ? (const void*)prefill_kernel<__nv_bfloat16> : (const void*)prefill_kernel<__half>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
