@@ -572,11 +572,13 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
   if (grid > max_grid) grid = max_grid;
   // Pairs left over when every tile has its own CTA take the k_pe pass of
   // all tiles (it re-reads the hidden tile, so the main CTAs save one full
-  // read of their rows): used when they are at least one per eight tiles.
+  // read of their rows): used when they are at least one per eight tiles,
+  // and not for the latent-cache variant, whose tile CTAs (no kv_b pass)
+  // would then wait for the workers.
   const int spare = max_grid - grid;
   a.p.main_ctas = grid;
   a.p.kpe_split = 0;
-  if (grid >= ntiles && spare >= kCl && spare * 8 >= ntiles) {
+  if (!p.latent && grid >= ntiles && spare >= kCl && spare * 8 >= ntiles) {
     const int workers = (spare < grid ? spare : grid) / kCl * kCl;
     a.p.kpe_split = 1;
     grid += workers;
