@@ -273,6 +273,27 @@ def kv_latent(inp: dict, rows=None, nthreads: int = 0):
     return latent, k_pe
 
 
+def scatter_paged(dense: tuple, b: int, s: int, slots, page_size: int, num_blocks: int):
+    """Paged KV-cache layout of the dense prolog outputs (k_nope, value
+    [b,H,s,d], k_pe [b,1,s,64]): token row t = bi*s + si goes to slot
+    slots[t] = block * page_size + offset, i.e. k_cache[block, h, offset, :]
+    (caches [num_blocks, H, page_size, d] and [num_blocks, 1, page_size,
+    64]); a negative slot drops the row.  Entries no row writes are NaN."""
+    slots = np.asarray(slots, dtype=np.int64)
+    outs = []
+    for a in dense:
+        H, d = a.shape[1], a.shape[3]
+        c = np.full((num_blocks, H, page_size, d), np.nan)
+        for t in range(b * s):
+            if slots[t] < 0:
+                continue
+            blk, off = divmod(int(slots[t]), page_size)
+            bi, si = divmod(t, s)
+            c[blk, :, off, :] = a[bi, :, si, :]
+        outs.append(c)
+    return tuple(outs)
+
+
 def _w8_dims(inp):
     cfg = inp["cfg"]
     return _W8Dims(cfg["hidden"], cfg["q_lora_rank"], cfg["kv_lora_rank"], cfg["rope_dim"],

@@ -347,6 +347,36 @@ def test_kv_latent_feeds_kv_b(oracle_mod):
     assert np.all(np.isnan(part[[0, 2, 3, 5]])) and np.all(np.isnan(kp2[0, 0, 0]))
 
 
+# ------------------------------------------------------------ paged KV-cache layout
+def test_scatter_paged_identity_and_permutation(oracle_mod):
+    """One block per sequence (slot = bi*s + si, page = s) reproduces the
+    dense layout exactly; a permuted block table moves whole rows, and
+    dropped rows (slot -1) leave NaN."""
+    cfg = I.small_config(I.V2_LITE, hidden=128, num_heads=2)
+    b, s = 3, 4
+    inp = I.kv_inputs(cfg, b, s, seed=31, positions="decode")
+    dense = oracle_mod.kv_prolog(inp, nthreads=1)
+    same = oracle_mod.scatter_paged(dense, b, s, np.arange(b * s), s, b)
+    for a, c in zip(dense, same):
+        assert np.array_equal(a, c)
+    page, nblk = 2, 9
+    slots = np.array([17, 3, 4, 0, -1, 9, 10, 6, 1, 12, 13, -1])
+    paged = oracle_mod.scatter_paged(dense, b, s, slots, page, nblk)
+    written = set()
+    for t in range(b * s):
+        bi, si = divmod(t, s)
+        if slots[t] < 0:
+            continue
+        blk, off = divmod(int(slots[t]), page)
+        written.add((blk, off))
+        for a, c in zip(dense, paged):
+            assert np.array_equal(c[blk, :, off], a[bi, :, si])
+    for blk in range(nblk):
+        for off in range(page):
+            if (blk, off) not in written:
+                assert all(np.all(np.isnan(c[blk, :, off])) for c in paged)
+
+
 # ------------------------------------------------------------ W8A8
 def test_quant_hand_values(oracle_mod):
     for c in _gold("quant_hand.json")["cases"]:
