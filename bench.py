@@ -208,7 +208,7 @@ class SingleCall:
     """One prolog call per step on one configuration (prefill, R1, W8A8, or
     the latent-cache variant: kv_a_proj + RMSNorm + RoPE(k_pe), no kv_b_proj)."""
 
-    def __init__(self, name, cfg, b, s, positions, path, seed, latent=False):
+    def __init__(self, name, cfg, b, s, positions, path, seed, latent=False, paged=None):
         self.name, self.cfg, self.b, self.s = name, cfg, b, s
         self.positions, self.path, self.seed = positions, path, seed
         self.T = b * s
@@ -216,6 +216,7 @@ class SingleCall:
         self.tokens_per_step = self.T
         self.w8 = cfg.get("quant") == "w8a8"
         self.latent = latent
+        self.paged = paged  # (page_size, num_blocks): outputs scattered into a paged KV cache
 
     def describe(self):
         c = self.cfg
@@ -226,6 +227,9 @@ class SingleCall:
             d["quant"] = "w8a8 (int8 weights, per-token int8 activations, int32 accumulators)"
         if self.latent:
             d["variant"] = "latent cache: normalised compressed_kv [T, 512] + k_pe, no kv_b_proj"
+        if self.paged:
+            d["variant"] = ("paged KV cache: rows scattered by a random slot mapping into %d blocks of %d rows"
+                            % (self.paged[1], self.paged[0]))
         return d
 
     def weight_bytes(self):
@@ -267,8 +271,15 @@ class SingleCall:
             self.m.set_path(self.path)
             self.m.prepare_weights(self.d)  # packed snapshot for the decode path
             torch.cuda.synchronize(dev)
-        self.out = (self.m.alloc_latent_outputs(self.b, self.s, dev) if self.latent
-                    else self.m.alloc_outputs(self.b, self.s, dev))
+        if self.paged:
+            page, nblk = self.paged
+            g = torch.Generator().manual_seed(self.seed)
+            self.slots = torch.randperm(page * nblk, generator=g)[:self.T].to(torch.int32).to(dev)
+            self.out = self.m.alloc_paged_caches(nblk, page, dev)
+        elif self.latent:
+            self.out = self.m.alloc_latent_outputs(self.b, self.s, dev)
+        else:
+            self.out = self.m.alloc_outputs(self.b, self.s, dev)
         self.hidden_h = inp["hidden"].pin_memory()
         self.positions_h = inp["positions"].pin_memory()
         self.out_h = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.out.items()}
@@ -284,7 +295,9 @@ class SingleCall:
             self.flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def call(self, stream):
-        if self.latent:
+        if self.paged:
+            self.m.run_paged(self.b, self.s, self.d, self.slots, self.paged[0], self.out, stream)
+        elif self.latent:
             self.m.run_latent(self.b, self.s, self.d, self.out, stream)
         else:
             self.m.run(self.b, self.s, self.d, self.out, stream)
@@ -358,9 +371,9 @@ class SingleCall:
             f"{done} token rows of {self.name} (fp64 oracle, per-call weight promotion included), {el:.1f} s"
 
 
-def _single(name, cfg, b, s, positions, path_name, seed, latent=False):
+def _single(name, cfg, b, s, positions, path_name, seed, latent=False, paged=None):
     return lambda: SingleCall(name, cfg, b, s, positions, {"decode": 1, "prefill": 2, "auto": 0}[path_name],
-                              seed, latent)
+                              seed, latent, paged)
 
 
 WORKLOADS = {
@@ -376,6 +389,10 @@ WORKLOADS = {
                                     1005, latent=True),
     "r1_latent_prefill": _single("r1_kv_latent_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1005,
                                  latent=True),
+    "v2lite_paged_decode": _single("v2lite_kv_prolog_paged_decode_b64s1", I.V2_LITE, 64, 1, "decode", "auto",
+                                   1006, paged=(16, 64)),
+    "r1_paged_prefill": _single("r1_kv_prolog_paged_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1006,
+                                paged=(64, 288)),
 }
 
 
@@ -591,6 +608,8 @@ def main():
     kernel = {"prefill": "prefill_kernel", "decode": "decode_kernel"}[path] if not is_w8 else "w8a8 pipeline"
     if getattr(wl, "latent", False):
         kernel += " (latent variant)"
+    if getattr(wl, "paged", None):
+        kernel += " (paged cache)"
     if t_mem >= t_cmp:
         achieved = alg_bytes / call_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

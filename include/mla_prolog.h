@@ -79,7 +79,8 @@ typedef enum mla_status {
   MLA_ERR_DEVICE_TIMEOUT = 6,  /* a device-side wait ran past config.spin_budget_ns       */
   MLA_ERR_BAD_POSITION = 7,    /* a position outside [0, max_pos) was seen (and clamped)  */
   MLA_ERR_NO_MEMORY = 8,       /* workspace allocation failed in create                   */
-  MLA_ERR_WRONG_MODE = 9       /* run of one quant mode on a handle made for the other    */
+  MLA_ERR_WRONG_MODE = 9,      /* run of one quant mode on a handle made for the other    */
+  MLA_ERR_BAD_SLOT = 10        /* a paged-cache slot past the cache was seen (row dropped)*/
 } mla_status;
 
 typedef enum mla_dtype { MLA_F16 = 0, MLA_BF16 = 1 } mla_dtype;
@@ -136,6 +137,26 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const int32_t* positions, const void* W_kva, const void* gamma_kv,
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream);
+
+/* Paged KV cache: the prolog of mla_kv_prolog_run with step 7 writing into
+ * block-paged caches instead of the dense [b, H, s, d] outputs -- the
+ * scatter into the attention's KV cache that follows the prolog.  Token row
+ * t = bi*s + si goes to slot slot_mapping[t] = block * page_size + offset:
+ *   k_cache   [num_blocks, H, page_size, 128]  dtype   k_nope of the row at [block, :, offset, :]
+ *   v_cache   [num_blocks, H, page_size, 128]  dtype   value
+ *   kpe_cache [num_blocks, 1, page_size, 64]   dtype   k_pe
+ *   slot_mapping [b*s] int32; a negative slot drops the row (padding)
+ * Other entries of the caches are left untouched.  A slot at or past
+ * num_blocks * page_size drops the row and is reported by
+ * mla_kv_prolog_status as MLA_ERR_BAD_SLOT.  Other arguments, errors and
+ * path selection as for mla_kv_prolog_run. */
+mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                   const int32_t* positions, const void* W_kva,
+                                   const void* gamma_kv, const void* W_kvb,
+                                   const float* cos_table, const float* sin_table,
+                                   const int32_t* slot_mapping, int page_size, int num_blocks,
+                                   void* k_cache, void* v_cache, void* kpe_cache,
+                                   cudaStream_t stream);
 
 /* Latent-cache variant: enqueue steps 1, 2, 3 and 6 of the prolog only --
  * kv_a_proj, split, RMSNorm of compressed_kv and RoPE of k_pe -- for an
@@ -203,8 +224,9 @@ mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_
 
 /* Synchronise `stream`, read the device status word of the handle, clear
  * it (and reset the device barrier counters if a wait timed out) and
- * return MLA_OK, MLA_ERR_BAD_POSITION or MLA_ERR_DEVICE_TIMEOUT (the first
- * fault recorded since the last call). */
+ * return MLA_OK, MLA_ERR_BAD_POSITION, MLA_ERR_DEVICE_TIMEOUT or
+ * MLA_ERR_BAD_SLOT (in that order of precedence, for the faults recorded
+ * since the last call). */
 mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream);
 
 /* Free the workspace and the handle.  The caller must make sure no run on

@@ -18,7 +18,7 @@ MLA_OK = 0
 STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_TOO_MANY_TOKENS", 4: "MLA_ERR_MISALIGNED", 5: "MLA_ERR_CUDA",
                 6: "MLA_ERR_DEVICE_TIMEOUT", 7: "MLA_ERR_BAD_POSITION", 8: "MLA_ERR_NO_MEMORY",
-                9: "MLA_ERR_WRONG_MODE"}
+                9: "MLA_ERR_WRONG_MODE", 10: "MLA_ERR_BAD_SLOT"}
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 MLA_F16, MLA_BF16 = 0, 1
 QUANT_NONE, QUANT_W8A8 = 0, 1
@@ -28,7 +28,7 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
             "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
-            "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent"]
+            "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent", "mla_kv_prolog_run_paged"]
 
 
 class MLAError(RuntimeError):
@@ -67,6 +67,7 @@ def load(path: str | None = None):
     L.mla_kv_prolog_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_void_p)]
     L.mla_kv_prolog_run.argtypes = [H, I, I] + [P] * 10 + [P]
     L.mla_kv_prolog_run_latent.argtypes = [H, I, I] + [P] * 8 + [P]
+    L.mla_kv_prolog_run_paged.argtypes = [H, I, I] + [P] * 8 + [I, I] + [P] * 3 + [P]
     L.mla_prolog_w8a8_run.argtypes = [H, I, I] + [P] * 19 + [P]
     L.mla_kv_prolog_status.argtypes = [H, P]
     L.mla_kv_prolog_destroy.argtypes = [H]
@@ -165,6 +166,19 @@ def mla_kv_prolog_run_latent(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, c
             _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
             _dev(latent, dt, "latent"), _dev(k_pe, dt, "k_pe")]
     _check(load().mla_kv_prolog_run_latent(h, b, s, *args, _stream(stream)), "mla_kv_prolog_run_latent")
+
+
+def mla_kv_prolog_run_paged(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, W_kvb, cos, sin,
+                            slot_mapping, page_size, num_blocks, k_cache, v_cache, kpe_cache,
+                            stream=None):
+    dt = _tdt(cfg)
+    args = [_dev(hidden, dt, "hidden_states"), _dev(positions, torch.int32, "positions"),
+            _dev(W_kva, dt, "W_kva"), _dev(gamma_kv, dt, "gamma_kv"), _dev(W_kvb, dt, "W_kvb"),
+            _dev(cos, torch.float32, "cos"), _dev(sin, torch.float32, "sin"),
+            _dev(slot_mapping, torch.int32, "slot_mapping")]
+    caches = [_dev(k_cache, dt, "k_cache"), _dev(v_cache, dt, "v_cache"), _dev(kpe_cache, dt, "kpe_cache")]
+    _check(load().mla_kv_prolog_run_paged(h, b, s, *args, page_size, num_blocks, *caches, _stream(stream)),
+           "mla_kv_prolog_run_paged")
 
 
 def mla_kv_prolog_prepare_weights(h, cfg, W_kva, W_kvb, stream=None):
@@ -293,6 +307,22 @@ class MLAProlog:
         mla_kv_prolog_run_latent(self.h, self.cfg, b, s, d["hidden"], d["positions"], d["W_kva"],
                                  d["gamma_kv"], d["cos"], d["sin"], out["latent"], out["k_pe"], stream)
         return out
+
+    def alloc_paged_caches(self, num_blocks: int, page_size: int, device="cuda"):
+        c = self.cfg
+        dt = _tdt(c)
+        H = c["num_heads"]
+        return dict(k_cache=torch.empty(num_blocks, H, page_size, c["nope_dim"], dtype=dt, device=device),
+                    v_cache=torch.empty(num_blocks, H, page_size, c["v_dim"], dtype=dt, device=device),
+                    kpe_cache=torch.empty(num_blocks, 1, page_size, c["rope_dim"], dtype=dt, device=device))
+
+    def run_paged(self, b, s, d: dict, slot_mapping, page_size: int, caches: dict, stream=None):
+        """Paged variant: rows scattered into caches (alloc_paged_caches) by slot_mapping."""
+        nb = caches["k_cache"].shape[0]
+        mla_kv_prolog_run_paged(self.h, self.cfg, b, s, d["hidden"], d["positions"], d["W_kva"],
+                                d["gamma_kv"], d["W_kvb"], d["cos"], d["sin"], slot_mapping, page_size,
+                                nb, caches["k_cache"], caches["v_cache"], caches["kpe_cache"], stream)
+        return caches
 
     def run(self, b, s, d: dict, out: dict, stream=None):
         """d: device tensors keyed as the input generator names them."""

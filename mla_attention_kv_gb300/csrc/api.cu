@@ -98,6 +98,7 @@ const char* mla_status_string(mla_status s) {
     case MLA_ERR_BAD_POSITION: return "position outside [0, max_pos)";
     case MLA_ERR_NO_MEMORY: return "workspace allocation failed";
     case MLA_ERR_WRONG_MODE: return "run does not match the handle's quant mode";
+    case MLA_ERR_BAD_SLOT: return "a cache slot past num_blocks * page_size was seen (row dropped)";
   }
   return "unknown status";
 }
@@ -210,6 +211,7 @@ mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
   }
   if (st & kStatusBadPosition) return MLA_ERR_BAD_POSITION;
   if (st & kStatusTimeout) return MLA_ERR_DEVICE_TIMEOUT;
+  if (st & kStatusBadSlot) return MLA_ERR_BAD_SLOT;
   return MLA_OK;
 }
 
@@ -218,7 +220,8 @@ mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
 static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states,
                          const int32_t* positions, const void* W_kva, const void* gamma_kv,
                          const void* W_kvb, const float* cos_table, const float* sin_table,
-                         void* k_nope, void* value, void* k_pe, void* latent, cudaStream_t stream) {
+                         void* k_nope, void* value, void* k_pe, void* latent, const OutLayout& lay,
+                         cudaStream_t stream) {
   if (!h || b < 0 || s < 0) return MLA_ERR_INVALID_ARG;
   if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
   const long long T = (long long)b * s;
@@ -241,7 +244,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     PrefillParams pp = {};
     pp.hidden = hidden_states; pp.positions = positions; pp.W_kva = W_kva; pp.gamma = gamma_kv;
     pp.W_kvb = W_kvb; pp.cos_t = cos_table; pp.sin_t = sin_table; pp.k_nope = k_nope;
-    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.status = h->status;
+    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.out = lay; pp.status = h->status;
     pp.hidden_dim = h->cfg.hidden; pp.heads = h->cfg.num_heads; pp.s = s; pp.T = (int)T;
     pp.max_pos = h->cfg.max_pos; pp.eps = h->cfg.eps; pp.budget_ns = h->budget_ns;
     int launches = 0;
@@ -269,7 +272,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
   }
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
-  p.k_pe = k_pe; p.latent = latent; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
+  p.k_pe = k_pe; p.latent = latent; p.out = lay; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
@@ -291,7 +294,23 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
-                k_nope, value, k_pe, nullptr, stream);
+                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0}, stream);
+}
+
+mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                   const int32_t* positions, const void* W_kva,
+                                   const void* gamma_kv, const void* W_kvb,
+                                   const float* cos_table, const float* sin_table,
+                                   const int32_t* slot_mapping, int page_size, int num_blocks,
+                                   void* k_cache, void* v_cache, void* kpe_cache,
+                                   cudaStream_t stream) {
+  if (!slot_mapping || page_size <= 0 || num_blocks <= 0 ||
+      (long long)page_size * num_blocks > 0x7fffffffLL)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(slot_mapping)) return MLA_ERR_MISALIGNED;
+  return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
+                k_cache, v_cache, kpe_cache, nullptr,
+                OutLayout{slot_mapping, page_size, page_size * num_blocks}, stream);
 }
 
 mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hidden_states,
@@ -301,7 +320,7 @@ mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hi
                                     cudaStream_t stream) {
   if (!latent) return MLA_ERR_INVALID_ARG;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, nullptr, cos_table, sin_table,
-                nullptr, nullptr, k_pe, latent, stream);
+                nullptr, nullptr, k_pe, latent, OutLayout{nullptr, 0, 0}, stream);
 }
 
 mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,

@@ -188,6 +188,28 @@ __device__ __forceinline__ void mma16832_s8(int* d, const uint32_t* a, uint32_t 
 // ---------------------------------------------------------------- timing / sync
 __device__ __forceinline__ uint64_t globaltimer_ns() { return globaltimer_ns_(); }
 
+// Where token row t goes (see OutLayout): false for a row to drop (a
+// negative slot; a slot past the cache is also recorded in *status).
+__device__ __forceinline__ bool out_place(const OutLayout& L, int t, int s, unsigned* status,
+                                          int* outer, int* inner, int* count) {
+  if (!L.slots) {
+    *outer = t / s;
+    *inner = t - *outer * s;
+    *count = s;
+    return true;
+  }
+  const int slot = L.slots[t];
+  if (slot < 0) return false;
+  if (slot >= L.nslots) {
+    atomicOr(status, kStatusBadSlot);
+    return false;
+  }
+  *outer = slot / L.page;
+  *inner = slot - *outer * L.page;
+  *count = L.page;
+  return true;
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel in
 // the stream (launched with programmatic stream serialisation) start while
 // this one runs; grid_dep_wait blocks until the kernel before this one has

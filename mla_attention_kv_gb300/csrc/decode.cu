@@ -633,11 +633,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         *reinterpret_cast<uint2*>(sN + t * kPitchN + c * 2) = pk;
       } else if (rope_row && tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
-        T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
-        *reinterpret_cast<uint32_t*>(kp + j0) =
-            E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
-        *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
-            E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+        int ou, in, cnt;
+        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt)) {
+          T* kp = static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope;
+          *reinterpret_cast<uint32_t*>(kp + j0) =
+              E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
+          *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
+              E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+        }
       }
     }
     // zero the padding rows of the last m-tile
@@ -681,11 +684,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       } else if (tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
-        T* kp = static_cast<T*>(p.k_pe) + (size_t)(p.t0 + t) * kRope;
-        *reinterpret_cast<uint32_t*>(kp + j0) =
-            E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
-        *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
-            E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+        int ou, in, cnt;
+        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt)) {
+          T* kp = static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope;
+          *reinterpret_cast<uint32_t*>(kp + j0) =
+              E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
+          *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
+              E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
+        }
       }
     }
     if (!p.latent && !bar_arrive_wait(p.counters + 1, G, p.budget_ns, p.status)) {
@@ -874,9 +880,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int hh = j / kHeadCols, e = j - hh * kHeadCols;
     T* base = (e < kNope) ? kn : vv;
     const int ee = (e < kNope) ? e : e - kNope;
-    const int tg = p.t0 + r;
-    const int bi = tg / p.s, si = tg - bi * p.s;
-    *reinterpret_cast<uint4*>(base + (((size_t)bi * H + hh) * p.s + si) * kNope + ee) =
+    int ou, in, cnt;
+    if (!out_place(p.out, p.t0 + r, p.s, p.status, &ou, &in, &cnt)) continue;
+    *reinterpret_cast<uint4*>(base + (((size_t)ou * H + hh) * cnt + in) * kNope + ee) =
         *reinterpret_cast<const uint4*>(sO + r * pitchB + gi * 16);
   }
 }

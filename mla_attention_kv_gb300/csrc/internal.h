@@ -11,7 +11,19 @@ namespace mla {
 void set_error_text(const char* what);
 
 // Device status bits (kept in the handle's workspace).
-enum : unsigned { kStatusBadPosition = 1u, kStatusTimeout = 2u };
+enum : unsigned { kStatusBadPosition = 1u, kStatusTimeout = 2u, kStatusBadSlot = 4u };
+
+// Output placement of token row t (shared by the decode and prefill
+// kernels): the dense layout [b, X, s, d] (outer = bi, inner = si, count =
+// s) or, with a slot mapping, the paged cache [num_blocks, X, page, d]
+// (slot = block * page + offset: outer = block, inner = offset, count =
+// page).  Element (head hh, column e) of the row is at
+// ((outer * X + hh) * count + inner) * d + e.
+struct OutLayout {
+  const int32_t* slots;  // [T] physical slot per row; null: dense
+  int page;              // rows per cache block
+  int nslots;            // num_blocks * page
+};
 
 // Fixed dimensions of the DeepSeek MLA KV prolog this library implements.
 constexpr int kRank = 512;         // kv_lora_rank
@@ -45,6 +57,7 @@ struct DecodeParams {
   void* value;              // [b, H, s, 128]
   void* k_pe;               // [b, 1, s, 64]
   void* latent;             // latent-cache variant: normalised compressed_kv [T, 512]; null: full prolog
+  OutLayout out;            // dense or paged placement of k_nope / value / k_pe
   float* partials;          // workspace [KC][kDecodeMaxTokens][576] fp32
   void* nrm;                // workspace [kDecodeMaxTokens][512] dtype
   unsigned* counters;       // workspace: grid barrier {arrivals, generation}
@@ -128,6 +141,7 @@ struct PrefillParams {
   void* value;
   void* k_pe;
   void* latent;    // latent-cache variant: normalised compressed_kv [T, 512] (no kv_b); null: full prolog
+  OutLayout out;   // dense or paged placement of k_nope / value / k_pe
   unsigned* status;
   int hidden_dim, heads, s, T, max_pos;
   float eps;

@@ -364,8 +364,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     bool ok = true;
     for (int it = 0; it < iters && ok; ++it, ++tiles_done) {
       const int t = tile_of(it) * kBM + r;
-      const bool live = t < ntok;
-      const int bi = live ? t / p.s : 0, si = live ? t - bi * p.s : 0;
+      // output place of this row (dense [b, X, s, d] or a paged cache slot)
+      int ou = 0, in = 0, cnt = 1;
+      const bool live = t < ntok && out_place(p.out, t, p.s, p.status, &ou, &in, &cnt);
       // (a) k_pe: RoPE on the 64 raw columns
       if (do_kpe) {
       if (!pf_wait(bar(&sh->tfull[0]), uf[0] & 1, abort, budget, p.status)) { ok = false; break; }
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             o[j / 2] = E::pack(a0 * cr[j] - b0 * sr[j], a1 * cr[j + 1] - b1 * sr[j + 1]);
             o[16 + j / 2] = E::pack(b0 * cr[j + 32] + a0 * sr[j + 32], b1 * cr[j + 33] + a1 * sr[j + 33]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_pe) + (size_t)t * kRope);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope);
 #pragma unroll
           for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         if (!pf_wait(bar(&sh->tfull[b]), uf[b] & 1, abort, budget, p.status)) { ok = false; break; }
         ++uf[b];
         tc::fence_after_sync();
-        const size_t orow = (((size_t)bi * H + j) * p.s + si) * kNope;
+        const size_t orow = (((size_t)ou * H + j) * cnt + in) * kNope;
 #pragma unroll 1
         for (int c = 0; c < kHeadCols / 32; c += 2) {  // two TMEM loads in flight
           uint32_t x[2][32];
