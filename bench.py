@@ -228,8 +228,9 @@ class SingleCall:
         if self.latent:
             d["variant"] = "latent cache: normalised compressed_kv [T, 512] + k_pe, no kv_b_proj"
         if self.paged:
-            d["variant"] = ("paged KV cache: rows scattered by a random slot mapping into %d blocks of %d rows"
-                            % (self.paged[1], self.paged[0]))
+            d["variant"] = ("paged KV cache of %d blocks of %d rows: a random block table, each sequence's "
+                            "rows at consecutive offsets of its blocks (decode: offset = position %% %d)"
+                            % (self.paged[1], self.paged[0], self.paged[0]))
         return d
 
     def weight_bytes(self):
@@ -272,9 +273,20 @@ class SingleCall:
             self.m.prepare_weights(self.d)  # packed snapshot for the decode path
             torch.cuda.synchronize(dev)
         if self.paged:
+            # a block table as a serving engine keeps it: random physical
+            # blocks, a sequence's rows at consecutive offsets within them
             page, nblk = self.paged
+            nbps = (self.s + page - 1) // page
             g = torch.Generator().manual_seed(self.seed)
-            self.slots = torch.randperm(page * nblk, generator=g)[:self.T].to(torch.int32).to(dev)
+            table = torch.randperm(nblk, generator=g)[:self.b * nbps].view(self.b, nbps)
+            t = torch.arange(self.T)
+            bi, si = t // self.s, t % self.s
+            if self.s == 1:
+                off = inp["positions"].long() % page
+                slot = table[bi, 0] * page + off
+            else:
+                slot = table[bi, si // page] * page + si % page
+            self.slots = slot.to(torch.int32).to(dev)
             self.out = self.m.alloc_paged_caches(nblk, page, dev)
         elif self.latent:
             self.out = self.m.alloc_latent_outputs(self.b, self.s, dev)
