@@ -273,6 +273,18 @@ def kv_latent(inp: dict, rows=None, nthreads: int = 0):
     return latent, k_pe
 
 
+def quant_c8(x: np.ndarray, scale: np.ndarray, dtype: int) -> np.ndarray:
+    """int8 KV-cache codes of prolog outputs x (float64, any shape whose
+    last axis is the channel): x is first rounded to the I/O dtype (the value
+    the dense output would hold), then, in IEEE float32 operations,
+    inv = 1 / scale[c], q = clamp(rint(x * inv), -127, 127).  NaN entries
+    (rows not computed) map to 0."""
+    xd = round_to(np.nan_to_num(x, nan=0.0), dtype).astype(np.float32)
+    inv = (np.float32(1.0) / np.asarray(scale, dtype=np.float32)).astype(np.float32)
+    y = (xd * inv).astype(np.float32)
+    return np.clip(np.rint(y), -127, 127).astype(np.int8)
+
+
 def scatter_paged(dense: tuple, b: int, s: int, slots, page_size: int, num_blocks: int):
     """Paged KV-cache layout of the dense prolog outputs (k_nope, value
     [b,H,s,d], k_pe [b,1,s,64]): token row t = bi*s + si goes to slot

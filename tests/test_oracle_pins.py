@@ -347,6 +347,20 @@ def test_kv_latent_feeds_kv_b(oracle_mod):
     assert np.all(np.isnan(part[[0, 2, 3, 5]])) and np.all(np.isnan(kp2[0, 0, 0]))
 
 
+# ------------------------------------------------------------ int8 KV-cache codes
+def test_quant_c8_hand_values(oracle_mod):
+    """x / scale rounded half to even and clamped to [-127, 127]; the input
+    is first rounded to the I/O dtype (fp16 here: 0.1 -> 0.0999755859375)."""
+    x = np.array([[0.5, -1.0, 0.015, 0.025, 3.0, -3.0, 0.1, 0.0]])
+    sc = np.array([0.01, 0.01, 0.01, 0.01, 0.01, 0.01, 0.001, 0.5], dtype=np.float32)
+    q = oracle_mod.quant_c8(x, sc, 0)
+    # 0.015 and 0.025 in fp16 are 0.01499938965 and 0.02499389648: 1.4999 -> 1, 2.4994 -> 2
+    assert q.tolist() == [[50, -100, 1, 2, 127, -127, 100, 0]]
+    # exact ties go to even: 2.5 -> 2, 3.5 -> 4, -0.5 -> 0 (bf16 holds these exactly)
+    q2 = oracle_mod.quant_c8(np.array([2.5, 3.5, -0.5, 1.5]), np.ones(4, dtype=np.float32), 1)
+    assert q2.tolist() == [2, 4, 0, 2]
+
+
 # ------------------------------------------------------------ paged KV-cache layout
 def test_scatter_paged_identity_and_permutation(oracle_mod):
     """One block per sequence (slot = bi*s + si, page = s) reproduces the
