@@ -208,7 +208,7 @@ class SingleCall:
     """One prolog call per step on one configuration (prefill, R1, W8A8, or
     the latent-cache variant: kv_a_proj + RMSNorm + RoPE(k_pe), no kv_b_proj)."""
 
-    def __init__(self, name, cfg, b, s, positions, path, seed, latent=False, paged=None):
+    def __init__(self, name, cfg, b, s, positions, path, seed, latent=False, paged=None, c8=False):
         self.name, self.cfg, self.b, self.s = name, cfg, b, s
         self.positions, self.path, self.seed = positions, path, seed
         self.T = b * s
@@ -217,6 +217,7 @@ class SingleCall:
         self.w8 = cfg.get("quant") == "w8a8"
         self.latent = latent
         self.paged = paged  # (page_size, num_blocks): outputs scattered into a paged KV cache
+        self.c8 = c8        # int8 KV-cache outputs with per-channel scales
 
     def describe(self):
         c = self.cfg
@@ -227,6 +228,8 @@ class SingleCall:
             d["quant"] = "w8a8 (int8 weights, per-token int8 activations, int32 accumulators)"
         if self.latent:
             d["variant"] = "latent cache: normalised compressed_kv [T, 512] + k_pe, no kv_b_proj"
+        if self.c8:
+            d["variant"] = "int8 KV cache: k_nope / value / k_pe codes with per-channel fp32 scales"
         if self.paged:
             d["variant"] = ("paged KV cache of %d blocks of %d rows: a random block table, each sequence's "
                             "rows at consecutive offsets of its blocks (decode: offset = position %% %d)"
@@ -257,6 +260,8 @@ class SingleCall:
         c = self.cfg
         H = c["num_heads"]
         out = 2 * (512 + 64) if self.latent else 2 * (H * 256 + 64) + (2 * H * 192 if self.w8 else 0)
+        if self.c8:
+            out = H * 256 + 64 + 4 * (H * 256 + 64) / max(T, 1)  # int8 codes; the scales once per call
         return self.weight_bytes() + T * (2 * c["hidden"] + 4 + 2 * 64 * 4 + out)
 
     def setup(self, dev):
@@ -290,6 +295,14 @@ class SingleCall:
             self.out = self.m.alloc_paged_caches(nblk, page, dev)
         elif self.latent:
             self.out = self.m.alloc_latent_outputs(self.b, self.s, dev)
+        elif self.c8:
+            g = torch.Generator().manual_seed(self.seed)
+            H = self.cfg["num_heads"]
+            hi = 0.04 if self.cfg["hidden"] <= 2048 else 0.08
+            self.scales = dict(k=(0.01 + 0.01 * torch.rand(H * 128, generator=g)).to(dev),
+                               v=(0.01 + 0.01 * torch.rand(H * 128, generator=g)).to(dev),
+                               kpe=(hi / 2 + hi / 2 * torch.rand(64, generator=g)).to(dev))
+            self.out = self.m.alloc_c8_outputs(self.b, self.s, dev)
         else:
             self.out = self.m.alloc_outputs(self.b, self.s, dev)
         self.hidden_h = inp["hidden"].pin_memory()
@@ -311,6 +324,8 @@ class SingleCall:
             self.m.run_paged(self.b, self.s, self.d, self.slots, self.paged[0], self.out, stream)
         elif self.latent:
             self.m.run_latent(self.b, self.s, self.d, self.out, stream)
+        elif self.c8:
+            self.m.run_c8(self.b, self.s, self.d, self.scales, self.out, stream)
         else:
             self.m.run(self.b, self.s, self.d, self.out, stream)
 
@@ -383,9 +398,9 @@ class SingleCall:
             f"{done} token rows of {self.name} (fp64 oracle, per-call weight promotion included), {el:.1f} s"
 
 
-def _single(name, cfg, b, s, positions, path_name, seed, latent=False, paged=None):
+def _single(name, cfg, b, s, positions, path_name, seed, latent=False, paged=None, c8=False):
     return lambda: SingleCall(name, cfg, b, s, positions, {"decode": 1, "prefill": 2, "auto": 0}[path_name],
-                              seed, latent, paged)
+                              seed, latent, paged, c8)
 
 
 WORKLOADS = {
@@ -405,6 +420,9 @@ WORKLOADS = {
                                    1006, paged=(16, 64)),
     "r1_paged_prefill": _single("r1_kv_prolog_paged_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1006,
                                 paged=(64, 288)),
+    "v2lite_c8_decode": _single("v2lite_kv_prolog_c8_decode_b64s1", I.V2_LITE, 64, 1, "decode", "auto", 1007,
+                                c8=True),
+    "r1_c8_prefill": _single("r1_kv_prolog_c8_prefill_b2s8192", I.R1, 2, 8192, "prefill", "auto", 1007, c8=True),
 }
 
 
@@ -622,6 +640,8 @@ def main():
         kernel += " (latent variant)"
     if getattr(wl, "paged", None):
         kernel += " (paged cache)"
+    if getattr(wl, "c8", False):
+        kernel += " (int8 cache)"
     if t_mem >= t_cmp:
         achieved = alg_bytes / call_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

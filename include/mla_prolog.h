@@ -138,6 +138,22 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream);
 
+/* int8 KV cache (the C8 cache of the W8A8C8 mode, [R1] §权重转换): the
+ * prolog of mla_kv_prolog_run with step 7 storing int8 codes instead of
+ * dtype values.  Per output channel c a static fp32 scale s_c (calibrated
+ * by the caller); the code of a value x -- the value the dtype output would
+ * hold -- is clamp(rint(x * (1 / s_c)), -127, 127), each step an IEEE fp32
+ * operation (rint half to even); x ~= code * s_c.
+ *   k_scale [H*128], v_scale [H*128], kpe_scale [64]   float32 (head-major:
+ *   channel hh*128 + e of k_nope / value)
+ *   k_nope [b, H, s, 128], value [b, H, s, 128], k_pe [b, 1, s, 64]  int8 outputs
+ * Other arguments, errors and path selection as for mla_kv_prolog_run. */
+mla_status mla_kv_prolog_run_c8(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                                const void* W_kvb, const float* cos_table, const float* sin_table,
+                                const float* k_scale, const float* v_scale, const float* kpe_scale,
+                                int8_t* k_nope, int8_t* value, int8_t* k_pe, cudaStream_t stream);
+
 /* Paged KV cache: the prolog of mla_kv_prolog_run with step 7 writing into
  * block-paged caches instead of the dense [b, H, s, d] outputs -- the
  * scatter into the attention's KV cache that follows the prolog.  Token row

@@ -28,7 +28,8 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
             "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
-            "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent", "mla_kv_prolog_run_paged"]
+            "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent", "mla_kv_prolog_run_paged",
+            "mla_kv_prolog_run_c8"]
 
 
 class MLAError(RuntimeError):
@@ -68,6 +69,7 @@ def load(path: str | None = None):
     L.mla_kv_prolog_run.argtypes = [H, I, I] + [P] * 10 + [P]
     L.mla_kv_prolog_run_latent.argtypes = [H, I, I] + [P] * 8 + [P]
     L.mla_kv_prolog_run_paged.argtypes = [H, I, I] + [P] * 8 + [I, I] + [P] * 3 + [P]
+    L.mla_kv_prolog_run_c8.argtypes = [H, I, I] + [P] * 13 + [P]
     L.mla_prolog_w8a8_run.argtypes = [H, I, I] + [P] * 19 + [P]
     L.mla_kv_prolog_status.argtypes = [H, P]
     L.mla_kv_prolog_destroy.argtypes = [H]
@@ -179,6 +181,17 @@ def mla_kv_prolog_run_paged(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, W_
     caches = [_dev(k_cache, dt, "k_cache"), _dev(v_cache, dt, "v_cache"), _dev(kpe_cache, dt, "kpe_cache")]
     _check(load().mla_kv_prolog_run_paged(h, b, s, *args, page_size, num_blocks, *caches, _stream(stream)),
            "mla_kv_prolog_run_paged")
+
+
+def mla_kv_prolog_run_c8(h, cfg, b, s, hidden, positions, W_kva, gamma_kv, W_kvb, cos, sin,
+                         k_scale, v_scale, kpe_scale, k_nope, value, k_pe, stream=None):
+    dt, f32, i8 = _tdt(cfg), torch.float32, torch.int8
+    args = [_dev(hidden, dt, "hidden_states"), _dev(positions, torch.int32, "positions"),
+            _dev(W_kva, dt, "W_kva"), _dev(gamma_kv, dt, "gamma_kv"), _dev(W_kvb, dt, "W_kvb"),
+            _dev(cos, f32, "cos"), _dev(sin, f32, "sin"), _dev(k_scale, f32, "k_scale"),
+            _dev(v_scale, f32, "v_scale"), _dev(kpe_scale, f32, "kpe_scale"),
+            _dev(k_nope, i8, "k_nope"), _dev(value, i8, "value"), _dev(k_pe, i8, "k_pe")]
+    _check(load().mla_kv_prolog_run_c8(h, b, s, *args, _stream(stream)), "mla_kv_prolog_run_c8")
 
 
 def mla_kv_prolog_prepare_weights(h, cfg, W_kva, W_kvb, stream=None):
@@ -323,6 +336,21 @@ class MLAProlog:
                                 d["gamma_kv"], d["W_kvb"], d["cos"], d["sin"], slot_mapping, page_size,
                                 nb, caches["k_cache"], caches["v_cache"], caches["kpe_cache"], stream)
         return caches
+
+    def alloc_c8_outputs(self, b: int, s: int, device="cuda"):
+        c = self.cfg
+        H, i8 = c["num_heads"], torch.int8
+        return dict(k_nope=torch.empty(b, H, s, c["nope_dim"], dtype=i8, device=device),
+                    value=torch.empty(b, H, s, c["v_dim"], dtype=i8, device=device),
+                    k_pe=torch.empty(b, 1, s, c["rope_dim"], dtype=i8, device=device))
+
+    def run_c8(self, b, s, d: dict, scales: dict, out: dict, stream=None):
+        """int8 KV-cache outputs (alloc_c8_outputs) with per-channel scales
+        scales["k"] [H*128], scales["v"] [H*128], scales["kpe"] [64]."""
+        mla_kv_prolog_run_c8(self.h, self.cfg, b, s, d["hidden"], d["positions"], d["W_kva"],
+                             d["gamma_kv"], d["W_kvb"], d["cos"], d["sin"], scales["k"], scales["v"],
+                             scales["kpe"], out["k_nope"], out["value"], out["k_pe"], stream)
+        return out
 
     def run(self, b, s, d: dict, out: dict, stream=None):
         """d: device tensors keyed as the input generator names them."""

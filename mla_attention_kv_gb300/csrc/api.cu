@@ -221,7 +221,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
                          const int32_t* positions, const void* W_kva, const void* gamma_kv,
                          const void* W_kvb, const float* cos_table, const float* sin_table,
                          void* k_nope, void* value, void* k_pe, void* latent, const OutLayout& lay,
-                         cudaStream_t stream) {
+                         const C8Scales& c8, cudaStream_t stream) {
   if (!h || b < 0 || s < 0) return MLA_ERR_INVALID_ARG;
   if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
   const long long T = (long long)b * s;
@@ -244,7 +244,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     PrefillParams pp = {};
     pp.hidden = hidden_states; pp.positions = positions; pp.W_kva = W_kva; pp.gamma = gamma_kv;
     pp.W_kvb = W_kvb; pp.cos_t = cos_table; pp.sin_t = sin_table; pp.k_nope = k_nope;
-    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.out = lay; pp.status = h->status;
+    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.out = lay; pp.c8 = c8; pp.status = h->status;
     pp.hidden_dim = h->cfg.hidden; pp.heads = h->cfg.num_heads; pp.s = s; pp.T = (int)T;
     pp.max_pos = h->cfg.max_pos; pp.eps = h->cfg.eps; pp.budget_ns = h->budget_ns;
     int launches = 0;
@@ -272,7 +272,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
   }
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
-  p.k_pe = k_pe; p.latent = latent; p.out = lay; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
+  p.k_pe = k_pe; p.latent = latent; p.out = lay; p.c8 = c8; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
@@ -294,7 +294,20 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
-                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0}, stream);
+                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr},
+                stream);
+}
+
+mla_status mla_kv_prolog_run_c8(mla_prolog_t h, int b, int s, const void* hidden_states,
+                                const int32_t* positions, const void* W_kva, const void* gamma_kv,
+                                const void* W_kvb, const float* cos_table, const float* sin_table,
+                                const float* k_scale, const float* v_scale, const float* kpe_scale,
+                                int8_t* k_nope, int8_t* value, int8_t* k_pe, cudaStream_t stream) {
+  if (!k_scale || !v_scale || !kpe_scale) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(k_scale) || !aligned16(v_scale) || !aligned16(kpe_scale)) return MLA_ERR_MISALIGNED;
+  return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
+                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0},
+                C8Scales{k_scale, v_scale, kpe_scale}, stream);
 }
 
 mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hidden_states,
@@ -310,7 +323,8 @@ mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hid
   if (!aligned16(slot_mapping)) return MLA_ERR_MISALIGNED;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
                 k_cache, v_cache, kpe_cache, nullptr,
-                OutLayout{slot_mapping, page_size, page_size * num_blocks}, stream);
+                OutLayout{slot_mapping, page_size, page_size * num_blocks}, C8Scales{nullptr, nullptr, nullptr},
+                stream);
 }
 
 mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hidden_states,
@@ -320,7 +334,8 @@ mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hi
                                     cudaStream_t stream) {
   if (!latent) return MLA_ERR_INVALID_ARG;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, nullptr, cos_table, sin_table,
-                nullptr, nullptr, k_pe, latent, OutLayout{nullptr, 0, 0}, stream);
+                nullptr, nullptr, k_pe, latent, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr},
+                stream);
 }
 
 mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,

@@ -598,6 +598,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     return;
   }
 
+  // k_pe outputs j0, j0 + 1, j0 + 32, j0 + 33 of the row at element offset o
+  // (dtype values, or their int8 codes)
+  auto store_kpe = [&](size_t o, int j0, float a, float b, float c, float d) {
+    if (p.c8.k) {
+      int8_t* kp = static_cast<int8_t*>(p.k_pe) + o;
+      const float* sc = p.c8.kpe;
+      const T ra = E::from_f(a), rb = E::from_f(b), rc = E::from_f(c), rd = E::from_f(d);
+      *reinterpret_cast<uint16_t*>(kp + j0) =
+          (uint16_t)(kv_code(E::to_f(ra), sc[j0]) | (kv_code(E::to_f(rb), sc[j0 + 1]) << 8));
+      *reinterpret_cast<uint16_t*>(kp + j0 + 32) =
+          (uint16_t)(kv_code(E::to_f(rc), sc[j0 + 32]) | (kv_code(E::to_f(rd), sc[j0 + 33]) << 8));
+    } else {
+      T* kp = static_cast<T*>(p.k_pe) + o;
+      *reinterpret_cast<uint32_t*>(kp + j0) = E::pack(a, b);
+      *reinterpret_cast<uint32_t*>(kp + j0 + 32) = E::pack(c, d);
+    }
+  };
+
   // ================================================================ phase R
   const float rms_scale = 1.0f / (float)kRank;
   if (p.single_barrier) {
@@ -634,13 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       } else if (rope_row && tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
         int ou, in, cnt;
-        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt)) {
-          T* kp = static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope;
-          *reinterpret_cast<uint32_t*>(kp + j0) =
-              E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
-          *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
-              E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
-        }
+        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt))
+          store_kpe(((size_t)ou * cnt + in) * kRope, j0, v.x * sCos[j0] - v.y * sSin[j0],
+                    v.z * sCos[j1] - v.w * sSin[j1], v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32],
+                    v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
       }
     }
     // zero the padding rows of the last m-tile
@@ -685,13 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       } else if (tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
         int ou, in, cnt;
-        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt)) {
-          T* kp = static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope;
-          *reinterpret_cast<uint32_t*>(kp + j0) =
-              E::pack(v.x * sCos[j0] - v.y * sSin[j0], v.z * sCos[j1] - v.w * sSin[j1]);
-          *reinterpret_cast<uint32_t*>(kp + j0 + 32) =
-              E::pack(v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32], v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
-        }
+        if (out_place(p.out, p.t0 + t, p.s, p.status, &ou, &in, &cnt))
+          store_kpe(((size_t)ou * cnt + in) * kRope, j0, v.x * sCos[j0] - v.y * sSin[j0],
+                    v.z * sCos[j1] - v.w * sSin[j1], v.y * sCos[j0 + 32] + v.x * sSin[j0 + 32],
+                    v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
       }
     }
     if (!p.latent && !bar_arrive_wait(p.counters + 1, G, p.budget_ns, p.status)) {
@@ -882,8 +894,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int ee = (e < kNope) ? e : e - kNope;
     int ou, in, cnt;
     if (!out_place(p.out, p.t0 + r, p.s, p.status, &ou, &in, &cnt)) continue;
-    *reinterpret_cast<uint4*>(base + (((size_t)ou * H + hh) * cnt + in) * kNope + ee) =
-        *reinterpret_cast<const uint4*>(sO + r * pitchB + gi * 16);
+    const size_t o = (((size_t)ou * H + hh) * cnt + in) * kNope + ee;
+    if (p.c8.k) {  // int8 KV cache: codes of the 8 dtype values
+      const T* x = reinterpret_cast<const T*>(sO + r * pitchB + gi * 16);
+      const float* sc = (e < kNope ? p.c8.k : p.c8.v) + hh * kNope + ee;
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i >> 2] |= kv_code(E::to_f(x[i]), sc[i]) << (8 * (i & 3));
+      *reinterpret_cast<uint2*>(reinterpret_cast<int8_t*>(e < kNope ? p.k_nope : p.value) + o) =
+          make_uint2(w[0], w[1]);
+    } else {
+      *reinterpret_cast<uint4*>(base + o) = *reinterpret_cast<const uint4*>(sO + r * pitchB + gi * 16);
+    }
   }
 }
 

@@ -25,6 +25,16 @@ struct OutLayout {
   int nslots;            // num_blocks * page
 };
 
+// int8 KV-cache outputs: per-channel fp32 scales of k_nope [H*128], value
+// [H*128] and k_pe [64]; k == null: outputs in the I/O dtype.  A code is
+// clamp(rint(x * (1 / scale)), -127, 127) of the value x the dtype output
+// would hold, in IEEE fp32 operations.
+struct C8Scales {
+  const float* k;
+  const float* v;
+  const float* kpe;
+};
+
 // Fixed dimensions of the DeepSeek MLA KV prolog this library implements.
 constexpr int kRank = 512;         // kv_lora_rank
 constexpr int kRope = 64;          // qk_rope_head_dim
@@ -58,6 +68,7 @@ struct DecodeParams {
   void* k_pe;               // [b, 1, s, 64]
   void* latent;             // latent-cache variant: normalised compressed_kv [T, 512]; null: full prolog
   OutLayout out;            // dense or paged placement of k_nope / value / k_pe
+  C8Scales c8;              // int8 outputs when c8.k is set
   float* partials;          // workspace [KC][kDecodeMaxTokens][576] fp32
   void* nrm;                // workspace [kDecodeMaxTokens][512] dtype
   unsigned* counters;       // workspace: grid barrier {arrivals, generation}
@@ -142,6 +153,7 @@ struct PrefillParams {
   void* k_pe;
   void* latent;    // latent-cache variant: normalised compressed_kv [T, 512] (no kv_b); null: full prolog
   OutLayout out;   // dense or paged placement of k_nope / value / k_pe
+  C8Scales c8;     // int8 outputs when c8.k is set
   unsigned* status;
   int hidden_dim, heads, s, T, max_pos;
   float eps;

@@ -402,9 +402,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             o[j / 2] = E::pack(a0 * cr[j] - b0 * sr[j], a1 * cr[j + 1] - b1 * sr[j + 1]);
             o[16 + j / 2] = E::pack(b0 * cr[j + 32] + a0 * sr[j + 32], b1 * cr[j + 33] + a1 * sr[j + 33]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope);
+          if (p.c8.k) {  // int8 KV cache: o[k] holds outputs 2k, 2k + 1
+            uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            for (int k = 0; k < 16; ++k) {
+              const T* e0 = reinterpret_cast<const T*>(&o[2 * k]);
+              const T* e1 = reinterpret_cast<const T*>(&o[2 * k + 1]);
+              w[k] = kv_code(E::to_f(e0[0]), p.c8.kpe[4 * k]) | (kv_code(E::to_f(e0[1]), p.c8.kpe[4 * k + 1]) << 8) |
+                     (kv_code(E::to_f(e1[0]), p.c8.kpe[4 * k + 2]) << 16) |
+                     (kv_code(E::to_f(e1[1]), p.c8.kpe[4 * k + 3]) << 24);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
         }
       }
       // release TMEM buffer 0 to the leader's MMA thread (one arrival per warp)
@@ -488,10 +503,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
               for (int i = 0; i < 16; ++i) o[i] = E::pack(__uint_as_float(x[h2][2 * i]), __uint_as_float(x[h2][2 * i + 1]));
               const int cc = c + h2;
-              T* dst = (cc < 4 ? kn : vv) + orow + (cc & 3) * 32;
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
+              if (p.c8.k) {  // int8 KV cache: codes of the 32 dtype values
+                const float* sc = (cc < 4 ? p.c8.k : p.c8.v) + j * kNope + (cc & 3) * 32;
+                uint32_t w[8];
 #pragma unroll
-              for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                for (int k = 0; k < 8; ++k) {
+                  const T* e0 = reinterpret_cast<const T*>(&o[2 * k]);
+                  const T* e1 = reinterpret_cast<const T*>(&o[2 * k + 1]);
+                  w[k] = kv_code(E::to_f(e0[0]), sc[4 * k]) | (kv_code(E::to_f(e0[1]), sc[4 * k + 1]) << 8) |
+                         (kv_code(E::to_f(e1[0]), sc[4 * k + 2]) << 16) | (kv_code(E::to_f(e1[1]), sc[4 * k + 3]) << 24);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<int8_t*>(cc < 4 ? p.k_nope : p.value) + orow +
+                                                     (cc & 3) * 32);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              } else {
+                T* dst = (cc < 4 ? kn : vv) + orow + (cc & 3) * 32;
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+              }
             }
           }
         }
