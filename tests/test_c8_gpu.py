@@ -2,9 +2,12 @@
 decode and the prefill kernel.  Bit-exact: the codes equal the oracle's
 quantiser applied to the same kernel's dtype outputs (a dense run on the
 same handle), so the fused epilogue quantises exactly as specified.  Against
-the fp64 oracle: codes within one step of the oracle's own codes, and equal
-on at least 99 % of entries (the dtype values themselves may differ in the
-last place, which moves a code when it sits at a rounding boundary)."""
+the fp64 oracle: codes within one step of the oracle's own codes everywhere.
+The dtype values themselves may differ in the last place (the parity
+tolerance allows it), which moves a code when the value sits near a
+rounding boundary: with these scales (about 0.015) one bf16 unit in the last
+place at |x| ~ 0.5 is about 0.13 code steps, one fp16 unit about 0.02, so the
+fraction of equal codes is required to be at least 90 % (bf16) / 99 % (fp16)."""
 import numpy as np
 import pytest
 import torch
@@ -74,7 +77,7 @@ def run_c8(cfg, b, s, seed, path, positions="decode", oracle_mod=None, rows=None
                 o = oracle_mod.quant_c8(r, chan[n].reshape(1, r.shape[1], 1, 128), dt)
             diff = np.abs(g.astype(np.int32) - o.astype(np.int32))[m_]
             assert diff.max() <= 1, n
-            assert (diff == 0).mean() >= 0.99, (n, (diff == 0).mean())
+            assert (diff == 0).mean() >= (0.99 if dt == 0 else 0.90), (n, (diff == 0).mean())
 
 
 @pytest.mark.parametrize("b,s", [(1, 2), (64, 1), (100, 2)])
