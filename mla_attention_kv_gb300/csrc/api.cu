@@ -28,6 +28,7 @@ struct mla_prolog_s {
   unsigned* counters;  // [2] grid barrier
   float* partials;
   void* nrm;
+  float* c8inv;  // reciprocal int8 KV-cache scales [H*256 + 64] (mla_kv_prolog_run_c8)
   DecodePlan dplan;
   bool decode_ok;
   // packed weight snapshot (mla_kv_prolog_prepare_weights): W_kva tiles then
@@ -144,6 +145,9 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
   const size_t nrm_off = off;
   off += kDecodeNrmBytes;
   off = (off + 255) & ~(size_t)255;
+  const size_t c8_off = off;
+  off += ((size_t)c.num_heads * kHeadCols + kRope) * sizeof(float);
+  off = (off + 255) & ~(size_t)255;
   size_t w8_off = off;
   if (c.quant == MLA_QUANT_W8A8)
     off += w8_workspace_bytes(c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens, h->num_sms);
@@ -165,6 +169,7 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
   h->counters = reinterpret_cast<unsigned*>(base + 64);
   h->partials = reinterpret_cast<float*>(base + part_off);
   h->nrm = base + nrm_off;
+  h->c8inv = reinterpret_cast<float*>(base + c8_off);
   if (c.quant == MLA_QUANT_W8A8) {
     w8_workspace_carve(base + w8_off, c.hidden, c.q_lora_rank, c.num_heads, c.max_tokens,
                        h->num_sms, &h->w8, &h->w8plan);
@@ -236,6 +241,13 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     if (!aligned16(q)) return MLA_ERR_MISALIGNED;
 
   const bool bf16 = h->cfg.dtype == MLA_BF16;
+  C8Scales c8q = c8;
+  if (c8q.k) {  // reciprocal scales, read by the kernel's store epilogue
+    c8q.inv = h->c8inv;
+    cudaError_t e = c8_reciprocals_launch(c8q, h->cfg.num_heads, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 cache scales");
+    h->last_launches = 1;
+  }
   int path = h->path_override;
   if (path == MLA_PATH_AUTO) path = prefill_preferred(h->cfg.hidden, h->cfg.num_heads, (int)T, h->num_sms) ? MLA_PATH_PREFILL : MLA_PATH_DECODE;
   h->last_path = path;
@@ -244,12 +256,12 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     PrefillParams pp = {};
     pp.hidden = hidden_states; pp.positions = positions; pp.W_kva = W_kva; pp.gamma = gamma_kv;
     pp.W_kvb = W_kvb; pp.cos_t = cos_table; pp.sin_t = sin_table; pp.k_nope = k_nope;
-    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.out = lay; pp.c8 = c8; pp.status = h->status;
+    pp.value = value; pp.k_pe = k_pe; pp.latent = latent; pp.out = lay; pp.c8 = c8q; pp.status = h->status;
     pp.hidden_dim = h->cfg.hidden; pp.heads = h->cfg.num_heads; pp.s = s; pp.T = (int)T;
     pp.max_pos = h->cfg.max_pos; pp.eps = h->cfg.eps; pp.budget_ns = h->budget_ns;
     int launches = 0;
     cudaError_t e = prefill_launch(bf16, pp, h->num_sms, stream, &launches);
-    h->last_launches = launches;
+    h->last_launches += launches;
     if (e == cudaErrorNotSupported) return MLA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return MLA_OK;
@@ -272,7 +284,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
   }
   p.hidden = hidden_states; p.positions = positions; p.W_kva = W_kva; p.gamma = gamma_kv;
   p.W_kvb = W_kvb; p.cos_t = cos_table; p.sin_t = sin_table; p.k_nope = k_nope; p.value = value;
-  p.k_pe = k_pe; p.latent = latent; p.out = lay; p.c8 = c8; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
+  p.k_pe = k_pe; p.latent = latent; p.out = lay; p.c8 = c8q; p.partials = h->partials; p.nrm = h->nrm; p.counters = h->counters;
   p.status = h->status; p.hidden_dim = h->cfg.hidden; p.heads = h->cfg.num_heads; p.s = s;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps;
   p.budget_ns = h->budget_ns;
@@ -294,7 +306,7 @@ mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_st
                              const void* W_kvb, const float* cos_table, const float* sin_table,
                              void* k_nope, void* value, void* k_pe, cudaStream_t stream) {
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
-                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr},
+                k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr, nullptr},
                 stream);
 }
 
@@ -307,7 +319,7 @@ mla_status mla_kv_prolog_run_c8(mla_prolog_t h, int b, int s, const void* hidden
   if (!aligned16(k_scale) || !aligned16(v_scale) || !aligned16(kpe_scale)) return MLA_ERR_MISALIGNED;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
                 k_nope, value, k_pe, nullptr, OutLayout{nullptr, 0, 0},
-                C8Scales{k_scale, v_scale, kpe_scale}, stream);
+                C8Scales{k_scale, v_scale, kpe_scale, nullptr}, stream);
 }
 
 mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hidden_states,
@@ -323,7 +335,7 @@ mla_status mla_kv_prolog_run_paged(mla_prolog_t h, int b, int s, const void* hid
   if (!aligned16(slot_mapping)) return MLA_ERR_MISALIGNED;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
                 k_cache, v_cache, kpe_cache, nullptr,
-                OutLayout{slot_mapping, page_size, page_size * num_blocks}, C8Scales{nullptr, nullptr, nullptr},
+                OutLayout{slot_mapping, page_size, page_size * num_blocks}, C8Scales{nullptr, nullptr, nullptr, nullptr},
                 stream);
 }
 
@@ -334,7 +346,7 @@ mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hi
                                     cudaStream_t stream) {
   if (!latent) return MLA_ERR_INVALID_ARG;
   return run_kv(h, b, s, hidden_states, positions, W_kva, gamma_kv, nullptr, cos_table, sin_table,
-                nullptr, nullptr, k_pe, latent, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr},
+                nullptr, nullptr, k_pe, latent, OutLayout{nullptr, 0, 0}, C8Scales{nullptr, nullptr, nullptr, nullptr},
                 stream);
 }
 

@@ -210,11 +210,10 @@ __device__ __forceinline__ bool out_place(const OutLayout& L, int t, int s, unsi
   return true;
 }
 
-// int8 KV-cache code of x (the value the dtype output holds) at channel
-// scale `scale`: clamp(rint(x * (1 / scale)), -127, 127), each step one IEEE
-// fp32 operation.
-__device__ __forceinline__ uint32_t kv_code(float x, float scale) {
-  const float inv = __fdiv_rn(1.0f, scale);
+// int8 KV-cache code of x (the value the dtype output holds) given the
+// channel's reciprocal scale inv = 1 / scale: clamp(rint(x * inv), -127,
+// 127), each step one IEEE fp32 operation.
+__device__ __forceinline__ uint32_t kv_code(float x, float inv) {
   float r = rintf(__fmul_rn(x, inv));
   r = fminf(fmaxf(r, -127.f), 127.f);
   return (uint32_t)(uint8_t)(int8_t)(int)r;

@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   auto store_kpe = [&](size_t o, int j0, float a, float b, float c, float d) {
     if (p.c8.k) {
       int8_t* kp = static_cast<int8_t*>(p.k_pe) + o;
-      const float* sc = p.c8.kpe;
+      const float* sc = p.c8.inv + 2 * H * kNope;
       const T ra = E::from_f(a), rb = E::from_f(b), rc = E::from_f(c), rd = E::from_f(d);
       *reinterpret_cast<uint16_t*>(kp + j0) =
           (uint16_t)(kv_code(E::to_f(ra), sc[j0]) | (kv_code(E::to_f(rb), sc[j0 + 1]) << 8));
@@ -897,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const size_t o = (((size_t)ou * H + hh) * cnt + in) * kNope + ee;
     if (p.c8.k) {  // int8 KV cache: codes of the 8 dtype values
       const T* x = reinterpret_cast<const T*>(sO + r * pitchB + gi * 16);
-      const float* sc = (e < kNope ? p.c8.k : p.c8.v) + hh * kNope + ee;
+      const float* sc = p.c8.inv + (e < kNope ? 0 : H * kNope) + hh * kNope + ee;
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i >> 2] |= kv_code(E::to_f(x[i]), sc[i]) << (8 * (i & 3));
@@ -920,6 +920,26 @@ const void* kernel_for(int variant) {
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------- int8 KV cache
+namespace {
+__global__ void c8_reciprocals_kernel(const float* __restrict__ k, const float* __restrict__ v,
+                                      const float* __restrict__ kpe, float* __restrict__ inv, int nkv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < nkv) {
+    inv[i] = __fdiv_rn(1.0f, k[i]);
+    inv[nkv + i] = __fdiv_rn(1.0f, v[i]);
+  }
+  if (i < kRope) inv[2 * nkv + i] = __fdiv_rn(1.0f, kpe[i]);
+}
+}  // namespace
+
+cudaError_t c8_reciprocals_launch(const C8Scales& c8, int heads, cudaStream_t stream) {
+  const int nkv = heads * kNope;
+  const int n = nkv > kRope ? nkv : kRope;
+  c8_reciprocals_kernel<<<(n + 255) / 256, 256, 0, stream>>>(c8.k, c8.v, c8.kpe, c8.inv, nkv);
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------- weight packing
 // W_kva [hidden, 576] -> one contiguous tile per phase-A unit u = kc * 18 + nb

@@ -28,12 +28,17 @@ struct OutLayout {
 // int8 KV-cache outputs: per-channel fp32 scales of k_nope [H*128], value
 // [H*128] and k_pe [64]; k == null: outputs in the I/O dtype.  A code is
 // clamp(rint(x * (1 / scale)), -127, 127) of the value x the dtype output
-// would hold, in IEEE fp32 operations.
+// would hold, in IEEE fp32 operations.  The kernels read the reciprocals
+// from `inv` ([H*128] of k_nope, [H*128] of value, [64] of k_pe), which
+// c8_reciprocals_launch writes before them.
 struct C8Scales {
   const float* k;
   const float* v;
   const float* kpe;
+  float* inv;
 };
+// inv[c] = 1 / scale[c] (IEEE fp32 division) for the three scale vectors.
+cudaError_t c8_reciprocals_launch(const C8Scales& c8, int heads, cudaStream_t stream);
 
 // Fixed dimensions of the DeepSeek MLA KV prolog this library implements.
 constexpr int kRank = 512;         // kv_lora_rank

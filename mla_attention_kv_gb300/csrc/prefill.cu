@@ -408,9 +408,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             for (int k = 0; k < 16; ++k) {
               const T* e0 = reinterpret_cast<const T*>(&o[2 * k]);
               const T* e1 = reinterpret_cast<const T*>(&o[2 * k + 1]);
-              w[k] = kv_code(E::to_f(e0[0]), p.c8.kpe[4 * k]) | (kv_code(E::to_f(e0[1]), p.c8.kpe[4 * k + 1]) << 8) |
-                     (kv_code(E::to_f(e1[0]), p.c8.kpe[4 * k + 2]) << 16) |
-                     (kv_code(E::to_f(e1[1]), p.c8.kpe[4 * k + 3]) << 24);
+              const float4 iv = reinterpret_cast<const float4*>(p.c8.inv + 2 * H * kNope)[k];
+              w[k] = kv_code(E::to_f(e0[0]), iv.x) | (kv_code(E::to_f(e0[1]), iv.y) << 8) |
+                     (kv_code(E::to_f(e1[0]), iv.z) << 16) | (kv_code(E::to_f(e1[1]), iv.w) << 24);
             }
             uint4* dst = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.k_pe) + ((size_t)ou * cnt + in) * kRope);
 #pragma unroll
@@ -504,14 +504,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
               for (int i = 0; i < 16; ++i) o[i] = E::pack(__uint_as_float(x[h2][2 * i]), __uint_as_float(x[h2][2 * i + 1]));
               const int cc = c + h2;
               if (p.c8.k) {  // int8 KV cache: codes of the 32 dtype values
-                const float* sc = (cc < 4 ? p.c8.k : p.c8.v) + j * kNope + (cc & 3) * 32;
+                const float4* iv4 = reinterpret_cast<const float4*>(p.c8.inv + (cc < 4 ? 0 : H * kNope) +
+                                                                    j * kNope + (cc & 3) * 32);
                 uint32_t w[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                   const T* e0 = reinterpret_cast<const T*>(&o[2 * k]);
                   const T* e1 = reinterpret_cast<const T*>(&o[2 * k + 1]);
-                  w[k] = kv_code(E::to_f(e0[0]), sc[4 * k]) | (kv_code(E::to_f(e0[1]), sc[4 * k + 1]) << 8) |
-                         (kv_code(E::to_f(e1[0]), sc[4 * k + 2]) << 16) | (kv_code(E::to_f(e1[1]), sc[4 * k + 3]) << 24);
+                  const float4 iv = iv4[k];
+                  w[k] = kv_code(E::to_f(e0[0]), iv.x) | (kv_code(E::to_f(e0[1]), iv.y) << 8) |
+                         (kv_code(E::to_f(e1[0]), iv.z) << 16) | (kv_code(E::to_f(e1[1]), iv.w) << 24);
                 }
                 uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<int8_t*>(cc < 4 ? p.k_nope : p.value) + orow +
                                                      (cc & 3) * 32);
