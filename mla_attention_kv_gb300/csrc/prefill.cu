@@ -58,6 +58,11 @@ constexpr uint32_t kS2Base = kS1Stages * kS1Bytes;  // kv_b stages after both: [
 constexpr uint32_t kS2Bytes = 16384;        // kv_b stage: this CTA's half of [64 K x 256 N]
 constexpr int kS2Stages = 5;
 constexpr uint32_t kBarBase = kS2Base + kS2Stages * kS2Bytes;  // 229376
+// kv_b epilogue staging (last tile): [128 KB, 144 KB), 4 KB per epilogue
+// warp, past the normalised tile and before the kv_b ring
+constexpr uint32_t kStageBase = kA2Bytes;
+constexpr uint32_t kStageWarp = 32 * 128;
+static_assert(kStageBase + 4 * kStageWarp <= kS2Base, "staging between the A2 tile and the kv_b ring");
 constexpr uint32_t kGamBase = kBarBase + 512;                  // gamma [512], I/O dtype
 constexpr uint32_t kSmemBytes = kGamBase + 1024 + 1024;        // + alignment slack
 static_assert(kS0Base + kS0Stages * kS0Bytes <= kA2Bytes, "k_pe ring inside the A2 area");
@@ -481,9 +486,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) tc::arrive_cluster(lead(&sh->a2_ready));
       if (p.latent) continue;
-      // (c) per head: split into k_nope / value, head-major stores
+      // (c) per head: split into k_nope / value, head-major stores.  On the
+      // CTA's last tile the rows are staged through [kStageBase, +16 KB),
+      // which no copy touches any more once the compressed_kv stages are
+      // consumed (on earlier tiles the next tile's stages land there).
       T* kn = static_cast<T*>(p.k_nope);
       T* vv = static_cast<T*>(p.value);
+      const bool staged = it == iters - 1 && !p.c8.k;
       for (int j = 0; j < H; ++j) {
         const int b = j & 1;
         if (!pf_wait(bar(&sh->tfull[b]), uf[b] & 1, abort, budget, p.status)) { ok = false; break; }
@@ -496,6 +505,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           tc::ld32(lane_addr + b * 256 + c * 32, x[0]);
           tc::ld32(lane_addr + b * 256 + (c + 1) * 32, x[1]);
           tc::wait_ld();
+          if (staged) {
+            // the warp's 32 rows x 64 columns (128 B each) go through shared
+            // memory (16-byte slots swizzled by row), then out as 128-byte
+            // row segments, four rows per store instruction
+            unsigned char* stg = smem + kStageBase + (warp & 3) * kStageWarp;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int sl = h2 * 4 + v;
+                *reinterpret_cast<uint4*>(stg + lane * 128 + ((sl ^ (lane & 7)) << 4)) = make_uint4(
+                    E::pack(__uint_as_float(x[h2][8 * v + 0]), __uint_as_float(x[h2][8 * v + 1])),
+                    E::pack(__uint_as_float(x[h2][8 * v + 2]), __uint_as_float(x[h2][8 * v + 3])),
+                    E::pack(__uint_as_float(x[h2][8 * v + 4]), __uint_as_float(x[h2][8 * v + 5])),
+                    E::pack(__uint_as_float(x[h2][8 * v + 6]), __uint_as_float(x[h2][8 * v + 7])));
+              }
+            __syncwarp();
+            T* half = (c < 4 ? kn : vv) + (c & 3) * 32;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int rr = 4 * k + (lane >> 3), sl = lane & 7;
+              const unsigned long long orow_r = __shfl_sync(0xffffffffu, (unsigned long long)orow, rr);
+              const int live_r = __shfl_sync(0xffffffffu, live ? 1 : 0, rr);
+              const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((sl ^ (rr & 7)) << 4));
+              if (live_r) *reinterpret_cast<uint4*>(half + orow_r + sl * 8) = val;
+            }
+            __syncwarp();  // the slots are rewritten by the next column pair
+            continue;
+          }
           if (live) {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
