@@ -475,6 +475,22 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------ main
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value of x over the ranks: the job's time is its slowest
+    rank's (every rank runs the same replicated work)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput of N independent replicas (weak scaling): the
+    tokens all ranks processed over the slowest rank's time."""
+    return tokens_per_step * steps * world / (ms / 1e3)
+
+
 def run_gpu(args, wl, rank, world, dev):
     from mla_attention_kv_gb300 import build as BLD
     if rank == 0:
@@ -523,10 +539,7 @@ def run_gpu(args, wl, rank, world, dev):
         calls = [(events[a].elapsed_time(events[b]), Ts) for a, b, Ts in intervals]
         # with an L2 flush between calls, the flush is not part of the work
         ms = sum(c for c, _ in calls) if getattr(wl, "flush", None) is not None else region_ms
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, world, dev)
         return ms, region_ms, calls, clk, launches
 
     # timed region: exactly K steps (graph replays) between CUDA events on the launching stream
@@ -547,10 +560,7 @@ def run_gpu(args, wl, rank, world, dev):
         h2d, d2h = wl.e2e_step(stream)
     torch.cuda.synchronize(dev)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     return dict(ms=ms, region_ms=region_ms, calls=calls, clk=clk, launches=total_launches,
                 e2e_s=e2e_s, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h, host_per_step=host_per_step,
                 ms_eager=ms_e, calls_eager=calls_e, clk_eager=clk_e)
@@ -619,8 +629,7 @@ def main():
     dev = torch.device("cuda", local)
     r = run_gpu(args, wl, rank, world, dev)
 
-    tokens = wl.tokens_per_step * args.steps * world
-    value = tokens / (r["ms"] / 1e3)
+    value = job_tokens_per_s(wl.tokens_per_step, args.steps, world, r["ms"])
     peaks, peak_kind = measured_peaks()
     calls = r["calls"]
     Tlist = [T for _, Ts in calls for T in Ts]
@@ -674,11 +683,12 @@ def main():
         "roofline": roof,
         "gpu_launches": r["launches"],
         "clocks": r["clk"],
-        "e2e": {"value": wl.tokens_per_step * r["e2e_steps"] * world / r["e2e_s"], "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(wl.tokens_per_step, r["e2e_steps"], world, r["e2e_s"] * 1e3),
+                "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
     ce = r["calls_eager"]
-    line["eager"] = {"value": tokens / (r["ms_eager"] / 1e3), "ms_per_step": r["ms_eager"] / args.steps,
+    line["eager"] = {"value": job_tokens_per_s(wl.tokens_per_step, args.steps, world, r["ms_eager"]), "ms_per_step": r["ms_eager"] / args.steps,
                      "mean_call_us": 1e3 * sum(c for c, _ in ce) / len(ce), "clocks": r["clk_eager"],
                      "note": "the same steps launched call by call through the binding (no CUDA graph)"}
     if len(wl.points) > 1:
