@@ -207,7 +207,6 @@ struct W8SmallPlan {
   int nblk_b1, nblk_b;  // 128-column blocks of q_b, of q_b + kv_b
   int grid_b;           // CTAs of the q_b / kv_b kernel
   int* units;           // device: [grid_b + 1] offsets, then block ids (workspace)
-  int max_units;        // longest per-CTA list
 };
 
 struct W8Params {

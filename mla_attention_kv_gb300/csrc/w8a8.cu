@@ -1176,7 +1176,7 @@ void small_plan(int hidden, int q_rank, int heads, int num_sms, W8SmallPlan* pl)
 
 // Longest-processing-time-first assignment of the q_b / kv_b blocks (cost:
 // boxes per block) to the back kernel's CTAs: [grid + 1] offsets, then ids.
-std::vector<int> small_units(int q_rank, int heads, const W8SmallPlan& pl, int* max_units) {
+std::vector<int> small_units(int q_rank, int heads, const W8SmallPlan& pl) {
   int bw, brows, nbox0, nbox1, kpad;
   back_geometry(q_rank, heads * (kNope + kRope), &bw, &brows, &nbox0, &kpad);
   back_geometry(kRank, heads * kHeadCols, &bw, &brows, &nbox1, &kpad);
@@ -1200,11 +1200,9 @@ std::vector<int> small_units(int q_rank, int heads, const W8SmallPlan& pl, int* 
   }
   std::vector<int> t(G + 1 + pl.nblk_b);
   int off = 0;
-  *max_units = 0;
   for (int c = 0; c < G; ++c) {
     t[c] = off;
     for (int b : lists[c]) t[G + 1 + off++] = b;
-    if ((int)lists[c].size() > *max_units) *max_units = (int)lists[c].size();
   }
   t[G] = off;
   return t;
@@ -1246,8 +1244,7 @@ cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int
   cudaError_t e = cudaMemset(w.acc1, 0, (size_t)max_tokens * (q_rank + kNa) * 4);
   if (e == cudaSuccess) e = cudaMemset(w.readers, 0, 256);
   if (e != cudaSuccess) return e;
-  int mu = 0;
-  const std::vector<int> t = small_units(q_rank, heads, plan, &mu);
+  const std::vector<int> t = small_units(q_rank, heads, plan);
   return cudaMemcpy(plan.units, t.data(), t.size() * sizeof(int), cudaMemcpyHostToDevice);
 }
 
