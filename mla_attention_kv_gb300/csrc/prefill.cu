@@ -438,57 +438,45 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       ++uf[0];
       tc::fence_after_sync();
       {
-        // two TMEM loads in flight per wait (the sum keeps its column order)
         float ss = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kRank / 32; c += 2) {
-          uint32_t x[2][32];
-          tc::ld32(lane_addr + c * 32, x[0]);
-          tc::ld32(lane_addr + (c + 1) * 32, x[1]);
+        for (int c = 0; c < kRank / 32; ++c) {
+          uint32_t x[32];
+          tc::ld32(lane_addr + c * 32, x);
           tc::wait_ld();
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float v = __uint_as_float(x[h2][j]);
-              ss += v * v;
-            }
+          for (int j = 0; j < 32; ++j) {
+            const float v = __uint_as_float(x[j]);
+            ss += v * v;
+          }
         }
         const float inv = 1.0f / sqrtf(ss / (float)kRank + p.eps);
         unsigned char* a2row = smem + r * 128;
-#pragma unroll 1
-        for (int c2 = 0; c2 < kRank / 32; c2 += 2) {
-          uint32_t xx[2][32];
-          tc::ld32(lane_addr + c2 * 32, xx[0]);
-          tc::ld32(lane_addr + (c2 + 1) * 32, xx[1]);
+        for (int c = 0; c < kRank / 32; ++c) {
+          uint32_t x[32];
+          tc::ld32(lane_addr + c * 32, x);
           tc::wait_ld();
+          uint32_t o[16];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = c2 + h2;
-            const uint32_t* x = xx[h2];
-            uint32_t o[16];
+          for (int j = 0; j < 32; j += 2) {
+            const int col = c * 32 + j;
+            o[j / 2] = E::pack(__uint_as_float(x[j]) * inv * E::to_f(gam[col]),
+                               __uint_as_float(x[j + 1]) * inv * E::to_f(gam[col + 1]));
+          }
+          if (p.latent) {  // latent-cache variant: the normalised row is an output
+            if (live) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.latent) + (size_t)t * kRank + c * 32);
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const int col = c * 32 + j;
-              o[j / 2] = E::pack(__uint_as_float(x[j]) * inv * E::to_f(gam[col]),
-                                 __uint_as_float(x[j + 1]) * inv * E::to_f(gam[col + 1]));
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
             }
-            if (p.latent) {  // latent-cache variant: the normalised row is an output
-              if (live) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.latent) + (size_t)t * kRank + c * 32);
+            continue;
+          }
+          // K-chunk c/2 (64 columns), 16-byte chunks (c%2)*4 .. +3 of this row
+          unsigned char* chunk = a2row + (c >> 1) * 16384;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-              }
-              continue;
-            }
-            // K-chunk c/2 (64 columns), 16-byte chunks (c%2)*4 .. +3 of this row
-            unsigned char* chunk = a2row + (c >> 1) * 16384;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int lc = (c & 1) * 4 + v;
-              *reinterpret_cast<uint4*>(chunk + ((lc ^ (r & 7)) << 4)) =
-                  make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-            }
+          for (int v = 0; v < 4; ++v) {
+            const int lc = (c & 1) * 4 + v;
+            *reinterpret_cast<uint4*>(chunk + ((lc ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
           }
         }
       }
