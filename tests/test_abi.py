@@ -83,3 +83,25 @@ def test_building_block_shape_checks(L):
     assert L.mla_w8a8_quant_rows(None, 4, 12, None, None, None) == 2
     assert L.mla_w8a8_quant_rows(None, 0, 16, None, None, None) == 0
     assert L.mla_w8a8_quant_rows(None, -1, 16, None, None, None) == 1
+
+
+def test_variant_entries_reject_bad_arguments(L):
+    """The latent, paged and int8-cache entries check their own arguments
+    before touching the handle or the device."""
+    P = ctypes.c_void_p
+    fake = P(16)  # never dereferenced: every call below fails its argument check first
+    # latent: a null latent output
+    assert L.mla_kv_prolog_run_latent(None, 1, 1, *([None] * 8), None) == 1
+    # paged: null slot mapping, non-positive page size or block count, slot-count overflow
+    args = [fake] * 7
+    assert L.mla_kv_prolog_run_paged(fake, 1, 1, *args, None, 16, 4, fake, fake, fake, None) == 1
+    assert L.mla_kv_prolog_run_paged(fake, 1, 1, *args, fake, 0, 4, fake, fake, fake, None) == 1
+    assert L.mla_kv_prolog_run_paged(fake, 1, 1, *args, fake, 16, 0, fake, fake, fake, None) == 1
+    assert L.mla_kv_prolog_run_paged(fake, 1, 1, *args, fake, 1 << 16, 1 << 16, fake, fake, fake, None) == 1
+    # paged: a slot mapping that is not 16-byte aligned
+    assert L.mla_kv_prolog_run_paged(fake, 1, 1, *args, P(20), 16, 4, fake, fake, fake, None) == 4
+    # int8 cache: null or misaligned scale vectors
+    assert L.mla_kv_prolog_run_c8(fake, 1, 1, *([fake] * 7), None, fake, fake, fake, fake, fake, None) == 1
+    assert L.mla_kv_prolog_run_c8(fake, 1, 1, *([fake] * 7), P(20), fake, fake, fake, fake, fake, None) == 4
+    assert B.STATUS_NAMES[10] == "MLA_ERR_BAD_SLOT"
+    assert b"slot" in L.mla_status_string(10)
