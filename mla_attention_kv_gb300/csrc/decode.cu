@@ -30,6 +30,13 @@
 //   phase B  kv_b_proj split-N over the resident W_kvb slice; the epilogue
 //            does the reshape/split (step 5) and the head-major stores
 //            (step 7) straight from the accumulators.
+// Consecutive launches are chained with programmatic dependent launch: the
+// next call's CTAs take each SM as this call's CTA there exits and copy
+// their packed weights before waiting for this call to finish.
+// Output options (DecodeParams): the latent-cache variant stops after phase
+// R (the owner CTA of each row writes the normalised row); a slot mapping
+// places rows in a paged cache; per-channel scales turn the stores into
+// int8 codes.
 #include <type_traits>
 #include <utility>
 

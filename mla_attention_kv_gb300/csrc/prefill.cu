@@ -10,21 +10,23 @@
 // outputs touches global memory.
 //
 // Warp roles (192 threads):
-//   warp 0   TMA producer: hidden tile [128 x 64] and W_kva / W_kvb boxes
-//            [64 x 64], 128-byte swizzled, into shared-memory rings: 6
-//            stages for the k_pe pass, 2 for the compressed_kv pass, 3 for
-//            kv_b (all three reuse the same 224 KB at different times).
-//   warp 1   allocates 512 TMEM columns; one thread issues every MMA.
+//   warp 0   TMA producer: hidden tile [128 x 64] and this CTA's half of
+//            every weight tile, 128-byte swizzled, into shared-memory rings:
+//            5 stages for the k_pe pass, 3 for the compressed_kv pass, 5 for
+//            kv_b (the rings reuse the same 224 KB at different times).
+//   warp 1   allocates 512 TMEM columns (both CTAs of the pair); one thread
+//            of the even CTA issues every MMA of the pair.
 //   warps 2-5 epilogue; warp w owns TMEM lanes 32*(w%4) .. +31, i.e. token
 //            rows of the tile, one row per thread.
-// CTAs run in clusters of two neighbouring tiles: every weight box is
-// fetched from L2 once per cluster and multicast into both CTAs' shared
-// memory (each CTA issues half of the boxes), which halves the L2 traffic
-// of the weight stream that bounds this kernel.  A stage is refilled only
-// when both CTAs' MMAs have released it (multicast tcgen05.commit).
+// CTAs run in pairs (clusters of two neighbouring tiles) on the 2-SM MMA
+// (tcgen05.mma.cta_group::2, M = 256): each CTA holds its own 128 token rows
+// and half of the N columns of every weight tile, and both CTAs' copies
+// complete on the even CTA's barriers.
 // Per tile:
-//   (a) k_pe pass: C[:, 512:576] = X * W_kva[:, 512:576] (N = 64), drained
-//       by the epilogue: RoPE (de-interleave + rotate_half) -> k_pe.
+//   (a) k_pe pass: C[:, 512:576] = X * W_kva[:, 512:576], drained by the
+//       epilogue: RoPE (de-interleave + rotate_half) -> k_pe.  When CTA
+//       pairs are left over after every tile has its own CTA, those pairs
+//       run pass (a) for all tiles and the tile CTAs skip it.
 //   (b) compressed_kv pass: C[:, 0:512] as two N = 256 MMAs per K step,
 //       filling all 512 TMEM columns; the epilogue reads each row twice
 //       (sum of squares, then normalise * gamma) and writes the normalised
@@ -33,9 +35,14 @@
 //   (c) kv_b: one N = 256 MMA tile per head (128 k_nope + 128 value
 //       columns), K = 512 from the shared-memory tile, accumulators
 //       double-buffered in TMEM so head j+1 runs while the epilogue stores
-//       head j as k_nope[b, j, s, :] / value[b, j, s, :].
+//       head j as k_nope[b, j, s, :] / value[b, j, s, :] (on the CTA's last
+//       tile through a shared-memory staging area, so that each store
+//       instruction writes whole 128-byte row segments).
+// Output options (PrefillParams): the latent-cache variant stops after (b)
+// and writes the normalised rows; a slot mapping places rows in a paged
+// cache; per-channel scales turn the stores into int8 codes.
 // The fp32 accumulator width is 512 TMEM columns, which is why the 576
-// kv_a columns take two passes (the second reads the hidden tile from L2).
+// kv_a columns take two passes.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
