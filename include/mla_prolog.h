@@ -239,7 +239,8 @@ mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_
                                cudaStream_t stream);
 
 /* Synchronise `stream`, read the device status word of the handle, clear
- * it (and reset the device barrier counters if a wait timed out) and
+ * it (and, if a wait timed out, reset the device barrier counters and the
+ * W8A8 accumulator rows and counters) and
  * return MLA_OK, MLA_ERR_BAD_POSITION, MLA_ERR_DEVICE_TIMEOUT or
  * MLA_ERR_BAD_SLOT (in that order of precedence, for the faults recorded
  * since the last call). */

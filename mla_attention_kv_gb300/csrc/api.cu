@@ -213,6 +213,13 @@ mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
     // clear the status word and, after a timeout, the barrier counters
     e = cudaMemset(h->ws, 0, 256);
     if (e != cudaSuccess) return cuda_fail(e, "clear status");
+    if ((st & kStatusTimeout) && h->cfg.quant == MLA_QUANT_W8A8) {
+      // a chain that gave up may have left partial sums in the accumulator
+      // rows, which every call expects zeroed, and a reader count behind
+      e = cudaMemset(h->w8.acc1, 0, (size_t)h->cfg.max_tokens * (h->cfg.q_lora_rank + kNa) * 4);
+      if (e == cudaSuccess) e = cudaMemset(h->w8.readers, 0, 256);
+      if (e != cudaSuccess) return cuda_fail(e, "reset W8A8 workspace");
+    }
   }
   if (st & kStatusBadPosition) return MLA_ERR_BAD_POSITION;
   if (st & kStatusTimeout) return MLA_ERR_DEVICE_TIMEOUT;
