@@ -30,7 +30,11 @@ _lock = threading.Lock()
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into _build/liboracle.so (OpenMP when available)."""
+    """Compile oracle.c into _build/liboracle.so (OpenMP when available).
+    With MLA_ORACLE_SO set, that prebuilt library is used instead (the
+    mutation tests load deliberately broken copies this way)."""
+    if os.environ.get("MLA_ORACLE_SO"):
+        return os.environ["MLA_ORACLE_SO"]
     src = os.path.join(_HERE, "oracle.c")
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(src):
         return _SO

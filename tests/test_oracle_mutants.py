@@ -1,0 +1,54 @@
+"""The pins hold the oracle to the mathematics: each of these planted
+mistakes, compiled into a copy of oracle.c, makes the pin suite fail
+(the mutant library is loaded through MLA_ORACLE_SO in a child pytest)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "rotate_half sign": ("double rot = (i < half) ? -xd[i + half] : xd[i - half];",
+                         "double rot = (i < half) ? xd[i + half] : xd[i - half];"),
+    "eps outside the sqrt": ("double denom = sqrt(ss / (double)n + eps);",
+                             "double denom = sqrt(ss / (double)n) + eps;"),
+    "dropped K term": ("for (int64_t k = 0; k < K; ++k) acc += x[k] * W[k * N + n];",
+                       "for (int64_t k = 1; k < K; ++k) acc += x[k] * W[k * N + n];"),
+    "value from the k_nope columns": ("value[hh * d->vdim + i] = KV[hh * hd + d->nope + i];",
+                                      "value[hh * d->vdim + i] = KV[hh * hd + i];"),
+    "k_pe slice off by one": ("const double* kpe = C + r;", "const double* kpe = C + r + 1;"),
+    "no de-interleave": ("xd[j] = x[2 * j];\n    xd[half + j] = x[2 * j + 1];",
+                         "xd[j] = x[j];\n    xd[half + j] = x[half + j];"),
+    "quantisation truncates": ("float r = rintf(y);", "float r = truncf(y);"),
+}
+
+
+def run_pins(src_text, tmp_path):
+    """Compile src_text as the oracle and run the pin suite on it in a child pytest."""
+    c = tmp_path / "oracle_variant.c"
+    c.write_text(src_text)
+    so = tmp_path / "liboracle_variant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fno-fast-math", "-ffp-contract=off", "-shared", "-fPIC",
+                    str(c), "-lm", "-o", str(so)], check=True, capture_output=True)
+    env = dict(os.environ, MLA_ORACLE_SO=str(so))
+    return subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                           os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+
+
+def test_unmutated_copy_passes(tmp_path):
+    r = run_pins(open(SRC).read(), tmp_path)
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_the_pins(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    r = run_pins(src.replace(old, new), tmp_path)
+    # a pin assertion failed (not a collection or import error)
+    assert r.returncode == 1 and " failed" in r.stdout, f"{name}: the pins did not catch it\n{r.stdout[-2000:]}"
