@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_abi_version_and_strings(L):
     assert L.mla_abi_version() == 1
-    for code in range(10):
+    for code in range(11):
         assert L.mla_status_string(code).decode() not in ("", "unknown status")
     assert L.mla_status_string(99).decode() == "unknown status"
 
