@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 
 from mla_attention_kv_gb300 import inputs as I  # noqa: E402
 
-# mma.sync m16n8k32 s8 throughput measured on this machine's GB300 (the
+# mma.sync m16n8k32 s8 throughput measured on a GB300 (the
 # tcgen05 int8 kind does not exist on sm_103a); see profiles/mma_sync_rates.md
 INT8_MMA_SYNC_TOPS = 148.8
 
