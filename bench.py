@@ -19,8 +19,9 @@ Timing rules kept here:
     copied in and the three outputs copied back every step (wall clock).
 
 ``--impl reference`` times the CPU oracle (the plain fp64 definition of
-the prolog) on a bounded sample of the same workload; there is no other
-reference implementation of this path.
+the prolog) on the host cores: W untimed and K timed steps, each the whole
+workload step or a bounded sample of it (``oracle_steps``); there is no
+other reference implementation of this path.
 """
 from __future__ import annotations
 
@@ -95,8 +96,7 @@ class DecodeSweep:
         self.cos = base["cos"].to(dev)
         self.sin = base["sin"].to(dev)
         self.pt = []
-        for i, (b, s) in enumerate(self.points):
-            inp = I.kv_inputs(self.cfg, b, s, I.seed_for(1, i))
+        for (b, s), inp in zip(self.points, self.host_inputs()):
             self.pt.append(dict(b=b, s=s, hidden=inp["hidden"].to(dev),
                                 positions=inp["positions"].to(dev),
                                 hidden_h=inp["hidden"].pin_memory(),
@@ -182,26 +182,34 @@ class DecodeSweep:
                 d2h += v.numel() * v.element_size()
         return h2d, d2h
 
-    # CPU oracle on a bounded sample
-    def cpu_sample(self, seconds):
+    def host_inputs(self):
+        """The seeded host inputs of every sweep point (built once)."""
+        if getattr(self, "_host", None) is None:
+            self._host = [I.kv_inputs(self.cfg, b, s, I.seed_for(1, i)) for i, (b, s) in enumerate(self.points)]
+        return self._host
+
+    # CPU oracle on a bounded sample: like a step, one oracle call per sweep
+    # point, each on at most m of the point's token rows
+    def sample_max(self):
+        return max(b * s for b, s in self.points)
+
+    def sample_rows(self, m):
+        return sum(min(b * s, m) for b, s in self.points)
+
+    def oracle_step(self, k, m, nthreads):
+        """Oracle on the k-th bounded sample of the sweep: every point, rows
+        k*m .. k*m + m - 1 of it (mod b*s).  Returns the rows computed."""
         import oracle
-        oracle.build()
-        nt = os.cpu_count() or 1
         done = 0
-        t0 = time.perf_counter()
-        pts = 0
-        while True:
-            i = pts % len(self.points)
-            b, s = self.points[i]
-            inp = I.kv_inputs(self.cfg, b, s, I.seed_for(1, i))
-            oracle.kv_prolog(inp, nthreads=nt)
-            done += b * s
-            pts += 1
-            if time.perf_counter() - t0 >= seconds:
-                break
-        el = time.perf_counter() - t0
-        return done / el, min(nt, oracle.max_threads()), \
-            f"{pts} sweep points in order ({done} token rows) of the V2-Lite decode sweep, fp64 oracle, {el:.1f} s"
+        for inp, (b, s) in zip(self.host_inputs(), self.points):
+            rows = sorted({(k * m + j) % (b * s) for j in range(min(m, b * s))})
+            oracle.kv_prolog(inp, rows=rows, nthreads=nthreads)
+            done += len(rows)
+        return done
+
+    def sample_text(self, m):
+        return (f"every point of the V2-Lite decode sweep per step, at most {m} of its token rows each "
+                f"({self.sample_rows(m)} of {self.tokens_per_step} rows), fp64 oracle")
 
 
 class SingleCall:
@@ -264,12 +272,17 @@ class SingleCall:
             out = H * 256 + 64 + 4 * (H * 256 + 64) / max(T, 1)  # int8 codes; the scales once per call
         return self.weight_bytes() + T * (2 * c["hidden"] + 4 + 2 * 64 * 4 + out)
 
+    def host_inputs(self):
+        """The seeded host inputs of the call (built once)."""
+        if getattr(self, "host", None) is None:
+            gen = I.w8a8_inputs if self.w8 else I.kv_inputs
+            self.host = gen(self.cfg, self.b, self.s, self.seed, self.positions)
+        return self.host
+
     def setup(self, dev):
         from mla_attention_kv_gb300 import binding as B
         self.B = B
-        gen = I.w8a8_inputs if self.w8 else I.kv_inputs
-        inp = gen(self.cfg, self.b, self.s, self.seed, self.positions)
-        self.host = inp
+        inp = self.host_inputs()
         self.d = B.to_device(inp, dev)
         self.R = 1
         self.m = B.MLAProlog(self.cfg, self.T)
@@ -379,23 +392,24 @@ class SingleCall:
             d2h += v.numel() * v.element_size()
         return self.hidden_h.numel() * 2 + self.positions_h.numel() * 4, d2h
 
-    def cpu_sample(self, seconds):
+    def sample_max(self):
+        return self.T
+
+    def sample_rows(self, n):
+        return min(n, self.T)
+
+    def oracle_step(self, k, n, nthreads):
+        """Oracle on the k-th bounded sample of the call: token rows
+        k*n .. k*n + n - 1 (mod T) in one oracle call.  Returns the rows."""
         import oracle
-        oracle.build()
-        nt = os.cpu_count() or 1
-        rows_per = max(nt, 8)
-        done, t0, k = 0, time.perf_counter(), 0
         fn = oracle.w8a8_prolog if self.w8 else (oracle.kv_latent if self.latent else oracle.kv_prolog)
-        while True:
-            rows = [(k * rows_per + i) % self.T for i in range(rows_per)]
-            fn(self.host, rows=sorted(set(rows)), nthreads=nt)
-            done += len(set(rows))
-            k += 1
-            if time.perf_counter() - t0 >= seconds:
-                break
-        el = time.perf_counter() - t0
-        return done / el, min(nt, oracle.max_threads()), \
-            f"{done} token rows of {self.name} (fp64 oracle, per-call weight promotion included), {el:.1f} s"
+        rows = sorted({(k * n + i) % self.T for i in range(n)})
+        fn(self.host_inputs(), rows=rows, nthreads=nthreads)
+        return len(rows)
+
+    def sample_text(self, n):
+        return (f"{n} token rows of {self.name} per step (consecutive, cyclic), fp64 oracle, "
+                f"per-call weight promotion included")
 
 
 def _single(name, cfg, b, s, positions, path_name, seed, latent=False, paged=None, c8=False):
@@ -464,6 +478,59 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_steps(wl, steps, warmup, seconds):
+    """Time the CPU oracle on the host cores: `warmup` untimed steps, then
+    exactly `steps` timed steps, each a bounded sample of the workload
+    (`wl.oracle_step(k, n)`, whose size parameter n gives
+    `wl.sample_rows(n)` token rows; the largest n is the whole step) sized
+    so that all warmup + steps take about `seconds`.  Two untimed
+    calibration steps at sizes n1 < n2 separate the oracle's fixed cost per
+    step (its calls' weight promotion) from its cost per row.  Returns
+    (tokens/s, threads used, description of the sample, size parameter,
+    timed seconds)."""
+    import oracle
+    oracle.build()
+    nt = os.cpu_count() or 1
+    wl.host_inputs()
+    steps = max(1, steps)
+    top = wl.sample_max()
+
+    def timed(k, n):
+        t0 = time.perf_counter()
+        wl.oracle_step(k, n, nt)
+        return time.perf_counter() - t0
+
+    n1 = 1
+    while n1 < top and wl.sample_rows(n1) < max(nt, 8):
+        n1 *= 2
+    n1 = min(n1, top)
+    n2 = min(top, 16 * n1)
+    r1, r2 = wl.sample_rows(n1), wl.sample_rows(n2)
+    timed(0, n1)  # first touch of the oracle's buffers, not counted
+    t1 = timed(1, n1)
+    t2 = timed(2, n2) if r2 > r1 else t1
+    per_row = (t2 - t1) / (r2 - r1) if r2 > r1 and t2 > t1 else t2 / r2
+    fixed = max(0.0, t1 - per_row * r1)
+    # the largest size whose predicted step time fits the share of `seconds`
+    target = seconds / (steps + warmup)
+    lo, hi = 1, top
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if fixed + per_row * wl.sample_rows(mid) <= target:
+            lo = mid
+        else:
+            hi = mid - 1
+    n = lo
+    for k in range(warmup):
+        wl.oracle_step(k, n, nt)
+    done = 0
+    t0 = time.perf_counter()
+    for k in range(steps):
+        done += wl.oracle_step(warmup + k, n, nt)
+    el = time.perf_counter() - t0
+    return done / el, min(nt, oracle.max_threads()), wl.sample_text(n), n, el
 
 
 def measured_peaks():
@@ -593,7 +660,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="decode_sweep", choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="seconds of the oracle's steps in the cpu_baseline leg")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="seconds of the oracle's warm-up + timed steps under --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -609,7 +679,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        v, cores, sample = wl.cpu_sample(min(args.cpu_seconds, 20.0))
+        v, cores, sample, n, el = oracle_steps(wl, args.steps, args.warmup, args.ref_seconds)
+        sample += f"; {args.warmup} untimed + {args.steps} timed steps, {el:.1f} s timed"
         line = {"metric": "tokens/s", "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": wl.tokens_per_step / v * 1e3, "higher_is_better": True,
@@ -702,7 +773,8 @@ def main():
         line["per_point"] = detail
         line["per_point_timing"] = "CUDA events around each call of the eager pass"
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, sample = wl.cpu_sample(args.cpu_seconds)
+        v, cores, sample, n, el = oracle_steps(wl, 4, 1, args.cpu_seconds)
+        sample += f"; 1 untimed + 4 timed steps, {el:.1f} s timed"
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
