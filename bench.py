@@ -54,6 +54,31 @@ def log(*a):
 
 
 # ------------------------------------------------------------------ workload
+def carve(specs, device, pin=False):
+    """One buffer holding tensors of the (shape, dtype) `specs` back to back,
+    each at a 256-byte boundary (the C ABI wants 16-byte aligned pointers),
+    so that a step's inputs or outputs cross between host and device in one
+    copy.  Returns (buffer, views); pin=True puts the buffer in page-locked
+    host memory."""
+    offs, total = [], 0
+    for shape, dt in specs:
+        n = math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        offs.append((total, n))
+        total += -(-n // 256) * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [buf[o:o + n].view(dt).view(shape) for (o, n), (shape, dt) in zip(offs, specs)]
+    return buf, views
+
+
+def carve_dicts(dicts, device, pin=False):
+    """carve() for a list of dicts of tensors (any device, "meta" included):
+    returns (buffer, list of dicts of views with the same keys, shapes and
+    dtypes)."""
+    buf, views = carve([(tuple(v.shape), v.dtype) for d in dicts for v in d.values()], device, pin)
+    it = iter(views)
+    return buf, [{k: next(it) for k in d} for d in dicts]
+
+
 class DecodeSweep:
     name = "v2lite_kv_prolog_decode_sweep"
 
@@ -95,12 +120,6 @@ class DecodeSweep:
             self.wcopies.append({k: base[k].to(dev) for k in ("W_kva", "gamma_kv", "W_kvb")})
         self.cos = base["cos"].to(dev)
         self.sin = base["sin"].to(dev)
-        self.pt = []
-        for (b, s), inp in zip(self.points, self.host_inputs()):
-            self.pt.append(dict(b=b, s=s, hidden=inp["hidden"].to(dev),
-                                positions=inp["positions"].to(dev),
-                                hidden_h=inp["hidden"].pin_memory(),
-                                positions_h=inp["positions"].pin_memory()))
         # one handle per weight copy, each with its packed snapshot (a serving
         # engine packs every layer's weights once at load time)
         tmax = max(b * s for b, s in self.points)
@@ -111,10 +130,26 @@ class DecodeSweep:
             self.ms.append(m)
         torch.cuda.synchronize(dev)
         self.m = self.ms[0]
-        self.out = [self.m.alloc_outputs(p["b"], p["s"], dev) for p in self.pt]
-        self.out_h = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in o.items()}
-                      for o in self.out]
+        self.stage_io(dev, [self.m.alloc_outputs(b, s, "meta") for b, s in self.points])
+        torch.cuda.synchronize(dev)
         self.calls = 0
+
+    def stage_io(self, dev, outs, pin=True):
+        """Every point's hidden rows and positions in one device buffer
+        `in_d`, every point's outputs (shapes of the dicts `outs`) in one
+        device buffer `out_d`, each with a host twin (`in_h`, `out_h`) of the
+        same layout; the calls use views into the device buffers, so that an
+        e2e step moves its inputs and outputs in one copy each."""
+        ins = [{"hidden": inp["hidden"], "positions": inp["positions"]} for inp in self.host_inputs()]
+        self.in_h, views_h = carve_dicts(ins, "cpu", pin)
+        self.in_d, views_d = carve_dicts(ins, dev)
+        for src, dst in zip(ins, views_h):
+            for k in src:
+                dst[k].copy_(src[k])
+        self.in_d.copy_(self.in_h)
+        self.pt = [dict(b=b, s=s, **v) for (b, s), v in zip(self.points, views_d)]
+        self.out_d, self.out = carve_dicts(outs, dev)
+        self.out_h, _ = carve_dicts(outs, "cpu", pin)
 
     def _run(self, i, stream):
         p = self.pt[i]
@@ -171,16 +206,14 @@ class DecodeSweep:
         return self.graph_launches
 
     def e2e_step(self, stream):
-        h2d = d2h = 0
-        for i, p in enumerate(self.pt):
-            p["hidden"].copy_(p["hidden_h"], non_blocking=True)
-            p["positions"].copy_(p["positions_h"], non_blocking=True)
-            h2d += p["hidden_h"].numel() * 2 + p["positions_h"].numel() * 4
+        """One step from host buffers: every point's inputs in one
+        host-to-device copy, the 16 calls, every output in one device-to-host
+        copy (pinned host memory; bytes are the copied buffers')."""
+        self.in_d.copy_(self.in_h, non_blocking=True)
+        for i in range(len(self.pt)):
             self._run(i, stream)
-            for k, v in self.out[i].items():
-                self.out_h[i][k].copy_(v, non_blocking=True)
-                d2h += v.numel() * v.element_size()
-        return h2d, d2h
+        self.out_h.copy_(self.out_d, non_blocking=True)
+        return self.in_h.numel(), self.out_h.numel()
 
     def host_inputs(self):
         """The seeded host inputs of every sweep point (built once)."""
@@ -305,9 +338,9 @@ class SingleCall:
             else:
                 slot = table[bi, si // page] * page + si % page
             self.slots = slot.to(torch.int32).to(dev)
-            self.out = self.m.alloc_paged_caches(nblk, page, dev)
+            out = self.m.alloc_paged_caches(nblk, page, "meta")
         elif self.latent:
-            self.out = self.m.alloc_latent_outputs(self.b, self.s, dev)
+            out = self.m.alloc_latent_outputs(self.b, self.s, "meta")
         elif self.c8:
             g = torch.Generator().manual_seed(self.seed)
             H = self.cfg["num_heads"]
@@ -315,12 +348,11 @@ class SingleCall:
             self.scales = dict(k=(0.01 + 0.01 * torch.rand(H * 128, generator=g)).to(dev),
                                v=(0.01 + 0.01 * torch.rand(H * 128, generator=g)).to(dev),
                                kpe=(hi / 2 + hi / 2 * torch.rand(64, generator=g)).to(dev))
-            self.out = self.m.alloc_c8_outputs(self.b, self.s, dev)
+            out = self.m.alloc_c8_outputs(self.b, self.s, "meta")
         else:
-            self.out = self.m.alloc_outputs(self.b, self.s, dev)
-        self.hidden_h = inp["hidden"].pin_memory()
-        self.positions_h = inp["positions"].pin_memory()
-        self.out_h = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in self.out.items()}
+            out = self.m.alloc_outputs(self.b, self.s, "meta")
+        self.stage_io(dev, out)
+        torch.cuda.synchronize(dev)
         # L2 flush between timed calls when the inputs fit in L2: a 2x L2 buffer
         # is written, then another 2x L2 buffer is read, so that none of the
         # call's data is in L2 and no dirty line is left to be written back
@@ -331,6 +363,23 @@ class SingleCall:
             self.flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
             self.flush_rd = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
             self.flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def stage_io(self, dev, out, pin=True):
+        """The hidden rows and positions in one device buffer `in_d` (the
+        call's `d` points into it), the outputs (shapes of the dict `out`) in
+        one device buffer `out_d`, each with a host twin (`in_h`, `out_h`)
+        of the same layout, so that an e2e step moves its inputs and outputs
+        in one copy each."""
+        inp = self.host_inputs()
+        ins = [{"hidden": inp["hidden"], "positions": inp["positions"]}]
+        self.in_h, (vh,) = carve_dicts(ins, "cpu", pin)
+        self.in_d, (vd,) = carve_dicts(ins, dev)
+        for k in vh:
+            vh[k].copy_(ins[0][k])
+        self.in_d.copy_(self.in_h)
+        self.d["hidden"], self.d["positions"] = vd["hidden"], vd["positions"]
+        self.out_d, (self.out,) = carve_dicts([out], dev)
+        self.out_h, _ = carve_dicts([out], "cpu", pin)
 
     def call(self, stream):
         if self.paged:
@@ -383,14 +432,12 @@ class SingleCall:
         return self.graph_launches
 
     def e2e_step(self, stream):
-        self.d["hidden"].copy_(self.hidden_h, non_blocking=True)
-        self.d["positions"].copy_(self.positions_h, non_blocking=True)
+        """One call from host buffers: the inputs in one host-to-device copy,
+        the outputs in one device-to-host copy (pinned host memory)."""
+        self.in_d.copy_(self.in_h, non_blocking=True)
         self.call(stream)
-        d2h = 0
-        for k, v in self.out.items():
-            self.out_h[k].copy_(v, non_blocking=True)
-            d2h += v.numel() * v.element_size()
-        return self.hidden_h.numel() * 2 + self.positions_h.numel() * 4, d2h
+        self.out_h.copy_(self.out_d, non_blocking=True)
+        return self.in_h.numel(), self.out_h.numel()
 
     def sample_max(self):
         return self.T
