@@ -1,6 +1,9 @@
 """The pins hold the oracle to the mathematics: each of these planted
 mistakes, compiled into a copy of oracle.c, makes the pin suite fail
-(the mutant library is loaded through MLA_ORACLE_SO in a child pytest)."""
+(the mutant library is loaded through MLA_ORACLE_SO in a child pytest).
+The mistakes cover the KV prolog, the latent-cache variant and the W8A8
+path (integer GEMM, dequantisation scales, both norms, requantisation,
+head pitches, RoPE positions)."""
 import os
 import subprocess
 import sys
@@ -23,6 +26,36 @@ MUTANTS = {
     "no de-interleave": ("xd[j] = x[2 * j];\n    xd[half + j] = x[2 * j + 1];",
                          "xd[j] = x[j];\n    xd[half + j] = x[half + j];"),
     "quantisation truncates": ("float r = rintf(y);", "float r = truncf(y);"),
+    "KV RoPE at position 0": (
+        "oracle_kv_prolog_token(d, x, Wa, g, Wb, cosb + (int64_t)p * dr, sinb + (int64_t)p * dr, kn,",
+        "oracle_kv_prolog_token(d, x, Wa, g, Wb, cosb, sinb, kn,"),
+    "latent without RMSNorm": ("oracle_rmsnorm(C, r, g, d->eps, latent + t * r);",
+                               "memcpy(latent + t * r, C, sizeof(double) * r);"),
+    # W8A8 path (the pin configurations keep q_lora_rank <= kv_lora_rank, so
+    # the gamma mix-up below stays inside the gamma_kv buffer)
+    "W8A8 int GEMM reads W transposed": (
+        "for (int64_t k = 0; k < K; ++k) a += (int64_t)q[k] * (int64_t)W[k * N + n];",
+        "for (int64_t k = 0; k < K; ++k) a += (int64_t)q[k] * (int64_t)W[n * K + k];"),
+    "W8A8 q heads at the kv head pitch": ("q_nope[hh * d->nope + i] = yb[hh * qhd + i];",
+                                          "q_nope[hh * d->nope + i] = yb[hh * kvhd + i];"),
+    "W8A8 kv_b dequantised with the q operand scale": (
+        "yb[j] = (double)acc_q[j] * (double)s2 * (double)s_kvb[j];",
+        "yb[j] = (double)acc_q[j] * (double)s1 * (double)s_kvb[j];"),
+    "W8A8 value from the k_nope columns": ("value[hh * d->vdim + i] = yb[hh * kvhd + d->nope + i];",
+                                           "value[hh * d->vdim + i] = yb[hh * kvhd + i];"),
+    "W8A8 RoPE at position 0": (
+        "const float* crow = cosb + (int64_t)p * dr;\n  const float* srow = sinb + (int64_t)p * dr;",
+        "const float* crow = cosb;\n  const float* srow = sinb;"),
+    "W8A8 k_pe without the activation scale": (
+        "ya[n] = (double)acc_a[n] * (double)s_x * (double)s_kva[n];",
+        "ya[n] = (double)acc_a[n] * (double)s_kva[n];"),
+    "W8A8 activation scale inverted": ("volatile float sc = amax / 127.0f;",
+                                       "volatile float sc = 127.0f / amax;"),
+    "W8A8 q norm with gamma_kv": ("oracle_rmsnorm(yq, rq, gq, d->eps, nq_);",
+                                  "oracle_rmsnorm(yq, rq, gk, d->eps, nq_);"),
+    "W8A8 q operand quantised before the norm": (
+        "for (int64_t c = 0; c < rq; ++c) nqf[c] = (float)nq_[c];",
+        "for (int64_t c = 0; c < rq; ++c) nqf[c] = (float)yq[c];"),
 }
 
 

@@ -262,6 +262,10 @@ def test_kv_prolog_routing_closed_form(oracle_mod, b, s):
                 u, v = k_pe[bi, 0, si, j], k_pe[bi, 0, si, j + 32]
                 assert u * u + v * v == pytest.approx(raw[2 * j] ** 2 + raw[2 * j + 1] ** 2,
                                                       rel=1e-6, abs=1e-12)
+            # the (hand-pinned) RoPE of the raw columns at this token's position
+            p = positions[t]
+            want = oracle_mod.rope(raw, inp["cos"][p].numpy(), inp["sin"][p].numpy())
+            np.testing.assert_allclose(k_pe[bi, 0, si], want, rtol=1e-14, atol=1e-15)
 
 
 def test_kv_prolog_token_independence_and_sampling(oracle_mod):
@@ -461,3 +465,93 @@ def test_w8a8_first_gemm_is_integer_exact(oracle_mod):
         acc = q.astype(np.int64) @ inp["W_kva"].numpy().astype(np.int64)
         y = acc[512:576] * np.float64(sx) * inp["s_kva"].numpy()[512:576].astype(np.float64)
         np.testing.assert_allclose(k_pe[t, 0, 0], np.concatenate([y[0::2], y[1::2]]), rtol=1e-13)
+
+
+def _w8_routing_case(positions):
+    """Closed-form W8A8 case: hidden rows v_t * sign (quantised to +-127
+    exactly), one-hot W_qa / W_kva (every latent column of a token has the
+    same magnitude, so both RMSNorms are known in closed form), constant
+    scales on the normalised columns, and one-hot W_qb / W_kvb."""
+    cfg = I.small_config(I.R1_W8A8, hidden=256, q_lora_rank=192, num_heads=2, max_pos=64)
+    T, h, rq, r, H = len(positions), 256, 192, 512, 2
+    nq, nkv = H * 192, H * 256
+    sign = np.where(np.arange(h) % 3 == 1, -1.0, 1.0)
+    v = np.array([0.75, 1.5, 3.0, 0.5])[:T]
+    hid = v[:, None] * sign[None, :]
+
+    def onehot(K, N, src, w):
+        W = np.zeros((K, N), dtype=np.int8)
+        W[src, np.arange(N)] = w
+        return W
+
+    src_qa = (3 * np.arange(rq) + 1) % h
+    w_qa = np.where(np.arange(rq) % 4 == 0, -1, 1)
+    src_kva = (5 * np.arange(r + 64) + 2) % h
+    w_kva = np.concatenate([np.where(np.arange(r) % 7 == 0, -1, 1), (np.arange(64) % 5) - 2])
+    src_qb = (7 * np.arange(nq) + 5) % rq
+    w_qb = np.where(np.arange(nq) % 3 == 0, -2, 1)
+    src_kvb = (11 * np.arange(nkv) + 3) % r
+    w_kvb = np.where(np.arange(nkv) % 5 == 0, 1, -1)
+    s_qa = np.full(rq, 0.01, dtype=np.float32)
+    s_kva = np.concatenate([np.full(r, 0.02), 0.01 * (1 + np.arange(64) / 64)]).astype(np.float32)
+    s_qb = (0.005 + 0.0001 * np.arange(nq)).astype(np.float32)
+    s_kvb = (0.004 + 0.0001 * (np.arange(nkv) % 97)).astype(np.float32)
+    gq = np.array([0.5, 2.0, 1.0, 1.5])[np.arange(rq) % 4]
+    gk = np.array([1.25, 0.75, 2.0])[np.arange(r) % 3]
+    cos, sin = I.rope_tables(64, 64, 10000.0)
+    bf = torch.bfloat16
+    inp = dict(cfg=cfg, b=1, s=T, hidden=torch.tensor(hid).to(bf),
+               positions=torch.tensor(positions, dtype=torch.int32), cos=cos, sin=sin,
+               W_qa=torch.from_numpy(onehot(h, rq, src_qa, w_qa)), s_qa=torch.from_numpy(s_qa),
+               gamma_q=torch.tensor(gq).to(bf),
+               W_qb=torch.from_numpy(onehot(rq, nq, src_qb, w_qb)), s_qb=torch.from_numpy(s_qb),
+               W_kva=torch.from_numpy(onehot(h, r + 64, src_kva, w_kva)), s_kva=torch.from_numpy(s_kva),
+               gamma_kv=torch.tensor(gk).to(bf),
+               W_kvb=torch.from_numpy(onehot(r, nkv, src_kvb, w_kvb)), s_kvb=torch.from_numpy(s_kvb))
+    return inp, dict(v=v, sign=sign, src_qa=src_qa, w_qa=w_qa, src_kva=src_kva, w_kva=w_kva,
+                     src_qb=src_qb, w_qb=w_qb, src_kvb=src_kvb, w_kvb=w_kvb, s_qa=s_qa, s_kva=s_kva,
+                     s_qb=s_qb, s_kvb=s_kvb, gq=gq, gk=gk, cos=cos.numpy(), sin=sin.numpy())
+
+
+def test_w8a8_routing_closed_form(oracle_mod):
+    """Every W8A8 output in closed form, at positions 0, 7 and 63.  A row
+    v * sign quantises to 127 * sign with scale fp32(v / 127); the one-hot
+    q_a / kv_a GEMMs then give latent columns of one magnitude c per token,
+    so RMSNorm is sign * c / sqrt(c^2 + eps) * gamma; the requantised
+    operands are the (hand-pinned) fp32 quantisation of those vectors; the
+    one-hot q_b / kv_b pick w * operand[src] * scale * s_w[j]; q_pe and
+    k_pe are the (hand-pinned) RoPE of their columns at the token's
+    position.  This pins the Q-side and KV-side norms separately (gamma_q
+    vs gamma_kv), both requantisations, the head pitches (192 for q, 256
+    for kv), the value columns and the positions."""
+    positions = [0, 7, 63]
+    inp, k = _w8_routing_case(positions)
+    q_nope, q_pe, k_nope, value, k_pe = oracle_mod.w8a8_prolog(inp, nthreads=1)
+    eps = 1e-6
+    for t, p in enumerate(positions):
+        s_x = np.float32(np.float32(k["v"][t]) / np.float32(127))
+        # q_a / kv_a: acc = 127 * sign[src] * w, dequantised with s_x * s_w
+        yq = 127.0 * k["sign"][k["src_qa"]] * k["w_qa"] * np.float64(s_x) * k["s_qa"].astype(np.float64)
+        ya = 127.0 * k["sign"][k["src_kva"]] * k["w_kva"] * np.float64(s_x) * k["s_kva"].astype(np.float64)
+        cq = abs(yq[0])
+        ck = abs(ya[0])
+        nq = np.sign(yq) * cq / math.sqrt(cq * cq + eps) * k["gq"]
+        nk = np.sign(ya[:512]) * ck / math.sqrt(ck * ck + eps) * k["gk"]
+        q1, s1 = oracle_mod.quant_row_f32(nq.astype(np.float32))
+        c1, s2 = oracle_mod.quant_row_f32(nk.astype(np.float32))
+        o_q1, o_s1, o_c1, o_s2 = oracle_mod.w8a8_operands(inp, t)
+        assert np.array_equal(o_q1, q1) and o_s1 == s1
+        assert np.array_equal(o_c1, c1) and o_s2 == s2
+        yqb = k["w_qb"] * q1[k["src_qb"]].astype(np.float64) * np.float64(s1) * k["s_qb"].astype(np.float64)
+        ykvb = k["w_kvb"] * c1[k["src_kvb"]].astype(np.float64) * np.float64(s2) * k["s_kvb"].astype(np.float64)
+        for hh in range(2):
+            np.testing.assert_allclose(q_nope[0, hh, t], yqb[hh * 192:hh * 192 + 128], rtol=1e-12)
+            np.testing.assert_allclose(q_pe[0, hh, t],
+                                       oracle_mod.rope(yqb[hh * 192 + 128:hh * 192 + 192], k["cos"][p],
+                                                       k["sin"][p]), rtol=1e-12, atol=1e-15)
+            np.testing.assert_allclose(k_nope[0, hh, t], ykvb[hh * 256:hh * 256 + 128], rtol=1e-12)
+            np.testing.assert_allclose(value[0, hh, t], ykvb[hh * 256 + 128:hh * 256 + 256], rtol=1e-12)
+        np.testing.assert_allclose(k_pe[0, 0, t], oracle_mod.rope(ya[512:576], k["cos"][p], k["sin"][p]),
+                                   rtol=1e-12, atol=1e-15)
+    # the RoPE is not the identity at these positions
+    assert not np.allclose(q_pe[0, 0, 1], q_pe[0, 0, 0])
