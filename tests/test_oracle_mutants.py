@@ -5,6 +5,7 @@ The mistakes cover the KV prolog, the latent-cache variant and the W8A8
 path (integer GEMM, dequantisation scales, both norms, requantisation,
 head pitches, RoPE positions)."""
 import os
+import shutil
 import subprocess
 import sys
 
@@ -84,4 +85,57 @@ def test_planted_mistake_fails_the_pins(name, tmp_path):
     assert src.count(old) == 1, name
     r = run_pins(src.replace(old, new), tmp_path)
     # a pin assertion failed (not a collection or import error)
+    assert r.returncode == 1 and " failed" in r.stdout, f"{name}: the pins did not catch it\n{r.stdout[-2000:]}"
+
+
+# Mistakes in the oracle's Python part (int8 KV-cache codes, paged layout):
+# the pin suite runs from a temporary tree holding a mutated copy of the
+# oracle package (its C library prebuilt, passed through MLA_ORACLE_SO).
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
+PY_MUTANTS = {
+    "int8 code without the dtype rounding": (
+        "xd = round_to(np.nan_to_num(x, nan=0.0), dtype).astype(np.float32)",
+        "xd = np.nan_to_num(x, nan=0.0).astype(np.float32)"),
+    "int8 code clamped at -128": ("return np.clip(np.rint(y), -127, 127).astype(np.int8)",
+                                  "return np.clip(np.rint(y), -128, 127).astype(np.int8)"),
+    "int8 code truncates": ("return np.clip(np.rint(y), -127, 127).astype(np.int8)",
+                            "return np.clip(np.trunc(y), -127, 127).astype(np.int8)"),
+    "paged slot split swapped": ("blk, off = divmod(int(slots[t]), page_size)",
+                                 "off, blk = divmod(int(slots[t]), page_size)"),
+    "paged negative slot not dropped": ("            if slots[t] < 0:\n                continue\n", ""),
+    "paged row from the wrong sequence": ("bi, si = divmod(t, s)\n            c[blk",
+                                          "si, bi = divmod(t, b)\n            c[blk"),
+}
+
+
+def run_pins_py(py_text, tmp_path):
+    """Run the pin suite against a copy of the oracle package whose Python
+    part is py_text."""
+    import oracle
+    so = oracle.build()
+    (tmp_path / "oracle").mkdir()
+    (tmp_path / "oracle" / "__init__.py").write_text(py_text)
+    shutil.copy(SRC, tmp_path / "oracle")
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tmp_path / "tests" / "golden")
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests")
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path)
+    os.symlink(os.path.join(ROOT, "mla_attention_kv_gb300"), tmp_path / "mla_attention_kv_gb300")
+    env = dict(os.environ, MLA_ORACLE_SO=so)
+    return subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                           str(tmp_path / "tests" / "test_oracle_pins.py")],
+                          env=env, cwd=tmp_path, capture_output=True, text=True, timeout=600)
+
+
+def test_unmutated_python_copy_passes(tmp_path):
+    r = run_pins_py(open(PY_SRC).read(), tmp_path)
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_python_mistake_fails_the_pins(name, tmp_path):
+    old, new = PY_MUTANTS[name]
+    src = open(PY_SRC).read()
+    assert src.count(old) == 1, name
+    r = run_pins_py(src.replace(old, new), tmp_path)
     assert r.returncode == 1 and " failed" in r.stdout, f"{name}: the pins did not catch it\n{r.stdout[-2000:]}"
