@@ -5,7 +5,6 @@ V2-Lite decode sweep (s in {1, 2} x b in {1 .. 128}), the R1-shaped decode
 (b=64, s=1, bf16), ragged token counts around the 16-row m-tiles and the
 64-row launch chunks, small head counts, determinism, the position check
 and the bounded device wait."""
-import numpy as np
 import pytest
 import torch
 

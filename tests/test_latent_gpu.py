@@ -3,7 +3,6 @@ compressed_kv, RoPE of k_pe; no kv_b_proj) against the fp64 oracle, through
 the C ABI, on both kernels: the decode kernel (one launch per 128 / 64 rows,
 raw and packed W_kva) and the tensor-core prefill kernel (with and without
 the k_pe worker CTAs).  k_pe must be bit-identical to the full prolog's."""
-import numpy as np
 import pytest
 import torch
 

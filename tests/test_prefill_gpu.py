@@ -3,7 +3,6 @@ the C ABI): small forced-prefill cases with ragged tiles and sequence
 boundaries inside a tile, both dtypes, small head counts, the full-size
 V2-Lite prefill (b=4, s=4096, T=16384) and the R1-shaped prefill (b=2,
 s=8192, bf16) on sampled rows, and agreement with the decode kernel."""
-import numpy as np
 import pytest
 import torch
 
