@@ -221,28 +221,36 @@ class DecodeSweep:
             self._host = [I.kv_inputs(self.cfg, b, s, I.seed_for(1, i)) for i, (b, s) in enumerate(self.points)]
         return self._host
 
-    # CPU oracle on a bounded sample: like a step, one oracle call per sweep
-    # point, each on at most m of the point's token rows
-    def sample_max(self):
-        return max(b * s for b, s in self.points)
+    # CPU oracle on a bounded sample: n whole calls of the sweep per step
+    # (consecutive points, cyclic), so that every call keeps the workload's
+    # own ratio of rows to the oracle's fixed cost per call
+    def oracle_size(self, target, nthreads):
+        """Points per step: one untimed pass over the sweep times each
+        point's call; the largest n whose mean step (n calls) fits target."""
+        import oracle
+        taus = []
+        for inp in self.host_inputs():
+            t0 = time.perf_counter()
+            oracle.kv_prolog(inp, nthreads=nthreads)
+            taus.append(time.perf_counter() - t0)
+        mean = sum(taus) / len(taus)
+        return int(max(1, min(len(self.points), target // max(mean, 1e-9))))
 
-    def sample_rows(self, m):
-        return sum(min(b * s, m) for b, s in self.points)
-
-    def oracle_step(self, k, m, nthreads):
-        """Oracle on the k-th bounded sample of the sweep: every point, rows
-        k*m .. k*m + m - 1 of it (mod b*s).  Returns the rows computed."""
+    def oracle_step(self, k, n, nthreads):
+        """Oracle on the k-th bounded sample of the sweep: sweep points
+        k*n .. k*n + n - 1 (mod 16), each a whole call.  Returns the rows."""
         import oracle
         done = 0
-        for inp, (b, s) in zip(self.host_inputs(), self.points):
-            rows = sorted({(k * m + j) % (b * s) for j in range(min(m, b * s))})
-            oracle.kv_prolog(inp, rows=rows, nthreads=nthreads)
-            done += len(rows)
+        host = self.host_inputs()
+        for j in range(n):
+            i = (k * n + j) % len(self.points)
+            oracle.kv_prolog(host[i], nthreads=nthreads)
+            done += self.points[i][0] * self.points[i][1]
         return done
 
-    def sample_text(self, m):
-        return (f"every point of the V2-Lite decode sweep per step, at most {m} of its token rows each "
-                f"({self.sample_rows(m)} of {self.tokens_per_step} rows), fp64 oracle")
+    def sample_text(self, n):
+        return (f"{n} of the 16 calls of a V2-Lite decode sweep step per step (whole calls, "
+                f"consecutive points, cyclic), fp64 oracle")
 
 
 class SingleCall:
@@ -439,11 +447,9 @@ class SingleCall:
         self.out_h.copy_(self.out_d, non_blocking=True)
         return self.in_h.numel(), self.out_h.numel()
 
-    def sample_max(self):
-        return self.T
-
-    def sample_rows(self, n):
-        return min(n, self.T)
+    def oracle_size(self, target, nthreads):
+        """Rows per step: the largest sample whose predicted time fits target."""
+        return fit_sample_size(self.oracle_step, lambda n: min(n, self.T), self.T, target, nthreads)
 
     def oracle_step(self, k, n, nthreads):
         """Oracle on the k-th bounded sample of the call: token rows
@@ -527,49 +533,52 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def fit_sample_size(run, rows, top, target, nthreads):
+    """The largest sample size n <= top whose predicted time fits `target`
+    seconds, for a sample made of one oracle call on rows(n) token rows
+    (`run(k, n, nthreads)` runs the k-th such sample).  One untimed call
+    first (the oracle's first touch of its buffers), then two calls at sizes
+    n1 and about 16 n1 separate the call's fixed cost (weight promotion)
+    from its cost per row."""
+    def timed(k, n):
+        t0 = time.perf_counter()
+        run(k, n, nthreads)
+        return time.perf_counter() - t0
+
+    n1 = 1
+    while n1 < top and rows(n1) < max(nthreads, 8):
+        n1 *= 2
+    n1 = min(n1, top)
+    n2 = min(top, 16 * n1)
+    r1, r2 = rows(n1), rows(n2)
+    timed(0, n1)
+    t1 = timed(1, n1)
+    t2 = timed(2, n2) if r2 > r1 else t1
+    per_row = (t2 - t1) / (r2 - r1) if r2 > r1 and t2 > t1 else t2 / r2
+    fixed = max(0.0, t1 - per_row * r1)
+    lo, hi = 1, top
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if fixed + per_row * rows(mid) <= target:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
 def oracle_steps(wl, steps, warmup, seconds):
     """Time the CPU oracle on the host cores: `warmup` untimed steps, then
     exactly `steps` timed steps, each a bounded sample of the workload
-    (`wl.oracle_step(k, n)`, whose size parameter n gives
-    `wl.sample_rows(n)` token rows; the largest n is the whole step) sized
-    so that all warmup + steps take about `seconds`.  Two untimed
-    calibration steps at sizes n1 < n2 separate the oracle's fixed cost per
-    step (its calls' weight promotion) from its cost per row.  Returns
-    (tokens/s, threads used, description of the sample, size parameter,
-    timed seconds)."""
+    (`wl.oracle_step(k, n)`; the workload's `oracle_size` picks n from an
+    untimed calibration so that all warmup + steps take about `seconds`).
+    Returns (tokens/s, threads used, description of the sample, size
+    parameter, timed seconds)."""
     import oracle
     oracle.build()
     nt = os.cpu_count() or 1
     wl.host_inputs()
     steps = max(1, steps)
-    top = wl.sample_max()
-
-    def timed(k, n):
-        t0 = time.perf_counter()
-        wl.oracle_step(k, n, nt)
-        return time.perf_counter() - t0
-
-    n1 = 1
-    while n1 < top and wl.sample_rows(n1) < max(nt, 8):
-        n1 *= 2
-    n1 = min(n1, top)
-    n2 = min(top, 16 * n1)
-    r1, r2 = wl.sample_rows(n1), wl.sample_rows(n2)
-    timed(0, n1)  # first touch of the oracle's buffers, not counted
-    t1 = timed(1, n1)
-    t2 = timed(2, n2) if r2 > r1 else t1
-    per_row = (t2 - t1) / (r2 - r1) if r2 > r1 and t2 > t1 else t2 / r2
-    fixed = max(0.0, t1 - per_row * r1)
-    # the largest size whose predicted step time fits the share of `seconds`
-    target = seconds / (steps + warmup)
-    lo, hi = 1, top
-    while lo < hi:
-        mid = (lo + hi + 1) // 2
-        if fixed + per_row * wl.sample_rows(mid) <= target:
-            lo = mid
-        else:
-            hi = mid - 1
-    n = lo
+    n = wl.oracle_size(seconds / (steps + warmup), nt)
     for k in range(warmup):
         wl.oracle_step(k, n, nt)
     done = 0

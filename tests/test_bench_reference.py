@@ -25,11 +25,12 @@ class FakeWorkload:
     def host_inputs(self):
         return None
 
-    def sample_max(self):
-        return self.tokens_per_step
-
     def sample_rows(self, n):
         return min(n, self.tokens_per_step)
+
+    def oracle_size(self, target, nthreads):
+        return bench.fit_sample_size(self.oracle_step, self.sample_rows, self.tokens_per_step, target,
+                                     nthreads)
 
     def oracle_step(self, k, n, nthreads):
         rows = self.sample_rows(n)
@@ -89,7 +90,24 @@ def test_reference_arm_decode_sweep():
     (d,) = run_reference("--steps", "2", "--warmup", "3", "--ref-seconds", "1")
     check_line(d, 2, 3)
     assert d["config"]["workload"] == "v2lite_kv_prolog_decode_sweep"
-    assert "every point of the V2-Lite decode sweep" in d["cpu_baseline"]["sample"]
+    assert "calls of a V2-Lite decode sweep step per step (whole calls" in d["cpu_baseline"]["sample"]
+
+
+def test_decode_sweep_samples_whole_calls(monkeypatch):
+    """A sweep sample of n calls runs points k*n .. k*n + n - 1 (mod 16),
+    each on all of its rows; the size is the number of mean calls that fit."""
+    import oracle
+    wl = bench.DecodeSweep()
+    seen = []
+    monkeypatch.setattr(oracle, "kv_prolog", lambda inp, rows=None, nthreads=0: seen.append((inp["b"], inp["s"], rows)))
+    wl._host = [dict(b=b, s=s) for b, s in wl.points]
+    assert wl.oracle_step(3, 5, 1) == sum(b * s for b, s in (wl.points * 2)[15:20])
+    assert seen == [(b, s, None) for b, s in (wl.points * 2)[15:20]]
+    seen.clear()
+    clock = iter(range(100))
+    monkeypatch.setattr(bench.time, "perf_counter", lambda: next(clock) * 0.5)  # every call 0.5 s
+    assert wl.oracle_size(2.2, 1) == 4 and len(seen) == 16
+    assert wl.oracle_size(100.0, 1) == 16
 
 
 def test_reference_arm_other_ranks_exit_quietly():
