@@ -737,53 +737,11 @@ def kernel_traffic(kernel: str, T: int, model: str = ""):
         return None
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="decode_sweep", choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
-                    help="seconds of the oracle's steps in the cpu_baseline leg")
-    ap.add_argument("--ref-seconds", type=float, default=120.0,
-                    help="seconds of the oracle's warm-up + timed steps under --impl reference")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = WORKLOADS[args.workload]()
-    is_w8 = getattr(wl, "w8", False)
-    dtype = "int8/int32 (bf16 io)" if is_w8 else ("f16" if wl.cfg["dtype"] == "fp16" else "bf16")
-
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        v, cores, sample, n, el = oracle_steps(wl, args.steps, args.warmup, args.ref_seconds)
-        sample += f"; {args.warmup} untimed + {args.steps} timed steps, {el:.1f} s timed"
-        line = {"metric": "tokens/s", "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": wl.tokens_per_step / v * 1e3, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "impl": "reference",
-                "config": dict(wl.describe(), parallelism="none (host cores)"),
-                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
-                                 "kind": "oracle", "sample": sample},
-                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-
-    if world > 1:
-        torch.distributed.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    r = run_gpu(args, wl, rank, world, dev)
-
+def gpu_line(args, wl, r, world, dtype, is_w8):
+    """The JSON line of the GPU arm from run_gpu's measurements: whole-job
+    tokens/s, the roofline of the dominant kernel, clocks, e2e, the eager
+    pass and (for the sweep) per-point figures; cpu_baseline is added by
+    the caller."""
     value = job_tokens_per_s(wl.tokens_per_step, args.steps, world, r["ms"])
     peaks, peak_kind = measured_peaks()
     calls = r["calls"]
@@ -859,6 +817,57 @@ def main():
                                     "hbm_frac": wl.alg_bytes(b * s_) / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
         line["per_point"] = detail
         line["per_point_timing"] = "CUDA events around each call of the eager pass"
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="decode_sweep", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="seconds of the oracle's steps in the cpu_baseline leg")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="seconds of the oracle's warm-up + timed steps under --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = WORKLOADS[args.workload]()
+    is_w8 = getattr(wl, "w8", False)
+    dtype = "int8/int32 (bf16 io)" if is_w8 else ("f16" if wl.cfg["dtype"] == "fp16" else "bf16")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        v, cores, sample, n, el = oracle_steps(wl, args.steps, args.warmup, args.ref_seconds)
+        sample += f"; {args.warmup} untimed + {args.steps} timed steps, {el:.1f} s timed"
+        line = {"metric": "tokens/s", "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": wl.tokens_per_step / v * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference",
+                "config": dict(wl.describe(), parallelism="none (host cores)"),
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = run_gpu(args, wl, rank, world, dev)
+
+    line = gpu_line(args, wl, r, world, dtype, is_w8)
     if rank == 0 and not args.no_cpu_baseline:
         v, cores, sample, n, el = oracle_steps(wl, 4, 1, args.cpu_seconds)
         sample += f"; 1 untimed + 4 timed steps, {el:.1f} s timed"
