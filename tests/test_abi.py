@@ -105,3 +105,44 @@ def test_variant_entries_reject_bad_arguments(L):
     assert L.mla_kv_prolog_run_c8(fake, 1, 1, *([fake] * 7), P(20), fake, fake, fake, fake, fake, None) == 4
     assert B.STATUS_NAMES[10] == "MLA_ERR_BAD_SLOT"
     assert b"slot" in L.mla_status_string(10)
+
+
+def header_prototypes():
+    """{name: [kind of each parameter]} from include/mla_prolog.h, kinds
+    'ptr' (pointers, handles, streams), 'int', 'float'."""
+    src = open(os.path.join(ROOT, "include", "mla_prolog.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(?:mla_status|int|const char\s*\*)\s+(mla_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        kinds = []
+        for p in params:
+            if "*" in p or "cudaStream_t" in p or "mla_prolog_t" in p:
+                kinds.append("ptr")
+            elif re.match(r"(const\s+)?float\b", p):
+                kinds.append("float")
+            else:
+                kinds.append("int")
+        protos[m.group(1)] = kinds
+    return protos
+
+
+def test_binding_argtypes_match_the_header(L):
+    """Every declared function is bound with the header's parameter count,
+    and pointer / integer parameters in the same places."""
+    protos = header_prototypes()
+    assert set(protos) == set(declared_functions())
+    for name, kinds in protos.items():
+        at = getattr(L, name).argtypes
+        if at is None:  # bound without argtypes: only zero-parameter functions
+            assert kinds == [], name
+            continue
+        assert len(at) == len(kinds), (name, len(at), len(kinds))
+        for i, (t, k) in enumerate(zip(at, kinds)):
+            is_ptr = t is ctypes.c_void_p or t is ctypes.c_char_p or hasattr(t, "_type_") and t.__name__.startswith("LP_")
+            if k == "ptr":
+                assert is_ptr, (name, i, t)
+            elif k == "int":
+                assert t is ctypes.c_int, (name, i, t)
+            else:
+                assert t is ctypes.c_float, (name, i, t)
