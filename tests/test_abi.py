@@ -146,3 +146,31 @@ def test_binding_argtypes_match_the_header(L):
                 assert t is ctypes.c_int, (name, i, t)
             else:
                 assert t is ctypes.c_float, (name, i, t)
+
+
+def test_config_struct_layout_matches_the_header(tmp_path):
+    """binding.Config has the header's fields in order with the same types,
+    and the same size and field offsets as the C compiler gives the struct."""
+    import shutil
+    import subprocess
+    src = open(os.path.join(ROOT, "include", "mla_prolog.h")).read()
+    body = re.search(r"typedef struct mla_prolog_config \{(.*?)\} mla_prolog_config;", src, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = [re.match(r"\s*(.*?)\s+(\w+)$", f.strip()).groups() for f in body.split(";") if f.strip()]
+    ctypes_of = {"int": ctypes.c_int, "float": ctypes.c_float, "unsigned long long": ctypes.c_ulonglong}
+    assert [(n, ctypes_of[t]) for t, n in fields] == list(B.Config._fields_)
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers are missing")
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "mla_prolog.h"\nint main(void) {\n'
+                    '  printf("%zu\\n", sizeof(mla_prolog_config));\n'
+                    + "".join(f'  printf("%zu\\n", offsetof(mla_prolog_config, {n}));\n' for _, n in fields)
+                    + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, str(prog), "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(B.Config)
+    assert out[1:] == [getattr(B.Config, n).offset for _, n in fields]
