@@ -174,3 +174,13 @@ def test_config_struct_layout_matches_the_header(tmp_path):
     out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert out[0] == ctypes.sizeof(B.Config)
     assert out[1:] == [getattr(B.Config, n).offset for _, n in fields]
+
+
+def test_enum_values_match_the_header():
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "mla_prolog.h")).read(), flags=re.S)
+    enums = {n: int(v) for n, v in re.findall(r"\b(MLA_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    assert {v: k for k, v in enums.items() if k.startswith(("MLA_OK", "MLA_ERR_"))} == B.STATUS_NAMES
+    assert (enums["MLA_F16"], enums["MLA_BF16"]) == (B.MLA_F16, B.MLA_BF16)
+    assert (enums["MLA_QUANT_NONE"], enums["MLA_QUANT_W8A8"]) == (B.QUANT_NONE, B.QUANT_W8A8)
+    assert (enums["MLA_PATH_AUTO"], enums["MLA_PATH_DECODE"], enums["MLA_PATH_PREFILL"]) == \
+        (B.PATH_AUTO, B.PATH_DECODE, B.PATH_PREFILL)
