@@ -184,3 +184,26 @@ def test_enum_values_match_the_header():
     assert (enums["MLA_QUANT_NONE"], enums["MLA_QUANT_W8A8"]) == (B.QUANT_NONE, B.QUANT_W8A8)
     assert (enums["MLA_PATH_AUTO"], enums["MLA_PATH_DECODE"], enums["MLA_PATH_PREFILL"]) == \
         (B.PATH_AUTO, B.PATH_DECODE, B.PATH_PREFILL)
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host(L):
+    """mla_kv_prolog_run_noalloc validates before any CUDA call: no config,
+    negative sizes, a W8A8 config, unsupported dimensions, null and
+    misaligned pointers; T = 0 is a no-op.  (Fake addresses: nothing is
+    dereferenced on these paths.)"""
+    good = [ctypes.c_void_p(0x10000 + 0x1000 * i) for i in range(10)]
+    status = ctypes.c_void_p(0x90000)
+    run = L.mla_kv_prolog_run_noalloc
+    assert run(None, 1, 1, *good, status, None) == 1
+    assert run(ctypes.byref(_cfg()), -1, 1, *good, status, None) == 1
+    assert run(ctypes.byref(_cfg(dtype=7)), 1, 1, *good, status, None) == 1
+    assert run(ctypes.byref(_cfg(quant=1, dtype=B.MLA_BF16, q_lora_rank=1536)), 1, 1, *good, status, None) == 9
+    assert run(ctypes.byref(_cfg(kv_lora_rank=256)), 1, 1, *good, status, None) == 2
+    assert run(ctypes.byref(_cfg(hidden=2000)), 1, 1, *good, status, None) == 2
+    assert run(ctypes.byref(_cfg()), 0, 5, *good, status, None) == 0
+    for i in range(10):
+        args = list(good)
+        args[i] = None
+        assert run(ctypes.byref(_cfg()), 1, 1, *args, status, None) == 1, i
+        args[i] = ctypes.c_void_p(good[i].value + 8)
+        assert run(ctypes.byref(_cfg()), 1, 1, *args, status, None) == 4, i
