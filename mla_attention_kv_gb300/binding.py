@@ -85,7 +85,8 @@ def load(path: str | None = None):
                "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
                "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
                "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_abi_version",
-               "mla_kv_prolog_run_noalloc"):
+               "mla_kv_prolog_run_noalloc", "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent",
+               "mla_kv_prolog_run_paged", "mla_kv_prolog_run_c8"):
         getattr(L, fn).restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
     L.mla_status_string.restype = ctypes.c_char_p

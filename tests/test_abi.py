@@ -132,6 +132,11 @@ def test_binding_argtypes_match_the_header(L):
     and pointer / integer parameters in the same places."""
     protos = header_prototypes()
     assert set(protos) == set(declared_functions())
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "mla_prolog.h")).read(), flags=re.S)
+    for name in protos:
+        ret = re.search(r"(mla_status|int|const char\s*\*)\s+" + name + r"\s*\(", src).group(1)
+        want = ctypes.c_char_p if ret.startswith("const char") else ctypes.c_int
+        assert getattr(L, name).restype is want, (name, ret)
     for name, kinds in protos.items():
         at = getattr(L, name).argtypes
         if at is None:  # bound without argtypes: only zero-parameter functions
