@@ -58,3 +58,18 @@ def test_variant_workloads():
     for name in ("v2lite_latent_decode", "v2lite_paged_decode", "v2lite_c8_decode"):
         d = bench.WORKLOADS[name]().describe()
         assert "variant" in d and d["T"] == 64
+
+
+@pytest.mark.parametrize("name", sorted(bench.WORKLOADS))
+def test_every_workload_describes_itself(name):
+    """Each workload names itself and its model with its sizes, serialises
+    as the JSON line's config, and has positive work per call."""
+    import json
+    wl = bench.WORKLOADS[name]()
+    d = wl.describe()
+    json.dumps(d)
+    assert d["workload"] and d["model"]
+    assert any(str(x) in d["workload"] for x in ("s2", "s1", "s4096", "s8192", "T1", "T64", "T8192", "sweep"))
+    for b, s in wl.points:
+        assert wl.alg_bytes(b * s) > wl.weight_bytes() > 0 and wl.flops(b * s) > 0
+    assert wl.tokens_per_step == sum(b * s for b, s in wl.points)
