@@ -112,7 +112,7 @@ def test_decode_sweep_gpu_arm(fake_cuda):
     assert line["gpu_launches"] == 3 * wl.graph_launches
 
 
-@pytest.mark.parametrize("name", ["v2lite_tiny", "v2lite_paged_decode", "w8a8_t1"])
+@pytest.mark.parametrize("name", sorted(n for n in bench.WORKLOADS if n != "decode_sweep"))
 def test_single_call_gpu_arm(fake_cuda, name):
     wl = bench.WORKLOADS[name]()
     a = args_for(steps=4)
