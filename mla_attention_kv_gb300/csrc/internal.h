@@ -243,7 +243,7 @@ void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_t
 cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int hidden,
                               int q_rank, int heads, int max_tokens, int num_sms);
 // Tensor maps of the decode-size chain for these weight pointers (false if
-// the driver rejects one).
+// the CUDA driver rejects one).
 bool w8_encode_maps(const W8Params& p, const W8SmallPlan& plan, W8Maps* maps);
 cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPlan& plan,
                         const W8Maps* maps, int num_sms, cudaStream_t stream, int* launches);

@@ -10,7 +10,7 @@ namespace mla {
 
 // Encode a 2-D row-major tensor map: `inner` elements per row (contiguous),
 // `outer` rows, `row_stride` bytes between rows (multiple of 16), box of
-// box_inner x box_outer elements.  Returns false if the driver rejects it.
+// box_inner x box_outer elements.  Returns false if the CUDA driver rejects it.
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t outer, uint64_t row_stride, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle);
