@@ -258,6 +258,14 @@ mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path);
 int mla_kv_prolog_last_launches(mla_prolog_t h);
 int mla_kv_prolog_last_path(mla_prolog_t h);
 
+/* The smallest b*s for which MLA_PATH_AUTO takes the prefill kernel on this
+ * handle (its model shape and device); smaller b*s take the decode kernel.
+ * It replaces the dynamic short / long selection of [MIG]
+ * §"源码级原理：KV Prolog 的混合优化实现" (last paragraph: fused op for short
+ * inputs, baseline for long ones) by a token-count bucket.  -1 for a null
+ * handle. */
+int mla_kv_prolog_auto_threshold(mla_prolog_t h);
+
 /* W8A8 building blocks, callable on their own (the full run uses the same
  * kernels; the tests check them bit-exactly):
  *   mla_w8a8_quant_rows: per-row symmetric int8 quantisation of a bf16
@@ -273,6 +281,21 @@ mla_status mla_w8a8_quant_rows(const void* x_bf16, int rows, int cols, int8_t* q
                                cudaStream_t stream);
 mla_status mla_w8a8_gemm_s32(const int8_t* A, const int8_t* W, int M, int K, int N,
                              int32_t* acc, cudaStream_t stream);
+/* Accumulator capture of the W8A8 prolog (diagnostics and tests; [R1]
+ * §"权重转换" W8A8 mode: the int32 accumulators are exact).  While set, every
+ * mla_prolog_w8a8_run on the handle also writes the int32 accumulators of
+ * its four int8 GEMMs, as its own kernels formed them, into the caller's
+ * device buffers (row t = bi*s + si):
+ *   acc_a   [T, q_lora_rank + 576]  q_a_proj (columns 0 .. q_lora_rank-1)
+ *                                   then kv_a_proj
+ *   acc_qb  [T, H*192]              q_b_proj
+ *   acc_kvb [T, H*256]              kv_b_proj
+ * Each pointer may be NULL (that GEMM is not captured); all NULL turns the
+ * capture off.  The buffers must hold the T of every run while set and stay
+ * valid until those runs finish.  MLA_ERR_WRONG_MODE on a handle that is
+ * not W8A8; MLA_ERR_MISALIGNED for a pointer not 16-byte aligned. */
+mla_status mla_prolog_w8a8_capture(mla_prolog_t h, int32_t* acc_a, int32_t* acc_qb,
+                                   int32_t* acc_kvb);
 mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1, int8_t* c1,
                                     float* s2, cudaStream_t stream);
 
@@ -296,9 +319,12 @@ mla_status mla_prolog_w8a8_operands(mla_prolog_t h, int T, int8_t* q1, float* s1
  * MLA_ERR_UNSUPPORTED and a message in mla_last_cuda_error().
  * All calls on a device share the array: each call clears the counters
  * and status word first, and calls that overlap on the same GPU race on
- * it (serialise them on one stream).  The first call on each device looks
- * up the array's address with cudaGetSymbolAddress while that device is
- * current; make that first call before any stream capture begins. */
+ * it (serialise them on one stream).  The first call in each CUDA context
+ * (normally once per device) looks up the array's address with
+ * cudaGetSymbolAddress while that device is current; the address is cached
+ * per context, so a new context (after cudaDeviceReset, say) looks it up
+ * again.  Make the first call before any stream capture begins.
+ * b * s above INT_MAX gives MLA_ERR_TOO_MANY_TOKENS. */
 mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, int b, int s,
                                      const void* hidden_states, const int32_t* positions,
                                      const void* W_kva, const void* gamma_kv, const void* W_kvb,

@@ -29,7 +29,7 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
             "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
             "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent", "mla_kv_prolog_run_paged",
-            "mla_kv_prolog_run_c8"]
+            "mla_kv_prolog_run_c8", "mla_kv_prolog_auto_threshold", "mla_prolog_w8a8_capture"]
 
 
 class MLAError(RuntimeError):
@@ -81,12 +81,15 @@ def load(path: str | None = None):
     L.mla_prolog_w8a8_operands.argtypes = [H, I, P, P, P, P, P]
     L.mla_kv_prolog_run_noalloc.argtypes = [ctypes.POINTER(Config), I, I] + [P] * 11 + [P]
     L.mla_kv_prolog_prepare_weights.argtypes = [H, P, P, P]
+    L.mla_kv_prolog_auto_threshold.argtypes = [H]
+    L.mla_prolog_w8a8_capture.argtypes = [H, P, P, P]
     for fn in ("mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
                "mla_kv_prolog_status", "mla_kv_prolog_destroy", "mla_kv_prolog_set_path",
                "mla_kv_prolog_last_launches", "mla_kv_prolog_last_path", "mla_w8a8_quant_rows",
                "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_abi_version",
                "mla_kv_prolog_run_noalloc", "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent",
-               "mla_kv_prolog_run_paged", "mla_kv_prolog_run_c8"):
+               "mla_kv_prolog_run_paged", "mla_kv_prolog_run_c8", "mla_kv_prolog_auto_threshold",
+               "mla_prolog_w8a8_capture"):
         getattr(L, fn).restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
     L.mla_status_string.restype = ctypes.c_char_p
@@ -260,6 +263,13 @@ def mla_prolog_w8a8_operands(h, T, q1, s1, c1, s2, stream=None):
            "mla_prolog_w8a8_operands")
 
 
+def mla_prolog_w8a8_capture(h, acc_a=None, acc_qb=None, acc_kvb=None):
+    def opt(t, name):
+        return None if t is None else _dev(t, torch.int32, name)
+    _check(load().mla_prolog_w8a8_capture(h, opt(acc_a, "acc_a"), opt(acc_qb, "acc_qb"),
+                                          opt(acc_kvb, "acc_kvb")), "mla_prolog_w8a8_capture")
+
+
 # ------------------------------------------------------------------ convenience wrapper
 class MLAProlog:
     """Owns one library handle (and so one device workspace)."""
@@ -290,6 +300,10 @@ class MLAProlog:
     @property
     def last_path(self) -> int:
         return load().mla_kv_prolog_last_path(self.h)
+
+    @property
+    def auto_threshold(self) -> int:
+        return load().mla_kv_prolog_auto_threshold(self.h)
 
     def status(self, stream=None) -> int:
         return mla_kv_prolog_status(self.h, stream)

@@ -44,6 +44,10 @@ struct mla_prolog_s {
   W8Workspace w8;
   W8SmallPlan w8plan;
   W8Maps w8maps;
+  // W8A8 accumulator capture (mla_prolog_w8a8_capture); null: off
+  int32_t* cap_a;
+  int32_t* cap_qb;
+  int32_t* cap_kvb;
   // tensor maps of recently seen W_kvb pointers (decode kernel)
   static constexpr int kMapCache = 64;
   const void* map_ptr[kMapCache];
@@ -200,6 +204,22 @@ mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path) {
 }
 
 int mla_kv_prolog_last_launches(mla_prolog_t h) { return h ? h->last_launches : -1; }
+
+int mla_kv_prolog_auto_threshold(mla_prolog_t h) {
+  if (!h) return -1;
+  return prefill_min_tokens(h->cfg.hidden, h->cfg.num_heads, h->num_sms);
+}
+
+mla_status mla_prolog_w8a8_capture(mla_prolog_t h, int32_t* acc_a, int32_t* acc_qb, int32_t* acc_kvb) {
+  if (!h) return MLA_ERR_INVALID_ARG;
+  if (h->cfg.quant != MLA_QUANT_W8A8) return MLA_ERR_WRONG_MODE;
+  if ((acc_a && !aligned16(acc_a)) || (acc_qb && !aligned16(acc_qb)) || (acc_kvb && !aligned16(acc_kvb)))
+    return MLA_ERR_MISALIGNED;
+  h->cap_a = acc_a;
+  h->cap_qb = acc_qb;
+  h->cap_kvb = acc_kvb;
+  return MLA_OK;
+}
 int mla_kv_prolog_last_path(mla_prolog_t h) { return h ? h->last_path : -1; }
 
 mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
@@ -256,7 +276,8 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     h->last_launches = 1;
   }
   int path = h->path_override;
-  if (path == MLA_PATH_AUTO) path = prefill_preferred(h->cfg.hidden, h->cfg.num_heads, (int)T, h->num_sms) ? MLA_PATH_PREFILL : MLA_PATH_DECODE;
+  if (path == MLA_PATH_AUTO)
+    path = T >= prefill_min_tokens(h->cfg.hidden, h->cfg.num_heads, h->num_sms) ? MLA_PATH_PREFILL : MLA_PATH_DECODE;
   h->last_path = path;
 
   if (path == MLA_PATH_PREFILL) {
@@ -419,6 +440,7 @@ mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_
   p.k_pe = k_pe; p.status = h->status; p.hidden_dim = h->cfg.hidden;
   p.q_rank = h->cfg.q_lora_rank; p.heads = h->cfg.num_heads; p.s = s; p.T = (int)T;
   p.max_pos = h->cfg.max_pos; p.eps = h->cfg.eps; p.budget_ns = h->budget_ns;
+  p.cap_a = h->cap_a; p.cap_qb = h->cap_qb; p.cap_kvb = h->cap_kvb;
   // tensor maps of the decode-size chain, re-encoded when a weight pointer changes
   const W8Maps* maps = nullptr;
   if (T <= kW8SmallRows) {

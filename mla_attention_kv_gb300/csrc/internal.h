@@ -168,10 +168,9 @@ struct PrefillParams {
   int kpe_split;   // 1: the CTAs past main_ctas run the k_pe pass of every tile
 };
 
-// Token count from which AUTO selects the tensor-core prefill kernel.
-constexpr int kPrefillMinTokens = 1024;
-// True when the tensor-core prefill kernel is the faster path for T rows.
-bool prefill_preferred(int hidden, int heads, int T, int num_sms);
+// Smallest token count for which AUTO selects the tensor-core prefill
+// kernel over the decode kernel, for this model shape and SM count.
+int prefill_min_tokens(int hidden, int heads, int num_sms);
 // Enqueue the prefill kernel(s); *launches receives the kernel count.
 // Returns cudaErrorNotSupported for shapes the kernel does not handle.
 cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaStream_t stream,
@@ -230,6 +229,11 @@ struct W8Params {
   void* value;
   void* k_pe;
   unsigned* status;
+  // accumulator capture (diagnostics; null: off): the int32 accumulators of
+  // q_a | kv_a [T, q_rank + 576], of q_b [T, H*192] and of kv_b [T, H*256]
+  int32_t* cap_a;
+  int32_t* cap_qb;
+  int32_t* cap_kvb;
   int hidden_dim, q_rank, heads, s, T, max_pos;
   float eps;
   unsigned long long budget_ns;

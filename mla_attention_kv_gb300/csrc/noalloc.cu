@@ -21,10 +21,20 @@
 //   - Two calls that overlap on the same GPU (for example on two streams
 //     without an ordering between them) race on the array and give wrong
 //     results.  Serialise them on one stream.
-//   - The first call on each device resolves the array's device address
-//     with cudaGetSymbolAddress while that device is current.  Make that
-//     first call before any stream capture begins.
+//   - The first call in each CUDA context (normally: once per device, in
+//     its primary context) resolves the array's device address with
+//     cudaGetSymbolAddress while that device is current.  Make that first
+//     call before any stream capture begins.  The address is cached per
+//     context, by the context's unique id: a __device__ symbol is placed
+//     anew in every context that loads the module, so after
+//     cudaDeviceReset, or in a second context on the same device, the
+//     lookup is simply done again.
+//   - Every T runs the decode kernel, in chunks of 64 or 128 rows (one
+//     launch per chunk); T above INT_MAX is rejected.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 
 #include <mutex>
 
@@ -46,10 +56,41 @@ constexpr size_t kScratchBytes = kHeaderBytes + kPartialBytes + kNrmBytes;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// Device address of g_scratch (and the SM count) per CUDA context, keyed by
+// the context's unique id, which the driver never reuses within a process.
+constexpr int kMaxContexts = 64;
+struct Slot {
+  unsigned long long ctx_id;  // 0: empty
+  unsigned char* ptr;
+  int sms;
+};
 std::mutex g_mu;
-unsigned char* g_ptr[kMaxDevices];  // device address of g_scratch, per device
-int g_sms[kMaxDevices];
+Slot g_slots[kMaxContexts];
+int g_next;
+
+// Unique id of the current context (the runtime's driver entry points, so
+// the library does not link libcuda); false when there is none.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &q1) == cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+    }
+  });
+  if (!get_cur || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
 
 mla_status fail(mla_status s, const char* what) {
   set_error_text(what);
@@ -80,6 +121,7 @@ extern "C" mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, in
     return MLA_ERR_UNSUPPORTED;
   const long long T = (long long)b * s;
   if (T == 0) return MLA_OK;
+  if (T > INT_MAX) return fail(MLA_ERR_TOO_MANY_TOKENS, "b * s exceeds INT_MAX");
   const void* ptrs[] = {hidden_states, positions, W_kva, gamma_kv, W_kvb, cos_table, sin_table,
                         k_nope, value, k_pe};
   for (const void* q : ptrs)
@@ -87,24 +129,38 @@ extern "C" mla_status mla_kv_prolog_run_noalloc(const mla_prolog_config* cfg, in
   for (const void* q : ptrs)
     if (reinterpret_cast<uintptr_t>(q) & 15u) return MLA_ERR_MISALIGNED;
 
-  // per-device set-up: resolve the scratch array's device address once
+  // set-up, once per CUDA context (normally once per device): resolve the
+  // scratch array's device address while the device is current.  If this
+  // thread has no current context yet, cudaSetDevice on the current device
+  // binds the device's primary context (it allocates nothing).
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_CUDA, "no usable current device");
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "no usable current device");
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) {
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess || !current_context_id(&ctx)) return fail(MLA_ERR_CUDA, "no current CUDA context");
+  }
   unsigned char* base = nullptr;
   int sms = 0;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_ptr[dev]) {
+    for (const Slot& sl : g_slots)
+      if (sl.ctx_id == ctx) {
+        base = sl.ptr;
+        sms = sl.sms;
+        break;
+      }
+    if (!base) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_scratch);
       if (e != cudaSuccess || !p) return fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
-      e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "device attribute query failed");
-      g_ptr[dev] = static_cast<unsigned char*>(p);
+      base = static_cast<unsigned char*>(p);
+      g_slots[g_next] = Slot{ctx, base, sms};
+      g_next = (g_next + 1) % kMaxContexts;
     }
-    base = g_ptr[dev];
-    sms = g_sms[dev];
   }
 
   DecodePlan plan;

@@ -593,11 +593,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
 }  // namespace
 
-bool prefill_preferred(int hidden, int heads, int T, int num_sms) {
+int prefill_min_tokens(int hidden, int heads, int num_sms) {
   (void)hidden;
   (void)heads;
   (void)num_sms;
-  return T >= kPrefillMinTokens;
+  return 1024;
 }
 
 cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaStream_t stream,

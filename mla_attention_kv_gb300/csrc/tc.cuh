@@ -91,15 +91,6 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                : "memory");
 }
 
-// Arrive (once) on the mbarrier at the same shared-memory offset in every
-// CTA of `mask` (cluster) when every MMA issued so far has completed.
-__device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- CTA pairs (cta_group::2)
 // The 2-SM form: the two CTAs of a cluster pair hold one half each of the
 // A rows (M = 256 -> 128 per CTA) and of the B columns (N / 2 each); one

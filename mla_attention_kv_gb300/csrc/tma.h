@@ -37,27 +37,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar)
       : "memory");
 }
-// Tiled 2-D load of one box into the same shared-memory offset of every
-// CTA in `mask` (this GPU's own memory, thread-block cluster multicast);
-// each destination CTA's mbarrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c_inner,
-                                               int c_outer, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
-      "l"(map), "r"(c_inner), "r"(c_outer), "r"(bar), "h"(mask)
-      : "memory");
-}
-// 3-D tiled load of one box into the same shared-memory offset of every CTA
-// in `mask` (cluster multicast); x * element size must be a multiple of 16.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               int z, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
-      : "memory");
-}
 // Tiled loads into this CTA's shared memory whose completion (bytes) is
 // counted on an mbarrier of either CTA of a pair (`bar` is a cluster
 // address): the 2-SM MMA's operands arrive on the issuing CTA's barrier.

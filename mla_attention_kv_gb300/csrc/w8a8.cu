@@ -373,7 +373,10 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   norm_row(a, sx[t], p, yrow, colsc, gq, gk, rope, scratch, w.q1 + (size_t)t * rq, w.s1 + t,
            w.c1 + (size_t)t * kRank, w.s2 + t,
            static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope);
-  // leave the accumulator row zeroed (the decode-size chain adds into it)
+  // leave the accumulator row zeroed (the decode-size chain adds into it),
+  // after copying it out when the accumulators are captured
+  if (p.cap_a)
+    for (int c = threadIdx.x; c < na; c += 256) p.cap_a[(size_t)t * na + c] = a[c];
   for (int c = threadIdx.x; c < na; c += 256) a[c] = 0;
 }
 
@@ -395,6 +398,9 @@ __global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __rest
   const size_t orow = ((size_t)bi * H + hh) * p.s + si;
   const int j = threadIdx.x;  // 0..63
   auto deq = [&](int c) { return __fmul_rn(__fmul_rn((float)a[c], s), sc[c]); };
+  int32_t* cap = mode == 0 ? p.cap_qb : p.cap_kvb;
+  if (cap)
+    for (int c = j; c < width; c += 64) cap[(size_t)t * ld + (size_t)hh * width + c] = a[c];
   if (mode == 0) {
     __nv_bfloat16* qn = static_cast<__nv_bfloat16*>(p.q_nope) + orow * kNope;
     qn[2 * j] = __float2bfloat16_rn(deq(2 * j));
@@ -769,6 +775,12 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
       norm_row(p.acc1 + (size_t)m * na, p.sx[m], p.pr, yrow, colsc, gq, gk, rope + m * 2 * kRope,
                scratch, sAct0 + m * p.kpad[0], srow + m, sAct1 + m * p.kpad[1], srow + MT + m,
                cta == 0 ? static_cast<__nv_bfloat16*>(p.pr.k_pe) + (size_t)m * kRope : nullptr);
+    // captured accumulators: CTA 0 copies the q_a / kv_a rows before it
+    // counts itself as a reader (the last reader clears them)
+    if (cta == 0 && p.pr.cap_a) {
+      for (int i = tid; i < p.M * na; i += 256) p.pr.cap_a[i] = p.acc1[i];
+      __syncthreads();
+    }
     // the last CTA to finish reading acc1 clears it for the next call
     if (tid == 0) s_last = atomicAdd(p.readers, 1u) == (unsigned)G - 1 ? 1 : 0;
     __syncthreads();
@@ -883,6 +895,8 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
         *reinterpret_cast<int2*>(p.raw + (size_t)m * p.raw_ld + gc) = make_int2(v0, v1);
         continue;
       }
+      int32_t* cap = sel ? p.pr.cap_kvb : p.pr.cap_qb;
+      if (cap) *reinterpret_cast<int2*>(cap + (size_t)m * p.N[sel] + gc) = make_int2(v0, v1);
       const float sr = srow[sel * MT + m];
       const float y0 = __fmul_rn(__fmul_rn((float)v0, sr), sc0);
       const float y1 = __fmul_rn(__fmul_rn((float)v1, sr), sc1);

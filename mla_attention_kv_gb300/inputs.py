@@ -152,3 +152,25 @@ def sampled_rows(b: int, s: int, n: int, seed: int) -> list:
         rows.update(torch.randint(0, T, (n,), generator=g).tolist())
     return sorted(rows)
 
+
+
+def tile_rows(b: int, s: int, n: int, seed: int, tile: int = 128) -> list:
+    """Token rows for sampled parity at full size that reach every part of a
+    tiled kernel: the first and last row of every sequence, at least one row
+    in every ``tile``-row tile and at least one row at every offset 0 ..
+    tile-1 within a tile (tiles and offsets paired by a seeded shuffle),
+    plus ``n`` seeded random rows; sorted and unique."""
+    g = torch.Generator().manual_seed(seed)
+    T = b * s
+    rows = set(sampled_rows(b, s, n, seed))
+    if T == 0:
+        return []
+    ntiles = (T + tile - 1) // tile
+    offs = torch.randperm(tile, generator=g).tolist()
+    tiles = torch.randperm(ntiles, generator=g).tolist()
+    for i in range(max(ntiles, tile)):
+        r = tiles[i % ntiles] * tile + offs[i % tile]
+        if r >= T:  # the last tile is ragged: any row of it
+            r = tiles[i % ntiles] * tile + offs[i % tile] % (T - tiles[i % ntiles] * tile)
+        rows.add(r)
+    return sorted(rows)

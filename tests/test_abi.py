@@ -72,6 +72,8 @@ def test_null_arguments(L):
     assert L.mla_kv_prolog_set_path(None, 0) == 1
     assert L.mla_kv_prolog_last_launches(None) == -1
     assert L.mla_prolog_w8a8_operands(None, 1, None, None, None, None, None) == 1
+    assert L.mla_kv_prolog_auto_threshold(None) == -1
+    assert L.mla_prolog_w8a8_capture(None, None, None, None) == 1
 
 
 def test_building_block_shape_checks(L):

@@ -91,6 +91,6 @@ def test_c8_decode_r1(oracle_mod):
 
 @pytest.mark.parametrize("T", [1024, 1061])
 def test_c8_prefill_v2lite(oracle_mod, T):
-    rows = I.sampled_rows(1, T, 48, seed=T + 1)
+    rows = I.tile_rows(1, T, 512, seed=T + 1)
     run_c8(I.V2_LITE, 1, T, 520 + T, B.PATH_PREFILL, positions="prefill", oracle_mod=oracle_mod,
            rows=rows)

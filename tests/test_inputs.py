@@ -90,3 +90,16 @@ def test_rope_tables():
     # column j at position p is cos(p * theta^(-2j/64)) rounded to fp32
     p, j = 37, 5
     assert cos[p, j].item() == pytest.approx(math.cos(p * 10000.0 ** (-2 * j / 64)), abs=1e-7)
+
+
+def test_tile_rows_cover_every_tile_and_offset():
+    for b, s in ((4, 4096), (2, 8192), (1, 8192), (1, 300), (3, 100)):
+        T = b * s
+        rows = I.tile_rows(b, s, 512, seed=7)
+        assert rows == sorted(set(rows)) and all(0 <= r < T for r in rows)
+        assert {r // 128 for r in rows} == set(range((T + 127) // 128))
+        if T >= 128:
+            assert {r % 128 for r in rows} == set(range(128))
+        for bi in range(b):
+            assert bi * s in rows and bi * s + s - 1 in rows
+        assert len(rows) >= min(T, 512) * 0.8

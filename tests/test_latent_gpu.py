@@ -81,7 +81,7 @@ def test_latent_prefill_v2lite(oracle_mod, T):
 
 def test_latent_prefill_r1_sampled(oracle_mod):
     b, s = 2, 8192
-    rows = I.sampled_rows(b, s, 24, seed=2005)
+    rows = I.tile_rows(b, s, 512, seed=2005)
     r = run_latent(I.R1, b, s, 341, positions="prefill", path=B.PATH_PREFILL, rows=rows,
                    oracle_mod=oracle_mod)
     assert r["status"] == 0

@@ -105,7 +105,7 @@ def test_paged_decode_two_launches(oracle_mod):
 def test_paged_prefill_v2lite(oracle_mod, T):
     page, nblk = 16, (T + 15) // 16 + 3
     slots = make_slots(T, page, nblk, 4, drop=(5, T - 1))
-    rows = I.sampled_rows(1, T, 48, seed=T)
+    rows = I.tile_rows(1, T, 512, seed=T)
     assert run_paged(I.V2_LITE, 1, T, 404, page, nblk, slots, B.PATH_PREFILL, positions="prefill",
                      oracle_mod=oracle_mod, rows=rows) == 0
 

@@ -68,14 +68,14 @@ def test_prefill_matches_decode_path():
 
 def test_prefill_v2lite_full_size_sampled(oracle_mod):
     b, s = 4, 4096
-    rows = I.sampled_rows(b, s, 96, seed=2002)
+    rows = I.tile_rows(b, s, 512, seed=2002)
     r = run(I.V2_LITE, b, s, I.seed_for(2), "prefill", B.PATH_AUTO, oracle_mod, rows=rows)
     assert r["status"] == 0 and r["path"] == B.PATH_PREFILL
 
 
 def test_prefill_r1_full_size_sampled(oracle_mod):
     b, s = 2, 8192
-    rows = I.sampled_rows(b, s, 40, seed=2003)
+    rows = I.tile_rows(b, s, 512, seed=2003)
     r = run(I.R1, b, s, I.seed_for(3), "prefill", B.PATH_AUTO, oracle_mod, rows=rows)
     assert r["status"] == 0 and r["path"] == B.PATH_PREFILL
 
@@ -85,3 +85,20 @@ def test_prefill_deterministic():
     b = run(I.V2_LITE, 1, 300, 5, "prefill", B.PATH_PREFILL)
     for k in ("k_nope", "value", "k_pe"):
         assert torch.equal(a["out"][k].view(torch.int16), b["out"][k].view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg", [I.V2_LITE, I.R1], ids=["v2lite", "r1"])
+def test_auto_path_around_threshold(oracle_mod, cfg):
+    """PATH_AUTO on the dense path just below, at and just above the token
+    count where it switches from the decode kernel to the prefill kernel
+    (the bucketed replacement of [MIG] §源码级原理's short / long
+    selection): the right kernel runs and the outputs match the oracle."""
+    m = B.MLAProlog(cfg, 1)
+    thr = m.auto_threshold
+    m.close()
+    assert thr > 1
+    for T in (thr - 1, thr, thr + 1):
+        rows = I.tile_rows(1, T, 64, seed=T)
+        r = run(cfg, 1, T, 900 + T, "prefill", B.PATH_AUTO, oracle_mod, rows=rows)
+        assert r["status"] == 0
+        assert r["path"] == (B.PATH_PREFILL if T >= thr else B.PATH_DECODE), (T, thr)

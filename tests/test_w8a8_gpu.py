@@ -94,7 +94,7 @@ def test_w8a8_r1_decode(oracle_mod, b, s):
 
 def test_w8a8_r1_prefill_sampled(oracle_mod):
     b, s = 1, 8192
-    rows = I.sampled_rows(b, s, 24, seed=2004)
+    rows = I.tile_rows(b, s, 512, seed=2004)
     r = run_w8(I.R1_W8A8, b, s, I.seed_for(4), positions="prefill", rows=rows, oracle_mod=oracle_mod)
     assert r["status"] == 0
 
@@ -166,3 +166,45 @@ def test_w8a8_small_chain_repeats_and_alternates(oracle_mod):
             compare(n, outs[0][n], r, oracle_mod)
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("b,s", [(1, 1), (2, 1), (4, 1), (8, 1), (64, 1), (3, 33)])
+def test_w8a8_run_accumulators_bit_exact(oracle_mod, b, s):
+    """The int32 accumulators that the run's own kernels formed (captured
+    from the kernels of the call: the decode-size chain at T <= 8, the
+    prefill-size path above), bit for bit against the oracle's brute-force
+    integer GEMM ([R1] §权重转换, W8A8: int32 accumulation is exact).
+    q_a | kv_a: the oracle quantises the bf16 hidden rows itself (the codes
+    are bit-identical on both sides).  q_b, kv_b: the operands are the
+    GPU's own requantised rows (they may differ from the oracle's by one
+    code at rounding ties, which the operand test bounds)."""
+    cfg = I.R1_W8A8
+    T, H, rq = b * s, cfg["num_heads"], cfg["q_lora_rank"]
+    inp = I.w8a8_inputs(cfg, b, s, 5150 + T, "decode")
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, T)
+    try:
+        cap_a = torch.full((T, rq + 576), -7, dtype=torch.int32, device="cuda")
+        cap_qb = torch.full((T, H * 192), -7, dtype=torch.int32, device="cuda")
+        cap_kvb = torch.full((T, H * 256), -7, dtype=torch.int32, device="cuda")
+        B.mla_prolog_w8a8_capture(m.h, cap_a, cap_qb, cap_kvb)
+        out = m.alloc_outputs(b, s)
+        m.run(b, s, d, out)
+        q1 = torch.empty(T, rq, dtype=torch.int8, device="cuda")
+        s1 = torch.empty(T, dtype=torch.float32, device="cuda")
+        c1 = torch.empty(T, 512, dtype=torch.int8, device="cuda")
+        s2 = torch.empty(T, dtype=torch.float32, device="cuda")
+        B.mla_prolog_w8a8_operands(m.h, T, q1, s1, c1, s2)
+        torch.cuda.synchronize()
+        assert m.status() == 0
+        B.mla_prolog_w8a8_capture(m.h)
+    finally:
+        m.close()
+    rows = sorted({0, T - 1, T // 2, min(1, T - 1)})
+    hid = inp["hidden"].float().numpy()
+    qx = np.stack([oracle_mod.quant_row_f32(hid[t])[0] for t in rows])
+    w_a = np.concatenate([inp["W_qa"].numpy(), inp["W_kva"].numpy()], axis=1)
+    assert np.array_equal(cap_a.cpu().numpy()[rows].astype(np.int64), oracle_mod.int_gemm(qx, w_a))
+    for cap, A, W in ((cap_qb, q1, inp["W_qb"]), (cap_kvb, c1, inp["W_kvb"])):
+        ref = oracle_mod.int_gemm(A.cpu().numpy()[rows], W.numpy())
+        assert np.array_equal(cap.cpu().numpy()[rows].astype(np.int64), ref)
