@@ -45,10 +45,6 @@ sys.path.insert(0, ROOT)
 
 from mla_attention_kv_gb300 import inputs as I  # noqa: E402
 
-# mma.sync m16n8k32 s8 throughput measured on a GB300 (the
-# tcgen05 int8 kind does not exist on sm_103a); see profiles/mma_sync_rates.md
-INT8_MMA_SYNC_TOPS = 148.8
-
 SWEEP_B = [1, 2, 4, 8, 16, 32, 64, 128]
 SWEEP_S = [1, 2]
 
@@ -84,9 +80,13 @@ def carve_dicts(dicts, device, pin=False):
 
 
 class DecodeSweep:
-    name = "v2lite_kv_prolog_decode_sweep"
+    """The V2-Lite decode sweep.  packed: every weight copy gets the decode
+    kernel's packed snapshot (mla_kv_prolog_prepare_weights, once, outside
+    the timed region); otherwise the calls read the raw [in, out] weights."""
 
-    def __init__(self):
+    def __init__(self, packed=True):
+        self.packed = packed
+        self.name = "v2lite_kv_prolog_decode_sweep" + ("" if packed else "_raw_weights")
         self.cfg = I.V2_LITE
         self.points = [(b, s) for s in SWEEP_S for b in SWEEP_B]
         self.tokens_per_step = sum(b * s for b, s in self.points)
@@ -96,8 +96,9 @@ class DecodeSweep:
                 "kv_lora_rank": 512, "rope_dim": 64, "num_heads": 16, "nope_dim": 128,
                 "v_dim": 128, "points": [f"b{b}s{s}" for b, s in self.points],
                 "tokens_per_step": self.tokens_per_step, "positions": "uniform per sequence in [0,4095]",
-                "weights": "one handle per weight copy, packed once by mla_kv_prolog_prepare_weights "
-                           "outside the timed region"}
+                "weights": ("one handle per weight copy, packed once by mla_kv_prolog_prepare_weights "
+                            "outside the timed region" if self.packed else
+                            "raw [in, out] weights passed to every call (no packed snapshot)")}
 
     def weight_bytes(self):
         c = self.cfg
@@ -130,7 +131,8 @@ class DecodeSweep:
         self.ms = []
         for w in self.wcopies:
             m = B.MLAProlog(self.cfg, tmax)
-            m.prepare_weights(w)
+            if self.packed:
+                m.prepare_weights(w)
             self.ms.append(m)
         torch.cuda.synchronize(dev)
         self.m = self.ms[0]
@@ -476,6 +478,7 @@ def _single(name, cfg, b, s, positions, path_name, seed, latent=False, paged=Non
 
 WORKLOADS = {
     "decode_sweep": DecodeSweep,
+    "decode_sweep_raw": lambda: DecodeSweep(packed=False),
     "v2lite_tiny": _single("v2lite_kv_prolog_tiny_b1s2", I.V2_LITE, 1, 2, [7, 8], "auto", 1000),
     "v2lite_prefill": _single("v2lite_kv_prolog_prefill_b4s4096", I.V2_LITE, 4, 4096, "prefill", "auto", 1002),
     "r1_decode": _single("r1_kv_prolog_decode_b64s1", I.R1, 64, 1, "decode", "auto", 1003),
@@ -633,7 +636,16 @@ def job_tokens_per_s(tokens_per_step: int, steps: int, world: int, ms: float) ->
     return tokens_per_step * steps * world / (ms / 1e3)
 
 
-def run_gpu(args, wl, rank, world, dev):
+# Workloads measured beside the default decode sweep (one GPU): every other
+# configuration of the benchmark, each as its own graph-replayed timed region.
+EXTRA_WORKLOADS = ["decode_sweep_raw", "v2lite_tiny", "v2lite_prefill", "r1_decode", "r1_prefill",
+                   "w8a8_t1", "w8a8_t64", "w8a8_t8192"]
+
+
+def run_gpu(args, wl, rank, world, dev, full=True):
+    """Time wl: W warm-up steps, then K graph-replayed steps (re-measured
+    once if the clocks disqualify them); with full, also the same K steps
+    launched eagerly and the e2e pass from host buffers."""
     from mla_attention_kv_gb300 import build as BLD
     if rank == 0:
         BLD.build()
@@ -696,6 +708,9 @@ def run_gpu(args, wl, rank, world, dev):
     if max_over_ranks(1.0 if why else 0.0, world, dev) > 0:
         first = {"ms_per_step": ms / args.steps, "clocks": clk, "why": why or "another rank's clocks"}
         ms, region_ms, calls, clk, total_launches = timed(graph_run)
+    if not full:
+        return dict(ms=ms, region_ms=region_ms, calls=calls, clk=clk, launches=total_launches,
+                    host_per_step=host_per_step, first_attempt=first)
     # the same K steps launched eagerly through the binding, call by call
     ms_e, _, calls_e, clk_e, _ = timed(lambda k, ev, iv: wl.step(stream, ev, iv))
 
@@ -718,8 +733,8 @@ def run_gpu(args, wl, rank, world, dev):
 
 
 def kernel_traffic(kernel: str, T: int, model: str = ""):
-    """DRAM bytes of one call of `kernel` at T rows (entry "<model>:<T>", else
-    "<T>") from the committed ncu summary, or None when the summary is missing
+    """DRAM bytes of one call of `kernel` at T rows (entry "<model>:<T>") from
+    the committed ncu summary, or None when the summary is missing
     or was taken on a different version of the kernel's source (its sha256 no
     longer matches)."""
     import hashlib
@@ -731,32 +746,30 @@ def kernel_traffic(kernel: str, T: int, model: str = ""):
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if h != t[kernel]["sha256_16"]:
             return None
-        b = t[kernel]["bytes_per_call"]
-        return b.get("%s:%d" % (model, T), b.get(str(T)))
+        return t[kernel]["bytes_per_call"].get("%s:%d" % (model, T))
     except Exception:
         return None
 
 
-def gpu_line(args, wl, r, world, dtype, is_w8):
-    """The JSON line of the GPU arm from run_gpu's measurements: whole-job
-    tokens/s, the roofline of the dominant kernel, clocks, e2e, the eager
-    pass and (for the sweep) per-point figures; cpu_baseline is added by
-    the caller."""
-    value = job_tokens_per_s(wl.tokens_per_step, args.steps, world, r["ms"])
+def roofline(wl, calls, is_w8):
+    """Roofline of the timed calls [(ms, [T, ...]), ...]: algorithmic bytes
+    or FLOPs (whichever takes longer at the measured peak) over the calls'
+    summed CUDA-event time, against that peak; plus the committed ncu DRAM
+    traffic per call when it matches the kernel source."""
     peaks, peak_kind = measured_peaks()
-    calls = r["calls"]
     Tlist = [T for _, Ts in calls for T in Ts]
     alg_bytes = sum(wl.alg_bytes(T) for T in Tlist)
     alg_flops = sum(wl.flops(T) for T in Tlist)
     call_s = sum(c for c, _ in calls) / 1e3
-    # roofline: the bound is the resource whose time at peak is larger
+    # the bound is the resource whose time at peak is larger; the W8A8 int8
+    # products run as exact bf16 tensor-core products, so their peak is bf16's
     bw = peaks["hbm_gbs"] * 1e9
-    if is_w8:
-        tensor_peak, tensor_unit = INT8_MMA_SYNC_TOPS * 1e12, "TOPS (measured mma.sync s8)"
-    else:
-        tensor_peak, tensor_unit = peaks["bf16_tflops"] * 1e12, "TFLOP/s"
+    tensor_peak = peaks["bf16_tflops"] * 1e12
+    tensor_unit = "TFLOP/s (bf16 tensor peak; int8 products as exact bf16)" if is_w8 else "TFLOP/s"
     t_mem, t_cmp = alg_bytes / bw, alg_flops / tensor_peak
-    path = "prefill" if (not is_w8 and getattr(wl, "T", 0) >= 1024) else "decode"
+    m = getattr(wl, "m", None)
+    last = getattr(m, "last_path", 1) if m is not None else 1
+    path = "prefill" if (not is_w8 and last == 2) else "decode"
     kernel = {"prefill": "prefill_kernel", "decode": "decode_kernel"}[path] if not is_w8 else "w8a8 pipeline"
     if getattr(wl, "latent", False):
         kernel += " (latent variant)"
@@ -783,6 +796,43 @@ def gpu_line(args, wl, r, world, dtype, is_w8):
                  "algorithmic_bytes_per_call": alg_bytes / len(Tlist),
                  "algorithmic_flops_per_call": alg_flops / len(Tlist),
                  "timing": "CUDA events around each CUDA-graph replay of a step"})
+    return roof
+
+
+def workload_summary(args, name, dev):
+    """One other workload, timed like the headline (graph replays, L2 rule,
+    clocks) with args.workload_steps steps: per-call time, tokens/s,
+    roofline and clocks."""
+    wl = WORKLOADS[name]()
+    a = argparse.Namespace(**vars(args))
+    a.steps, a.warmup = args.workload_steps, 3
+    r = run_gpu(a, wl, 0, 1, dev, full=False)
+    calls = r["calls"]
+    ntok = sum(T for _, Ts in calls for T in Ts)
+    out = {"config": wl.describe(), "steps": a.steps, "ms_per_step": r["ms"] / a.steps,
+           "mean_call_us": 1e3 * sum(c for c, _ in calls) / sum(len(Ts) for _, Ts in calls),
+           "tokens_per_s": ntok / (sum(c for c, _ in calls) / 1e3),
+           "roofline": roofline(wl, calls, getattr(wl, "w8", False)),
+           "gpu_launches": r["launches"], "clocks": r["clk"], "clocks_ok": clocks_rejected(r["clk"]) is None}
+    if r["first_attempt"] is not None:
+        out["remeasured"] = r["first_attempt"]
+    for m in getattr(wl, "ms", [getattr(wl, "m", None)]):
+        if m is not None:
+            m.close()
+    del wl
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+def gpu_line(args, wl, r, world, dtype, is_w8):
+    """The JSON line of the GPU arm from run_gpu's measurements: whole-job
+    tokens/s, the roofline of the dominant kernel, clocks, e2e, the eager
+    pass and (for the sweep) per-point figures; cpu_baseline is added by
+    the caller."""
+    value = job_tokens_per_s(wl.tokens_per_step, args.steps, world, r["ms"])
+    peaks, _ = measured_peaks()
+    roof = roofline(wl, r["calls"], is_w8)
     line = {
         "metric": "tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
@@ -832,6 +882,10 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="seconds of the oracle's warm-up + timed steps under --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload-steps", type=int, default=10,
+                    help="timed steps of each other workload measured beside the default sweep")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only the chosen workload (no 'workloads' object)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -868,6 +922,13 @@ def main():
     r = run_gpu(args, wl, rank, world, dev)
 
     line = gpu_line(args, wl, r, world, dtype, is_w8)
+    if args.workload == "decode_sweep" and world == 1 and not args.no_workloads:
+        line["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            try:
+                line["workloads"][name] = workload_summary(args, name, dev)
+            except Exception as e:  # a failure is reported in the line, not hidden
+                line["workloads"][name] = {"error": repr(e)[:300]}
     if rank == 0 and not args.no_cpu_baseline:
         v, cores, sample, n, el = oracle_steps(wl, 4, 1, args.cpu_seconds)
         sample += f"; 1 untimed + 4 timed steps, {el:.1f} s timed"

@@ -40,6 +40,9 @@ class FakeProlog:
     def set_path(self, path):
         self.path = path
 
+    def close(self):
+        self.closed = True
+
     def prepare_weights(self, d):
         self.packed = d["W_kva"].data_ptr()
 

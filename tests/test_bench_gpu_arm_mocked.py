@@ -98,8 +98,9 @@ def check_line(line, wl, steps):
     assert line["remeasured"]["why"] == "throttled: hw_slowdown"
 
 
-def test_decode_sweep_gpu_arm(fake_cuda):
-    wl = bench.DecodeSweep()
+@pytest.mark.parametrize("packed", [True, False])
+def test_decode_sweep_gpu_arm(fake_cuda, packed):
+    wl = bench.DecodeSweep(packed=packed)
     a = args_for(steps=3)
     r = bench.run_gpu(a, wl, 0, 1, fake_cuda)
     line = bench.gpu_line(a, wl, r, 1, "f16", False)
@@ -110,9 +111,20 @@ def test_decode_sweep_gpu_arm(fake_cuda):
     assert len(r["calls_eager"]) == 3 * len(wl.points)
     assert set(line["per_point"]) == {f"b{b}s{s}" for b, s in wl.points}
     assert line["gpu_launches"] == 3 * wl.graph_launches
+    assert all((m.packed is not None) == packed for m in FakeProlog.made)
 
 
-@pytest.mark.parametrize("name", sorted(n for n in bench.WORKLOADS if n != "decode_sweep"))
+def test_workload_summary(fake_cuda):
+    a = args_for(steps=3)
+    a.workload_steps = 2
+    for name in bench.EXTRA_WORKLOADS:
+        out = bench.workload_summary(a, name, fake_cuda)
+        json.dumps(out)
+        assert out["steps"] == 2 and out["mean_call_us"] > 0 and out["tokens_per_s"] > 0
+        assert out["roofline"]["frac"] == pytest.approx(out["roofline"]["achieved"] / out["roofline"]["peak"])
+
+
+@pytest.mark.parametrize("name", sorted(n for n in bench.WORKLOADS if not n.startswith("decode_sweep")))
 def test_single_call_gpu_arm(fake_cuda, name):
     wl = bench.WORKLOADS[name]()
     a = args_for(steps=4)
