@@ -2,6 +2,7 @@
 // kernel translation units.  Not installed; not part of the ABI.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -178,14 +179,22 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
 
 // ---------------------------------------------------------------- W8A8 path
 struct W8Workspace {
-  int8_t* xq;     // [max_tokens, hidden]
+  __half* xh;     // [max_tokens, hidden] fp16 codes of the quantised hidden rows
   float* sx;      // [max_tokens]
   int32_t* acc1;  // [max_tokens, q_rank + 576]
   int8_t* q1;     // [max_tokens, q_rank]
   float* s1;      // [max_tokens]
   int8_t* c1;     // [max_tokens, 512]
   float* s2;      // [max_tokens]
-  int32_t* acc2;  // [max_tokens, max(H*192, H*256)]
+  __half* q1h;    // [max_tokens, q_rank] fp16 codes of q1 (the q_b operand)
+  __half* c1h;    // [max_tokens, 512] fp16 codes of c1 (the kv_b operand)
+  // fp16 copies of the int8 weights for the prefill-size GEMMs (null when
+  // max_tokens < kW8PairMinRows): [W_qa | W_kva] [hidden, lda], W_qb [q_rank,
+  // ldqb], W_kvb [512, ldkvb], rows padded to multiples of 256 with zeros
+  __half* wa16;
+  __half* wqb16;
+  __half* wkvb16;
+  int lda, ldqb, ldkvb;
   unsigned* readers;  // decode-size chain: CTAs done reading acc1
 };
 
@@ -238,6 +247,83 @@ struct W8Params {
   float eps;
   unsigned long long budget_ns;
 };
+
+// Tensor-core int8 GEMMs of the W8A8 prolog (w8mma.cu): up to two weight
+// matrices W_i [K_i, N_i] int8 against fp16 activation codes X_i [T, K_i],
+// exact int32 sums.  raw: added into C (q_a | kv_a accumulator rows);
+// otherwise dequantised into the head-major outputs (q_b, kv_b).
+struct W8MmaParams {
+  CUtensorMap tw[2];        // filled by w8mma_launch
+  CUtensorMap tx[2];
+  int K[2], N[2];           // K multiple of 64, N multiple of 32 (N = 0: no matrix)
+  int mt[2], ks[2], kbps[2], nunits[2];  // filled: 128-column tiles, K splits, K blocks per split, units
+  int mfast[2];             // filled: unit order, weight tiles fastest (1) or token tiles fastest (0)
+  unsigned s_mul, s_shift;  // filled: t / s = (umulhi(t, s_mul) + t) >> s_shift
+  int NT, xrows, ntiles, stages;         // filled: tokens per tile, box rows, token tiles, ring depth
+  int T;
+  int raw;                  // 1: int32 sums added into C
+  int32_t* C;               // raw: [T, ldc]
+  int ldc;
+  int coff[2];              // raw: column of matrix i in C
+  const float* sx[2];       // heads: per-token activation scales of X_i
+  const float* sw[2];       // heads: per-column weight scales of W_i
+  const int32_t* positions;
+  const float* cos_t;
+  const float* sin_t;
+  int max_pos;
+  void* q_nope;             // heads, matrix 0 (q_b): [b,H,s,128], q_pe [b,H,s,64]
+  void* q_pe;
+  void* k_nope;             // heads, matrix 1 (kv_b): [b,H,s,128] each
+  void* value;
+  int32_t* cap[2];          // heads: accumulator capture [T, N_i] (null: off)
+  int heads, s;
+  unsigned* status;
+  unsigned long long budget_ns;
+};
+size_t w8mma_smem(int NT, int stages);
+
+// Prefill-size int8 GEMMs of the W8A8 prolog on the 2-SM MMA (w8pair.cu):
+// activations X_i fp16 codes [T, K_i], weights widened to fp16 [K_i, ldw_i]
+// (ldw_i a multiple of 256, columns N_i .. ldw_i-1 zero).
+struct W8PairParams {
+  int K[2], N[2], ldw[2];   // N = 0: no matrix
+  int ntiles[2], nn[2];     // filled: pair tiles per matrix, 256-column tiles
+  unsigned s_mul, s_shift;  // filled: t / s
+  int T;
+  int raw;                  // 1: int32 sums stored into C
+  int32_t* C;
+  int ldc;
+  int coff[2];
+  const float* sx[2];
+  const float* sw[2];
+  const int32_t* positions;
+  const float* cos_t;
+  const float* sin_t;
+  int max_pos;
+  void* q_nope;
+  void* q_pe;
+  void* k_nope;
+  void* value;
+  int32_t* cap[2];
+  int heads, s;
+  unsigned* status;
+  unsigned long long budget_ns;
+};
+cudaError_t w8pair_launch(W8PairParams p, const void* X0, const void* X1, const __half* W0, const __half* W1,
+                          int num_sms, cudaStream_t stream);
+// One int8 matrix [K, N] widened to fp16 rows of ldn elements at `out`,
+// columns [0, wcols) written (zeros past N).
+struct W8WidenJob {
+  const int8_t* W;
+  __half* out;
+  int K, N, ldn, wcols;
+};
+cudaError_t w8_widen_launch(const W8WidenJob* jobs, int n, int num_sms, cudaStream_t stream);
+// Token count from which the W8A8 prolog runs its GEMMs on the 2-SM kernel
+// (widened weights); below it the int8-converting single-SM kernel.
+constexpr int kW8PairMinRows = 512;
+cudaError_t w8mma_launch(W8MmaParams p, const int8_t* W0, const int8_t* W1, const void* X0, const void* X1,
+                         int num_sms, cudaStream_t stream, bool pdl);
 
 size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens, int num_sms);
 void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,

@@ -23,6 +23,7 @@
 // few output tiles to fill the GPU the K range is split across CTAs and
 // the int32 partials are added with atomics, which is exact and
 // order-independent.
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -185,9 +186,12 @@ __device__ __forceinline__ int8_t q8(float x, float inv) {
   return (int8_t)(int)r;
 }
 
-// One CTA (256 threads) per row of a bf16 matrix [rows, cols] -> int8 + scale.
+// One CTA (256 threads) per row of a bf16 matrix [rows, cols] -> codes +
+// scale.  The codes are stored as int8, or (Q = __half) as the fp16 values
+// of the same integers (the tensor-core GEMM operand; exact for |q| <= 127).
+template <typename Q>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ x, int cols,
-                                                         int8_t* __restrict__ q,
+                                                         Q* __restrict__ q,
                                                          float* __restrict__ scale) {
   __shared__ float scratch[8];
   const int row = blockIdx.x;
@@ -204,13 +208,20 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   for (int c = threadIdx.x * 8; c < cols; c += 256 * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-    char4 lo, hi;
-    lo.x = q8(__bfloat162float(e[0]), inv); lo.y = q8(__bfloat162float(e[1]), inv);
-    lo.z = q8(__bfloat162float(e[2]), inv); lo.w = q8(__bfloat162float(e[3]), inv);
-    hi.x = q8(__bfloat162float(e[4]), inv); hi.y = q8(__bfloat162float(e[5]), inv);
-    hi.z = q8(__bfloat162float(e[6]), inv); hi.w = q8(__bfloat162float(e[7]), inv);
-    *reinterpret_cast<char4*>(q + (size_t)row * cols + c) = lo;
-    *reinterpret_cast<char4*>(q + (size_t)row * cols + c + 4) = hi;
+    if constexpr (std::is_same<Q, int8_t>::value) {
+      char4 lo, hi;
+      lo.x = q8(__bfloat162float(e[0]), inv); lo.y = q8(__bfloat162float(e[1]), inv);
+      lo.z = q8(__bfloat162float(e[2]), inv); lo.w = q8(__bfloat162float(e[3]), inv);
+      hi.x = q8(__bfloat162float(e[4]), inv); hi.y = q8(__bfloat162float(e[5]), inv);
+      hi.z = q8(__bfloat162float(e[6]), inv); hi.w = q8(__bfloat162float(e[7]), inv);
+      *reinterpret_cast<char4*>(q + (size_t)row * cols + c) = lo;
+      *reinterpret_cast<char4*>(q + (size_t)row * cols + c + 4) = hi;
+    } else {
+      __align__(16) __half h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = __int2half_rn((int)q8(__bfloat162float(e[i]), inv));
+      *reinterpret_cast<uint4*>(q + (size_t)row * cols + c) = *reinterpret_cast<const uint4*>(h);
+    }
   }
   if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 }
@@ -278,7 +289,7 @@ __device__ __forceinline__ void rope_load(const W8Params& p, int t, float* rope)
 __device__ void norm_row(const int32_t* a, float s, const W8Params& p, float* yrow,
                          const float* colsc, const float* gq, const float* gk, const float* rope,
                          float* scratch, int8_t* q_out, float* s1_out, int8_t* c_out, float* s2_out,
-                         __nv_bfloat16* kpe_out) {
+                         __nv_bfloat16* kpe_out, __half* qh_out = nullptr, __half* ch_out = nullptr) {
   const int rq = p.q_rank, na4 = (rq + kNa) / 4;
   int4 av[kNormVec];
 #pragma unroll
@@ -314,7 +325,11 @@ __device__ void norm_row(const int32_t* a, float s, const W8Params& p, float* yr
   amax = block_reduce<true>(amax, scratch);
   {
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    for (int c = threadIdx.x; c < rq; c += 256) q_out[c] = q8(yrow[c], inv);
+    for (int c = threadIdx.x; c < rq; c += 256) {
+      const int8_t v = q8(yrow[c], inv);
+      q_out[c] = v;
+      if (qh_out) qh_out[c] = __int2half_rn((int)v);
+    }
     if (threadIdx.x == 0) *s1_out = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
   }
   // compressed_kv
@@ -333,7 +348,11 @@ __device__ void norm_row(const int32_t* a, float s, const W8Params& p, float* yr
   amax = block_reduce<true>(amax, scratch);
   {
     const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-    for (int i = 0; i < 2; ++i) c_out[threadIdx.x + i * 256] = q8(nv[i], inv);
+    for (int i = 0; i < 2; ++i) {
+      const int8_t v = q8(nv[i], inv);
+      c_out[threadIdx.x + i * 256] = v;
+      if (ch_out) ch_out[threadIdx.x + i * 256] = __int2half_rn((int)v);
+    }
     if (threadIdx.x == 0) *s2_out = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
   }
   // RoPE of k_pe (raw columns 512..575 of the kv_a output)
@@ -372,7 +391,8 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   int32_t* a = acc1 + (size_t)t * na;
   norm_row(a, sx[t], p, yrow, colsc, gq, gk, rope, scratch, w.q1 + (size_t)t * rq, w.s1 + t,
            w.c1 + (size_t)t * kRank, w.s2 + t,
-           static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope);
+           static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope, w.q1h + (size_t)t * rq,
+           w.c1h + (size_t)t * kRank);
   // leave the accumulator row zeroed (the decode-size chain adds into it),
   // after copying it out when the accumulators are captured
   if (p.cap_a)
@@ -380,48 +400,129 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   for (int c = threadIdx.x; c < na; c += 256) a[c] = 0;
 }
 
-// Dequantise q_b / kv_b accumulators and write the head-major outputs.
-// mode 0: row = [H, 192] -> q_nope [b,H,s,128], RoPE(q_pe) [b,H,s,64]
-// mode 1: row = [H, 256] -> k_nope [b,H,s,128], value [b,H,s,128]
-// Grid (T, H); 64 threads, each 2 (mode 1: 4) columns.
-__global__ void __launch_bounds__(64) head_epilogue_kernel(const int32_t* __restrict__ acc,
-                                                           const float* __restrict__ srow,
-                                                           const float* __restrict__ scol,
-                                                           W8Params p, int mode) {
-  const int t = blockIdx.x, hh = blockIdx.y, H = p.heads;
-  const int bi = t / p.s, si = t - bi * p.s;
-  const int width = mode == 0 ? kNope + kRope : kHeadCols;
-  const size_t ld = (size_t)H * width;
-  const int32_t* a = acc + (size_t)t * ld + (size_t)hh * width;
-  const float* sc = scol + (size_t)hh * width;
-  const float s = srow[t];
-  const size_t orow = ((size_t)bi * H + hh) * p.s + si;
-  const int j = threadIdx.x;  // 0..63
-  auto deq = [&](int c) { return __fmul_rn(__fmul_rn((float)a[c], s), sc[c]); };
-  int32_t* cap = mode == 0 ? p.cap_qb : p.cap_kvb;
-  if (cap)
-    for (int c = j; c < width; c += 64) cap[(size_t)t * ld + (size_t)hh * width + c] = a[c];
-  if (mode == 0) {
-    __nv_bfloat16* qn = static_cast<__nv_bfloat16*>(p.q_nope) + orow * kNope;
-    qn[2 * j] = __float2bfloat16_rn(deq(2 * j));
-    qn[2 * j + 1] = __float2bfloat16_rn(deq(2 * j + 1));
-    if (j < 32) {
-      int pos = p.positions[t];
-      pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);
-      const float a0 = deq(kNope + 2 * j), b0 = deq(kNope + 2 * j + 1);
-      const float* cr = p.cos_t + (size_t)pos * kRope;
-      const float* sr = p.sin_t + (size_t)pos * kRope;
-      __nv_bfloat16* qp = static_cast<__nv_bfloat16*>(p.q_pe) + orow * kRope;
-      qp[j] = __float2bfloat16_rn(a0 * cr[j] - b0 * sr[j]);
-      qp[j + 32] = __float2bfloat16_rn(b0 * cr[j + 32] + a0 * sr[j + 32]);
+// Prefill sizes: the same per-token steps as norm_quant_kernel with one warp
+// per token row (8 rows per CTA, warp-level reductions only), so that the
+// per-column inputs (weight scales, gammas) are read once per 8 rows.
+// Shared memory: column scales [q_rank + 576] | gamma_q [q_rank] | gamma_kv
+// [512] | per warp: its dequantised row [q_rank + 576].
+constexpr int kNormRowsPerCta = 8;
+__host__ __device__ constexpr size_t norm_warp_smem(int q_rank) {
+  return (size_t)((q_rank + kNa) + q_rank + kRank + kNormRowsPerCta * (q_rank + kNa)) * sizeof(float);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__global__ void __launch_bounds__(256) norm_quant_warp_kernel(int32_t* __restrict__ acc1,
+                                                              const float* __restrict__ sx,
+                                                              W8Params p, W8Workspace w) {
+  extern __shared__ float smf[];
+  const int rq = p.q_rank, na = rq + kNa;
+  float* colsc = smf;
+  float* gq = colsc + na;
+  float* gk = gq + rq;
+  norm_load_inputs(p, colsc, gq, gk);
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kNormRowsPerCta + warp;
+  if (t >= p.T) return;
+  float* y = gk + kRank + (size_t)warp * na;
+  int32_t* a = acc1 + (size_t)t * na;
+  const float s = sx[t];
+  // the row in pieces of 8 int4 per lane, every load of a piece issued
+  // before the first is used (one memory round trip per piece)
+  const int n4 = na / 4;
+  for (int b0 = 0; b0 < n4; b0 += 32 * 8) {
+    int4 av[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = b0 + lane + 32 * i;
+      av[i] = idx < n4 ? reinterpret_cast<const int4*>(a)[idx] : make_int4(0, 0, 0, 0);
     }
-  } else {
-    __nv_bfloat16* kn = static_cast<__nv_bfloat16*>(p.k_nope) + orow * kNope;
-    __nv_bfloat16* vv = static_cast<__nv_bfloat16*>(p.value) + orow * kV;
-    kn[2 * j] = __float2bfloat16_rn(deq(2 * j));
-    kn[2 * j + 1] = __float2bfloat16_rn(deq(2 * j + 1));
-    vv[2 * j] = __float2bfloat16_rn(deq(kNope + 2 * j));
-    vv[2 * j + 1] = __float2bfloat16_rn(deq(kNope + 2 * j + 1));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = b0 + lane + 32 * i;
+      if (idx >= n4) continue;
+      if (p.cap_a) reinterpret_cast<int4*>(p.cap_a + (size_t)t * na)[idx] = av[i];
+      const float4 cs = reinterpret_cast<const float4*>(colsc)[idx];
+      reinterpret_cast<float4*>(y)[idx] =
+          make_float4(__fmul_rn(__fmul_rn((float)av[i].x, s), cs.x), __fmul_rn(__fmul_rn((float)av[i].y, s), cs.y),
+                      __fmul_rn(__fmul_rn((float)av[i].z, s), cs.z), __fmul_rn(__fmul_rn((float)av[i].w, s), cs.w));
+      // leave the accumulator row zeroed (the decode-size chain adds into it)
+      reinterpret_cast<int4*>(a)[idx] = make_int4(0, 0, 0, 0);
+    }
+  }
+  __syncwarp();
+  // q latent: RMSNorm (gamma_q), requantisation
+  float ss = 0.f;
+  for (int c = lane; c < rq; c += 32) ss += y[c] * y[c];
+  ss = warp_sum(ss);
+  const float invq = 1.0f / sqrtf(ss / (float)rq + p.eps);
+  float amax = 0.f;
+  for (int c = lane; c < rq; c += 32) {
+    const float v = y[c] * invq * gq[c];
+    y[c] = v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+  amax = warp_max(amax);
+  {
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+    for (int c = lane; c < rq; c += 32) {
+      const int8_t v = q8(y[c], inv);
+      w.q1[(size_t)t * rq + c] = v;
+      w.q1h[(size_t)t * rq + c] = __int2half_rn((int)v);
+    }
+    if (lane == 0) w.s1[t] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+  }
+  // compressed_kv: RMSNorm (gamma_kv), requantisation
+  const float* ck = y + rq;
+  ss = 0.f;
+  for (int c = lane; c < kRank; c += 32) ss += ck[c] * ck[c];
+  ss = warp_sum(ss);
+  const float invk = 1.0f / sqrtf(ss / (float)kRank + p.eps);
+  float nv[kRank / 32];
+  amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRank / 32; ++i) {
+    const int c = lane + 32 * i;
+    nv[i] = ck[c] * invk * gk[c];
+    amax = fmaxf(amax, fabsf(nv[i]));
+  }
+  amax = warp_max(amax);
+  {
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kRank / 32; ++i) {
+      const int c = lane + 32 * i;
+      const int8_t v = q8(nv[i], inv);
+      w.c1[(size_t)t * kRank + c] = v;
+      w.c1h[(size_t)t * kRank + c] = __int2half_rn((int)v);
+    }
+    if (lane == 0) w.s2[t] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+  }
+  // RoPE of k_pe (raw columns 512..575 of the kv_a output): lane j < 32
+  {
+    int pos = p.positions[t];
+    if (pos < 0 || pos >= p.max_pos) {
+      if (lane == 0) atomicOr(p.status, kStatusBadPosition);
+      pos = pos < 0 ? 0 : p.max_pos - 1;
+    }
+    const float* kp = ck + kRank;
+    const int j = lane;
+    const float a0 = kp[2 * j], b0 = kp[2 * j + 1];
+    const float* cr = p.cos_t + (size_t)pos * kRope;
+    const float* sr = p.sin_t + (size_t)pos * kRope;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.k_pe) + (size_t)t * kRope;
+    out[j] = __float2bfloat16_rn(a0 * cr[j] - b0 * sr[j]);
+    out[j + 32] = __float2bfloat16_rn(b0 * cr[j + 32] + a0 * sr[j + 32]);
   }
 }
 
@@ -1224,31 +1325,54 @@ std::vector<int> small_units(int q_rank, int heads, const W8SmallPlan& pl) {
 
 }  // namespace
 
+// Row pitch (elements) of a widened fp16 weight copy: a multiple of 256.
+int wide_ld(int n) { return (n + 255) / 256 * 256; }
+
+// Bytes of the widened weight copies (none below kW8PairMinRows tokens).
+size_t wide_bytes(int hidden, int q_rank, int heads, int max_tokens) {
+  if (max_tokens < kW8PairMinRows) return 0;
+  return align256((size_t)hidden * wide_ld(q_rank + kNa) * 2) +
+         align256((size_t)q_rank * wide_ld(heads * (kNope + kRope)) * 2) +
+         align256((size_t)kRank * wide_ld(heads * kHeadCols) * 2);
+}
+
 size_t w8_workspace_bytes(int hidden, int q_rank, int heads, int max_tokens, int num_sms) {
   const size_t T = (size_t)max_tokens;
-  const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
-  return align256(T * hidden) + align256(T * 4) + align256(T * (q_rank + kNa) * 4) +
+  return align256(T * hidden * 2) + align256(T * 4) + align256(T * (q_rank + kNa) * 4) +
          align256(T * q_rank) + align256(T * 4) + align256(T * kRank) + align256(T * 4) +
-         align256(T * nb * 4) + align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4) + 256;
+         align256(T * q_rank * 2) + align256(T * kRank * 2) +
+         align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4) + 256 +
+         wide_bytes(hidden, q_rank, heads, max_tokens);
 }
 
 void w8_workspace_carve(void* base, int hidden, int q_rank, int heads, int max_tokens,
                         int num_sms, W8Workspace* w, W8SmallPlan* plan) {
   const size_t T = (size_t)max_tokens;
-  const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
   unsigned char* b = static_cast<unsigned char*>(base);
-  w->xq = reinterpret_cast<int8_t*>(b); b += align256(T * hidden);
+  w->xh = reinterpret_cast<__half*>(b); b += align256(T * hidden * 2);
   w->sx = reinterpret_cast<float*>(b); b += align256(T * 4);
   w->acc1 = reinterpret_cast<int32_t*>(b); b += align256(T * (q_rank + kNa) * 4);
   w->q1 = reinterpret_cast<int8_t*>(b); b += align256(T * q_rank);
   w->s1 = reinterpret_cast<float*>(b); b += align256(T * 4);
   w->c1 = reinterpret_cast<int8_t*>(b); b += align256(T * kRank);
   w->s2 = reinterpret_cast<float*>(b); b += align256(T * 4);
-  w->acc2 = reinterpret_cast<int32_t*>(b); b += align256(T * nb * 4);
+  w->q1h = reinterpret_cast<__half*>(b); b += align256(T * q_rank * 2);
+  w->c1h = reinterpret_cast<__half*>(b); b += align256(T * kRank * 2);
   small_plan(hidden, q_rank, heads, num_sms, plan);
   plan->units = reinterpret_cast<int*>(b);
   b += align256((size_t)(num_sms + 1 + small_nblk_b(q_rank, heads)) * 4);
   w->readers = reinterpret_cast<unsigned*>(b);
+  b += 256;
+  w->lda = wide_ld(q_rank + kNa);
+  w->ldqb = wide_ld(heads * (kNope + kRope));
+  w->ldkvb = wide_ld(heads * kHeadCols);
+  if (max_tokens >= kW8PairMinRows) {
+    w->wa16 = reinterpret_cast<__half*>(b); b += align256((size_t)hidden * w->lda * 2);
+    w->wqb16 = reinterpret_cast<__half*>(b); b += align256((size_t)q_rank * w->ldqb * 2);
+    w->wkvb16 = reinterpret_cast<__half*>(b);
+  } else {
+    w->wa16 = w->wqb16 = w->wkvb16 = nullptr;
+  }
 }
 
 cudaError_t w8_workspace_init(const W8Workspace& w, const W8SmallPlan& plan, int hidden,
@@ -1283,7 +1407,7 @@ bool w8_encode_maps(const W8Params& p, const W8SmallPlan& pl, W8Maps* m) {
 
 cudaError_t w8a8_quant_rows_launch(const void* x_bf16, int rows, int cols, int8_t* q,
                                    float* scale, cudaStream_t stream) {
-  quant_rows_kernel<<<rows, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x_bf16), cols, q, scale);
+  quant_rows_kernel<int8_t><<<rows, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x_bf16), cols, q, scale);
   return cudaGetLastError();
 }
 
@@ -1322,18 +1446,62 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
     }
     return e;
   }
-  // 1. quantise hidden rows
-  quant_rows_kernel<<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(p.hidden), h, w.xq, w.sx);
+  // 1. quantise hidden rows (fp16 codes: the tensor-core GEMM operand)
+  quant_rows_kernel<__half><<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(p.hidden), h, w.xh, w.sx);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The accumulator rows are left zeroed by every call (norm_quant_kernel,
-  // or the decode-size chain), so the q_a / kv_a split-K adds need no clear.
-  // (Programmatic dependent launch measured slower here: the early
-  // dependents share the SMs with the compute-bound GEMM CTAs.)
+  // or the decode-size chain), so the q_a / kv_a sums are added into them.
+  const bool pairk = T >= kW8PairMinRows && w.wa16;
+  auto chain_pair = [&]() -> cudaError_t {
+    // 1b. the int8 weights widened to fp16 copies ([W_qa | W_kva], W_qb, W_kvb)
+    W8WidenJob jobs[4] = {
+        {p.W_qa, w.wa16, h, rq, w.lda, rq},
+        {p.W_kva, w.wa16 + rq, h, kNa, w.lda, w.lda - rq},
+        {p.W_qb, w.wqb16, rq, H * (kNope + kRope), w.ldqb, w.ldqb},
+        {p.W_kvb, w.wkvb16, kRank, H * kHeadCols, w.ldkvb, w.ldkvb}};
+    cudaError_t e2 = w8_widen_launch(jobs, 4, g_num_sms, st);
+    ++*launches;
+    if (e2 != cudaSuccess) return e2;
+    // 2. q_a_proj and kv_a_proj as one [T, q_rank + 576] accumulator (stored)
+    W8PairParams g1 = {};
+    g1.K[0] = h; g1.N[0] = na; g1.ldw[0] = w.lda;
+    g1.T = T; g1.raw = 1; g1.C = w.acc1; g1.ldc = na; g1.coff[0] = 0;
+    g1.heads = H; g1.s = p.s; g1.status = p.status; g1.budget_ns = p.budget_ns;
+    e2 = w8pair_launch(g1, w.xh, w.xh, w.wa16, w.wa16, g_num_sms, st);
+    ++*launches;
+    if (e2 != cudaSuccess) return e2;
+    // 3-4. RMSNorms, requantisation, RoPE(k_pe): a warp per token row
+    const size_t smem = norm_warp_smem(rq);
+    e2 = cudaFuncSetAttribute(norm_quant_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e2 == cudaSuccess)
+      e2 = launch_k(norm_quant_warp_kernel, dim3((T + kNormRowsPerCta - 1) / kNormRowsPerCta), dim3(256), smem, st,
+                    false, w.acc1, (const float*)w.sx, p, w);
+    ++*launches;
+    if (e2 != cudaSuccess) return e2;
+    // 5-6. q_b_proj -> q_nope, RoPE(q_pe); kv_b_proj -> k_nope, value (one launch)
+    W8PairParams g2 = {};
+    g2.K[0] = rq; g2.N[0] = H * (kNope + kRope); g2.ldw[0] = w.ldqb;
+    g2.K[1] = kRank; g2.N[1] = H * kHeadCols; g2.ldw[1] = w.ldkvb;
+    g2.T = T; g2.raw = 0;
+    g2.sx[0] = w.s1; g2.sx[1] = w.s2; g2.sw[0] = p.sW_qb; g2.sw[1] = p.sW_kvb;
+    g2.positions = p.positions; g2.cos_t = p.cos_t; g2.sin_t = p.sin_t; g2.max_pos = p.max_pos;
+    g2.q_nope = p.q_nope; g2.q_pe = p.q_pe; g2.k_nope = p.k_nope; g2.value = p.value;
+    g2.cap[0] = p.cap_qb; g2.cap[1] = p.cap_kvb;
+    g2.heads = H; g2.s = p.s; g2.status = p.status; g2.budget_ns = p.budget_ns;
+    e2 = w8pair_launch(g2, w.q1h, w.c1h, w.wqb16, w.wkvb16, g_num_sms, st);
+    ++*launches;
+    return e2;
+  };
   auto chain = [&]() -> cudaError_t {
+    if (pairk) return chain_pair();
     // 2. q_a_proj and kv_a_proj into one [T, q_rank + 576] accumulator
-    cudaError_t e2 = gemm(w.xq, p.W_qa, T, h, rq, w.acc1, na, st, launches, true);
-    if (e2 == cudaSuccess) e2 = gemm(w.xq, p.W_kva, T, h, kNa, w.acc1 + rq, na, st, launches, true);
+    W8MmaParams g1 = {};
+    g1.K[0] = h; g1.N[0] = rq; g1.K[1] = h; g1.N[1] = kNa;
+    g1.T = T; g1.raw = 1; g1.C = w.acc1; g1.ldc = na; g1.coff[0] = 0; g1.coff[1] = rq;
+    g1.status = p.status; g1.budget_ns = p.budget_ns;
+    cudaError_t e2 = w8mma_launch(g1, p.W_qa, p.W_kva, w.xh, w.xh, g_num_sms, st, false);
+    ++*launches;
     if (e2 != cudaSuccess) return e2;
     // 3-4. RMSNorms, requantisation, RoPE(k_pe)
     const size_t smem = norm_smem(rq);
@@ -1341,18 +1509,16 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
     if (e2 == cudaSuccess) e2 = launch_k(norm_quant_kernel, dim3(T), dim3(256), smem, st, false, w.acc1, (const float*)w.sx, p, w);
     ++*launches;
     if (e2 != cudaSuccess) return e2;
-    // 5. q_b_proj -> q_nope, RoPE(q_pe)
-    e2 = gemm(w.q1, p.W_qb, T, rq, H * (kNope + kRope), w.acc2, H * (kNope + kRope), st, launches);
-    if (e2 == cudaSuccess)
-      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, false, (const int32_t*)w.acc2,
-                    (const float*)w.s1, p.sW_qb, p, 0);
-    ++*launches;
-    if (e2 != cudaSuccess) return e2;
-    // 6. kv_b_proj -> k_nope, value
-    e2 = gemm(w.c1, p.W_kvb, T, kRank, H * kHeadCols, w.acc2, H * kHeadCols, st, launches);
-    if (e2 == cudaSuccess)
-      e2 = launch_k(head_epilogue_kernel, dim3(T, H), dim3(64), 0, st, false, (const int32_t*)w.acc2,
-                    (const float*)w.s2, p.sW_kvb, p, 1);
+    // 5-6. q_b_proj -> q_nope, RoPE(q_pe); kv_b_proj -> k_nope, value (one launch)
+    W8MmaParams g2 = {};
+    g2.K[0] = rq; g2.N[0] = H * (kNope + kRope); g2.K[1] = kRank; g2.N[1] = H * kHeadCols;
+    g2.T = T; g2.raw = 0;
+    g2.sx[0] = w.s1; g2.sx[1] = w.s2; g2.sw[0] = p.sW_qb; g2.sw[1] = p.sW_kvb;
+    g2.positions = p.positions; g2.cos_t = p.cos_t; g2.sin_t = p.sin_t; g2.max_pos = p.max_pos;
+    g2.q_nope = p.q_nope; g2.q_pe = p.q_pe; g2.k_nope = p.k_nope; g2.value = p.value;
+    g2.cap[0] = p.cap_qb; g2.cap[1] = p.cap_kvb;
+    g2.heads = H; g2.s = p.s; g2.status = p.status; g2.budget_ns = p.budget_ns;
+    e2 = w8mma_launch(g2, p.W_qb, p.W_kvb, w.q1h, w.c1h, g_num_sms, st, false);
     ++*launches;
     return e2;
   };

@@ -175,22 +175,28 @@ void check_w8_workspace(int hidden, int q_rank, int heads, int max_tokens, int s
   W8SmallPlan pl{};
   w8_workspace_carve(reinterpret_cast<void*>(base), hidden, q_rank, heads, max_tokens, sms, &w, &pl);
   const size_t T = (size_t)max_tokens;
-  const size_t nb = (size_t)heads * (kHeadCols > kNope + kRope ? kHeadCols : kNope + kRope);
   const size_t units = (size_t)(sms + 1 + pl.nblk_b) * 4;
   struct Region { const char* name; uintptr_t at; size_t len; } rg[] = {
-      {"xq", (uintptr_t)w.xq, T * hidden},
+      {"xh", (uintptr_t)w.xh, T * hidden * 2},
       {"sx", (uintptr_t)w.sx, T * 4},
       {"acc1", (uintptr_t)w.acc1, T * (q_rank + kNa) * 4},
       {"q1", (uintptr_t)w.q1, T * q_rank},
       {"s1", (uintptr_t)w.s1, T * 4},
       {"c1", (uintptr_t)w.c1, T * kRank},
       {"s2", (uintptr_t)w.s2, T * 4},
-      {"acc2", (uintptr_t)w.acc2, T * nb * 4},
+      {"q1h", (uintptr_t)w.q1h, T * q_rank * 2},
+      {"c1h", (uintptr_t)w.c1h, T * kRank * 2},
       {"units", (uintptr_t)pl.units, units},
       {"readers", (uintptr_t)w.readers, 256},
+      {"wa16", (uintptr_t)w.wa16, w.wa16 ? (size_t)hidden * w.lda * 2 : 0},
+      {"wqb16", (uintptr_t)w.wqb16, w.wqb16 ? (size_t)q_rank * w.ldqb * 2 : 0},
+      {"wkvb16", (uintptr_t)w.wkvb16, w.wkvb16 ? (size_t)kRank * w.ldkvb * 2 : 0},
   };
+  CHECK((max_tokens >= kW8PairMinRows) == (w.wa16 != nullptr), "widened copies at max_tokens %d", max_tokens);
+  CHECK(w.lda % 256 == 0 && w.ldqb % 256 == 0 && w.ldkvb % 256 == 0, "widened pitches");
   uintptr_t end = base;
   for (const Region& r : rg) {
+    if (r.len == 0) continue;
     CHECK(r.at % 256 == 0, "%s not 256-byte aligned", r.name);
     CHECK(r.at >= end, "%s overlaps the region before it", r.name);
     end = r.at + r.len;

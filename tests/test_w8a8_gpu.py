@@ -168,19 +168,10 @@ def test_w8a8_small_chain_repeats_and_alternates(oracle_mod):
         m.close()
 
 
-@pytest.mark.parametrize("b,s", [(1, 1), (2, 1), (4, 1), (8, 1), (64, 1), (3, 33)])
-def test_w8a8_run_accumulators_bit_exact(oracle_mod, b, s):
-    """The int32 accumulators that the run's own kernels formed (captured
-    from the kernels of the call: the decode-size chain at T <= 8, the
-    prefill-size path above), bit for bit against the oracle's brute-force
-    integer GEMM ([R1] §权重转换, W8A8: int32 accumulation is exact).
-    q_a | kv_a: the oracle quantises the bf16 hidden rows itself (the codes
-    are bit-identical on both sides).  q_b, kv_b: the operands are the
-    GPU's own requantised rows (they may differ from the oracle's by one
-    code at rounding ties, which the operand test bounds)."""
-    cfg = I.R1_W8A8
+def _capture_run(cfg, inp, b, s):
+    """Run the W8A8 prolog on `inp` with the accumulator capture on; return
+    the captured accumulators and the GPU's own q_b / kv_b operands."""
     T, H, rq = b * s, cfg["num_heads"], cfg["q_lora_rank"]
-    inp = I.w8a8_inputs(cfg, b, s, 5150 + T, "decode")
     d = B.to_device(inp)
     m = B.MLAProlog(cfg, T)
     try:
@@ -200,7 +191,11 @@ def test_w8a8_run_accumulators_bit_exact(oracle_mod, b, s):
         B.mla_prolog_w8a8_capture(m.h)
     finally:
         m.close()
-    rows = sorted({0, T - 1, T // 2, min(1, T - 1)})
+    return cap_a, cap_qb, cap_kvb, q1, c1
+
+
+def _check_captured(oracle_mod, inp, caps, rows):
+    cap_a, cap_qb, cap_kvb, q1, c1 = caps
     hid = inp["hidden"].float().numpy()
     qx = np.stack([oracle_mod.quant_row_f32(hid[t])[0] for t in rows])
     w_a = np.concatenate([inp["W_qa"].numpy(), inp["W_kva"].numpy()], axis=1)
@@ -208,3 +203,50 @@ def test_w8a8_run_accumulators_bit_exact(oracle_mod, b, s):
     for cap, A, W in ((cap_qb, q1, inp["W_qb"]), (cap_kvb, c1, inp["W_kvb"])):
         ref = oracle_mod.int_gemm(A.cpu().numpy()[rows], W.numpy())
         assert np.array_equal(cap.cpu().numpy()[rows].astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("pattern", ["all_max", "random_signs", "full_range"])
+@pytest.mark.parametrize("b,s", [(64, 1), (3, 5), (2, 300)])
+def test_w8a8_accumulators_adversarial(oracle_mod, pattern, b, s):
+    """Inputs that push the exact-integer argument of the tensor-core paths
+    to its limit: every code +127 (each fp32 chunk sum reaches 512 * 127^2
+    on the single-SM kernel, T = 64 and 15, and 1024 * 127^2 < 2^24 on the
+    2-SM kernel, T = 600), the same magnitudes with random signs, and
+    full-range random int8 weights; the captured int32 accumulators of all
+    four GEMMs stay bit-exact."""
+    cfg = I.R1_W8A8
+    T = b * s
+    inp = I.w8a8_inputs(cfg, b, s, 6000 + T, "decode")
+    g = torch.Generator().manual_seed(6100 + T)
+    wk = ("W_qa", "W_kva", "W_qb", "W_kvb")
+    if pattern == "all_max":
+        inp["hidden"] = torch.ones_like(inp["hidden"])  # every code +127
+        for k in wk:
+            inp[k] = torch.full_like(inp[k], 127)
+    elif pattern == "random_signs":
+        inp["hidden"] = (torch.randint(0, 2, inp["hidden"].shape, generator=g) * 2 - 1).to(torch.bfloat16)
+        for k in wk:
+            inp[k] = ((torch.randint(0, 2, inp[k].shape, generator=g) * 2 - 1) * 127).to(torch.int8)
+    else:
+        inp["hidden"] = (torch.randn(inp["hidden"].shape, generator=g) * 3).to(torch.bfloat16)
+        for k in wk:
+            inp[k] = torch.randint(-127, 128, inp[k].shape, generator=g, dtype=torch.int8)
+    caps = _capture_run(cfg, inp, b, s)
+    _check_captured(oracle_mod, inp, caps, sorted({0, T // 2, T - 1}))
+
+
+@pytest.mark.parametrize("b,s", [(1, 1), (2, 1), (4, 1), (8, 1), (64, 1), (3, 33), (1, 8192)])
+def test_w8a8_run_accumulators_bit_exact(oracle_mod, b, s):
+    """The int32 accumulators that the run's own kernels formed (captured
+    from the kernels of the call: the decode-size chain at T <= 8, the
+    prefill-size path above), bit for bit against the oracle's brute-force
+    integer GEMM ([R1] §权重转换, W8A8: int32 accumulation is exact).
+    q_a | kv_a: the oracle quantises the bf16 hidden rows itself (the codes
+    are bit-identical on both sides).  q_b, kv_b: the operands are the
+    GPU's own requantised rows (they may differ from the oracle's by one
+    code at rounding ties, which the operand test bounds)."""
+    cfg = I.R1_W8A8
+    T = b * s
+    inp = I.w8a8_inputs(cfg, b, s, 5150 + T, "decode" if s == 1 else "prefill")
+    caps = _capture_run(cfg, inp, b, s)
+    _check_captured(oracle_mod, inp, caps, sorted({0, T - 1, T // 2, min(1, T - 1)}))
