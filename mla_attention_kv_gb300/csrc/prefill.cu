@@ -593,11 +593,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
 }  // namespace
 
+// AUTO's switch from the decode kernel to the prefill kernel.  Measured on a
+// GB300 (CUDA events per call, L2 flushed, T = 128 .. 4096):
+//   - the decode kernel costs one launch per tt rows (128 for V2-Lite shapes,
+//     64 for R1 shapes), about 14 us + weight bytes / 1.9 TB/s each
+//     (V2-Lite 18.5 us, R1 36 us);
+//   - the prefill kernel gives each CTA of a pair one 128-row tile over all
+//     columns, so until every SM has a tile a call costs one tile pair's
+//     FLOPs at about 22 TFLOP/s (V2-Lite 83 us, R1 475 us), whatever T is.
+// The switch is the first T past the largest whole number of decode
+// launches that still costs less than one prefill call: V2-Lite 513 (4 x
+// 18.5 < 83 < 5 x 18.5), R1 833 (13 x 36 < 475 < 14 x 36).
 int prefill_min_tokens(int hidden, int heads, int num_sms) {
-  (void)hidden;
-  (void)heads;
-  (void)num_sms;
-  return 1024;
+  DecodePlan plan;
+  if (!decode_plan(hidden, heads, num_sms, &plan)) return 1;
+  const double flops_per_row = 2.0 * ((double)hidden * kNa + (double)kRank * heads * kHeadCols);
+  const double weight_bytes = 2.0 * ((double)hidden * kNa + (double)kRank * heads * kHeadCols);
+  const double prefill_us = 2.0 * kBM * flops_per_row / 22.0e6;
+  const double decode_us = 14.0 + weight_bytes / 1.9e6;
+  int launches = (int)(prefill_us / decode_us);
+  if (launches < 1) launches = 1;
+  return launches * plan.tt_max + 1;
 }
 
 cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaStream_t stream,
