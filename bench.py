@@ -735,16 +735,18 @@ def run_gpu(args, wl, rank, world, dev, full=True):
 def kernel_traffic(kernel: str, T: int, model: str = ""):
     """DRAM bytes of one call of `kernel` at T rows (entry "<model>:<T>") from
     the committed ncu summary, or None when the summary is missing
-    or was taken on a different version of the kernel's source (its sha256 no
-    longer matches)."""
+    or was taken on a different version of the kernel's sources (the sha256
+    of their concatenation no longer matches)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        src = os.path.join(ROOT, "mla_attention_kv_gb300", "csrc", t[kernel]["source"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if h != t[kernel]["sha256_16"]:
+        srcs = t[kernel]["source"]
+        h = hashlib.sha256()
+        for src in ([srcs] if isinstance(srcs, str) else srcs):
+            h.update(open(os.path.join(ROOT, "mla_attention_kv_gb300", "csrc", src), "rb").read())
+        if h.hexdigest()[:16] != t[kernel]["sha256_16"]:
             return None
         return t[kernel]["bytes_per_call"].get("%s:%d" % (model, T))
     except Exception:

@@ -288,6 +288,8 @@ size_t w8mma_smem(int NT, int stages);
 struct W8PairParams {
   int K[2], N[2], ldw[2];   // N = 0: no matrix
   int ntiles[2], nn[2];     // filled: pair tiles per matrix, 256-column tiles
+  int nm;                   // filled: 256-row token tiles
+  int mfast[2];             // filled: tile order, token tiles fastest (1) or weight tiles fastest (0)
   unsigned s_mul, s_shift;  // filled: t / s
   int T;
   int raw;                  // 1: int32 sums stored into C

@@ -89,10 +89,18 @@ __device__ __forceinline__ PTile ptile_of(const W8PairParams& p, int u) {
   PTile r;
   r.sel = u < p.ntiles[0] ? 0 : 1;
   const int v = u - (r.sel ? p.ntiles[0] : 0);
-  const int nn = p.nn[r.sel];
-  // weight tiles fastest: the pairs running at the same time share token rows
-  r.nt = v % nn;
-  r.mt = v / nn;
+  // mfast: token tiles fastest (the pairs running at the same time share a
+  // weight panel, which is then read from DRAM once; for activations smaller
+  // than the weights), otherwise weight tiles fastest (they share token rows)
+  if (p.mfast[r.sel]) {
+    const int nm = p.nm;
+    r.mt = v % nm;
+    r.nt = v / nm;
+  } else {
+    const int nn = p.nn[r.sel];
+    r.nt = v % nn;
+    r.mt = v / nn;
+  }
   return r;
 }
 
@@ -428,7 +436,9 @@ cudaError_t w8pair_launch(W8PairParams p, const void* X0, const void* X1, const 
       return cudaErrorInvalidValue;
     p.nn[i] = (p.N[i] + kPBN - 1) / kPBN;
     p.ntiles[i] = mtiles * p.nn[i];
+    p.mfast[i] = (size_t)p.T * p.K[i] < (size_t)p.K[i] * p.ldw[i] ? 1 : 0;
   }
+  p.nm = mtiles;
   {
     const unsigned d = (unsigned)(p.s > 0 ? p.s : 1);
     unsigned l = 0;
