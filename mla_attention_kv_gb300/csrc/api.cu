@@ -31,6 +31,8 @@ struct mla_prolog_s {
   float* c8inv;  // reciprocal int8 KV-cache scales [H*256 + 64] (mla_kv_prolog_run_c8)
   DecodePlan dplan;
   bool decode_ok;
+  DecodePlan dplan_small;  // <= kDecodeSmallTokens rows per launch, two CTAs per SM
+  bool small_ok;
   // packed weight snapshot (mla_kv_prolog_prepare_weights): W_kva tiles then
   // W_kvb slices, and the caller pointers they were taken from
   void* pk;
@@ -137,6 +139,8 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
     return cuda_fail(e, "device query");
   }
   h->decode_ok = decode_plan(c.hidden, c.num_heads, h->num_sms, &h->dplan);
+  h->small_ok = h->decode_ok && decode_plan_small(c.hidden, c.num_heads, h->num_sms, &h->dplan_small) &&
+                h->dplan_small.KB == h->dplan.KB && h->dplan_small.KC == h->dplan.KC;
   if (c.quant == MLA_QUANT_NONE && !h->decode_ok) {
     delete h;
     return MLA_ERR_UNSUPPORTED;
@@ -321,7 +325,11 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
   for (long long t0 = 0; t0 < T; t0 += tt) {
     p.t0 = (int)t0;
     p.TT = (int)((T - t0) < tt ? (T - t0) : tt);
-    cudaError_t e = decode_launch(bf16, packed, h->dplan, p, !(packed && h->pk_fresh), stream);
+    // small launches on the packed snapshot: the two-CTA-per-SM plan (its
+    // CTAs copy the snapshot before the dependency wait; raw weights may come
+    // from the previous kernel, so they gain nothing from an early start)
+    const DecodePlan& pl = (h->small_ok && packed && p.TT <= h->dplan_small.tt_max) ? h->dplan_small : h->dplan;
+    cudaError_t e = decode_launch(bf16, packed, pl, p, !(packed && h->pk_fresh), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (packed) h->pk_fresh = false;
     h->last_launches += 1;

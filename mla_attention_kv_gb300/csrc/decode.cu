@@ -57,6 +57,7 @@ constexpr int kPitchX = 144;       // smem row pitch of a 64-column hidden tile
 constexpr int kPitchN = kNrmPitch; // smem row pitch of a 512-column latent row (= workspace pitch)
 constexpr int kMaxMT = kDecodeMaxTokens / 16;
 constexpr int kSmemBudget = 227 * 1024;
+constexpr int kSmemBudget2 = 112 * 1024;  // two CTAs per SM (228 KB, 1 KB reserved per CTA)
 constexpr int kRedBytes = 16384;   // cross-warp reduction scratch (<= 32 chains x 512 B)
 constexpr int kMiscBytes = 2048;   // gamma, cos/sin row, mbarriers, flag
 constexpr int kMaxStagesA = 16;    // deepest phase-A cp.async ring
@@ -131,8 +132,12 @@ __device__ __forceinline__ void for_each_c(std::integer_sequence<int, Cs...>, F&
   (f(std::integral_constant<int, Cs>{}), ...);
 }
 
-template <typename T, int IM, int QM, bool PK>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+// NC: CTAs per SM the launch is built for.  NC = 2 (the plan for <= 32 rows:
+// under half the shared memory and 128 registers) lets the CTAs of the next
+// call in the stream become resident beside this call's and copy their packed
+// weights while it runs.
+template <typename T, int IM, int QM, bool PK, int NC>
+__global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   // 1024-byte aligned base (the hidden-state boxes use the 128-byte swizzle)
@@ -452,6 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           if (lane < gsz && i < nsub) issue_stage_w(i, (k & 1) * gsz + lane);
         }
       }
+      // two CTAs per SM: this call may start while the previous one runs, so
+      // the resident W_kvb rows (read-only snapshot) go out now as well
+      if constexpr (NC == 2) {
+        if (warp == 1 && nsub > 0) issue_wkvb_warp();
+      }
       prologue_inputs();
       if (warp == 0) {
         for (int k = 0; k < 2 && k < ngroups; ++k) {
@@ -460,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       }
       // warp 1: the W_kvb slice goes out once the first kv_a stage is in
-      if (warp == 1 && nsub > 0) {
+      if (NC == 1 && warp == 1 && nsub > 0) {
         int ok = 0;
         if (lane == 0) ok = mbar_wait_bounded(bar_a0, 0, p.budget_ns) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -920,10 +930,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 constexpr int kVariants[3][2] = {{1, 4}, {1, 8}, {2, 8}};
 
 template <typename T, bool PK>
-const void* kernel_for(int variant) {
-  if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK>;
-  if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK>;
-  return (const void*)decode_kernel<T, 2, 8, PK>;
+const void* kernel_for(int variant, bool two_per_sm) {
+  if (two_per_sm) {
+    if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 2>;
+    if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 2>;
+    return (const void*)decode_kernel<T, 2, 8, PK, 2>;
+  }
+  if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 1>;
+  if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 1>;
+  return (const void*)decode_kernel<T, 2, 8, PK, 1>;
 }
 
 }  // namespace
@@ -994,7 +1009,7 @@ cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, c
 // Shared-memory plan for `tt` token rows per launch; false if it cannot be
 // laid out (or, with `resident_only`, if W_kvb would have to be streamed).
 static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_sms,
-                     DecodePlan* plan) {
+                     DecodePlan* plan, int budget = kSmemBudget) {
   const int G = num_sms;
   // split-K of kv_a: the smallest KB (multiple of 64 dividing hidden) with
   // at most one (KB x 32-column) tile per CTA
@@ -1027,14 +1042,14 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   // keeps W_kvb rows resident from kernel start.
   int regionA = nstA * stageA;
   if (regionA < nrm_bytes) regionA = nrm_bytes;
-  int kpre = (kSmemBudget - fixed - regionA) / pitchB;
+  int kpre = (budget - fixed - regionA) / pitchB;
   int kchunk = kWkvbBoxRows;
   if (kpre >= kRank) {
     kpre = kRank;
   } else {
     if (resident_only) return false;
     if (regionA < nrm_bytes + 2 * kWkvbBoxRows * pitchB) regionA = nrm_bytes + 2 * kWkvbBoxRows * pitchB;
-    kpre = (kSmemBudget - fixed - regionA) / pitchB / kWkvbBoxRows * kWkvbBoxRows;
+    kpre = (budget - fixed - regionA) / pitchB / kWkvbBoxRows * kWkvbBoxRows;
     kchunk = (regionA - nrm_bytes) / (2 * pitchB) / kWkvbBoxRows * kWkvbBoxRows;
     if (kpre < 0 || kchunk < kWkvbBoxRows) return false;
   }
@@ -1052,7 +1067,8 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   plan->off_red = plan->off_a + (regionA + 127) / 128 * 128;
   plan->off_misc = plan->off_red + kRedBytes;
   plan->smem = (size_t)plan->off_misc + kMiscBytes + 1024;  // + base alignment slack
-  if (plan->smem > (size_t)kSmemBudget) return false;
+  if (plan->smem > (size_t)budget) return false;
+  plan->two_per_sm = budget <= kSmemBudget2;
   if (kpre < tt) return false;  // the output tile is staged in the W_kvb area
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
   return true;
@@ -1085,6 +1101,12 @@ bool decode_phase_b(int mt, int ngmax, int* variant, int* wm_out, int* ks_out) {
   return best >= 0;
 }
 
+bool decode_plan_small(int hidden, int heads, int num_sms, DecodePlan* plan) {
+  // rows per launch for which two CTAs fit on an SM, W_kvb slice resident
+  return num_sms >= kDecodeSmallTokens &&
+         plan_for(kDecodeSmallTokens, true, hidden, heads, num_sms, plan, kSmemBudget2);
+}
+
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   if (hidden % 64 != 0 || heads < 1) return false;
   // 128 rows per launch when the whole W_kvb slice still stays resident
@@ -1100,8 +1122,9 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   while (mt * 16 < p0.TT) mt *= 2;
   int variant, wm, ks;
   if (!decode_phase_b(mt, plan.ngmax, &variant, &wm, &ks)) return cudaErrorInvalidValue;
-  const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant) : kernel_for<__half, true>(variant))
-                          : (bf16 ? kernel_for<__nv_bfloat16, false>(variant) : kernel_for<__half, false>(variant));
+  const bool two = plan.two_per_sm;
+  const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant, two) : kernel_for<__half, true>(variant, two))
+                          : (bf16 ? kernel_for<__nv_bfloat16, false>(variant, two) : kernel_for<__half, false>(variant, two));
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
   if (e != cudaSuccess) return e;
   DecodeParams p = p0;

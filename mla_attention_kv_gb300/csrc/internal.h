@@ -99,6 +99,7 @@ constexpr int kSingleBarrierRowsTimesChunks = 16;
 
 struct DecodePlan {
   int grid;        // CTAs (cooperative, one per SM)
+  bool two_per_sm; // built to fit two CTAs per SM (the <= kDecodeSmallTokens plan)
   int tt_max;      // token rows per launch (64 or 128)
   int KB, KC;      // split-K of kv_a
   int kpre, kchunk, nstA, ngbox;
@@ -111,6 +112,12 @@ struct DecodePlan {
 // Plan for a given model shape on the current device; returns false if the
 // shape cannot be handled (shared memory or register budget).
 bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan);
+// Launches of at most this many rows can use a plan that fits two CTAs per
+// SM (so that a chained next call is resident, copying its weights, while
+// this one runs).
+constexpr int kDecodeSmallTokens = 32;
+// That plan (false if the shape does not fit it: W_kvb slice not resident).
+bool decode_plan_small(int hidden, int heads, int num_sms, DecodePlan* plan);
 // Phase-B work split for mt m-tiles (a power of two <= 8) and at most ngmax
 // column groups per CTA: register-tile variant, warp-grid rows, k-slices.
 // False if no variant holds the tile.

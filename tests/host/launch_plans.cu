@@ -62,6 +62,21 @@ void check_decode_shape(int hidden, int heads, int sms) {
   CHECK(ok, "hidden %d heads %d sms %d: no plan", hidden, heads, sms);
   if (!ok) return;
   const int NG = heads * kHeadCols / 8;
+  CHECK(!p.two_per_sm, "the main plan is built for one CTA per SM");
+  // the <= 32-row plan: two CTAs per SM, W_kvb slice resident, same split-K
+  DecodePlan q;
+  if (decode_plan_small(hidden, heads, sms, &q)) {
+    CHECK(q.two_per_sm && q.tt_max == kDecodeSmallTokens, "small plan tt_max %d", q.tt_max);
+    CHECK(2 * (q.smem + 1024) <= 228 * 1024, "small plan smem %zu: two CTAs do not fit", q.smem);
+    CHECK(q.kpre == kRank, "small plan kpre %d", q.kpre);
+    CHECK(q.KB == p.KB && q.KC == p.KC && q.ngmax == p.ngmax && q.grid == p.grid, "small plan split");
+    CHECK(q.nstA * (kSubK * kPitchWA + q.tt_max * kPitchX) <= q.off_red - q.off_a, "small plan ring");
+    CHECK(q.tt_max * kPitchN <= q.off_red - q.off_a, "small plan latent rows");
+  } else {
+    // only shapes whose W_kvb slice cannot stay resident in half the SM may go without
+    CHECK(p.kpre < kRank || heads * kHeadCols / sms * 2 * kRank > 40 * 1024, "no small plan for hidden %d heads %d",
+          hidden, heads);
+  }
   CHECK(p.grid == sms, "grid %d", p.grid);
   CHECK(p.tt_max == 64 || p.tt_max == 128, "tt_max %d", p.tt_max);
   CHECK(p.KB % 64 == 0 && p.KB * p.KC == hidden, "KB %d KC %d hidden %d", p.KB, p.KC, hidden);
