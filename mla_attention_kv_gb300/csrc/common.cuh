@@ -136,6 +136,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
   return true;
 }
+// Limit of the waits that let a CTA's own copies and MMAs in flight finish
+// before it leaves after an abort: independent of the caller's spin budget
+// (which may be tiny), so that no copy lands after the CTA has exited.
+constexpr unsigned long long kDrainBudgetNs = 1000000000ull;
+__device__ __forceinline__ unsigned long long drain_budget(unsigned long long budget) {
+  return budget > kDrainBudgetNs ? budget : kDrainBudgetNs;
+}
 // Bulk copy global -> shared (16-byte aligned, size multiple of 16),
 // completion counted on an mbarrier in bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

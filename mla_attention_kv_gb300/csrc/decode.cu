@@ -498,8 +498,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
             atomicOr(p.status, kStatusTimeout);
             for (int kk = k; kk < issuedG; ++kk)
               for (int i = kk * gsz; i < (kk + 1) * gsz && i < nsub; ++i)
-                mbar_wait_bounded(bar_a0 + 8 * ((kk & 1) * gsz + i - kk * gsz), (kk >> 1) & 1, p.budget_ns);
-            if (*reinterpret_cast<volatile int*>(sWkvbOn)) mbar_wait_bounded(bar_res, 0, p.budget_ns);
+                mbar_wait_bounded(bar_a0 + 8 * ((kk & 1) * gsz + i - kk * gsz), (kk >> 1) & 1,
+                                  drain_budget(p.budget_ns));
+            if (*reinterpret_cast<volatile int*>(sWkvbOn)) mbar_wait_bounded(bar_res, 0, drain_budget(p.budget_ns));
           }
           cp_async_wait<0>();
           __syncthreads();
@@ -599,9 +600,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   auto drain = [&]() {
     cp_async_wait<0>();
     if (tid == 0) {
-      mbar_wait_bounded(bar_res, 0, p.budget_ns);
-      if (lat_issued) mbar_wait_bounded(bar_lat, 0, p.budget_ns);
-      for (int b = 0; b < nbatch; ++b) mbar_wait_bounded(bar_r0 + 8 * b, 0, p.budget_ns);
+      mbar_wait_bounded(bar_res, 0, drain_budget(p.budget_ns));
+      if (lat_issued) mbar_wait_bounded(bar_lat, 0, drain_budget(p.budget_ns));
+      for (int b = 0; b < nbatch; ++b) mbar_wait_bounded(bar_r0 + 8 * b, 0, drain_budget(p.budget_ns));
     }
     __syncthreads();
   };

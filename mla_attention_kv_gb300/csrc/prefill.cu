@@ -252,14 +252,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
       }
       // drain: on the leader every issued copy of both CTAs has landed (the
-      // leader's full barriers count them) before the pair may exit
+      // leader's full barriers count them) before the pair may exit; bounded,
+      // but neither cut short by an abort nor by a tiny spin budget
       if (leader) {
         for (uint32_t u = (u0 > (uint32_t)kS0Stages ? u0 - kS0Stages : 0); u < u0; ++u)
-          pf_wait(bar(&sh->full0[u % kS0Stages]), (u / kS0Stages) & 1, abort, budget, p.status);
+          mbar_wait_bounded(bar(&sh->full0[u % kS0Stages]), (u / kS0Stages) & 1, drain_budget(budget));
         for (uint32_t u = (u1 > (uint32_t)kS1Stages ? u1 - kS1Stages : 0); u < u1; ++u)
-          pf_wait(bar(&sh->full1[u % kS1Stages]), (u / kS1Stages) & 1, abort, budget, p.status);
+          mbar_wait_bounded(bar(&sh->full1[u % kS1Stages]), (u / kS1Stages) & 1, drain_budget(budget));
         for (uint32_t u = (u2 > (uint32_t)kS2Stages ? u2 - kS2Stages : 0); u < u2; ++u)
-          pf_wait(bar(&sh->full2[u % kS2Stages]), (u / kS2Stages) & 1, abort, budget, p.status);
+          mbar_wait_bounded(bar(&sh->full2[u % kS2Stages]), (u / kS2Stages) & 1, drain_budget(budget));
       }
     }
   } else if (warp == 1) {
@@ -354,10 +355,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
       // every MMA issued so far has completed (in both CTAs) before TMEM is released
       tc::commit2_both(bar(&sh->mma_done));
-      pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
+      mbar_wait_bounded(bar(&sh->mma_done), 0, drain_budget(budget));
     } else if (lane == 0) {
       // the peer CTA releases its tensor memory only after the pair's last MMA
-      pf_wait(bar(&sh->mma_done), 0, abort, budget, p.status);
+      mbar_wait_bounded(bar(&sh->mma_done), 0, drain_budget(budget));
     }
   } else {
     // ============================================================ epilogue

@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(256) w8_front_kernel(const __grid_constant__ W
   if (*reinterpret_cast<volatile int*>(s_flag) == 0) {
     if (tid == 0) {
       if (p.status) atomicOr(p.status, kStatusTimeout);
-      mbar_wait_bounded(bar, 0, p.budget_ns);
+      mbar_wait_bounded(bar, 0, drain_budget(p.budget_ns));
     }
     return;
   }
@@ -939,7 +939,7 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
           if (p.status) atomicOr(p.status, kStatusTimeout);
           for (int q = consumed; q < issued; ++q)
             mbar_wait_bounded(smem_u32(s_bar + q % nst), (uint32_t)(q / nst) & 1u,
-                              p.budget_ns);
+                              drain_budget(p.budget_ns));
         }
         return;
       }

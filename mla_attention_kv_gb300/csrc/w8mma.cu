@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) w8mma_kernel(const __grid_const
       // every issued copy has landed before the CTA may exit (bounded, but
       // not cut short by another role's abort)
       for (uint32_t q = (s > (uint32_t)S ? s - S : 0); q < s; ++q)
-        mbar_wait_bounded(bar(&sh->st_full[q % S]), (q / S) & 1, budget);
+        mbar_wait_bounded(bar(&sh->st_full[q % S]), (q / S) & 1, drain_budget(budget));
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kMmThreads, 1) w8mma_kernel(const __grid_const
       }
       // every MMA issued has completed before tensor memory is released
       tc::commit(bar(&sh->mma_done));
-      mbar_wait_bounded(bar(&sh->mma_done), 0, budget);
+      mbar_wait_bounded(bar(&sh->mma_done), 0, drain_budget(budget));
     }
   } else if (warp < 6) {
     // ============================================================ converters

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kPThreads, 1) w8pair_kernel(const __grid_const
       // has landed before the pair may exit
       if (leader)
         for (uint32_t q = (s > (uint32_t)kPStages ? s - kPStages : 0); q < s; ++q)
-          mbar_wait_bounded(bar(&sh->full[q % kPStages]), (q / kPStages) & 1, budget);
+          mbar_wait_bounded(bar(&sh->full[q % kPStages]), (q / kPStages) & 1, drain_budget(budget));
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer (leader)
@@ -204,9 +204,9 @@ __global__ void __launch_bounds__(kPThreads, 1) w8pair_kernel(const __grid_const
         }
       }
       tc::commit2_both(bar(&sh->mma_done));
-      mbar_wait_bounded(bar(&sh->mma_done), 0, budget);
+      mbar_wait_bounded(bar(&sh->mma_done), 0, drain_budget(budget));
     } else if (lane == 0) {
-      mbar_wait_bounded(bar(&sh->mma_done), 0, budget);
+      mbar_wait_bounded(bar(&sh->mma_done), 0, drain_budget(budget));
     }
   } else {
     // ============================================================ epilogue
