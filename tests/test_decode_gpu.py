@@ -234,3 +234,45 @@ def test_packed_snapshot_only_serves_its_own_weights(oracle_mod):
     torch.cuda.synchronize()
     assert m.status() == 0
     m.close()
+
+
+# ---------------------------------------------------------------- CUDA graphs
+# A replayed graph re-runs the captured launch with the same arguments and
+# workspace: the grid-barrier counters must be back at zero after each
+# replay, and nothing a replay reads (split-K partials, latent rows) may be
+# taken from the previous replay.  New hidden rows and positions are copied
+# into the captured buffers before each replay; a replay that read the
+# previous replay's partials would give the previous input's kv rows.
+
+@pytest.mark.parametrize("b,packed", [(2, False), (16, True), (128, False)])
+def test_graph_replays_read_their_own_partials(oracle_mod, b, packed):
+    cfg = I.V2_LITE
+    inp = I.kv_inputs(cfg, b, 1, 900 + b)
+    d = B.to_device(inp)
+    m = B.MLAProlog(cfg, b)
+    m.set_path(B.PATH_DECODE)
+    if packed:
+        m.prepare_weights(d)
+    out = m.alloc_outputs(b, 1)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        m.run(b, 1, d, out, stream=st)  # first call outside capture
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            m.run(b, 1, d, out, stream=st)
+    torch.cuda.synchronize()
+    for rep in range(3):
+        new = I.kv_inputs(cfg, b, 1, 950 + 10 * b + rep)
+        d["hidden"].copy_(new["hidden"])
+        d["positions"].copy_(new["positions"])
+        for t in out.values():
+            t.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.status() == 0
+        ref = oracle_mod.kv_prolog(dict(inp, hidden=new["hidden"], positions=new["positions"]))
+        for name, r in zip(("k_nope", "value", "k_pe"), ref):
+            compare(name, out[name], r, oracle_mod)
+    m.close()
