@@ -55,7 +55,29 @@ struct mla_prolog_s {
   const void* map_ptr[kMapCache];
   CUtensorMap map[kMapCache];
   int map_next;
+  // tensor maps of recently seen hidden-row buffers (packed decode path),
+  // keyed by pointer, row count and box height
+  static constexpr int kXMapCache = 32;
+  const void* xmap_ptr[kXMapCache];
+  int xmap_ntok[kXMapCache];
+  int xmap_rows[kXMapCache];
+  CUtensorMap xmap[kXMapCache];
+  int xmap_next;
 };
+
+// Tensor map of the hidden rows for a packed decode launch, cached.
+static const CUtensorMap* hidden_map(mla_prolog_s* h, const void* hidden, int ntok, int rows) {
+  for (int i = 0; i < mla_prolog_s::kXMapCache; ++i)
+    if (h->xmap_ptr[i] == hidden && h->xmap_ntok[i] == ntok && h->xmap_rows[i] == rows) return &h->xmap[i];
+  const int slot = h->xmap_next;
+  if (!decode_encode_xmap(&h->xmap[slot], h->cfg.dtype == MLA_BF16, hidden, h->cfg.hidden, ntok, rows))
+    return nullptr;
+  h->xmap_ptr[slot] = hidden;
+  h->xmap_ntok[slot] = ntok;
+  h->xmap_rows[slot] = rows;
+  h->xmap_next = (slot + 1) % mla_prolog_s::kXMapCache;
+  return &h->xmap[slot];
+}
 
 // Tensor map of W_kvb [512, H*256] for the decode kernel, cached per pointer.
 static const CUtensorMap* wkvb_map(mla_prolog_s* h, const void* W_kvb) {
@@ -329,7 +351,15 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     // CTAs copy the snapshot before the dependency wait; raw weights may come
     // from the previous kernel, so they gain nothing from an early start)
     const DecodePlan& pl = (h->small_ok && packed && p.TT <= h->dplan_small.tt_max) ? h->dplan_small : h->dplan;
-    cudaError_t e = decode_launch(bf16, packed, pl, p, !(packed && h->pk_fresh), stream);
+    const CUtensorMap* xm = nullptr;
+    if (packed) {
+      xm = hidden_map(h, hidden_states, p.ntok, decode_box_rows(p.TT, p.ntok));
+      if (!xm) {
+        snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed for the hidden rows");
+        return MLA_ERR_CUDA;
+      }
+    }
+    cudaError_t e = decode_launch(bf16, packed, pl, p, !(packed && h->pk_fresh), stream, xm);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (packed) h->pk_fresh = false;
     h->last_launches += 1;

@@ -1,6 +1,6 @@
 // decode.cu -- fused MLA KV prolog for small token counts (decode).
 //
-// One cooperative launch (one CTA per SM) performs all seven prolog steps
+// One launch (one CTA per SM, all resident at once) performs all seven prolog steps
 // of "DeepSeek-V2-Lite-Chat MLA KV Prolog 迁移指南" §背景 for up to
 // kDecodeMaxTokens token rows.  At these sizes the work is bound by the
 // weight stream (W_kva + W_kvb: 6.5 MB for V2-Lite, 41.8 MB for R1), so the
@@ -37,6 +37,7 @@
 // R (the owner CTA of each row writes the normalised row); a slot mapping
 // places rows in a paged cache; per-channel scales turn the stores into
 // int8 codes.
+#include <mutex>
 #include <type_traits>
 #include <utility>
 
@@ -1117,8 +1118,72 @@ bool decode_plan(int hidden, int heads, int num_sms, DecodePlan* plan) {
   return num_sms >= 64 && plan_for(64, false, hidden, heads, num_sms, plan);
 }
 
+int decode_box_rows(int TT, int ntok) {
+  int mt = 1;
+  while (mt * 16 < TT) mt *= 2;
+  return 16 * mt < ntok ? 16 * mt : ntok;
+}
+
+bool decode_encode_xmap(CUtensorMap* map, bool bf16, const void* hidden, int hidden_dim, int ntok,
+                        int rows) {
+  return encode_tmap_2d(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        hidden, (uint64_t)hidden_dim, (uint64_t)ntok, (uint64_t)hidden_dim * 2, 64,
+                        (uint32_t)rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Per kernel instance and device: the dynamic shared-memory limit, raised
+// when a plan needs more than any before (the attribute belongs to the
+// kernel, so it is never lowered: another handle's plan may need more), and
+// per shared-memory size the number of CTAs the device holds at once, which
+// must cover the grid (the CTAs wait for one another at the grid barriers).
+// Both are cached: the driver calls cost about a microsecond each, and a
+// decode call launches one of 24 instances.
+static cudaError_t prepare_instance(const void* fn, size_t smem, int grid) {
+  struct Limit {
+    const void* fn;
+    int dev;
+    size_t smem;
+  };
+  struct Fit {
+    const void* fn;
+    int dev;
+    size_t smem;
+    int resident;  // CTAs resident at once at this shared-memory size
+  };
+  static std::mutex mu;
+  static Limit lim[128];
+  static Fit fit[256];
+  static int nl = 0, nf = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int i = 0;
+  while (i < nl && !(lim[i].fn == fn && lim[i].dev == dev)) ++i;
+  if (i == nl || lim[i].smem < smem) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (i < nl) lim[i].smem = smem;
+    else if (nl < 128) lim[nl++] = Limit{fn, dev, smem};
+  }
+  int j = 0;
+  while (j < nf && !(fit[j].fn == fn && fit[j].dev == dev && fit[j].smem == smem)) ++j;
+  int resident;
+  if (j < nf) {
+    resident = fit[j].resident;
+  } else {
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    resident = per_sm * sms;
+    if (nf < 256) fit[nf++] = Fit{fn, dev, smem, resident};
+  }
+  return resident < grid ? cudaErrorCooperativeLaunchTooLarge : cudaSuccess;
+}
+
 cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p0,
-                          bool pdl, cudaStream_t stream) {
+                          bool pdl, cudaStream_t stream, const CUtensorMap* xmap) {
   int mt = 1;
   while (mt * 16 < p0.TT) mt *= 2;
   int variant, wm, ks;
@@ -1126,7 +1191,7 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   const bool two = plan.two_per_sm;
   const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant, two) : kernel_for<__half, true>(variant, two))
                           : (bf16 ? kernel_for<__nv_bfloat16, false>(variant, two) : kernel_for<__half, false>(variant, two));
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  cudaError_t e = prepare_instance(fn, plan.smem, plan.grid);
   if (e != cudaSuccess) return e;
   DecodeParams p = p0;
   p.KB = plan.KB;
@@ -1145,10 +1210,10 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
     // hidden rows [ntok, hidden]: boxes of 64 columns x xrows rows, 128-byte
     // swizzle; rows past ntok read as zero.  The box is at most the tensor's
     // height; smem rows past it only feed output rows that are not stored.
-    p.xrows = 16 * mt < p.ntok ? 16 * mt : p.ntok;
-    if (!encode_tmap_2d(&p.tmap_x, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        p.hidden, (uint64_t)p.hidden_dim, (uint64_t)p.ntok, (uint64_t)p.hidden_dim * 2, 64,
-                        (uint32_t)p.xrows, CU_TENSOR_MAP_SWIZZLE_128B))
+    p.xrows = decode_box_rows(p.TT, p.ntok);
+    if (xmap)
+      p.tmap_x = *xmap;
+    else if (!decode_encode_xmap(&p.tmap_x, bf16, p.hidden, p.hidden_dim, p.ntok, p.xrows))
       return cudaErrorInvalidValue;
   }
   // one barrier when every CTA can afford to reduce all rows itself
@@ -1159,25 +1224,30 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  // Not a cooperative launch: a cooperative grid starts only once the
+  // previous grid has left every SM, which cancels the programmatic
+  // dependency (measured: 14.1 us per eager V2-Lite call with both
+  // attributes, 10.7 us with the dependency alone).  The grid barriers need
+  // every CTA resident at once; prepare_instance checked that the device
+  // holds the whole grid, and the dependency launches this grid only after
+  // every CTA of the previous one has started, so no CTA of this grid waits
+  // for a slot held by a later grid.  A CTA that another process's work
+  // keeps off the GPU for longer than the spin budget makes the others
+  // give up at the barrier with MLA_ERR_DEVICE_TIMEOUT instead of hanging.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   void* args[] = {&p};
-  // programmatic serialisation together with a cooperative launch: if the
-  // runtime refuses the pair, launch cooperatively alone from then on
-  static int pdl_ok = 1;
-  if (pdl && pdl_ok) {
-    cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-    if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported && e != cudaErrorInvalidConfiguration)
-      return e;
+  if (pdl) {
+    // a runtime that does not take the dependency attribute: launch this
+    // call without it
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
     cudaGetLastError();
-    pdl_ok = 0;
   }
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 0;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

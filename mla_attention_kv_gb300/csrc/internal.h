@@ -98,7 +98,7 @@ struct DecodeParams {
 constexpr int kSingleBarrierRowsTimesChunks = 16;
 
 struct DecodePlan {
-  int grid;        // CTAs (cooperative, one per SM)
+  int grid;        // CTAs (one per SM, all resident at once)
   bool two_per_sm; // built to fit two CTAs per SM (the <= kDecodeSmallTokens plan)
   int tt_max;      // token rows per launch (64 or 128)
   int KB, KC;      // split-K of kv_a
@@ -145,8 +145,18 @@ constexpr int kWkvbBoxRows = 32;
 // previous kernel in the stream ends; it reads only the packed snapshot
 // before its dependency wait, so the snapshot must not be the previous
 // kernel's output).
+// xmap (packed path, may be null): the tensor map of the hidden rows for
+// this launch's box height (decode_box_rows), encoded by the caller;
+// null: encoded here.
 cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const DecodeParams& p,
-                          bool pdl, cudaStream_t stream);
+                          bool pdl, cudaStream_t stream, const CUtensorMap* xmap = nullptr);
+// Rows of one hidden-row TMA box (packed path) for a launch of TT rows of a
+// call with ntok rows: 16 * MT, at most ntok.
+int decode_box_rows(int TT, int ntok);
+// Tensor map of the hidden rows [ntok, hidden] in boxes of 64 columns x
+// rows rows with the 128-byte swizzle (packed decode path).
+bool decode_encode_xmap(CUtensorMap* map, bool bf16, const void* hidden, int hidden_dim, int ntok,
+                        int rows);
 
 }  // namespace mla
 
