@@ -111,14 +111,17 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _dev(t: torch.Tensor, dtype, name: str) -> ctypes.c_void_p:
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    """Device address of a contiguous CUDA tensor of `dtype` (None: any)."""
+    # one combined test on the common path (this runs ~10 times per call)
+    if isinstance(t, torch.Tensor) and t.is_cuda and (dtype is None or t.dtype is dtype) \
+            and t.is_contiguous():
+        return t.data_ptr()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    raise ValueError(f"{name} must be contiguous")
 
 
 def _tdt(cfg: dict) -> torch.dtype:

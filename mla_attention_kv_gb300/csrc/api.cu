@@ -161,7 +161,9 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
     return cuda_fail(e, "device query");
   }
   h->decode_ok = decode_plan(c.hidden, c.num_heads, h->num_sms, &h->dplan);
-  h->small_ok = h->decode_ok && decode_plan_small(c.hidden, c.num_heads, h->num_sms, &h->dplan_small) &&
+  // (the small plan shares the packed snapshot, so it needs the same W_kvb layout)
+  h->small_ok = h->decode_ok && !h->dplan.tc_b &&
+                decode_plan_small(c.hidden, c.num_heads, h->num_sms, &h->dplan_small) &&
                 h->dplan_small.KB == h->dplan.KB && h->dplan_small.KC == h->dplan.KC;
   if (c.quant == MLA_QUANT_NONE && !h->decode_ok) {
     delete h;

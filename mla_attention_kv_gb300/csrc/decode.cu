@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 #include "tma.h"
 
 namespace mla {
@@ -63,6 +64,7 @@ constexpr int kRedBytes = 16384;   // cross-warp reduction scratch (<= 32 chains
 constexpr int kMiscBytes = 2048;   // gamma, cos/sin row, mbarriers, flag
 constexpr int kMaxStagesA = 16;    // deepest phase-A cp.async ring
 constexpr int kMaxStreamBufs = 6;  // W_kvb chunk buffers (mbarriers at misc + 1544 ..)
+constexpr int kTcbMinCols = 128;   // narrowest column slice for phase B on the tensor cores
 
 __device__ __forceinline__ int col_group_begin(int cta, int ngroups, int grid) {
   return (int)(((long long)cta * ngroups) / grid);
@@ -176,6 +178,10 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   const uint32_t bar_a0 = bar_res + 128;  // phase-A stages 0 .. kMaxStagesA-1 (packed weights)
   const uint32_t bar_lat = bar_res + 256; // latent rows from the workspace (two-barrier mode)
   const uint32_t bar_r0 = bar_res + 272;  // streamed W_kvb chunk batches 0 .. 15 (one use each)
+  // phase B on the tensor cores: all MMAs done; the TMEM address (bar_s0 + 8 j
+  // then marks the MMAs of K block j done, freeing its slot for a refill)
+  const uint32_t bar_tb = bar_res + 72;
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + p.off_misc + 1632);
   if (tid == 0) {
     if constexpr (PK) {
       tma_prefetch_desc(&p.tmap_x);
@@ -185,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
     }
     mbar_init(bar_res, 1);
     for (int i = 0; i < kMaxStreamBufs; ++i) mbar_init(bar_s0 + 8 * i, 1);
+    mbar_init(bar_tb, 1);
     fence_mbar_init();
     sFlag[1] = 0;  // resident W_kvb copies not issued yet (packed path)
     mbar_init(bar_lat, 1);
@@ -219,7 +226,21 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   // lane (thread 0 alone spends ~40 ns per copy instruction), and records
   // that it did in *sWkvbOn for the drains
   int* sWkvbOn = sFlag + 1;
+  // K-major blocks (phase B on the tensor cores): N x 128 bytes per 64 K rows
+  const int tbB = ng * 8 * 128;
   auto issue_wkvb_warp = [&]() {  // warp 1
+    if (PK && p.tcb) {
+      // the first tb_res K blocks, contiguous: 16 KB per lane (the later
+      // blocks are prefetched into L2 once phase A's copies are all out: a
+      // bulk prefetch occupies the SM's copy engine)
+      const uint32_t bytes = (uint32_t)(ng > 0 ? p.tb_res * tbB : 0);
+      if (lane == 0) mbar_arrive_expect_tx(bar_res, bytes);
+      __syncwarp();
+      for (uint32_t o = lane * 16384u; o < bytes; o += 32u * 16384u)
+        bulk_g2s(smem_u32(sWB) + o, wkvb_blk + o, bytes - o < 16384u ? bytes - o : 16384u, bar_res);
+      if (lane == 0) *reinterpret_cast<volatile int*>(sWkvbOn) = 1;
+      return;
+    }
     if (lane == 0) mbar_arrive_expect_tx(bar_res, (uint32_t)(ng > 0 ? p.kpre * pitchW : 0));
     __syncwarp();
     if (ng > 0) {
@@ -555,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   constexpr int CR = kWkvbBoxRows;
   constexpr int nch = kRank / CR;
   const int nres = p.kpre / CR;
-  const bool ring = ng > 0 && nres < nch;
+  const bool ring = ng > 0 && nres < nch && !(PK && p.tcb);
   int nbuf = (p.off_red - p.off_a - nrm_bytes) / (CR * pitchW);
   if (nbuf > kMaxStreamBufs) nbuf = kMaxStreamBufs;
   if (nbuf < 2) nbuf = 2;  // the plan reserves two at the largest row count
@@ -593,6 +614,22 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   if (ring) {
     if (warp == 0) issue_batch(nres, issued);
     note_batch(nres, issued);
+  }
+  // phase B on the tensor cores: K blocks tb_res .. tb_res + tb_buf - 1 go
+  // to the buffers behind the 64 KB of latent rows now, one barrier each
+  // (bar_r0 + 8 j, j = block - tb_res)
+  unsigned char* sTbBuf = sA + 64 * 128 * 8;
+  if (PK && p.tcb && ng > 0) {
+    if (warp == 0 && lane < p.tb_buf) {
+      const uint32_t bar = bar_r0 + 8 * lane;
+      mbar_arrive_expect_tx(bar, (uint32_t)tbB);
+      bulk_g2s(smem_u32(sTbBuf) + lane * tbB, wkvb_blk + (size_t)(p.tb_res + lane) * tbB, (uint32_t)tbB, bar);
+    }
+    // the blocks refilled in phase B: into L2 during the barrier and phase R
+    const int nsl = p.tb_res + p.tb_buf;
+    if (warp == 0 && lane >= 16 && lane - 16 < 8 - nsl)
+      prefetch_l2_bulk(wkvb_blk + (size_t)(nsl + lane - 16) * tbB, (uint32_t)tbB);
+    nbatch = p.tb_buf;
   }
   // on an early exit, wait (bounded) for this CTA's copies still in flight:
   // the resident rows and every issued chunk not yet observed (at most one
@@ -637,6 +674,14 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
 
   // ================================================================ phase R
   const float rms_scale = 1.0f / (float)kRank;
+  // Phase B on the tensor cores reads the latent rows as its A operand: 8
+  // K blocks of 64 rows x 128 bytes (64 columns), 8-row groups 1024 bytes
+  // apart, the 16-byte chunk q of row t at chunk q ^ (t & 7).  Byte offset
+  // of element (t, c) -- the same in shared memory and in the workspace.
+  auto lat_off = [](int t, int c) -> int {
+    return (c >> 6) * (64 * 128) + t * 128 + ((((c >> 3) & 7) ^ (t & 7)) << 4) + (c & 7) * 2;
+  };
+  const bool tcb = PK && p.tcb;
   if (p.single_barrier) {
     // every CTA reduces every row into its own shared memory
     for (int t = 0; t < TT; ++t) {
@@ -667,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
         const int c = tid * 4;
         uint2 pk = make_uint2(E::pack(v.x * inv * E::to_f(sGam[c]), v.y * inv * E::to_f(sGam[c + 1])),
                               E::pack(v.z * inv * E::to_f(sGam[c + 2]), v.w * inv * E::to_f(sGam[c + 3])));
-        *reinterpret_cast<uint2*>(sN + t * kPitchN + c * 2) = pk;
+        *reinterpret_cast<uint2*>(sN + (tcb ? lat_off(t, c) : t * kPitchN + c * 2)) = pk;
       } else if (rope_row && tid < kNa / 4) {
         const int i = tid - kRank / 4, j0 = 2 * i, j1 = 2 * i + 1;
         int ou, in, cnt;
@@ -677,8 +722,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
                     v.w * sCos[j1 + 32] + v.z * sSin[j1 + 32]);
       }
     }
-    // zero the padding rows of the last m-tile
-    for (int c = tid; c < (rows_x - TT) * 64; c += kThreads) {
+    // zero the padding rows of the last m-tile (the tensor-core phase B
+    // leaves them: they only reach accumulator rows that are not stored)
+    for (int c = tid; !tcb && c < (rows_x - TT) * 64; c += kThreads) {
       const int r = TT + (c >> 6), ch = c & 63;
       *reinterpret_cast<uint4*>(sN + r * kPitchN + ch * 16) = make_uint4(0, 0, 0, 0);
     }
@@ -712,7 +758,10 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
         if (p.latent) {  // latent-cache variant: the row is an output
           *reinterpret_cast<uint2*>(static_cast<T*>(p.latent) + (size_t)(p.t0 + t) * kRank + c) = pk;
         } else {
-          *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * (kNrmPitch / 2) + c) = pk;
+          if (tcb)
+            *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.nrm) + lat_off(t, c)) = pk;
+          else
+            *reinterpret_cast<uint2*>(static_cast<T*>(p.nrm) + (size_t)t * (kNrmPitch / 2) + c) = pk;
           // the row is read back by bulk copies (async proxy)
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
@@ -730,14 +779,16 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       return;
     }
     // latent rows -> shared memory: the workspace rows have the shared-memory
-    // pitch, so one bulk copy moves all TT of them; rows past TT are zeroed
+    // layout, so one bulk copy moves all TT of them (all 64 K blocks' rows
+    // for the tensor-core phase B); rows past TT are zeroed (mma.sync phase B)
+    const uint32_t lat_bytes = tcb ? 64u * 128u * 8u : (uint32_t)(TT * kNrmPitch);
     if (tid == 0 && !p.latent) {
       asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_arrive_expect_tx(bar_lat, (uint32_t)(TT * kNrmPitch));
-      bulk_g2s(smem_u32(sN), p.nrm, (uint32_t)(TT * kNrmPitch), bar_lat);
+      mbar_arrive_expect_tx(bar_lat, lat_bytes);
+      bulk_g2s(smem_u32(sN), p.nrm, lat_bytes, bar_lat);
       lat_issued = true;
     }
-    for (int c = tid; c < (rows_x - TT) * (kPitchN / 16); c += kThreads)
+    for (int c = tid; !tcb && c < (rows_x - TT) * (kPitchN / 16); c += kThreads)
       *reinterpret_cast<uint4*>(sN + TT * kPitchN + c * 16) = make_uint4(0, 0, 0, 0);
   }
   const unsigned exit_old = bar_exit_arrive(p.counters);
@@ -788,6 +839,116 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
     bar_exit_finish(p.counters, exit_old, G);
     return;
   }
+  // ---- kv_b on the tensor cores (packed weights, wide slices): D [64 token
+  // rows, N = 8 ng columns] in 256 TMEM columns, one MMA (M = 64, N, K = 16)
+  // per k16 step, A = the latent rows, B = the K-major W_kvb block; thread
+  // 0 issues block by block as each is in shared memory.  Blocks [0, R) are
+  // resident, [R, R + NBUF) sit in the buffers, block R + NBUF + j is
+  // copied into block j's slot once a commit marks block j's MMAs done.
+  bool tcb_done = false;
+  if constexpr (PK) {
+    if (tcb) {
+      const int N = ng * 8;
+      const int R = p.tb_res, NBUF = p.tb_buf, NSL = R + NBUF;
+      const int nref = 8 - NSL > 0 ? 8 - NSL : 0;
+      tc::fence_proxy_async_smem();  // latent rows written by this CTA's threads (one-barrier mode)
+      if (warp == 2) tc::tmem_alloc(smem_u32(sTmem), 256);
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      const uint32_t tmem = *sTmem;
+      auto slot_addr = [&](int a) -> uint32_t {
+        int si = a;
+        while (si >= NSL) si -= NSL;
+        return si < R ? smem_u32(sWB) + si * tbB : smem_u32(sTbBuf) + (si - R) * tbB;
+      };
+      const uint32_t idesc = tc::idesc_f16(E::kBf16, 64, N, false, false);
+      if (tid == 0) {
+        int ok = 1, nref_issued = 0;
+        auto issue_refill = [&](int j) {  // block NSL + j into block j's slot
+          const uint32_t bar = bar_r0 + 8 * (NBUF + j);
+          mbar_arrive_expect_tx(bar, (uint32_t)tbB);
+          bulk_g2s(slot_addr(NSL + j), wkvb_blk + (size_t)(NSL + j) * tbB, (uint32_t)tbB, bar);
+        };
+        for (int a = 0; a < 8 && ok; ++a) {
+          if (a >= R) {
+            if (a >= NSL) {  // a refill: its slot must be free first
+              while (nref_issued <= a - NSL && ok) {
+                ok = mbar_wait_bounded(bar_s0 + 8 * nref_issued, 0, p.budget_ns) ? 1 : 0;
+                if (ok) issue_refill(nref_issued++);
+              }
+              if (!ok) break;
+            }
+            ok = mbar_wait_bounded(bar_r0 + 8 * (a - R), 0, p.budget_ns) ? 1 : 0;
+            if (!ok) break;
+            tc::fence_after_sync();
+          }
+          const uint32_t wb = slot_addr(a);
+          const uint32_t ab = smem_u32(sN) + a * (64 * 128);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_f16(tmem, tc::sdesc_sw128(ab + kk * 32, 16, 1024), tc::sdesc_sw128(wb + kk * 32, 16, 1024),
+                        idesc, a > 0 || kk > 0);
+          if (a < nref) tc::commit(bar_s0 + 8 * a);
+          // refills whose slots are already free go out now
+          while (nref_issued < nref && nref_issued <= a && mbar_test_wait(bar_s0 + 8 * nref_issued, 0))
+            issue_refill(nref_issued++);
+        }
+        tc::commit(bar_tb);
+        if (!ok) {
+          // wait (bounded) for the refills and MMAs in flight before leaving
+          atomicOr(p.status, kStatusTimeout);
+          for (int j = 0; j < nref_issued; ++j)
+            mbar_wait_bounded(bar_r0 + 8 * (NBUF + j), 0, drain_budget(p.budget_ns));
+          mbar_wait_bounded(bar_tb, 0, drain_budget(p.budget_ns));
+        }
+        *sFlag = ok;
+      }
+      __syncthreads();
+      const bool mma_ok = *reinterpret_cast<volatile int*>(sFlag) != 0;
+      __syncthreads();
+      if (!mma_ok || !mbar_wait_cta(bar_tb, 0, p.budget_ns, sFlag)) {
+        if (tid == 0 && mma_ok) {
+          atomicOr(p.status, kStatusTimeout);
+          mbar_wait_bounded(bar_tb, 0, drain_budget(p.budget_ns));
+        }
+        drain();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 2) tc::tmem_dealloc(tmem, 256);
+        bar_exit_finish(p.counters, exit_old, G);
+        return;
+      }
+      tc::fence_after_sync();
+      // D row r (token row r) is TMEM lane 32 (r / 16) + r % 16 (M = 64);
+      // warps q and q + 4 read lane quadrant q, 32 columns at a time, and
+      // stage the rows in the I/O dtype in the W area (free now), the
+      // layout the store loop below reads
+      {
+        const int q = warp & 3;
+        for (int ch = warp >> 2; ch * 32 < N; ch += 2) {
+          uint32_t v[32];
+          tc::ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32), v);
+          tc::wait_ld();
+          const int r = q * 16 + lane;
+          if (lane < 16 && r < TT) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              if (ch * 32 + g * 8 < N)
+                *reinterpret_cast<uint4*>(sWB + r * pitchB + (ch * 4 + g) * 16) = make_uint4(
+                    E::pack(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1])),
+                    E::pack(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3])),
+                    E::pack(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5])),
+                    E::pack(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7])));
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncthreads();
+      if (warp == 2) tc::tmem_dealloc(tmem, 256);
+      tcb_done = true;
+    }
+  }
   // k16 steps of rows [kbase, kbase + krows) whose W_kvb rows start at
   // shared address wbase; a warp walks only the steps of its k-slice
   auto mma_rows = [&](uint32_t wbase, int kbase, int krows) {
@@ -814,7 +975,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       }
     }
   };
-  if (!ring) {
+  if (tcb_done) {
+    // (phase B ran on the tensor cores above)
+  } else if (!ring) {
     mma_rows(smem_u32(sWB), 0, p.kpre);
   } else {
     // Chunks are consumed in runs that are contiguous in shared memory (same
@@ -873,7 +1036,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
     *reinterpret_cast<uint32_t*>(d) = E::pack(v[0], v[1]);
     *reinterpret_cast<uint32_t*>(d + 8 * pitchB) = E::pack(v[2], v[3]);
   };
-  if (ks == 1) {
+  if (tcb_done) {
+    // (the tile is staged already)
+  } else if (ks == 1) {
 #pragma unroll
     for (int q = 0; q < QM; ++q)
       if (qv[q]) {
@@ -998,13 +1163,45 @@ __global__ void pack_wkvb_kernel(const uint4* __restrict__ W, uint4* __restrict_
   }
 }
 
+// W_kvb for phase B on the tensor cores: CTA c's slice (groups [g0, g0 +
+// ng), N = 8 ng columns) is 8 blocks of 64 K rows; block a holds N rows,
+// one per output column n, of 64 K values (128 bytes), the 16-byte chunk q
+// of row n stored at chunk q ^ (n & 7) -- the K-major, 128-byte-swizzle
+// operand layout, 8-row groups 1024 bytes apart.  One output chunk (8 K
+// values of one column) per thread step; the slice of CTA c starts where
+// the row-major packing's does (g0 * 512 chunks).
+__global__ void pack_wkvb_kmajor_kernel(const uint16_t* __restrict__ W, uint4* __restrict__ out, int NG,
+                                        int G) {
+  const int NB = NG * 8;
+  const long n = (long)NB * (kRank / 8);
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int col = (int)(i / (kRank / 8)), q8 = (int)(i % (kRank / 8));
+    const int g = col / 8;
+    const int c = (int)(((long)(g + 1) * G + NG - 1) / NG) - 1;
+    const int g0 = col_group_begin(c, NG, G), ng = col_group_begin(c + 1, NG, G) - g0;
+    const int nrow = col - g0 * 8, N = ng * 8;
+    const int a = q8 / 8, q = q8 % 8;
+    uint32_t v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      v[t] = (uint32_t)W[(size_t)(q8 * 8 + 2 * t) * NB + col] |
+             ((uint32_t)W[(size_t)(q8 * 8 + 2 * t + 1) * NB + col] << 16);
+    out[(long)g0 * (kRank * 16 / 16) + (long)a * N * 8 + (long)nrow * 8 + (q ^ (nrow & 7))] =
+        make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, const void* W_kva,
                                 const void* W_kvb, void* pk_kva, void* pk_kvb, cudaStream_t stream) {
   const int NG = heads * kHeadCols / 8;
   pack_wkva_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kva),
                                                      static_cast<uint4*>(pk_kva), hidden, plan.KB);
-  pack_wkvb_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kvb),
-                                                     static_cast<uint4*>(pk_kvb), NG, plan.grid);
+  if (plan.tc_b)
+    pack_wkvb_kmajor_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint16_t*>(W_kvb),
+                                                              static_cast<uint4*>(pk_kvb), NG, plan.grid);
+  else
+    pack_wkvb_kernel<<<plan.grid * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kvb),
+                                                       static_cast<uint4*>(pk_kvb), NG, plan.grid);
   return cudaGetLastError();
 }
 
@@ -1072,6 +1269,22 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
   if (plan->smem > (size_t)budget) return false;
   plan->two_per_sm = budget <= kSmemBudget2;
   if (kpre < tt) return false;  // the output tile is staged in the W_kvb area
+  // phase B on the tensor cores for wide column slices (one MMA per k16 step
+  // costs the same issue time whatever N is, so it pays from N = 128 on):
+  // M = 64 token rows, the latent rows as 8 K blocks of 64 rows x 128 bytes
+  // (64 KB) at the start of region A, W_kvb K blocks of N x 128 bytes in
+  // the W area and in whole buffers behind the latent rows
+  plan->tc_b = false;
+  plan->tb_res = plan->tb_buf = 0;
+  const int blk = ngmax * 8 * 128;
+  const int spare = plan->off_red - plan->off_a - 64 * 128 * 8;
+  if (tt <= 64 && !plan->two_per_sm && ngmax * 8 >= kTcbMinCols && spare >= 0 &&
+      plan->off_a >= blk && plan->off_a >= 64 * pitchB) {
+    plan->tc_b = true;
+    plan->tb_res = plan->off_a / blk < 8 ? plan->off_a / blk : 8;
+    const int nb = spare / blk;
+    plan->tb_buf = nb < 8 - plan->tb_res ? nb : 8 - plan->tb_res;
+  }
   plan->partial_floats = (size_t)KC * kDecodeMaxTokens * kNa;
   return true;
 }
@@ -1206,6 +1419,9 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   p.off_a = plan.off_a;
   p.off_red = plan.off_red;
   p.off_misc = plan.off_misc;
+  p.tcb = (packed && plan.tc_b) ? 1 : 0;
+  p.tb_res = plan.tb_res;
+  p.tb_buf = plan.tb_buf;
   if (packed) {
     // hidden rows [ntok, hidden]: boxes of 64 columns x xrows rows, 128-byte
     // swizzle; rows past ntok read as zero.  The box is at most the tensor's

@@ -91,6 +91,8 @@ struct DecodeParams {
   int off_wb, off_a, off_red, off_misc;  // smem layout (bytes)
   int single_barrier;       // 1: every CTA reduces every row (one grid barrier)
   int pb_wm, pb_ks;         // phase-B warp grid rows (m side) and k-slices
+  int tcb;                  // packed weights, phase B on the tensor cores (plan tc_b)
+  int tb_res, tb_buf;       // ... W_kvb K blocks resident from the start / in spare buffers
 };
 
 // Rows x split-K chunks up to which every CTA reduces all partial rows itself
@@ -104,6 +106,13 @@ struct DecodePlan {
   int KB, KC;      // split-K of kv_a
   int kpre, kchunk, nstA, ngbox;
   int ngmax;       // most 8-column W_kvb groups of one CTA
+  // Phase B on the tensor cores (packed weights; wide column slices, at most
+  // 64 rows per launch): the W_kvb slice is packed as 8 K blocks of 64 rows
+  // in the MMA's K-major layout; tb_res blocks stay resident from the start,
+  // tb_buf more fit in the buffers behind the latent rows, the rest reuse
+  // the slots of consumed blocks.
+  bool tc_b;
+  int tb_res, tb_buf;
   int off_wb, off_a, off_red, off_misc;
   size_t smem;     // dynamic shared memory bytes
   size_t partial_floats;  // workspace floats needed for partials

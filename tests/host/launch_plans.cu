@@ -102,6 +102,24 @@ void check_decode_shape(int hidden, int heads, int sms) {
   if (p.kpre < kRank)
     CHECK(p.tt_max * kPitchN + 2 * kWkvbBoxRows * pitchB <= regionA, "no room for two stream buffers");
 
+  // phase B on the tensor cores: wide slices, at most 64 rows, one CTA per
+  // SM; the resident K blocks fit the W area, the 64 KB latent operand and
+  // the buffer blocks fit region A, the refills have a slot-free barrier
+  // each (6), and the output tile fits the W area
+  const int blk = p.ngmax * 8 * 128;
+  if (p.tc_b) {
+    CHECK(p.tt_max <= 64 && !p.two_per_sm && p.ngmax * 8 >= 128, "tc_b plan tt %d ngmax %d", p.tt_max, p.ngmax);
+    CHECK(p.tb_res >= 1 && p.tb_res <= 8 && p.tb_res * blk <= p.off_a, "tb_res %d", p.tb_res);
+    CHECK(p.tb_buf >= 0 && p.tb_res + p.tb_buf <= 8 && 64 * 1024 + p.tb_buf * blk <= regionA, "tb_buf %d",
+          p.tb_buf);
+    CHECK(8 - p.tb_res - p.tb_buf <= 6, "refills %d", 8 - p.tb_res - p.tb_buf);
+    CHECK(64 * pitchB <= p.off_a, "output tile");
+  } else {
+    CHECK(p.ngmax * 8 < 128 || p.tt_max > 64, "wide slice without tc_b: ngmax %d", p.ngmax);
+  }
+  std::printf("plan hidden %d heads %d sms %d: tt %d KC %d kpre %d off_a %d off_red %d tc_b %d res %d buf %d\n",
+              hidden, heads, sms, p.tt_max, p.KC, p.kpre, p.off_a, p.off_red, (int)p.tc_b, p.tb_res, p.tb_buf);
+
   // phase B for every row count the plan takes
   for (int mt = 1; mt * 16 <= p.tt_max; mt *= 2) {
     int v = -1, wm = 0, ks = 0;
