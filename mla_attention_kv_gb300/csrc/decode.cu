@@ -139,7 +139,9 @@ __device__ __forceinline__ void for_each_c(std::integer_sequence<int, Cs...>, F&
 // under half the shared memory and 128 registers) lets the CTAs of the next
 // call in the stream become resident beside this call's and copy their packed
 // weights while it runs.
-template <typename T, int IM, int QM, bool PK, int NC>
+// TB: phase B on the tensor cores (packed weights, plan tc_b; a separate
+// instance, so that the other instances carry no tensor-memory code).
+template <typename T, int IM, int QM, bool PK, int NC, bool TB>
 __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_constant__ DecodeParams p) {
   using E = Elem<T>;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   // K-major blocks (phase B on the tensor cores): N x 128 bytes per 64 K rows
   const int tbB = ng * 8 * 128;
   auto issue_wkvb_warp = [&]() {  // warp 1
-    if (PK && p.tcb) {
+    if constexpr (TB) {
       // the first tb_res K blocks, contiguous: 16 KB per lane (the later
       // blocks are prefetched into L2 once phase A's copies are all out: a
       // bulk prefetch occupies the SM's copy engine)
@@ -576,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   constexpr int CR = kWkvbBoxRows;
   constexpr int nch = kRank / CR;
   const int nres = p.kpre / CR;
-  const bool ring = ng > 0 && nres < nch && !(PK && p.tcb);
+  const bool ring = ng > 0 && nres < nch && !TB;
   int nbuf = (p.off_red - p.off_a - nrm_bytes) / (CR * pitchW);
   if (nbuf > kMaxStreamBufs) nbuf = kMaxStreamBufs;
   if (nbuf < 2) nbuf = 2;  // the plan reserves two at the largest row count
@@ -619,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   // to the buffers behind the 64 KB of latent rows now, one barrier each
   // (bar_r0 + 8 j, j = block - tb_res)
   unsigned char* sTbBuf = sA + 64 * 128 * 8;
-  if (PK && p.tcb && ng > 0) {
+  if (TB && ng > 0) {
     if (warp == 0 && lane < p.tb_buf) {
       const uint32_t bar = bar_r0 + 8 * lane;
       mbar_arrive_expect_tx(bar, (uint32_t)tbB);
@@ -681,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   auto lat_off = [](int t, int c) -> int {
     return (c >> 6) * (64 * 128) + t * 128 + ((((c >> 3) & 7) ^ (t & 7)) << 4) + (c & 7) * 2;
   };
-  const bool tcb = PK && p.tcb;
+  constexpr bool tcb = TB;
   if (p.single_barrier) {
     // every CTA reduces every row into its own shared memory
     for (int t = 0; t < TT; ++t) {
@@ -846,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   // resident, [R, R + NBUF) sit in the buffers, block R + NBUF + j is
   // copied into block j's slot once a commit marks block j's MMAs done.
   bool tcb_done = false;
-  if constexpr (PK) {
-    if (tcb) {
+  if constexpr (TB) {
+    {
       const int N = ng * 8;
       const int R = p.tb_res, NBUF = p.tb_buf, NSL = R + NBUF;
       const int nref = 8 - NSL > 0 ? 8 - NSL : 0;
@@ -1097,15 +1099,18 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
 constexpr int kVariants[3][2] = {{1, 4}, {1, 8}, {2, 8}};
 
 template <typename T, bool PK>
-const void* kernel_for(int variant, bool two_per_sm) {
-  if (two_per_sm) {
-    if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 2>;
-    if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 2>;
-    return (const void*)decode_kernel<T, 2, 8, PK, 2>;
+const void* kernel_for(int variant, bool two_per_sm, bool tcb) {
+  if constexpr (PK) {
+    if (tcb) return (const void*)decode_kernel<T, 1, 4, true, 1, true>;  // (no mma.sync phase B)
   }
-  if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 1>;
-  if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 1>;
-  return (const void*)decode_kernel<T, 2, 8, PK, 1>;
+  if (two_per_sm) {
+    if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 2, false>;
+    if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 2, false>;
+    return (const void*)decode_kernel<T, 2, 8, PK, 2, false>;
+  }
+  if (variant == 0) return (const void*)decode_kernel<T, 1, 4, PK, 1, false>;
+  if (variant == 1) return (const void*)decode_kernel<T, 1, 8, PK, 1, false>;
+  return (const void*)decode_kernel<T, 2, 8, PK, 1, false>;
 }
 
 }  // namespace
@@ -1402,8 +1407,11 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   int variant, wm, ks;
   if (!decode_phase_b(mt, plan.ngmax, &variant, &wm, &ks)) return cudaErrorInvalidValue;
   const bool two = plan.two_per_sm;
-  const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant, two) : kernel_for<__half, true>(variant, two))
-                          : (bf16 ? kernel_for<__nv_bfloat16, false>(variant, two) : kernel_for<__half, false>(variant, two));
+  const bool tcb = packed && plan.tc_b;
+  const void* fn = packed ? (bf16 ? kernel_for<__nv_bfloat16, true>(variant, two, tcb)
+                                  : kernel_for<__half, true>(variant, two, tcb))
+                          : (bf16 ? kernel_for<__nv_bfloat16, false>(variant, two, false)
+                                  : kernel_for<__half, false>(variant, two, false));
   cudaError_t e = prepare_instance(fn, plan.smem, plan.grid);
   if (e != cudaSuccess) return e;
   DecodeParams p = p0;
@@ -1419,7 +1427,7 @@ cudaError_t decode_launch(bool bf16, bool packed, const DecodePlan& plan, const 
   p.off_a = plan.off_a;
   p.off_red = plan.off_red;
   p.off_misc = plan.off_misc;
-  p.tcb = (packed && plan.tc_b) ? 1 : 0;
+  p.tcb = tcb ? 1 : 0;
   p.tb_res = plan.tb_res;
   p.tb_buf = plan.tb_buf;
   if (packed) {
