@@ -811,6 +811,7 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(srow + (prolog ? 2 * MT : 0));
   __shared__ float scratch[8];
   __shared__ int s_last;
+  unsigned ticket = 0;  // thread 0: this CTA's place among acc1's readers (prolog mode)
   // this CTA's blocks
   int u0, nu;
   const int* ulist = nullptr;
@@ -882,13 +883,10 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
       for (int i = tid; i < p.M * na; i += 256) p.pr.cap_a[i] = p.acc1[i];
       __syncthreads();
     }
-    // the last CTA to finish reading acc1 clears it for the next call
-    if (tid == 0) s_last = atomicAdd(p.readers, 1u) == (unsigned)G - 1 ? 1 : 0;
-    __syncthreads();
-    if (s_last) {
-      for (int i = tid; i < p.M * na; i += 256) p.acc1[i] = 0;
-      if (tid == 0) *p.readers = 0u;
-    }
+    // the last CTA to finish reading acc1 clears it for the next call; it
+    // learns that it is last from this add, whose result is only looked at
+    // once its blocks are done, so the round trip stays off the critical path
+    if (tid == 0) ticket = atomicAdd(p.readers, 1u);
     if (cta == 0) {  // operand copies for inspection
       for (int i = tid; i < p.M * rq; i += 256) p.ws.q1[i] = sAct0[(i / rq) * p.kpad[0] + i % rq];
       for (int i = tid; i < p.M * kRank; i += 256) p.ws.c1[i] = sAct1[(i / kRank) * p.kpad[1] + i % kRank];
@@ -1025,6 +1023,14 @@ __global__ void __launch_bounds__(256) w8_back_kernel(const __grid_constant__ W8
       }
     }
     __syncthreads();  // the reduction area is reused by the next block
+  }
+  if (prolog) {
+    if (tid == 0) s_last = ticket == (unsigned)G - 1 ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+      for (int i = tid; i < p.M * na; i += 256) p.acc1[i] = 0;
+      if (tid == 0) *p.readers = 0u;
+    }
   }
 }
 
