@@ -38,13 +38,15 @@ def make_scales(cfg, seed):
                 kpe=g.uniform(kpe_hi / 2, kpe_hi, 64).astype(np.float32))
 
 
-def run_c8(cfg, b, s, seed, path, positions="decode", oracle_mod=None, rows=None):
+def run_c8(cfg, b, s, seed, path, positions="decode", oracle_mod=None, rows=None, packed=False):
     inp = I.kv_inputs(cfg, b, s, seed, positions)
     d = B.to_device(inp)
     sc = make_scales(cfg, seed)
     scd = {k: torch.tensor(v, device="cuda") for k, v in sc.items()}
     m = B.MLAProlog(cfg, b * s)
     m.set_path(path)
+    if packed:
+        m.prepare_weights(d)
     q = m.alloc_c8_outputs(b, s)
     m.run_c8(b, s, d, scd, q)
     torch.cuda.synchronize()
@@ -85,8 +87,10 @@ def test_c8_decode_v2lite(oracle_mod, b, s):
     run_c8(I.V2_LITE, b, s, 500 + b * s, B.PATH_DECODE, oracle_mod=oracle_mod)
 
 
-def test_c8_decode_r1(oracle_mod):
-    run_c8(I.R1, 64, 1, 510, B.PATH_DECODE, oracle_mod=oracle_mod)
+@pytest.mark.parametrize("packed", [False, True])
+def test_c8_decode_r1(oracle_mod, packed):
+    # packed R1 weights: kv_b on the tensor cores, the same int8 store epilogue
+    run_c8(I.R1, 64, 1, 510, B.PATH_DECODE, oracle_mod=oracle_mod, packed=packed)
 
 
 @pytest.mark.parametrize("T", [1024, 1061])

@@ -170,7 +170,7 @@ def test_packed_decode_v2lite(oracle_mod, b, s):
     assert r["status"] == 0
 
 
-@pytest.mark.parametrize("T", [1, 17, 64])
+@pytest.mark.parametrize("T", [1, 17, 64, 100])
 def test_packed_decode_r1(oracle_mod, T):
     r = run_case(I.R1, T, 1, 800 + T, oracle_mod=oracle_mod, packed=True)
     assert r["status"] == 0
@@ -244,9 +244,9 @@ def test_packed_snapshot_only_serves_its_own_weights(oracle_mod):
 # into the captured buffers before each replay; a replay that read the
 # previous replay's partials would give the previous input's kv rows.
 
-@pytest.mark.parametrize("b,packed", [(2, False), (16, True), (128, False)])
-def test_graph_replays_read_their_own_partials(oracle_mod, b, packed):
-    cfg = I.V2_LITE
+@pytest.mark.parametrize("cfg,b,packed", [(I.V2_LITE, 2, False), (I.V2_LITE, 16, True),
+                                          (I.V2_LITE, 128, False), (I.R1, 64, True)])
+def test_graph_replays_read_their_own_partials(oracle_mod, cfg, b, packed):
     inp = I.kv_inputs(cfg, b, 1, 900 + b)
     d = B.to_device(inp)
     m = B.MLAProlog(cfg, b)

@@ -37,11 +37,13 @@ def make_slots(T, page, nblocks, seed, drop=()):
 
 
 def run_paged(cfg, b, s, seed, page, nblocks, slots, path, positions="decode", oracle_mod=None,
-              rows=None):
+              rows=None, packed=False):
     inp = I.kv_inputs(cfg, b, s, seed, positions)
     d = B.to_device(inp)
     m = B.MLAProlog(cfg, b * s)
     m.set_path(path)
+    if packed:
+        m.prepare_weights(d)
     caches = m.alloc_paged_caches(nblocks, page)
     for c in caches.values():
         c.fill_(float("nan"))
@@ -89,10 +91,13 @@ def test_paged_decode_v2lite(oracle_mod):
     assert run_paged(I.V2_LITE, b, s, 401, page, nblk, slots, B.PATH_DECODE, oracle_mod=oracle_mod) == 0
 
 
-def test_paged_decode_r1(oracle_mod):
+@pytest.mark.parametrize("packed", [False, True])
+def test_paged_decode_r1(oracle_mod, packed):
+    # packed R1 weights: kv_b on the tensor cores, the same paged store epilogue
     b, s, page, nblk = 64, 1, 16, 8
     slots = make_slots(b * s, page, nblk, 2)
-    assert run_paged(I.R1, b, s, 402, page, nblk, slots, B.PATH_DECODE, oracle_mod=oracle_mod) == 0
+    assert run_paged(I.R1, b, s, 402, page, nblk, slots, B.PATH_DECODE, oracle_mod=oracle_mod,
+                     packed=packed) == 0
 
 
 def test_paged_decode_two_launches(oracle_mod):
