@@ -194,6 +194,9 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
                                                          Q* __restrict__ q,
                                                          float* __restrict__ scale) {
   __shared__ float scratch[8];
+  // the next kernel of the chain may launch now (it waits for this one
+  // before reading its codes)
+  grid_dep_launch_dependents();
   const int row = blockIdx.x;
   const __nv_bfloat16* xr = x + (size_t)row * cols;
   float amax = 0.f;
@@ -386,8 +389,13 @@ __global__ void __launch_bounds__(256) norm_quant_kernel(int32_t* __restrict__ a
   float* gq = colsc + na;
   float* gk = gq + rq;
   float* rope = gk + kRank;
+  // launched with the programmatic dependency: the caller's inputs (scales,
+  // gammas, positions, cos/sin) are read while the GEMM before runs; its
+  // accumulator rows and the row scales only after it
+  grid_dep_launch_dependents();
   norm_load_inputs(p, colsc, gq, gk);
   rope_load(p, t, rope);
+  grid_dep_wait();
   int32_t* a = acc1 + (size_t)t * na;
   norm_row(a, sx[t], p, yrow, colsc, gq, gk, rope, scratch, w.q1 + (size_t)t * rq, w.s1 + t,
            w.c1 + (size_t)t * kRank, w.s2 + t,
@@ -1506,13 +1514,16 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
     g1.K[0] = h; g1.N[0] = rq; g1.K[1] = h; g1.N[1] = kNa;
     g1.T = T; g1.raw = 1; g1.C = w.acc1; g1.ldc = na; g1.coff[0] = 0; g1.coff[1] = rq;
     g1.status = p.status; g1.budget_ns = p.budget_ns;
-    cudaError_t e2 = w8mma_launch(g1, p.W_qa, p.W_kva, w.xh, w.xh, g_num_sms, st, false);
+    // (the three launches after the quantisation carry the programmatic
+    // dependency: each starts while the one before finishes and waits for
+    // it before reading its results; the weights are read after that wait)
+    cudaError_t e2 = w8mma_launch(g1, p.W_qa, p.W_kva, w.xh, w.xh, g_num_sms, st, true);
     ++*launches;
     if (e2 != cudaSuccess) return e2;
     // 3-4. RMSNorms, requantisation, RoPE(k_pe)
     const size_t smem = norm_smem(rq);
     e2 = cudaFuncSetAttribute(norm_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e2 == cudaSuccess) e2 = launch_k(norm_quant_kernel, dim3(T), dim3(256), smem, st, false, w.acc1, (const float*)w.sx, p, w);
+    if (e2 == cudaSuccess) e2 = launch_k(norm_quant_kernel, dim3(T), dim3(256), smem, st, true, w.acc1, (const float*)w.sx, p, w);
     ++*launches;
     if (e2 != cudaSuccess) return e2;
     // 5-6. q_b_proj -> q_nope, RoPE(q_pe); kv_b_proj -> k_nope, value (one launch)
@@ -1524,7 +1535,7 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
     g2.q_nope = p.q_nope; g2.q_pe = p.q_pe; g2.k_nope = p.k_nope; g2.value = p.value;
     g2.cap[0] = p.cap_qb; g2.cap[1] = p.cap_kvb;
     g2.heads = H; g2.s = p.s; g2.status = p.status; g2.budget_ns = p.budget_ns;
-    e2 = w8mma_launch(g2, p.W_qb, p.W_kvb, w.q1h, w.c1h, g_num_sms, st, false);
+    e2 = w8mma_launch(g2, p.W_qb, p.W_kvb, w.q1h, w.c1h, g_num_sms, st, true);
     ++*launches;
     return e2;
   };

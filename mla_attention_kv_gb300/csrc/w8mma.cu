@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kMmThreads, 1) w8mma_kernel(const __grid_const
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
   // the activations (and, in RAW mode, the accumulator rows) come from the
-  // kernels before this one
+  // kernels before this one; the kernel after this one may launch now
+  grid_dep_launch_dependents();
   grid_dep_wait();
 
   if (warp == 0) {
