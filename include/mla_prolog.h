@@ -131,8 +131,13 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
  *   k_pe          [b, 1, s, 64]        dtype      output
  * T = 0 is a no-op returning MLA_OK.  Errors: MLA_ERR_INVALID_ARG,
  * MLA_ERR_TOO_MANY_TOKENS, MLA_ERR_MISALIGNED, MLA_ERR_WRONG_MODE (handle
- * created for W8A8), MLA_ERR_CUDA.  Device-side faults: see
- * mla_kv_prolog_status. */
+ * created for W8A8), MLA_ERR_CUDA (also when the device cannot hold all CTAs
+ * of the decode kernel at once).  The decode kernel's CTAs wait for one
+ * another at grid barriers; it is launched as a plain (not cooperative)
+ * launch, so if other work on the device keeps some of its CTAs from
+ * starting for longer than spin_budget_ns, the others give up and the call
+ * reports MLA_ERR_DEVICE_TIMEOUT through mla_kv_prolog_status.  Device-side
+ * faults: see mla_kv_prolog_status. */
 mla_status mla_kv_prolog_run(mla_prolog_t h, int b, int s, const void* hidden_states,
                              const int32_t* positions, const void* W_kva, const void* gamma_kv,
                              const void* W_kvb, const float* cos_table, const float* sin_table,
