@@ -90,8 +90,18 @@ typedef enum mla_quant { MLA_QUANT_NONE = 0, MLA_QUANT_W8A8 = 1 } mla_quant;
  * selection that replaces the short/long dynamic selection of [MIG]
  * §"源码级原理", last paragraph): the fused split-K decode kernel for small
  * T, the tcgen05 tensor-core prefill kernel for large T.  DECODE / PREFILL
- * force one path (for tests and benchmarks). */
-typedef enum mla_path { MLA_PATH_AUTO = 0, MLA_PATH_DECODE = 1, MLA_PATH_PREFILL = 2 } mla_path;
+ * force one path (for tests and benchmarks).  On the decode path, launches
+ * of at most 16 rows on the packed snapshot (mla_kv_prolog_prepare_weights)
+ * with dtype outputs take the cluster kernel where the shape allows it
+ * (hidden 2048, the V2-Lite shape, and a device that holds 16-CTA
+ * clusters); DECODE_GRID forces the decode path without it (the grid-barrier
+ * kernel for every launch).  last_path reports DECODE for both. */
+typedef enum mla_path {
+  MLA_PATH_AUTO = 0,
+  MLA_PATH_DECODE = 1,
+  MLA_PATH_PREFILL = 2,
+  MLA_PATH_DECODE_GRID = 3
+} mla_path;
 
 typedef struct mla_prolog_config {
   int hidden;       /* model width: 2048 (V2-Lite), 7168 (R1); multiple of 64          */
@@ -211,7 +221,9 @@ mla_status mla_kv_prolog_run_latent(mla_prolog_t h, int b, int s, const void* hi
  *   is made on `stream` (two kernels); call again after changing the
  *   weights in place.  Passing NULL for both forgets the snapshot.
  *   The first call allocates hidden*576*2 + 512*H*256*2 bytes of device
- *   memory owned by the handle (freed by destroy); later calls reuse it.
+ *   memory owned by the handle (freed by destroy), plus another 512*H*256*2
+ *   where the cluster decode kernel applies (its own W_kvb slices, see
+ *   mla_path); later calls reuse it.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_MISALIGNED, MLA_ERR_WRONG_MODE
  * (W8A8 handle), MLA_ERR_NO_MEMORY, MLA_ERR_CUDA. */
 mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, const void* W_kvb,
@@ -262,6 +274,9 @@ mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path);
  * (mla_path, never AUTO) it took. */
 int mla_kv_prolog_last_launches(mla_prolog_t h);
 int mla_kv_prolog_last_path(mla_prolog_t h);
+/* How many of the last run's launches were the cluster decode kernel
+ * (-1 for a null handle). */
+int mla_kv_prolog_last_cluster_launches(mla_prolog_t h);
 
 /* The smallest b*s for which MLA_PATH_AUTO takes the prefill kernel on this
  * handle (its model shape and device); smaller b*s take the decode kernel.

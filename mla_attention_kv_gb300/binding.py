@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
                 3: "MLA_ERR_TOO_MANY_TOKENS", 4: "MLA_ERR_MISALIGNED", 5: "MLA_ERR_CUDA",
                 6: "MLA_ERR_DEVICE_TIMEOUT", 7: "MLA_ERR_BAD_POSITION", 8: "MLA_ERR_NO_MEMORY",
                 9: "MLA_ERR_WRONG_MODE", 10: "MLA_ERR_BAD_SLOT"}
-PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_GRID = 0, 1, 2, 3
 MLA_F16, MLA_BF16 = 0, 1
 QUANT_NONE, QUANT_W8A8 = 0, 1
 
@@ -29,7 +29,8 @@ EXPORTED = ["mla_kv_prolog_create", "mla_kv_prolog_run", "mla_prolog_w8a8_run",
             "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_status_string",
             "mla_last_cuda_error", "mla_abi_version", "mla_kv_prolog_run_noalloc",
             "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent", "mla_kv_prolog_run_paged",
-            "mla_kv_prolog_run_c8", "mla_kv_prolog_auto_threshold", "mla_prolog_w8a8_capture"]
+            "mla_kv_prolog_run_c8", "mla_kv_prolog_auto_threshold", "mla_prolog_w8a8_capture",
+            "mla_kv_prolog_last_cluster_launches"]
 
 
 class MLAError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str | None = None):
     L.mla_kv_prolog_set_path.argtypes = [H, I]
     L.mla_kv_prolog_last_launches.argtypes = [H]
     L.mla_kv_prolog_last_path.argtypes = [H]
+    L.mla_kv_prolog_last_cluster_launches.argtypes = [H]
     L.mla_w8a8_quant_rows.argtypes = [P, I, I, P, P, P]
     L.mla_w8a8_gemm_s32.argtypes = [P, P, I, I, I, P, P]
     L.mla_prolog_w8a8_operands.argtypes = [H, I, P, P, P, P, P]
@@ -89,7 +91,7 @@ def load(path: str | None = None):
                "mla_w8a8_gemm_s32", "mla_prolog_w8a8_operands", "mla_abi_version",
                "mla_kv_prolog_run_noalloc", "mla_kv_prolog_prepare_weights", "mla_kv_prolog_run_latent",
                "mla_kv_prolog_run_paged", "mla_kv_prolog_run_c8", "mla_kv_prolog_auto_threshold",
-               "mla_prolog_w8a8_capture"):
+               "mla_prolog_w8a8_capture", "mla_kv_prolog_last_cluster_launches"):
         getattr(L, fn).restype = ctypes.c_int
     L.mla_status_string.argtypes = [ctypes.c_int]
     L.mla_status_string.restype = ctypes.c_char_p
@@ -303,6 +305,10 @@ class MLAProlog:
     @property
     def last_path(self) -> int:
         return load().mla_kv_prolog_last_path(self.h)
+
+    @property
+    def last_cluster_launches(self) -> int:
+        return load().mla_kv_prolog_last_cluster_launches(self.h)
 
     @property
     def auto_threshold(self) -> int:

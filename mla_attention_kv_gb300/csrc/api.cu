@@ -20,6 +20,7 @@ struct mla_prolog_s {
   int path_override;
   int last_launches;
   int last_path;
+  int last_cl_launches;
   unsigned long long budget_ns;
   // workspace
   void* ws;
@@ -33,10 +34,13 @@ struct mla_prolog_s {
   bool decode_ok;
   DecodePlan dplan_small;  // <= kDecodeSmallTokens rows per launch, two CTAs per SM
   bool small_ok;
-  // packed weight snapshot (mla_kv_prolog_prepare_weights): W_kva tiles then
-  // W_kvb slices, and the caller pointers they were taken from
+  ClPlan clplan;  // cluster decode kernel (launches of <= kClMaxTokens rows)
+  bool cl_ok;
+  // packed weight snapshot (mla_kv_prolog_prepare_weights): W_kva tiles, W_kvb
+  // slices, then (cl_ok) the W_kvb slices of the cluster kernel's grid, and
+  // the caller pointers they were taken from
   void* pk;
-  size_t pk_kva_bytes, pk_bytes;
+  size_t pk_kva_bytes, pk_kvb_bytes, pk_bytes;
   const void* pk_src_kva;
   const void* pk_src_kvb;
   // the snapshot was just written: the next decode launch must not read it
@@ -169,6 +173,9 @@ mla_status mla_kv_prolog_create(const mla_prolog_config* cfg, mla_prolog_t* out)
     delete h;
     return MLA_ERR_UNSUPPORTED;
   }
+  // (the cluster kernel reads the packed W_kva snapshot, laid out by dplan)
+  h->cl_ok = c.quant == MLA_QUANT_NONE &&
+             decode_cl_plan(c.dtype == MLA_BF16, c.hidden, c.num_heads, h->dplan.KB, &h->clplan);
   // workspace: [status][counters x2][pad] | partials | nrm | w8a8
   size_t off = 256;
   const size_t part_off = off;
@@ -226,7 +233,7 @@ mla_status mla_kv_prolog_destroy(mla_prolog_t h) {
 }
 
 mla_status mla_kv_prolog_set_path(mla_prolog_t h, int path) {
-  if (!h || path < MLA_PATH_AUTO || path > MLA_PATH_PREFILL) return MLA_ERR_INVALID_ARG;
+  if (!h || path < MLA_PATH_AUTO || path > MLA_PATH_DECODE_GRID) return MLA_ERR_INVALID_ARG;
   h->path_override = path;
   return MLA_OK;
 }
@@ -249,6 +256,7 @@ mla_status mla_prolog_w8a8_capture(mla_prolog_t h, int32_t* acc_a, int32_t* acc_
   return MLA_OK;
 }
 int mla_kv_prolog_last_path(mla_prolog_t h) { return h ? h->last_path : -1; }
+int mla_kv_prolog_last_cluster_launches(mla_prolog_t h) { return h ? h->last_cl_launches : -1; }
 
 mla_status mla_kv_prolog_status(mla_prolog_t h, cudaStream_t stream) {
   if (!h) return MLA_ERR_INVALID_ARG;
@@ -286,6 +294,7 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
   if (h->cfg.quant != MLA_QUANT_NONE) return MLA_ERR_WRONG_MODE;
   const long long T = (long long)b * s;
   h->last_launches = 0;
+  h->last_cl_launches = 0;
   if (T == 0) return MLA_OK;
   if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
   const void* ptrs[] = {hidden_states, positions, W_kva, gamma_kv, cos_table, sin_table, k_pe,
@@ -304,6 +313,8 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
     h->last_launches = 1;
   }
   int path = h->path_override;
+  const bool grid_only = path == MLA_PATH_DECODE_GRID;
+  if (grid_only) path = MLA_PATH_DECODE;
   if (path == MLA_PATH_AUTO)
     path = T >= prefill_min_tokens(h->cfg.hidden, h->cfg.num_heads, h->num_sms) ? MLA_PATH_PREFILL : MLA_PATH_DECODE;
   h->last_path = path;
@@ -361,7 +372,23 @@ static mla_status run_kv(mla_prolog_t h, int b, int s, const void* hidden_states
         return MLA_ERR_CUDA;
       }
     }
-    cudaError_t e = decode_launch(bf16, packed, pl, p, !(packed && h->pk_fresh), stream, xm);
+    cudaError_t e;
+    if (packed && h->cl_ok && !grid_only && !latent && !c8q.k && p.TT <= kClMaxTokens) {
+      // the cluster kernel (no grid-wide barrier)
+      ClParams cp = {};
+      cp.tmap_x = *xm;
+      cp.W_kvb = static_cast<const unsigned char*>(h->pk) + h->pk_kva_bytes + h->pk_kvb_bytes;
+      cp.positions = positions; cp.W_kva = W_kva; cp.gamma = gamma_kv; cp.cos_t = cos_table;
+      cp.sin_t = sin_table; cp.k_nope = k_nope; cp.value = value; cp.k_pe = k_pe; cp.out = lay;
+      cp.status = h->status; cp.heads = h->cfg.num_heads; cp.s = s; cp.t0 = p.t0; cp.TT = p.TT;
+      cp.max_pos = h->cfg.max_pos; cp.xrows = decode_box_rows(p.TT, p.ntok); cp.KB = h->dplan.KB;
+      cp.off_misc = h->clplan.off_misc; cp.eps = h->cfg.eps;
+      cp.budget_ns = h->budget_ns;
+      e = decode_cl_launch(bf16, h->clplan, cp, !h->pk_fresh, stream);
+      if (e == cudaSuccess) h->last_cl_launches += 1;
+    } else {
+      e = decode_launch(bf16, packed, pl, p, !(packed && h->pk_fresh), stream, xm);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (packed) h->pk_fresh = false;
     h->last_launches += 1;
@@ -431,19 +458,22 @@ mla_status mla_kv_prolog_prepare_weights(mla_prolog_t h, const void* W_kva, cons
   const size_t kva_bytes = (size_t)h->cfg.hidden * kNa * 2;
   const size_t kvb_bytes = (size_t)kRank * h->cfg.num_heads * kHeadCols * 2;
   if (!h->pk) {
-    cudaError_t e = cudaMalloc(&h->pk, kva_bytes + kvb_bytes);
+    cudaError_t e = cudaMalloc(&h->pk, kva_bytes + kvb_bytes * (h->cl_ok ? 2 : 1));
     if (e != cudaSuccess) {
       h->pk = nullptr;
       cuda_fail(e, "cudaMalloc packed weights");
       return MLA_ERR_NO_MEMORY;
     }
     h->pk_kva_bytes = kva_bytes;
-    h->pk_bytes = kva_bytes + kvb_bytes;
+    h->pk_kvb_bytes = kvb_bytes;
+    h->pk_bytes = kva_bytes + kvb_bytes * (h->cl_ok ? 2 : 1);
   }
   h->pk_src_kva = h->pk_src_kvb = nullptr;
   unsigned char* base = static_cast<unsigned char*>(h->pk);
   cudaError_t e = decode_pack_weights(h->dplan, h->cfg.hidden, h->cfg.num_heads, W_kva, W_kvb, base,
                                       base + kva_bytes, stream);
+  if (e == cudaSuccess && h->cl_ok)
+    e = decode_cl_pack_wkvb(h->clplan, h->cfg.num_heads, W_kvb, base + kva_bytes + kvb_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack weights");
   h->pk_src_kva = W_kva;
   h->pk_src_kvb = W_kvb;
@@ -463,6 +493,7 @@ mla_status mla_prolog_w8a8_run(mla_prolog_t h, int b, int s, const void* hidden_
   if (h->cfg.quant != MLA_QUANT_W8A8) return MLA_ERR_WRONG_MODE;
   const long long T = (long long)b * s;
   h->last_launches = 0;
+  h->last_cl_launches = 0;
   if (T == 0) return MLA_OK;
   if (T > h->cfg.max_tokens) return MLA_ERR_TOO_MANY_TOKENS;
   const void* ptrs[] = {hidden_states, positions, W_qa, sW_qa, gamma_q, W_qb, sW_qb, W_kva,

@@ -1210,6 +1210,14 @@ cudaError_t decode_pack_weights(const DecodePlan& plan, int hidden, int heads, c
   return cudaGetLastError();
 }
 
+cudaError_t decode_cl_pack_wkvb(const ClPlan& plan, int heads, const void* W_kvb, void* out,
+                                cudaStream_t stream) {
+  const int ctas = plan.clusters * kClSize;
+  pack_wkvb_kernel<<<ctas * 4, 256, 0, stream>>>(static_cast<const uint4*>(W_kvb), static_cast<uint4*>(out),
+                                                  heads * kHeadCols / 8, ctas);
+  return cudaGetLastError();
+}
+
 // Shared-memory plan for `tt` token rows per launch; false if it cannot be
 // laid out (or, with `resident_only`, if W_kvb would have to be streamed).
 static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_sms,

@@ -167,6 +167,55 @@ int decode_box_rows(int TT, int ntok);
 bool decode_encode_xmap(CUtensorMap* map, bool bf16, const void* hidden, int hidden_dim, int ntok,
                         int rows);
 
+// ---------------------------------------------------------------- cluster decode kernel
+// The smallest decode launches (at most kClMaxTokens rows, packed snapshot,
+// dense or paged outputs in the I/O dtype) run without a grid-wide barrier:
+// each 16-CTA cluster computes the whole kv_a row block itself and reduces it
+// in distributed shared memory (decode_cl.cu).
+constexpr int kClSize = 16;       // CTAs per cluster
+constexpr int kClMaxTokens = 16;  // rows per launch
+constexpr int kClHidden = 2048;   // hidden size the kernel is built for (128 K rows per CTA)
+
+struct ClPlan {
+  int clusters;  // clusters per launch (all resident at once)
+  int ngmax;     // most 8-column W_kvb groups of one CTA
+  int off_misc;  // shared-memory offset of the barriers / gamma block
+  size_t smem;   // dynamic shared memory bytes
+};
+
+struct ClParams {
+  CUtensorMap tmap_x;       // hidden [ntok, hidden], box = (64 columns, xrows rows), 128-byte swizzle
+  const int32_t* positions; // [T]
+  const void* W_kva;        // packed snapshot (decode_pack_weights layout, KB rows per unit)
+  const void* W_kvb;        // packed snapshot (decode_cl_pack_wkvb: the slices of this grid)
+  const void* gamma;        // [512]
+  const float* cos_t;       // [max_pos, 64]
+  const float* sin_t;
+  void* k_nope;             // [b, H, s, 128]
+  void* value;              // [b, H, s, 128]
+  void* k_pe;               // [b, 1, s, 64]
+  OutLayout out;            // dense or paged placement
+  unsigned* status;         // workspace: device status word
+  int heads, s, t0, TT, max_pos, xrows, KB;
+  int off_misc;
+  float eps;
+  unsigned long long budget_ns;
+};
+
+// Plan for this model shape on the current device: false if the shape is
+// not the one the kernel is built for (hidden == kClHidden, packed units of
+// a multiple of 128 rows) or the device cannot hold a 16-CTA cluster of it.
+bool decode_cl_plan(bool bf16, int hidden, int heads, int KB, ClPlan* plan);
+// Launch one cluster decode of p.TT <= kClMaxTokens rows.  pdl as for
+// decode_launch (the kernel copies only the packed W_kva snapshot before its
+// dependency wait).
+cudaError_t decode_cl_launch(bool bf16, const ClPlan& plan, const ClParams& p, bool pdl,
+                             cudaStream_t stream);
+// W_kvb [512, H*256] -> the cluster kernel's per-CTA column slices (the
+// decode kernel's packed slice layout for a grid of clusters * 16 CTAs).
+cudaError_t decode_cl_pack_wkvb(const ClPlan& plan, int heads, const void* W_kvb, void* out,
+                                cudaStream_t stream);
+
 }  // namespace mla
 
 namespace mla {

@@ -71,6 +71,7 @@ def test_null_arguments(L):
     assert L.mla_kv_prolog_destroy(None) == 1
     assert L.mla_kv_prolog_set_path(None, 0) == 1
     assert L.mla_kv_prolog_last_launches(None) == -1
+    assert L.mla_kv_prolog_last_cluster_launches(None) == -1
     assert L.mla_prolog_w8a8_operands(None, 1, None, None, None, None, None) == 1
     assert L.mla_kv_prolog_auto_threshold(None) == -1
     assert L.mla_prolog_w8a8_capture(None, None, None, None) == 1
@@ -189,8 +190,8 @@ def test_enum_values_match_the_header():
     assert {v: k for k, v in enums.items() if k.startswith(("MLA_OK", "MLA_ERR_"))} == B.STATUS_NAMES
     assert (enums["MLA_F16"], enums["MLA_BF16"]) == (B.MLA_F16, B.MLA_BF16)
     assert (enums["MLA_QUANT_NONE"], enums["MLA_QUANT_W8A8"]) == (B.QUANT_NONE, B.QUANT_W8A8)
-    assert (enums["MLA_PATH_AUTO"], enums["MLA_PATH_DECODE"], enums["MLA_PATH_PREFILL"]) == \
-        (B.PATH_AUTO, B.PATH_DECODE, B.PATH_PREFILL)
+    assert (enums["MLA_PATH_AUTO"], enums["MLA_PATH_DECODE"], enums["MLA_PATH_PREFILL"],
+            enums["MLA_PATH_DECODE_GRID"]) == (B.PATH_AUTO, B.PATH_DECODE, B.PATH_PREFILL, B.PATH_DECODE_GRID)
 
 
 def test_noalloc_rejects_bad_arguments_on_the_host(L):
