@@ -164,6 +164,7 @@ class DecodeSweep:
         self.calls += 1
         d = dict(hidden=p["hidden"], positions=p["positions"], cos=self.cos, sin=self.sin, **w)
         m.run(p["b"], p["s"], d, self.out[i], stream)
+        self.cl_calls = getattr(self, "cl_calls", 0) + getattr(m, "last_cluster_launches", 0)
         return m.last_launches
 
     def step(self, stream, events=None, intervals=None):
@@ -404,6 +405,7 @@ class SingleCall:
             self.m.run_c8(self.b, self.s, self.d, self.scales, self.out, stream)
         else:
             self.m.run(self.b, self.s, self.d, self.out, stream)
+        self.cl_calls = getattr(self, "cl_calls", 0) + getattr(self.m, "last_cluster_launches", 0)
 
     def flush_l2(self):
         self.flush.zero_()
@@ -779,6 +781,9 @@ def roofline(wl, calls, is_w8):
         kernel += " (paged cache)"
     if getattr(wl, "c8", False):
         kernel += " (int8 cache)"
+    # launches of at most 16 rows on the packed V2-Lite snapshot run the
+    # cluster decode kernel (its traffic is under the same entry)
+    label = kernel + (" + decode_cl_kernel (launches of <= 16 rows)" if getattr(wl, "cl_calls", 0) else "")
     if t_mem >= t_cmp:
         achieved = alg_bytes / call_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -793,7 +798,7 @@ def roofline(wl, calls, is_w8):
     tr = [kernel_traffic(kernel, T, model) for T in Ts]
     roof["traffic"] = None if any(x is None for x in tr) else \
         sum(kernel_traffic(kernel, T, model) for T in Tlist) / len(Tlist)
-    roof.update({"peak_kind": peak_kind, "kernel": kernel, "calls_timed": len(Tlist),
+    roof.update({"peak_kind": peak_kind, "kernel": label, "calls_timed": len(Tlist),
                  "mean_call_us": 1e6 * call_s / len(Tlist),
                  "algorithmic_bytes_per_call": alg_bytes / len(Tlist),
                  "algorithmic_flops_per_call": alg_flops / len(Tlist),

@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
   // W_kvb: this CTA's column groups [g0, g0 + ng) are one contiguous block of
   // 512 rows x ng 16-byte chunks, chunk j of row k stored at j ^ pack_swizzle(ng, k)
   const unsigned char* Wbpk = static_cast<const unsigned char*>(p.W_kvb) + (size_t)g0 * (kRank * 16);
+  // (each cluster starts at another tile, so that the clusters, which all
+  // read the same W_kva lines, spread over the L2 slices)
+  // (W_kvb copies after W_kva's: a CTA's copies share its copy engine, and
+  // so do the bulk copies of the two exchange rounds later on)
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_wa, (uint32_t)kWaBytes);
@@ -176,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
     }
     __syncwarp();
     if (lane < kNa / 32) {
+      const int nb = (lane + 5 * (int)(blockIdx.x / kClSize)) % (kNa / 32);
       const int krow = r * kKr, kc = krow / p.KB, rr = krow - kc * p.KB;
-      bulk_g2s(sWa + lane * (kKr * 64), Wpk + (((size_t)kc * (kNa / 32) + lane) * p.KB + rr) * 64, kKr * 64,
-               bar_wa);
+      bulk_g2s(sWa + nb * (kKr * 64), Wpk + (((size_t)kc * (kNa / 32) + nb) * p.KB + rr) * 64, kKr * 64, bar_wa);
     } else if (lane - kNa / 32 < ng) {
       const int j = lane - kNa / 32;
       bulk_g2s(sWb + j * (kRank * 16), Wbpk + (size_t)j * (kRank * 16), kRank * 16, bar_wb);
@@ -403,7 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
 
   // ================================================================ phase B
   if (good) {
-    if (tid == 0) sFlag[3] = mbar_wait_bounded(bar_wb, 0, p.budget_ns) ? 1 : 0;
     if (tid < kRank / 4) {
       // thread c4 normalises columns 4 c4 .. 4 c4 + 3 of every row; lane t
       // of each warp takes the 1 / rms of row t (the 16 partial sums of
@@ -434,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
       for (int e = tid - kRank / 4; e < (16 - TT) * kChunks; e += kThreads - kRank / 4)
         *reinterpret_cast<uint4*>(sN + (TT + e / kChunks) * kNrmPitch + (e % kChunks) * 16) = make_uint4(0, 0, 0, 0);
     }
+    if (tid == 0) sFlag[3] = mbar_wait_bounded(bar_wb, 0, p.budget_ns) ? 1 : 0;
     __syncthreads();
     if (sFlag[3] == 0) {
       if (tid == 0) atomicOr(p.status, kStatusTimeout);
