@@ -156,14 +156,22 @@ class DecodeSweep:
         self.pt = [dict(b=b, s=s, **v) for (b, s), v in zip(self.points, views_d)]
         self.out_d, self.out = carve_dicts(outs, dev)
         self.out_h, _ = carve_dicts(outs, "cpu", pin)
+        # a second device set for the e2e steps (double buffering, below)
+        self.e2e_sets = None
+        if self.in_d.is_cuda:
+            in_d2, views_d2 = carve_dicts(ins, dev)
+            out_d2, out2 = carve_dicts(outs, dev)
+            pt2 = [dict(b=b, s=s, **v) for (b, s), v in zip(self.points, views_d2)]
+            self.e2e_sets = [(self.in_d, self.out_d, self.pt, self.out), (in_d2, out_d2, pt2, out2)]
+            self.e2e_k = 0
 
-    def _run(self, i, stream):
-        p = self.pt[i]
+    def _run(self, i, stream, pt=None, out=None):
+        p = (pt or self.pt)[i]
         w = self.wcopies[self.calls % self.R]
         m = self.ms[self.calls % self.R]
         self.calls += 1
         d = dict(hidden=p["hidden"], positions=p["positions"], cos=self.cos, sin=self.sin, **w)
-        m.run(p["b"], p["s"], d, self.out[i], stream)
+        m.run(p["b"], p["s"], d, (out or self.out)[i], stream)
         self.cl_calls = getattr(self, "cl_calls", 0) + getattr(m, "last_cluster_launches", 0)
         return m.last_launches
 
@@ -215,11 +223,48 @@ class DecodeSweep:
     def e2e_step(self, stream):
         """One step from host buffers: every point's inputs in one
         host-to-device copy, the 16 calls, every output in one device-to-host
-        copy (pinned host memory; bytes are the copied buffers')."""
-        self.in_d.copy_(self.in_h, non_blocking=True)
-        for i in range(len(self.pt)):
-            self._run(i, stream)
-        self.out_h.copy_(self.out_d, non_blocking=True)
+        copy (pinned host memory; bytes are the copied buffers').  On a GPU the
+        two copies run on streams of their own and the steps alternate between
+        two device buffer sets, so that a step's copies overlap the calls of
+        its neighbours (as a serving loop would stage the next batch while
+        this one runs); every step still makes both copies of its own."""
+        if self.e2e_sets is None or stream is None:
+            self.in_d.copy_(self.in_h, non_blocking=True)
+            for i in range(len(self.pt)):
+                self._run(i, stream)
+            self.out_h.copy_(self.out_d, non_blocking=True)
+            return self.in_h.numel(), self.out_h.numel()
+        if getattr(self, "e2e_streams", None) is None:
+            self.e2e_streams = (torch.cuda.Stream(), torch.cuda.Stream())
+            self.e2e_calls_done = [None, None]  # per set: the event after its last calls
+            self.e2e_out_read = [None, None]    # per set: the event after its last D2H copy
+        up, down = self.e2e_streams
+        k = self.e2e_k % 2
+        self.e2e_k += 1
+        in_d, out_d, pt, out = self.e2e_sets[k]
+        # inputs: the set's previous calls must have read it
+        if self.e2e_calls_done[k] is not None:
+            up.wait_event(self.e2e_calls_done[k])
+        with torch.cuda.stream(up):
+            in_d.copy_(self.in_h, non_blocking=True)
+        staged = torch.cuda.Event()
+        staged.record(up)
+        # the calls: after the inputs landed and the set's previous outputs were read
+        stream.wait_event(staged)
+        if self.e2e_out_read[k] is not None:
+            stream.wait_event(self.e2e_out_read[k])
+        for i in range(len(pt)):
+            self._run(i, stream, pt, out)
+        done = torch.cuda.Event()
+        done.record(stream)
+        self.e2e_calls_done[k] = done
+        # outputs
+        down.wait_event(done)
+        with torch.cuda.stream(down):
+            self.out_h.copy_(out_d, non_blocking=True)
+        read = torch.cuda.Event()
+        read.record(down)
+        self.e2e_out_read[k] = read
         return self.in_h.numel(), self.out_h.numel()
 
     def host_inputs(self):
