@@ -16,7 +16,8 @@
 //            the same K columns of the hidden rows (TMA), gamma and the
 //            positions.
 //   phase A  kv_a partial sums [T, 576] over its 128 K rows (mma.sync
-//            m16n8k16, tokens as M, fp32 accumulate).
+//            m16n8k16, fp32 accumulate; the tokens are the N side for T <= 8,
+//            the M side above).
 //   round 1  reduce-scatter: CTA r owns latent columns [32 r, 32 r + 32) and
 //            raw k_pe columns [512 + 4 r, 512 + 4 r + 4); every CTA sends each
 //            owner its [T, 36] partial block with one bulk copy into the
@@ -36,8 +37,8 @@
 //
 // Two cluster barriers, neither on the critical path: one after the
 // mbarriers are initialised (peers signal them), waited for while the
-// phase-A operands are landing; and one at exit, so that no CTA leaves while a copy
-// into or out of its shared memory is in flight.  Every mbarrier wait is
+// phase-A operands are landing; and one at exit, so that no CTA leaves while
+// a copy into or out of its shared memory is in flight.  Every mbarrier wait is
 // bounded; a CTA whose inputs time out still sends its blocks (the outputs
 // are then undefined and the status word says so), so every CTA reaches the
 // exit barrier in bounded time.
@@ -82,7 +83,7 @@ constexpr int kOffN = kOffRope + kClMaxTokens * kOwnR * 4;   // normalised rows 
 constexpr int kOffRed = kOffN + 16 * kNrmPitch;              // phase-B k-slice sums [8 warps][kMaxNg][32][4] f32
 static_assert(kOffRed + 8 * kMaxNg * 32 * 16 <= kWaBytes, "phase-B scratch exceeds the W_kva area");
 static_assert(kOffX % 1024 == 0, "the swizzled hidden boxes need 1024-byte alignment");
-// misc block (at plan.off_misc): mbarriers, positions, cos/sin, flags, gamma
+// misc block (at plan.off_misc): mbarriers, cos/sin of the k_pe columns, flags, gamma
 constexpr int kMiscBytes = 2048;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -139,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
   unsigned char* misc = smem + p.off_misc;
   const uint32_t bar_wa = smem_u32(misc), bar_x = bar_wa + 8, bar_wb = bar_wa + 16;
   const uint32_t bar_r1 = bar_wa + 24, bar_r2 = bar_wa + 32;
-  int* sPos = reinterpret_cast<int*>(misc + 64);                // [16]
   float* sCS = reinterpret_cast<float*>(misc + 128);            // [16][8]: cos j0, j0+1, j0+32, j0+33, then sin
   volatile int* sFlag = reinterpret_cast<volatile int*>(misc + 704);
   T* sGam = reinterpret_cast<T*>(misc + 1024);                  // [512]
@@ -169,10 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
   // W_kvb: this CTA's column groups [g0, g0 + ng) are one contiguous block of
   // 512 rows x ng 16-byte chunks, chunk j of row k stored at j ^ pack_swizzle(ng, k)
   const unsigned char* Wbpk = static_cast<const unsigned char*>(p.W_kvb) + (size_t)g0 * (kRank * 16);
-  // (each cluster starts at another tile, so that the clusters, which all
-  // read the same W_kva lines, spread over the L2 slices)
-  // (W_kvb copies after W_kva's: a CTA's copies share its copy engine, and
-  // so do the bulk copies of the two exchange rounds later on)
+  // Lanes 0..17 copy the W_kva tiles, each cluster starting at another tile
+  // (the clusters all read the same W_kva lines); the next ng lanes copy the
+  // W_kvb slice, queued behind W_kva on the CTA's copy engine (which the
+  // bulk copies of the two exchange rounds use later on as well).
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(bar_wa, (uint32_t)kWaBytes);
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
   grid_dep_launch_dependents();
   grid_dep_wait();
   // ---- after the dependency wait: hidden columns of this CTA's K rows,
-  // gamma, positions and the cos/sin values of the k_pe columns
+  // gamma, and the positions' cos/sin values of the k_pe columns
   if (warp == 1 && lane == 0) {
     mbar_arrive_expect_tx(bar_x, (uint32_t)(kXBoxes * p.xrows * 128));
     for (int b = 0; b < kXBoxes; ++b) tma_load_2d(sX + b * 2048, &p.tmap_x, r * kKr + b * kXBox, p.t0, bar_x);
@@ -204,7 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_cl_kernel(const __grid_con
       atomicOr(p.status, kStatusBadPosition);
       pp = pp < 0 ? 0 : p.max_pos - 1;
     }
-    sPos[lane] = pp;
     if (first_cluster) {
       const int j0 = 2 * r;
       const float* c = p.cos_t + (size_t)pp * kRope;
