@@ -230,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
   int* sWkvbOn = sFlag + 1;
   // K-major blocks (phase B on the tensor cores): N x 128 bytes per 64 K rows
   const int tbB = ng * 8 * 128;
+  // Phase A's ring holds every stage of the unit (the packed plans for phase
+  // B on the tensor cores): all its copies are issued at the start, so the
+  // streamed W_kvb blocks can follow them into L2 right away
+  const bool tb_early = TB && (p.off_red - p.off_a) / (rows_x * 128 + kSubK * 64) >= p.KB / kSubK;
   auto issue_wkvb_warp = [&]() {  // warp 1
     if constexpr (TB) {
       // the first tb_res K blocks, contiguous: 16 KB per lane (the later
@@ -240,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       __syncwarp();
       for (uint32_t o = lane * 16384u; o < bytes; o += 32u * 16384u)
         bulk_g2s(smem_u32(sWB) + o, wkvb_blk + o, bytes - o < 16384u ? bytes - o : 16384u, bar_res);
+      if (tb_early && ng > 0 && lane < 8 - p.tb_res)
+        prefetch_l2_bulk(wkvb_blk + (size_t)(p.tb_res + lane) * tbB, (uint32_t)tbB);
       if (lane == 0) *reinterpret_cast<volatile int*>(sWkvbOn) = 1;
       return;
     }
@@ -628,8 +634,9 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       bulk_g2s(smem_u32(sTbBuf) + lane * tbB, wkvb_blk + (size_t)(p.tb_res + lane) * tbB, (uint32_t)tbB, bar);
     }
     // the blocks refilled in phase B: into L2 during the barrier and phase R
+    // (unless they went there during phase A)
     const int nsl = p.tb_res + p.tb_buf;
-    if (warp == 0 && lane >= 16 && lane - 16 < 8 - nsl)
+    if (!tb_early && warp == 0 && lane >= 16 && lane - 16 < 8 - nsl)
       prefetch_l2_bulk(wkvb_blk + (size_t)(nsl + lane - 16) * tbB, (uint32_t)tbB);
     nbatch = p.tb_buf;
   }
@@ -1262,6 +1269,26 @@ static bool plan_for(int tt, bool resident_only, int hidden, int heads, int num_
     if (resident_only) return false;
     if (regionA < nrm_bytes + 2 * kWkvbBoxRows * pitchB) regionA = nrm_bytes + 2 * kWkvbBoxRows * pitchB;
     kpre = (budget - fixed - regionA) / pitchB / kWkvbBoxRows * kWkvbBoxRows;
+    // Slices for phase B on the tensor cores (below): most of the slice
+    // streams in after phase A anyway, so the shared memory goes to a
+    // phase-A ring that holds every stage of the CTA's unit (packed path:
+    // all its copies in flight at once; resident W_kvb rows would share the
+    // copy engine with them), keeping one K block of the slice resident.
+    const int blk_tb = ngmax * 8 * 128;
+    if (tt <= 64 && budget > kSmemBudget2 && ngmax * 8 >= kTcbMinCols) {
+      const int keep = blk_tb > 64 * pitchB ? blk_tb : 64 * pitchB;
+      int kpre_tb = (keep + pitchB - 1) / pitchB;
+      kpre_tb = (kpre_tb + kWkvbBoxRows - 1) / kWkvbBoxRows * kWkvbBoxRows;
+      if (kpre_tb < tt) kpre_tb = tt;
+      const int off_a_tb = (kpre_tb * pitchB + 1023) / 1024 * 1024;
+      const int all_stages = subs * (tt * 128 + kSubK * 64);
+      int region_tb = (budget - 1024 - kMiscBytes - kRedBytes - off_a_tb) / 128 * 128;
+      if (region_tb > all_stages) region_tb = all_stages;
+      if (region_tb > regionA && kpre_tb <= kpre) {
+        regionA = region_tb;
+        kpre = kpre_tb;
+      }
+    }
     kchunk = (regionA - nrm_bytes) / (2 * pitchB) / kWkvbBoxRows * kWkvbBoxRows;
     if (kpre < 0 || kchunk < kWkvbBoxRows) return false;
   }
