@@ -387,6 +387,43 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
         }
       }
     };
+    // Four or eight m-tiles (M = 4 or 8, compile time): warp w takes m-tiles
+    // w & 3 (and (w & 3) + 4) of its k-half for all four 8-column groups, so
+    // every hidden fragment crosses shared memory once (the mapping above
+    // reads the hidden tile once per column group, four times; the W tile is
+    // the small operand).  Accumulator slots: M = 4: j * 4 + g (k16 step j of
+    // the stage, group g); M = 8: g * 2 + mi (m-tile (w & 3) + 4 mi).
+    const int mg = warp & 3;
+    auto stage_mma_m = [&](auto mt_c, int slot) {
+      constexpr int MI = decltype(mt_c)::value / 4;
+      const unsigned char* st = sA + slot * stage_bytes;
+      const uint32_t x_s = smem_u32(st), w_s = smem_u32(st + xbytes);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int kk = khalf + 2 * j;
+        uint32_t b[4][2];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          if constexpr (PK)
+            ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * 64 + ((g ^ ((lane >> 1) & 3)) * 16), b[g][0], b[g][1]);
+          else
+            ldsm_x2_trans(w_s + (kk * 16 + (lane & 15)) * kPitchWA + g * 16, b[g][0], b[g][1]);
+        }
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi) {
+          const int m = mg + 4 * mi;
+          uint32_t a[4];
+          if constexpr (PK)
+            ldsm_x4(x_s + (m * 16 + (lane & 15)) * 128 + (((kk * 2 + (lane >> 4)) ^ (lane & 7)) * 16), a[0], a[1],
+                    a[2], a[3]);
+          else
+            ldsm_x4(x_s + (m * 16 + (lane & 15)) * kPitchX + (kk * 16 + (lane >> 4) * 8) * 2, a[0], a[1], a[2],
+                    a[3]);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mma16816<E::kBf16>(acc[MI == 1 ? j * 4 + g : g * 2 + mi], a, b[g][0], b[g][1]);
+        }
+      }
+    };
     // stages [i0, i1), stage i in smem slot slot0 + i - i0 and chain i % SC
     auto stages_mma = [&](int i0, int i1, int slot0) {
       auto run = [&](auto mt_c) {
@@ -400,14 +437,20 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
           });
         }
       };
+      auto run_m = [&](auto mt_c) {
+#pragma unroll 1
+        for (int i = i0; i < i1; ++i) stage_mma_m(mt_c, slot0 + i - i0);
+      };
       switch (MT) {
         case 1: run(std::integral_constant<int, 1>{}); break;
         case 2: run(std::integral_constant<int, 2>{}); break;
-        case 4: run(std::integral_constant<int, 4>{}); break;
-        default: run(std::integral_constant<int, 8>{}); break;
+        case 4: run_m(std::integral_constant<int, 4>{}); break;
+        default: run_m(std::integral_constant<int, 8>{}); break;
       }
     };
-    // fold the chain slots of each m-tile into acc[m] (fixed order)
+    // fold the chain slots of each m-tile into acc[m] (fixed order); with the
+    // m-tile mapping the two k16 steps' slots of each group (M = 4; M = 8
+    // has one slot per group and m-tile)
     auto fold = [&]() {
       auto run = [&](auto mt_c) {
         constexpr int M = decltype(mt_c)::value;
@@ -422,7 +465,13 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       switch (MT) {
         case 1: run(std::integral_constant<int, 1>{}); break;
         case 2: run(std::integral_constant<int, 2>{}); break;
-        case 4: run(std::integral_constant<int, 4>{}); break;
+        case 4:
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            acc[g][0] += acc[4 + g][0]; acc[g][1] += acc[4 + g][1];
+            acc[g][2] += acc[4 + g][2]; acc[g][3] += acc[4 + g][3];
+          }
+          break;
         default: break;
       }
     };
@@ -431,6 +480,39 @@ __global__ void __launch_bounds__(kThreads, NC) decode_kernel(const __grid_const
       fold();
       const int u = cta + (i / subs) * G;
       const int kc = u / kNblkA, nb = u - kc * kNblkA;
+      if (MT >= 4) {
+        // m-tile mapping: slot s holds group s (M = 4, folded) or group s / 2
+        // of m-tile mg + 4 (s % 2) (M = 8); the k-half 1 warps hand theirs over
+        const int ns = MT == 4 ? 4 : 8;
+        if (khalf == 1) {
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            if (s < ns)
+              *reinterpret_cast<float4*>(sRed + ((mg * 8 + s) * 32 + lane) * 4) =
+                  make_float4(acc[s][0], acc[s][1], acc[s][2], acc[s][3]);
+        }
+        __syncthreads();
+        if (khalf == 0) {
+          float* P = p.partials + (size_t)kc * kDecodeMaxTokens * kNa;
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            if (s < ns) {
+              const int g = MT == 4 ? s : s >> 1, m = mg + 4 * (MT == 4 ? 0 : s & 1);
+              const int col = nb * kNbA + g * 8 + 2 * (lane & 3);
+              const float4 o = *reinterpret_cast<const float4*>(sRed + ((mg * 8 + s) * 32 + lane) * 4);
+              const int r0 = m * 16 + (lane >> 2);
+              if (r0 < TT)
+                *reinterpret_cast<float2*>(P + (size_t)r0 * kNa + col) = make_float2(acc[s][0] + o.x, acc[s][1] + o.y);
+              if (r0 + 8 < TT)
+                *reinterpret_cast<float2*>(P + (size_t)(r0 + 8) * kNa + col) =
+                    make_float2(acc[s][2] + o.z, acc[s][3] + o.w);
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < kMaxMT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+        return;
+      }
       if (khalf == 1) {
 #pragma unroll
         for (int m = 0; m < kMaxMT; ++m)
