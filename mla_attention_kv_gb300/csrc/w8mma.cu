@@ -272,11 +272,19 @@ __global__ void __launch_bounds__(kMmThreads, 1) w8mma_kernel(const __grid_const
         }
         const unsigned char* src = sSt + (size_t)st * stage_bytes;
         unsigned char* dst = sA + (size_t)as * kABytes;
+        // all four loads before the first store (the compiler keeps a load
+        // of shared memory behind an earlier store that may alias it)
+        uint4 vin[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int item = ct + 128 * it;
+          vin[it] = *reinterpret_cast<const uint4*>(src + (item >> 3) * 128 + (item & 7) * 16);
+        }
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int item = ct + 128 * it;      // 512 items of 16 int8
           const int k = item >> 3, c = item & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + k * 128 + c * 16);
+          const uint4 v = vin[it];
           uint32_t h[8];
           i8x4_to_f16(v.x, h[0], h[1]);
           i8x4_to_f16(v.y, h[2], h[3]);

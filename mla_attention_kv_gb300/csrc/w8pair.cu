@@ -48,7 +48,10 @@ constexpr uint32_t kPStage = 32768;       // A 16 KB + this CTA's half of B 16 K
 constexpr int kPStages = 6;
 constexpr uint32_t kPBarBase = kPStages * kPStage;  // 196608
 constexpr uint32_t kPIntCol = 256;
-constexpr uint32_t kPSmem = kPBarBase + 512 + 1024;
+// HEADS output staging: per epilogue warp its 32 token rows x 128 bytes
+constexpr uint32_t kPStgBase = kPBarBase + 512;
+constexpr uint32_t kPStgWarp = 32 * 128;
+constexpr uint32_t kPSmem = kPStgBase + kPEpiWarps * kPStgWarp + 1024;  // + base alignment slack
 
 struct PShared {
   uint64_t full[kPStages], empty[kPStages];
@@ -276,13 +279,12 @@ __global__ void __launch_bounds__(kPThreads, 1) w8pair_kernel(const __grid_const
         const int bi = (int)((__umulhi((unsigned)t, p.s_mul) + (unsigned)t) >> p.s_shift);
         const int si = t - bi * p.s;
         int32_t* cap = p.cap[w.sel];
-#pragma unroll 1
-        for (int j = c0; j < c0 + kPBN / 2; j += 32) {
-          uint32_t iv[32];
-          tc::ld32(lane_addr + kPIntCol + j, iv);
-          tc::wait_ld();
-          const int col = n0 + j;  // 32 columns inside one head part
-          if (!live || col >= p.N[w.sel]) continue;
+        unsigned char* stg = smem + kPStgBase + (warp - 2) * kPStgWarp;
+        // 32 columns (one head part) straight from registers: q_pe (RoPE
+        // pairs), and any pair of 32-column groups that is not 64 columns of
+        // one plain part
+        auto direct = [&](const uint32_t* iv, int col) {
+          if (!live || col >= p.N[w.sel]) return;
           if (cap) {
             int4* cp = reinterpret_cast<int4*>(cap + (size_t)t * p.N[w.sel] + col);
 #pragma unroll
@@ -343,6 +345,75 @@ __global__ void __launch_bounds__(kPThreads, 1) w8pair_kernel(const __grid_const
             reinterpret_cast<uint4*>(qp + 32 + j0)[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             reinterpret_cast<uint4*>(qp + 32 + j0)[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
           }
+        };
+        // 64 columns per step.  The tile, the warp's 128-column half and the
+        // step all start at multiples of 64 columns, and 64 divides both head
+        // parts' boundaries (128 and 192 or 256), so a step lies inside one
+        // part.  A plain part (q_nope, k_nope, value) goes through the warp's
+        // staging area: each lane writes its row's 128 bytes (16-byte slots
+        // swizzled by row), then each store instruction writes four rows as
+        // whole 128-byte segments instead of 32 rows' 16-byte pieces.
+#pragma unroll 1
+        for (int j = c0; j < c0 + kPBN / 2; j += 64) {
+          const int col = n0 + j;
+          const int hh = col / width, e = col - hh * width;
+          if (!((w.sel == 1 || e < kNope) && col + 64 <= p.N[w.sel])) {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint32_t iv[32];
+              tc::ld32(lane_addr + kPIntCol + j + 32 * h, iv);
+              tc::wait_ld();
+              direct(iv, col + 32 * h);
+            }
+            continue;
+          }
+          __nv_bfloat16* rowp = nullptr;
+          if (live) {
+            const size_t orow = ((size_t)bi * p.heads + hh) * p.s + si;
+            rowp = w.sel == 0 ? static_cast<__nv_bfloat16*>(p.q_nope) + orow * kNope + e
+                   : (e < kNope ? static_cast<__nv_bfloat16*>(p.k_nope) + orow * kNope + e
+                                : static_cast<__nv_bfloat16*>(p.value) + orow * kV + (e - kNope));
+          }
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {  // 32 columns: 16-byte slots 4h .. 4h+3
+            uint32_t iv[32];
+            tc::ld32(lane_addr + kPIntCol + j + 32 * h, iv);
+            tc::wait_ld();
+            if (cap && live) {
+              int4* cp = reinterpret_cast<int4*>(cap + (size_t)t * p.N[w.sel] + col + 32 * h);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                cp[k] = make_int4((int)iv[4 * k], (int)iv[4 * k + 1], (int)iv[4 * k + 2], (int)iv[4 * k + 3]);
+            }
+            const float* swp = p.sw[w.sel] + col + 32 * h;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int sl = 4 * h + k;
+              const float4 sa = __ldg(reinterpret_cast<const float4*>(swp + 8 * k));
+              const float4 sb = __ldg(reinterpret_cast<const float4*>(swp + 8 * k + 4));
+              const uint32_t* x = iv + 8 * k;
+              __nv_bfloat162 o0 = __floats2bfloat162_rn(__fmul_rn(__fmul_rn((float)(int)x[0], sx), sa.x),
+                                                        __fmul_rn(__fmul_rn((float)(int)x[1], sx), sa.y));
+              __nv_bfloat162 o1 = __floats2bfloat162_rn(__fmul_rn(__fmul_rn((float)(int)x[2], sx), sa.z),
+                                                        __fmul_rn(__fmul_rn((float)(int)x[3], sx), sa.w));
+              __nv_bfloat162 o2 = __floats2bfloat162_rn(__fmul_rn(__fmul_rn((float)(int)x[4], sx), sb.x),
+                                                        __fmul_rn(__fmul_rn((float)(int)x[5], sx), sb.y));
+              __nv_bfloat162 o3 = __floats2bfloat162_rn(__fmul_rn(__fmul_rn((float)(int)x[6], sx), sb.z),
+                                                        __fmul_rn(__fmul_rn((float)(int)x[7], sx), sb.w));
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((sl ^ (lane & 7)) << 4)) =
+                  make_uint4(*reinterpret_cast<uint32_t*>(&o0), *reinterpret_cast<uint32_t*>(&o1),
+                             *reinterpret_cast<uint32_t*>(&o2), *reinterpret_cast<uint32_t*>(&o3));
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), sl = lane & 7;
+            const unsigned long long pr = __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(rowp), rr);
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((sl ^ (rr & 7)) << 4));
+            if (pr) reinterpret_cast<uint4*>(pr)[sl] = val;
+          }
+          __syncwarp();  // the slots are rewritten by the next step
         }
       }
     }
