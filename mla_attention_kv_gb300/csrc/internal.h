@@ -256,7 +256,7 @@ cudaError_t prefill_launch(bool bf16, const PrefillParams& p, int num_sms, cudaS
 struct W8Workspace {
   __half* xh;     // [max_tokens, hidden] fp16 codes of the quantised hidden rows
   float* sx;      // [max_tokens]
-  int32_t* acc1;  // [max_tokens, q_rank + 576]
+  int32_t* acc1;  // [max_tokens, q_rank + 576]; rows [0, kW8PairMinRows) zero between calls
   int8_t* q1;     // [max_tokens, q_rank]
   float* s1;      // [max_tokens]
   int8_t* c1;     // [max_tokens, 512]

@@ -464,8 +464,10 @@ __global__ void __launch_bounds__(256) norm_quant_warp_kernel(int32_t* __restric
       reinterpret_cast<float4*>(y)[idx] =
           make_float4(__fmul_rn(__fmul_rn((float)av[i].x, s), cs.x), __fmul_rn(__fmul_rn((float)av[i].y, s), cs.y),
                       __fmul_rn(__fmul_rn((float)av[i].z, s), cs.z), __fmul_rn(__fmul_rn((float)av[i].w, s), cs.w));
-      // leave the accumulator row zeroed (the decode-size chain adds into it)
-      reinterpret_cast<int4*>(a)[idx] = make_int4(0, 0, 0, 0);
+      // leave the row zeroed if a call of fewer rows can add into it (the
+      // paths below kW8PairMinRows rows add their q_a / kv_a sums; this
+      // one's GEMM stores them, so the rows past that stay as they are)
+      if (t < kW8PairMinRows) reinterpret_cast<int4*>(a)[idx] = make_int4(0, 0, 0, 0);
     }
   }
   __syncwarp();
@@ -1464,8 +1466,10 @@ cudaError_t w8a8_launch(const W8Params& p, const W8Workspace& w, const W8SmallPl
   quant_rows_kernel<__half><<<T, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(p.hidden), h, w.xh, w.sx);
   ++*launches;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // The accumulator rows are left zeroed by every call (norm_quant_kernel,
-  // or the decode-size chain), so the q_a / kv_a sums are added into them.
+  // Accumulator rows [0, kW8PairMinRows) are left zeroed by every call
+  // (norm_quant_kernel, norm_quant_warp_kernel or the decode-size chain), so
+  // the paths below kW8PairMinRows rows add their q_a / kv_a sums into them;
+  // the pair path stores its sums (every column of rows [0, T)).
   const bool pairk = T >= kW8PairMinRows && w.wa16;
   auto chain_pair = [&]() -> cudaError_t {
     // 1b. the int8 weights widened to fp16 copies ([W_qa | W_kva], W_qb, W_kvb)

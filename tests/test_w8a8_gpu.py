@@ -168,6 +168,38 @@ def test_w8a8_small_chain_repeats_and_alternates(oracle_mod):
         m.close()
 
 
+def test_w8a8_paths_alternate_on_one_handle(oracle_mod):
+    """All three W8A8 paths on one handle, twice in a row: the 2-SM path
+    (T = 600, which stores its q_a | kv_a sums and leaves only the rows that
+    smaller calls use zeroed), the single-SM path (T = 64) and the
+    decode-size chain (T = 3), which both add into accumulator rows the call
+    before left zeroed.  Every call matches the oracle and its repetition."""
+    cfg = I.small_config(I.R1_W8A8, hidden=512, q_lora_rank=256, num_heads=4, max_pos=512)
+    sizes = [(2, 300), (64, 1), (3, 1)]
+    inps = [I.w8a8_inputs(cfg, b, s, 7100 + b * s, "decode") for b, s in sizes]
+    devs = [B.to_device(x) for x in inps]
+    m = B.MLAProlog(cfg, 600)
+    try:
+        rounds = []
+        for _ in range(2):
+            outs = []
+            for (b, s), d in zip(sizes, devs):
+                out = m.alloc_outputs(b, s)
+                m.run(b, s, d, out)
+                torch.cuda.synchronize()
+                outs.append({k: v.clone() for k, v in out.items()})
+            rounds.append(outs)
+        assert m.status() == 0
+        for o0, o1 in zip(*rounds):
+            for k in NAMES:
+                assert torch.equal(o0[k], o1[k]), k
+        for inp, o in zip(inps, rounds[0]):
+            for n, r in zip(NAMES, oracle_mod.w8a8_prolog(inp)):
+                compare(n, o[n], r, oracle_mod)
+    finally:
+        m.close()
+
+
 def _capture_run(cfg, inp, b, s):
     """Run the W8A8 prolog on `inp` with the accumulator capture on; return
     the captured accumulators and the GPU's own q_b / kv_b operands."""
