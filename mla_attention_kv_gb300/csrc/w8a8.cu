@@ -186,6 +186,9 @@ __device__ __forceinline__ int8_t q8(float x, float inv) {
   return (int8_t)(int)r;
 }
 
+// Rows of at most this many columns are held in registers by quant_rows_kernel.
+constexpr int kQuantRegCols = 256 * 8 * 4;
+
 // One CTA (256 threads) per row of a bf16 matrix [rows, cols] -> codes +
 // scale.  The codes are stored as int8, or (Q = __half) as the fp16 values
 // of the same integers (the tensor-core GEMM operand; exact for |q| <= 127).
@@ -199,17 +202,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
   grid_dep_launch_dependents();
   const int row = blockIdx.x;
   const __nv_bfloat16* xr = x + (size_t)row * cols;
-  float amax = 0.f;
-  for (int c = threadIdx.x * 8; c < cols; c += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
-    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(__bfloat162float(e[i])));
-  }
-  amax = block_reduce<true>(amax, scratch);
-  const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
-  for (int c = threadIdx.x * 8; c < cols; c += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xr + c);
+  // 8 values per 16-byte vector, vector k of thread i at column (i + 256 k) * 8
+  auto codes = [&](const uint4& v, int c, float inv) {
     const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
     if constexpr (std::is_same<Q, int8_t>::value) {
       char4 lo, hi;
@@ -225,6 +219,36 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __
       for (int i = 0; i < 8; ++i) h[i] = __int2half_rn((int)q8(__bfloat162float(e[i]), inv));
       *reinterpret_cast<uint4*>(q + (size_t)row * cols + c) = *reinterpret_cast<const uint4*>(h);
     }
+  };
+  auto vmax = [](const uint4& v, float m) {
+    const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(__bfloat162float(e[i])));
+    return m;
+  };
+  float amax = 0.f;
+  if (cols <= kQuantRegCols) {
+    // the whole row in registers: every load issued at once, read once
+    uint4 v[kQuantRegCols / 2048];
+#pragma unroll
+    for (int k = 0; k < kQuantRegCols / 2048; ++k) {
+      const int c = (threadIdx.x + 256 * k) * 8;
+      v[k] = c < cols ? *reinterpret_cast<const uint4*>(xr + c) : make_uint4(0, 0, 0, 0);
+      amax = vmax(v[k], amax);
+    }
+    amax = block_reduce<true>(amax, scratch);
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kQuantRegCols / 2048; ++k) {
+      const int c = (threadIdx.x + 256 * k) * 8;
+      if (c < cols) codes(v[k], c, inv);
+    }
+  } else {
+    for (int c = threadIdx.x * 8; c < cols; c += 256 * 8)
+      amax = vmax(*reinterpret_cast<const uint4*>(xr + c), amax);
+    amax = block_reduce<true>(amax, scratch);
+    const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+    for (int c = threadIdx.x * 8; c < cols; c += 256 * 8) codes(*reinterpret_cast<const uint4*>(xr + c), c, inv);
   }
   if (threadIdx.x == 0) scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
 }

@@ -440,26 +440,44 @@ struct WidenJobs {
 };
 
 __global__ void widen_kernel(const __grid_constant__ WidenJobs J) {
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < J.start[J.n]; i += (long)gridDim.x * blockDim.x) {
-    int q = 0;
-    while (i >= J.start[q + 1]) ++q;
-    const W8WidenJob& jb = J.j[q];
-    const long g = i - J.start[q];
-    const int gpr = jb.wcols / 16;
-    const int k = (int)(g / gpr), c = (int)(g % gpr) * 16;
-    __align__(16) __half h[16];
-    if (c + 16 <= jb.N) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(jb.W + (size_t)k * jb.N + c));
-      const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+  // four 16-column groups per thread and pass, all loads issued first
+  const long n = J.start[J.n], stride = (long)gridDim.x * blockDim.x;
+  for (long i0 = blockIdx.x * (long)blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
+    uint4 v[4];
+    int job[4], row[4], col[4];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) h[x] = __int2half_rn((int)b[x]);
-    } else {
-#pragma unroll
-      for (int x = 0; x < 16; ++x) h[x] = __int2half_rn(c + x < jb.N ? (int)jb.W[(size_t)k * jb.N + c + x] : 0);
+    for (int u = 0; u < 4; ++u) {
+      const long i = i0 + u * stride;
+      job[u] = -1;
+      if (i >= n) continue;
+      int q = 0;
+      while (i >= J.start[q + 1]) ++q;
+      const W8WidenJob& jb = J.j[q];
+      const long g = i - J.start[q];
+      const int gpr = jb.wcols / 16;
+      job[u] = q;
+      row[u] = (int)(g / gpr);
+      col[u] = (int)(g % gpr) * 16;
+      if (col[u] + 16 <= jb.N) v[u] = __ldg(reinterpret_cast<const uint4*>(jb.W + (size_t)row[u] * jb.N + col[u]));
     }
-    uint4* d = reinterpret_cast<uint4*>(jb.out + (size_t)k * jb.ldn + c);
-    d[0] = *reinterpret_cast<const uint4*>(h);
-    d[1] = *reinterpret_cast<const uint4*>(h + 8);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (job[u] < 0) continue;
+      const W8WidenJob& jb = J.j[job[u]];
+      const int k = row[u], c = col[u];
+      __align__(16) __half h[16];
+      if (c + 16 <= jb.N) {
+        const int8_t* b = reinterpret_cast<const int8_t*>(&v[u]);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) h[x] = __int2half_rn((int)b[x]);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) h[x] = __int2half_rn(c + x < jb.N ? (int)jb.W[(size_t)k * jb.N + c + x] : 0);
+      }
+      uint4* d = reinterpret_cast<uint4*>(jb.out + (size_t)k * jb.ldn + c);
+      d[0] = *reinterpret_cast<const uint4*>(h);
+      d[1] = *reinterpret_cast<const uint4*>(h + 8);
+    }
   }
 }
 

@@ -27,7 +27,7 @@ def _lib():
     B.load()
 
 
-@pytest.mark.parametrize("rows,cols", [(1, 64), (7, 7168), (33, 1536), (3, 512)])
+@pytest.mark.parametrize("rows,cols", [(1, 64), (7, 7168), (33, 1536), (3, 512), (5, 8184), (3, 8200)])
 def test_quant_rows_bit_exact(oracle_mod, rows, cols):
     g = torch.Generator().manual_seed(rows * 1000 + cols)
     x = (torch.randn(rows, cols, generator=g) * 3).to(torch.bfloat16)
